@@ -1,0 +1,178 @@
+"""fp64 CPU oracle for the Kimi Delta Attention (KDA) recurrence -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference legs of
+``bench.py`` may import this package.  The product path (the CUDA library and its Python
+binding) never calls it, and the two share no code.
+
+The arithmetic lives in ``kda_oracle.c`` (plain C, double precision, OpenMP over independent
+(sequence, head, value-column block) units).  This module only marshals arrays:
+
+* every input is converted to a C-contiguous float64 array (bf16 and fp32 values are upcast
+  exactly), and
+* results come back as float64 numpy arrays.
+
+What is computed (see the C file for the step-by-step statement):
+
+* ``gate``        -- Equation 5 of "Kimi K3: the paper and proofs side by side" (section 2.1.1):
+                     g = g_min * sigmoid(exp(A_h) z), alpha = exp(g).
+* ``recurrence``  -- Equation 1 with alpha given directly, token by token:
+                     S_t = (I - b k k^T) Diag(alpha) S_{t-1} + b k v^T, o_t = S_t^T q_t.
+* ``forward``     -- Equation 1 driven by the Equation 5 gate (what ``kda_forward`` computes).
+* ``decode_step`` -- one token per sequence (what ``kda_decode_step`` computes).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libkda_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+
+
+def build(force: bool = False) -> str:
+    """Compile ``kda_oracle.c`` into ``libkda_oracle.so`` beside it (gcc, OpenMP, no FMA contraction)."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-Wall", "-Wextra", "-fopenmp", "-ffp-contract=off",
+           "-shared", "-fPIC", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.kda_oracle_gate.restype = None
+            lib.kda_oracle_gate.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _dp, _dp,
+                                            ctypes.c_double, _dp, _dp]
+            run_args = [ctypes.c_int32, _i64p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                        _dp, _dp, _dp]
+            lib.kda_oracle_recurrence.restype = ctypes.c_int
+            lib.kda_oracle_recurrence.argtypes = run_args + [_dp, _dp, _dp, _dp, _dp,
+                                                             ctypes.c_int32, ctypes.c_int32]
+            lib.kda_oracle_forward.restype = ctypes.c_int
+            lib.kda_oracle_forward.argtypes = run_args + [_dp, _dp, ctypes.c_double, _dp, _dp, _dp, _dp,
+                                                          ctypes.c_int32, ctypes.c_int32]
+            lib.kda_oracle_decode_step.restype = ctypes.c_int
+            lib.kda_oracle_decode_step.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                   ctypes.c_int32, _dp, _dp, _dp, _dp, _dp,
+                                                   ctypes.c_double, _dp, _dp, _dp, _dp, ctypes.c_int32]
+            lib.kda_oracle_max_threads.restype = ctypes.c_int
+            lib.kda_oracle_max_threads.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def _f64(x) -> np.ndarray:
+    """Exact upcast of a numpy array or a CPU/GPU torch tensor to C-contiguous float64."""
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor
+        import torch
+        x = x.detach().to(device="cpu", dtype=torch.float64).contiguous().numpy()
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(_dp)
+
+
+def _cu(cu_seqlens, T: int) -> np.ndarray:
+    if cu_seqlens is None:
+        return np.array([0, T], dtype=np.int64)
+    if hasattr(cu_seqlens, "detach"):
+        cu_seqlens = cu_seqlens.detach().cpu().numpy()
+    return np.ascontiguousarray(cu_seqlens, dtype=np.int64)
+
+
+def max_threads() -> int:
+    """OpenMP threads the oracle uses by default."""
+    return int(_load().kda_oracle_max_threads())
+
+
+def gate(z, A, g_min: float = -5.0):
+    """Equation 5 over z [T, H, d_k] with A [H]; returns (g, alpha) as float64 arrays."""
+    z = _f64(z)
+    A = _f64(A)
+    T, H, dk = z.shape
+    g = np.empty_like(z)
+    al = np.empty_like(z)
+    _load().kda_oracle_gate(T, H, dk, _ptr(z), _ptr(A), float(g_min), _ptr(g), _ptr(al))
+    return g, al
+
+
+def _check(rc: int):
+    if rc == -1:
+        raise ValueError("oracle: invalid arguments")
+    if rc != 0:
+        raise MemoryError("oracle: allocation failed")
+
+
+def recurrence(q, k, v, alpha, beta, S0=None, cu_seqlens=None, col_block: int = 0, threads: int = 0,
+               want_out: bool = True):
+    """Equation 1 with retentions ``alpha`` [T, H, d_k] given directly.
+
+    q, k: [T, H, d_k]; v: [T, H, d_v]; beta: [T, H]; S0: [N, H, d_k, d_v] or None (zeros);
+    cu_seqlens: [N+1] offsets or None (one sequence).  Returns (out [T,H,d_v], S_final [N,H,d_k,d_v]).
+    """
+    q, k, v, alpha, beta, S0 = map(_f64, (q, k, v, alpha, beta, S0))
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    cu = _cu(cu_seqlens, T)
+    N = cu.shape[0] - 1
+    out = np.zeros((T, H, dv), dtype=np.float64) if want_out else None
+    Sf = np.zeros((N, H, dk, dv), dtype=np.float64)
+    rc = _load().kda_oracle_recurrence(N, cu.ctypes.data_as(_i64p), H, dk, dv, _ptr(q), _ptr(k),
+                                       _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0), _ptr(out),
+                                       _ptr(Sf), int(col_block), int(threads))
+    _check(rc)
+    return out, Sf
+
+
+def forward(q, k, v, z, A, beta, S0=None, cu_seqlens=None, g_min: float = -5.0, col_block: int = 0,
+            threads: int = 0, want_out: bool = True):
+    """Equation 1 driven by the Equation 5 gate: the result ``kda_forward`` must reproduce.
+
+    Shapes as in :func:`recurrence`, with z [T, H, d_k] and A [H] in place of alpha.
+    """
+    q, k, v, z, A, beta, S0 = map(_f64, (q, k, v, z, A, beta, S0))
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    cu = _cu(cu_seqlens, T)
+    N = cu.shape[0] - 1
+    out = np.zeros((T, H, dv), dtype=np.float64) if want_out else None
+    Sf = np.zeros((N, H, dk, dv), dtype=np.float64)
+    rc = _load().kda_oracle_forward(N, cu.ctypes.data_as(_i64p), H, dk, dv, _ptr(q), _ptr(k), _ptr(v),
+                                    _ptr(z), _ptr(A), float(g_min), _ptr(beta), _ptr(S0), _ptr(out),
+                                    _ptr(Sf), int(col_block), int(threads))
+    _check(rc)
+    return out, Sf
+
+
+def decode_step(q, k, v, z, A, beta, S, g_min: float = -5.0, threads: int = 0):
+    """One token for each of N sequences: q, k, z [N, H, d_k]; v [N, H, d_v]; beta [N, H];
+    S [N, H, d_k, d_v].  Returns (out [N, H, d_v], S_new)."""
+    q, k, v, z, A, beta, S = map(_f64, (q, k, v, z, A, beta, S))
+    N, H, dk = k.shape
+    dv = v.shape[2]
+    out = np.zeros((N, H, dv), dtype=np.float64)
+    S_new = np.empty_like(S)
+    rc = _load().kda_oracle_decode_step(N, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A),
+                                        float(g_min), _ptr(beta), _ptr(S), _ptr(S_new), _ptr(out),
+                                        int(threads))
+    _check(rc)
+    return out, S_new

@@ -1,0 +1,356 @@
+"""Pins for the fp64 oracle: values the pages print, closed forms, special cases, brute force
+and invariants.  None of these re-types the oracle's loop; each would fail for a plausible
+mistake in it (a dropped term, the erase and decay swapped, a wrong index, a transposed state,
+reading before the update, a wrong gate sign or scale)."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from conftest import GOLDEN
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _one(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+def _run(q, k, v, alpha, beta, S0=None, cu=None, **kw):
+    """Oracle with [T,H,*] inputs built from per-token lists (H=1 unless already 3-D)."""
+    return oracle.recurrence(q, k, v, alpha, beta, S0=S0, cu_seqlens=cu, **kw)
+
+
+# ---------------------------------------------------------------- values printed on the pages
+
+def test_golden_scalar_delta_update():
+    g = _golden("scalar_delta_update.json")
+    for case in g["cases"]:
+        out, Sf = _run(_one([[g["q"]]]), _one([[g["k"]]]), _one([[[g["v"]]]]), _one([[[g["alpha"]]]]),
+                       _one([[case["beta"]]]), S0=_one([[[[g["S0"]]]]]))
+        assert abs(Sf[0, 0, 0, 0] - case["S1"]) < 1e-12
+        # the query reads the updated state
+        assert abs(out[0, 0, 0] - case["S1"]) < 1e-12
+        if "decayed" in case:
+            assert abs(g["alpha"] * g["S0"] - case["decayed"]) < 1e-12
+            assert abs(g["v"] - case["decayed"] - case["error"]) < 1e-12
+
+
+def test_golden_scalar_token_order():
+    g = _golden("scalar_token_order.json")
+    finals = []
+    for case in g["cases"]:
+        T = len(case["values"])
+        q = np.ones((T, 1, 1))
+        k = np.ones((T, 1, 1))
+        v = np.asarray(case["values"], dtype=np.float64).reshape(T, 1, 1)
+        al = np.full((T, 1, 1), g["alpha"])
+        b = np.full((T, 1), g["beta"])
+        _, Sf = _run(q, k, v, al, b, S0=np.full((1, 1, 1, 1), g["S0"]))
+        assert abs(Sf[0, 0, 0, 0] - case["S_T"]) < 1e-12
+        finals.append(Sf[0, 0, 0, 0])
+    # tokens cannot be permuted
+    assert abs(finals[0] - finals[1]) > 1.0
+
+
+def test_golden_lean_step_2x1():
+    g = _golden("lean_step_2x1.json")
+    out, Sf = _run(_one([[g["q"]]]), _one([[g["k"]]]), _one([[g["v"]]]), _one([[g["alpha"]]]),
+                   _one([[g["beta"]]]), S0=_one([[g["S0"]]]))
+    assert out[0, 0, 0] == g["out0"]
+
+
+def test_golden_worked_2x2():
+    g = _golden("worked_2x2.json")
+    out, Sf = _run(_one([[g["q"]]]), _one([[g["k"]]]), _one([[g["v"]]]), _one([[g["alpha"]]]),
+                   _one([[g["beta"]]]), S0=_one([[g["S0"]]]))
+    np.testing.assert_allclose(Sf[0, 0], g["S1"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(out[0, 0], g["out"], rtol=0, atol=1e-12)
+    # the intermediate quantities printed on the page are consistent with the final state
+    decayed = np.asarray(g["alpha"])[:, None] * np.asarray(g["S0"])
+    np.testing.assert_allclose(decayed, g["decayed"], atol=1e-12)
+    np.testing.assert_allclose(np.asarray(g["k"]) @ decayed, g["old_value"], atol=1e-12)
+    np.testing.assert_allclose(np.asarray(g["v"]) - np.asarray(g["old_value"]), g["correction"], atol=1e-12)
+
+
+def test_golden_gate_slider():
+    g = _golden("gate_slider.json")
+    for A in (-3.0, -0.5, 0.0, 0.7, 2.0):
+        gg, al = oracle.gate(np.full((1, 1, 1), g["z"]), np.array([A]), g_min=g["g_min"])
+        assert gg[0, 0, 0] == g["g"]
+        assert round(al[0, 0, 0], 4) == g["alpha_4dp"]
+        assert abs(al[0, 0, 0] - math.exp(-2.5)) < 1e-15
+
+
+# ---------------------------------------------------------------- the gate (Equation 5)
+
+def test_gate_bounds_monotone_and_scale():
+    z = np.linspace(-30, 30, 601).reshape(-1, 1, 1)
+    for A in (-1.0, 0.0, 1.0):
+        g, al = oracle.gate(z, np.array([A]))
+        g = g.ravel()
+        al = al.ravel()
+        assert np.all(g <= 0.0) and np.all(g >= -5.0)
+        assert np.all(al <= 1.0) and np.all(al >= math.exp(-5.0))
+        # moving the logit right forgets faster (smaller retention); strictly so until the
+        # sigmoid saturates in double precision
+        assert np.all(np.diff(g) <= 0)
+        inner = np.abs(z.ravel()[1:]) < 10
+        assert np.all(np.diff(g)[inner] < 0)
+        # strict interior for moderate logits, as in paper_retention_bounds
+        mid = np.abs(z.ravel()) < 5
+        assert np.all(al[mid] < 1.0) and np.all(al[mid] > math.exp(-5.0))
+        # e^A scales the logit: g(z; A) = g(z e^A; 0)
+        g0, _ = oracle.gate(z * math.exp(A), np.array([0.0]))
+        np.testing.assert_allclose(g, g0.ravel(), rtol=1e-14, atol=1e-14)
+    # the limits are g_min (z -> +inf) and 0 (z -> -inf); the midpoint is g_min / 2
+    g, _ = oracle.gate(np.array([[[60.0]], [[-60.0]], [[0.0]]]), np.array([0.0]), g_min=-7.0)
+    assert abs(g[0, 0, 0] + 7.0) < 1e-12 and abs(g[1, 0, 0]) < 1e-12 and g[2, 0, 0] == -3.5
+
+
+def test_gate_tile_cumulative_log_decay_bound():
+    rng = np.random.default_rng(1)
+    z = rng.normal(size=(16 * 64, 2, 32)) * 4.0
+    A = rng.normal(size=2)
+    g, _ = oracle.gate(z, A)
+    G = g.reshape(64, 16, 2, 32).sum(axis=1)
+    assert np.all(G <= 0.0) and np.all(G >= -80.0)
+
+
+def test_gate_driven_forward_equals_recurrence_with_gate_alpha():
+    rng = np.random.default_rng(2)
+    T, H, dk, dv = 21, 2, 5, 3
+    q, k = rng.normal(size=(T, H, dk)), rng.normal(size=(T, H, dk))
+    v, z = rng.normal(size=(T, H, dv)), rng.normal(size=(T, H, dk))
+    A, b = rng.normal(size=H), rng.uniform(size=(T, H))
+    S0 = rng.normal(size=(1, H, dk, dv))
+    _, al = oracle.gate(z, A)
+    o1, s1 = oracle.forward(q, k, v, z, A, b, S0=S0)
+    o2, s2 = oracle.recurrence(q, k, v, al, b, S0=S0)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(s1, s2)
+
+
+# ---------------------------------------------------------------- closed forms / special cases
+
+def _rand(rng, T, H, dk, dv, unit_keys=True):
+    k = rng.normal(size=(T, H, dk))
+    if unit_keys:
+        k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    q = rng.normal(size=(T, H, dk))
+    v = rng.normal(size=(T, H, dv))
+    al = rng.uniform(0.2, 0.99, size=(T, H, dk))
+    b = rng.uniform(0.05, 0.95, size=(T, H))
+    S0 = rng.normal(size=(1, H, dk, dv))
+    return q, k, v, al, b, S0
+
+
+def test_beta_zero_is_pure_decay():
+    rng = np.random.default_rng(3)
+    T, H, dk, dv = 13, 2, 6, 4
+    q, k, v, al, _, S0 = _rand(rng, T, H, dk, dv)
+    out, Sf = oracle.recurrence(q, k, v, al, np.zeros((T, H)), S0=S0)
+    Gam = np.cumprod(al, axis=0)  # [T, H, dk]
+    for t in range(T):
+        for h in range(H):
+            St = Gam[t, h][:, None] * S0[0, h]
+            np.testing.assert_allclose(out[t, h], St.T @ q[t, h], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(Sf[0], Gam[-1][:, :, None] * S0[0], rtol=1e-12, atol=1e-12)
+
+
+def test_alpha_one_beta_one_orthonormal_keys_read_back_value():
+    rng = np.random.default_rng(4)
+    T, dk, dv = 7, 9, 5
+    # distinct standard-basis keys from a zero state: bit-exact
+    idx = rng.permutation(dk)[:T]
+    k = np.zeros((T, 1, dk))
+    k[np.arange(T), 0, idx] = 1.0
+    v = rng.normal(size=(T, 1, dv))
+    out, _ = oracle.recurrence(k, k, v, np.ones((T, 1, dk)), np.ones((T, 1)))
+    np.testing.assert_array_equal(out, v)
+    # general orthonormal keys (rows of a random orthogonal matrix) and a random state
+    Qm, _ = np.linalg.qr(rng.normal(size=(dk, dk)))
+    k = Qm[:T].reshape(T, 1, dk)
+    S0 = rng.normal(size=(1, 1, dk, dv))
+    out, _ = oracle.recurrence(k, k, v, np.ones((T, 1, dk)), np.ones((T, 1)), S0=S0)
+    np.testing.assert_allclose(out, v, rtol=0, atol=1e-12)
+
+
+def test_alpha_one_beta_zero_constant_state():
+    rng = np.random.default_rng(5)
+    T, H, dk, dv = 9, 3, 4, 6
+    q, k, v, _, _, S0 = _rand(rng, T, H, dk, dv)
+    out, Sf = oracle.recurrence(q, k, v, np.ones((T, H, dk)), np.zeros((T, H)), S0=S0)
+    np.testing.assert_array_equal(Sf, S0)
+    np.testing.assert_allclose(out, np.einsum("thc,hcj->thj", q, S0[0]), rtol=1e-13, atol=1e-13)
+
+
+def test_scalar_case_is_the_textbook_delta_rule():
+    rng = np.random.default_rng(6)
+    T = 40
+    q, k, v = rng.normal(size=T), rng.normal(size=T), rng.normal(size=T)
+    al, b = rng.uniform(0.1, 1.0, size=T), rng.uniform(size=T)
+    s = 0.3
+    ref_o = []
+    for t in range(T):
+        pred = k[t] * al[t] * s
+        s = al[t] * s + b[t] * k[t] * (v[t] - pred)
+        ref_o.append(q[t] * s)
+    out, Sf = oracle.recurrence(q.reshape(T, 1, 1), k.reshape(T, 1, 1), v.reshape(T, 1, 1),
+                                al.reshape(T, 1, 1), b.reshape(T, 1), S0=np.full((1, 1, 1, 1), 0.3))
+    np.testing.assert_allclose(out.ravel(), ref_o, rtol=1e-13, atol=1e-13)
+    assert abs(Sf.item() - s) < 1e-13
+
+
+# ---------------------------------------------------------------- brute force (dense affine maps)
+
+def _affine(k, v, a, b):
+    dk = k.shape[0]
+    M = (np.eye(dk) - b * np.outer(k, k)) @ np.diag(a)
+    return M, b * np.outer(k, v)
+
+
+def _compose(later, earlier):
+    M2, U2 = later
+    M1, U1 = earlier
+    return M2 @ M1, M2 @ U1 + U2
+
+
+@pytest.mark.parametrize("T", [1, 2, 5, 8])
+def test_bruteforce_affine_maps(T):
+    rng = np.random.default_rng(10 + T)
+    H, dk, dv = 2, 4, 3
+    q, k, v, al, b, S0 = _rand(rng, T, H, dk, dv, unit_keys=False)
+    b = rng.uniform(0, 1.5, size=(T, H))  # the algebra holds for any beta
+    out, Sf = oracle.recurrence(q, k, v, al, b, S0=S0)
+    for h in range(H):
+        agg = (np.eye(dk), np.zeros((dk, dv)))
+        for t in range(T):
+            agg = _compose(_affine(k[t, h], v[t, h], al[t, h], b[t, h]), agg)
+            St = agg[0] @ S0[0, h] + agg[1]
+            np.testing.assert_allclose(out[t, h], St.T @ q[t, h], rtol=1e-11, atol=1e-11)
+        np.testing.assert_allclose(Sf[0, h], agg[0] @ S0[0, h] + agg[1], rtol=1e-11, atol=1e-11)
+        # S_T = M_{T:1} S_0 + sum_i M_{T:i+1} U_i, summed explicitly
+        acc = np.zeros((dk, dv))
+        for i in range(T):
+            Mi = np.eye(dk)
+            for s in range(i + 1, T):
+                Mi = _affine(k[s, h], v[s, h], al[s, h], b[s, h])[0] @ Mi
+            acc += Mi @ _affine(k[i, h], v[i, h], al[i, h], b[i, h])[1]
+        Mall = np.eye(dk)
+        for s in range(T):
+            Mall = _affine(k[s, h], v[s, h], al[s, h], b[s, h])[0] @ Mall
+        np.testing.assert_allclose(Sf[0, h], Mall @ S0[0, h] + acc, rtol=1e-11, atol=1e-11)
+    if T >= 3:
+        maps = [_affine(k[t, 0], v[t, 0], al[t, 0], b[t, 0]) for t in range(3)]
+        left = _compose(maps[2], _compose(maps[1], maps[0]))
+        right = _compose(_compose(maps[2], maps[1]), maps[0])
+        for x, y in zip(left, right):
+            np.testing.assert_allclose(x, y, atol=1e-12)
+
+
+def test_mutations_are_detected():
+    """Plausible mistakes in an oracle (swapped erase/decay, reading before the update,
+    a dropped erase, a transposed read) disagree with it on a single random token."""
+    rng = np.random.default_rng(20)
+    dk = dv = 4
+    q, k, v, al, b, S0 = _rand(rng, 1, 1, dk, dv)
+    out, Sf = oracle.recurrence(q, k, v, al, b, S0=S0)
+    S, kk, vv, a, bb, qq = S0[0, 0], k[0, 0], v[0, 0], al[0, 0], b[0, 0], q[0, 0]
+    wrong_order = np.diag(a) @ (np.eye(dk) - bb * np.outer(kk, kk)) @ S + bb * np.outer(kk, vv)
+    no_erase = np.diag(a) @ S + bb * np.outer(kk, vv)
+    assert np.max(np.abs(wrong_order - Sf[0, 0])) > 1e-3
+    assert np.max(np.abs(no_erase - Sf[0, 0])) > 1e-3
+    assert np.max(np.abs(S.T @ qq - out[0, 0])) > 1e-3  # read before the update
+    # retention applied to value columns instead of key rows
+    cols = S * a[None, :]
+    transposed = cols + bb * np.outer(kk, vv - kk @ cols)
+    assert np.max(np.abs(transposed - Sf[0, 0])) > 1e-3
+
+
+# ---------------------------------------------------------------- invariants
+
+def test_chunk_split_invariance():
+    rng = np.random.default_rng(30)
+    T, H, dk, dv = 37, 2, 5, 4
+    q, k, v, al, b, S0 = _rand(rng, T, H, dk, dv)
+    out, Sf = oracle.recurrence(q, k, v, al, b, S0=S0)
+    for cut in (1, 16, 18, 36):
+        o1, s1 = oracle.recurrence(q[:cut], k[:cut], v[:cut], al[:cut], b[:cut], S0=S0)
+        o2, s2 = oracle.recurrence(q[cut:], k[cut:], v[cut:], al[cut:], b[cut:], S0=s1)
+        np.testing.assert_array_equal(np.concatenate([o1, o2]), out)
+        np.testing.assert_array_equal(s2, Sf)
+
+
+def test_head_and_column_independence():
+    rng = np.random.default_rng(31)
+    T, H, dk, dv = 19, 3, 6, 5
+    q, k, v, al, b, S0 = _rand(rng, T, H, dk, dv)
+    out, Sf = oracle.recurrence(q, k, v, al, b, S0=S0)
+    for h in range(H):
+        o, s = oracle.recurrence(q[:, h:h + 1], k[:, h:h + 1], v[:, h:h + 1], al[:, h:h + 1],
+                                 b[:, h:h + 1], S0=S0[:, h:h + 1])
+        np.testing.assert_array_equal(o[:, 0], out[:, h])
+        np.testing.assert_array_equal(s[:, 0], Sf[:, h])
+    for cb in (1, 2, 3):
+        o, s = oracle.recurrence(q, k, v, al, b, S0=S0, col_block=cb)
+        np.testing.assert_array_equal(o, out)
+        np.testing.assert_array_equal(s, Sf)
+    perm = rng.permutation(dv)
+    o, s = oracle.recurrence(q, k, v[:, :, perm], al, b, S0=S0[..., perm])
+    np.testing.assert_array_equal(o, out[:, :, perm])
+    np.testing.assert_array_equal(s, Sf[..., perm])
+
+
+def test_varlen_packing_equals_separate_runs_and_empty_sequence():
+    rng = np.random.default_rng(32)
+    lens = [5, 0, 17, 1, 16]
+    T = sum(lens)
+    H, dk, dv = 2, 4, 3
+    q, k, v, al, b, _ = _rand(rng, T, H, dk, dv)
+    S0 = rng.normal(size=(len(lens), H, dk, dv))
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    out, Sf = oracle.recurrence(q, k, v, al, b, S0=S0, cu_seqlens=cu)
+    for n, L in enumerate(lens):
+        sl = slice(cu[n], cu[n + 1])
+        o, s = oracle.recurrence(q[sl], k[sl], v[sl], al[sl], b[sl], S0=S0[n:n + 1])
+        np.testing.assert_array_equal(o, out[sl])
+        np.testing.assert_array_equal(s[0], Sf[n])
+        if L == 0:
+            np.testing.assert_array_equal(Sf[n], S0[n])
+
+
+def test_stability_bound():
+    rng = np.random.default_rng(33)
+    T, H, dk, dv = 200, 2, 8, 8
+    q, k, v, al, b, S0 = _rand(rng, T, H, dk, dv)
+    k *= rng.uniform(0.1, 1.0, size=(T, H, 1))  # ||k|| <= 1
+    _, Sf = oracle.recurrence(q, k, v, np.ones_like(al), b, S0=S0)
+    for h in range(H):
+        bound = np.linalg.norm(S0[0, h]) + np.sum(b[:, h] * np.linalg.norm(k[:, h], axis=-1)
+                                                   * np.linalg.norm(v[:, h], axis=-1))
+        assert np.linalg.norm(Sf[0, h]) <= bound + 1e-9
+
+
+def test_decode_step_is_one_token_of_the_recurrence():
+    rng = np.random.default_rng(34)
+    N, H, dk, dv, T = 3, 2, 6, 5, 9
+    q, k, v, _, b, _ = _rand(rng, N * (T + 1), H, dk, dv)
+    z = rng.normal(size=(N * (T + 1), H, dk))
+    A = rng.normal(size=H) * 0.5
+    S0 = rng.normal(size=(N, H, dk, dv))
+    cu_full = np.arange(N + 1) * (T + 1)
+    o_full, s_full = oracle.forward(q, k, v, z, A, b, S0=S0, cu_seqlens=cu_full)
+    # prefill T tokens per sequence, then one decode step on the last token of each
+    pre = np.concatenate([np.arange(n * (T + 1), n * (T + 1) + T) for n in range(N)])
+    last = np.array([n * (T + 1) + T for n in range(N)])
+    _, s_pre = oracle.forward(q[pre], k[pre], v[pre], z[pre], A, b[pre], S0=S0, cu_seqlens=np.arange(N + 1) * T)
+    o_dec, s_dec = oracle.decode_step(q[last], k[last], v[last], z[last], A, b[last], s_pre)
+    np.testing.assert_allclose(o_dec, o_full[last], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(s_dec, s_full, rtol=1e-13, atol=1e-13)
