@@ -1,0 +1,433 @@
+"""Benchmark: KDA chunked prefill (B=1, H=16, T=4096, d_k=d_v=128, bf16 inputs, fp32 state) and
+the decode step (256 sequences x 32 heads, d=128, 512 MiB fp32 state), on one GB300 per rank.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line.  `value` is prefill throughput in million tokens per second (tokens of all
+16 heads) with inputs resident in HBM, timed with CUDA events on the launching stream; L2 is
+flushed (a 512 MiB write) before every timed step because the workload's 86 MB fit in L2.
+`decode` reports the decode step's state bandwidth.  `e2e` repeats the prefill through the same
+public call with pinned host buffers, host<->device copies inside the timed region.  `roofline`
+is for the kernel with the largest device time, measured live with per-launch CUDA events.
+`cpu_baseline` times the fp64 oracle on the host cores on a bounded sample of the same workload.
+
+Under torchrun (N > 1) every rank runs its own copy of the workload (weak scaling, no collective
+on the data path); the step time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill Mtok/s & % BF16 tensor peak; decode-step state GB/s & % HBM"
+WORKLOAD = 1        # B=1, H=16, T=4096, d=128 bf16 prefill
+DECODE_WORKLOAD = 4  # 256 x 32 heads decode
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def prefill_bytes_per_token_head(dk, dv, io_bytes):
+    """Minimum HBM bytes per token-head: read q, k, z (d_k each), v (d_v), beta (fp32); write out."""
+    return (3 * dk + dv) * io_bytes + 4 + dv * io_bytes
+
+
+def prefill_flops_per_token_head(dk, dv, C=16):
+    """Dense matmul FLOPs per token-head of the chunk form (W S, Q S, K^T U at d_k x d_v, and the
+    C x C tiles A = K K^T, P = Q K^T, T applied to K and V, P U)."""
+    return 6 * dk * dv + 2 * C * (3 * dk + 2 * dv)
+
+
+def decode_bytes_per_head(dk, dv, io_bytes):
+    return 2 * dk * dv * 4 + (3 * dk + dv) * io_bytes + 4 + dv * io_bytes
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id=None):
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if gpu_id is not None:
+            cmd += ["-i", str(gpu_id)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        with open(self.file.name) as f:
+            rows = [r.split(",") for r in f.read().strip().splitlines() if r.count(",") >= 8]
+        os.unlink(self.file.name)
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def src_sha(kernel):
+    name = {"kda_gate": "kda_gate.cu", "kda_ut_wy": "kda_ut_wy.cu", "kda_chunk_fwd": "kda_chunk_fwd.cu",
+            "kda_decode_step": "kda_decode.cu"}.get(kernel)
+    if name is None:
+        return None
+    p = os.path.join(ROOT, "linear_attention_recurrence_kda_gb300", "csrc", name)
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16] if os.path.exists(p) else None
+
+
+def ncu_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f).get(kernel)
+    if not d or d.get("source_sha") != src_sha(kernel):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+
+def oracle_rate(inp, target_s=10.0, threads=0):
+    """fp64 oracle throughput on a bounded prefix sample of the workload: heads [0, h) over the
+    first t tokens, sized from a short calibration run to take about `target_s` seconds."""
+    import numpy as np  # noqa: F401
+    import oracle
+    T = inp["q"].shape[0]
+    H = inp["q"].shape[1]
+
+    def run(h, t):
+        sl = lambda x: x[:t, :h]
+        t0 = time.perf_counter()
+        oracle.forward(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["z"]), inp["A"][:h], sl(inp["beta"]),
+                       S0=None if inp["S0"] is None else inp["S0"][:, :h], threads=threads)
+        return time.perf_counter() - t0
+
+    cal_t = min(T, 256)
+    dt = run(1, cal_t)
+    per_th = dt / cal_t
+    budget = max(1, int(target_s / per_th))
+    h = max(1, min(H, budget // T))
+    t = T if budget >= T else max(16, budget)
+    el = run(h, t)
+    th_per_s = h * t / el
+    return {"token_heads_per_s": th_per_s, "tok_per_s": th_per_s / H, "heads": h, "tokens": t, "seconds": el}
+
+
+def reference_arm(args):
+    """The fp64 oracle as the reference implementation, on the host cores, same metric/config."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import torch
+    from linear_attention_recurrence_kda_gb300 import inputs as I
+    import oracle
+    oracle.build()
+    inp = I.make_inputs(WORKLOAD)
+    H = inp["q"].shape[1]
+    T = inp["q"].shape[0]
+    cores = oracle.max_threads()
+    # per step: a prefix of head 0 sized to ~0.25 s so that warm-up + steps stay within minutes
+    cal = oracle_rate(inp, target_s=0.25)
+    h, t = cal["heads"], cal["tokens"]
+    sl = lambda x: x[:t, :h]
+
+    def step():
+        oracle.forward(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["z"]), inp["A"][:h], sl(inp["beta"]),
+                       S0=inp["S0"][:, :h])
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    ms = el / args.steps * 1e3
+    mtok = h * t / (el / args.steps) / H / 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": mtok, "unit": "Mtok/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": I.WORKLOADS[WORKLOAD].name, "B": 1, "H": H, "T": T, "d_k": 128, "d_v": 128},
+        "cpu_baseline": {"value": mtok, "unit": "Mtok/s", "cores": cores, "kind": "oracle",
+                         "sample": f"heads [0,{h}) x first {t} tokens of the workload per step (fp64, OpenMP)"},
+        "e2e": {"value": mtok, "unit": "Mtok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--decode-steps", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+    import torch.distributed as dist
+    import __graft_entry__
+    __graft_entry__.build()
+    from linear_attention_recurrence_kda_gb300 import binding as B
+    from linear_attention_recurrence_kda_gb300 import inputs as I
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- CPU oracle baseline first (rank 0 only, before any timed GPU work)
+    cpu = None
+    inp = I.make_inputs(WORKLOAD, seed=I.WORKLOADS[WORKLOAD].seed + rank)
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        r = oracle_rate(inp, target_s=12.0)
+        cpu = {"value": r["tok_per_s"] / 1e6, "unit": "Mtok/s", "cores": oracle.max_threads(), "kind": "oracle",
+               "sample": f"heads [0,{r['heads']}) x first {r['tokens']} tokens of the workload, fp64, "
+                         f"{r['seconds']:.1f} s; scaled to tokens of all {inp['q'].shape[1]} heads"}
+
+    T, H, dk = inp["k"].shape
+    dv = inp["v"].shape[2]
+    io_bytes = inp["k"].element_size()
+    d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in inp.items()}
+    out = torch.empty(T, H, dv, dtype=inp["k"].dtype, device=dev)
+    fin = torch.empty(1, H, dk, dv, dtype=torch.float32, device=dev)
+    prob = B.make_problem(1, T, T, H, dk, dv, inp["k"].dtype)
+    ws = torch.empty(B.kda_forward_workspace_bytes(prob), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def fwd():
+        B.kda_forward(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], initial_state=d["S0"], out=out,
+                      final_state=fin, workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        fwd()
+    torch.cuda.synchronize()
+
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(gpu_id) if rank == 0 else None
+    time.sleep(0.3)
+
+    # ---- timed prefill: K steps, L2 flushed before each, per-step events on the launching stream
+    B.kda_profile_enable(True)
+    barrier()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        fwd()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    prof = B.kda_profile_read()
+    B.kda_profile_enable(False)
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    ms = max_over_ranks(sum(step_ms) / len(step_ms))
+    tokens = T * world
+    value = tokens / (ms * 1e-3) / 1e6
+    launches = sum(n for n, _ in prof.values())
+
+    # roofline of the kernel with the largest device time
+    pk, pk_src = peaks()
+    top = max(prof.items(), key=lambda kv: kv[1][1])
+    top_name, (top_n, top_ms) = top
+    top_avg_ms = top_ms / top_n
+    th = T * H
+    alg_bytes = th * prefill_bytes_per_token_head(dk, dv, io_bytes) + 2 * H * dk * dv * 4
+    achieved = alg_bytes / (top_avg_ms * 1e-3) / 1e9
+    traffic = ncu_traffic(top_name)
+    roofline = {"bound": "hbm", "kernel": top_name, "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "traffic": traffic, "peak_source": pk_src,
+                "algorithmic_bytes_per_launch": alg_bytes, "avg_launch_ms": top_avg_ms,
+                "kernel_times_ms": {k: v[1] / v[0] for k, v in prof.items()}}
+    flops = th * prefill_flops_per_token_head(dk, dv)
+    tensor = {"achieved_tflops": flops / (ms * 1e-3) / 1e12,
+              "frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"],
+              "flops_per_step": flops, "peak_tflops": pk["bf16_tflops"], "peak_source": pk_src}
+
+    # ---- decode step (config: 256 sequences x 32 heads, d = 128)
+    decode = None
+    if not args.no_decode:
+        decode = bench_decode(args, B, I, dev, stream, max_over_ranks, barrier, pk, pk_src)
+
+    # ---- e2e through the public call with pinned host buffers
+    e2e = bench_e2e(args, B, inp, dev, stream, max_over_ranks, barrier, world)
+
+    clk = clocks.stop() if clocks else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "Mtok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": I.WORKLOADS[WORKLOAD].name, "B": 1, "H": H, "T": T, "d_k": dk, "d_v": dv,
+                   "chunk": 16, "io_dtype": "bf16", "state_dtype": "f32",
+                   "l2": "flushed by a 512 MiB write before every timed step"},
+        "roofline": roofline, "tensor": tensor, "decode": decode, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches, "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def bench_decode(args, B, I, dev, stream, max_over_ranks, barrier, pk, pk_src):
+    import torch
+    w = I.WORKLOADS[DECODE_WORKLOAD]
+    N, H, dd = len(w.lengths), w.num_heads, w.d
+    L = w.lengths[0]
+    steps = args.decode_steps
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+
+    def toks(*shape):
+        q = torch.randn(*shape, dd, generator=g, device=dev)
+        k = torch.randn(*shape, dd, generator=g, device=dev)
+        v = torch.randn(*shape, dd, generator=g, device=dev)
+        z = torch.randn(*shape, dd, generator=g, device=dev)
+        n = lambda x: x / torch.sqrt((x * x).sum(-1, keepdim=True) + I.L2_EPS)
+        return [t.to(w.io_dtype).contiguous() for t in (n(q), n(k), v, z)]
+
+    A = (torch.randn(H, generator=g, device=dev) * I.A_STD).float()
+    # the state comes from a 512-token varlen prefill from a random initial state
+    pq, pk_, pv, pz = toks(N * L, H)
+    pb = torch.sigmoid(torch.randn(N * L, H, generator=g, device=dev)).float()
+    s0 = (torch.randn(N, H, dd, dd, generator=g, device=dev) * I.S0_STD).float()
+    cu = (torch.arange(N + 1, device=dev, dtype=torch.int32) * L)
+    _, state = B.kda_forward(pq, pk_, pv, pz, A, pb, initial_state=s0, cu_seqlens=cu, max_seqlen=L)
+    del pq, pk_, pv, pz, pb
+    dq, dk_, dv_, dz = toks(steps, N, H)
+    db = torch.sigmoid(torch.randn(steps, N, H, generator=g, device=dev)).float()
+    outs = torch.empty(steps, N, H, dd, dtype=w.io_dtype, device=dev)
+    for s in range(3):
+        B.kda_decode_step(dq[s], dk_[s], dv_[s], dz[s], A, db[s], state, out=outs[s])
+    torch.cuda.synchronize()
+    B.kda_profile_enable(True)
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(steps):
+        B.kda_decode_step(dq[s], dk_[s], dv_[s], dz[s], A, db[s], state, out=outs[s])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    prof = B.kda_profile_read()
+    B.kda_profile_enable(False)
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps)
+    nbytes = N * H * decode_bytes_per_head(dd, dd, 2)
+    kn, kms = prof.get("kda_decode_step", (steps, ms * steps))
+    kavg = kms / kn
+    gbs = nbytes / (kavg * 1e-3) / 1e9
+    return {"workload": w.name, "ms_per_step": ms, "tokens_per_s": N / (ms * 1e-3),
+            "state_gbs": nbytes / (ms * 1e-3) / 1e9,
+            "roofline": {"bound": "hbm", "kernel": "kda_decode_step", "achieved": gbs, "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": gbs / pk["hbm_gbs"], "frac_of_8tbs": gbs / 8000.0,
+                         "traffic": ncu_traffic("kda_decode_step"), "peak_source": pk_src,
+                         "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": kavg},
+            "gpu_launches": kn}
+
+
+def bench_e2e(args, B, inp, dev, stream, max_over_ranks, barrier, world):
+    import torch
+    keys = ("q", "k", "v", "z", "A", "beta", "S0")
+    host = {k: inp[k].pin_memory() for k in keys}
+    dbuf = {k: torch.empty_like(host[k], device=dev) for k in keys}
+    T, H, dk = inp["k"].shape
+    dv = inp["v"].shape[2]
+    out = torch.empty(T, H, dv, dtype=inp["k"].dtype, device=dev)
+    fin = torch.empty(1, H, dk, dv, dtype=torch.float32, device=dev)
+    h_out = torch.empty_like(out, device="cpu").pin_memory()
+    h_fin = torch.empty_like(fin, device="cpu").pin_memory()
+    prob = B.make_problem(1, T, T, H, dk, dv, inp["k"].dtype)
+    ws = torch.empty(B.kda_forward_workspace_bytes(prob), dtype=torch.uint8, device=dev)
+    h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
+    d2h = h_out.numel() * h_out.element_size() + h_fin.numel() * h_fin.element_size()
+
+    def step():
+        for k in keys:
+            dbuf[k].copy_(host[k], non_blocking=True)
+        B.kda_forward(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["z"], dbuf["A"], dbuf["beta"], initial_state=dbuf["S0"],
+                      out=out, final_state=fin, workspace=ws)
+        h_out.copy_(out, non_blocking=True)
+        h_fin.copy_(fin, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+    return {"value": T * world / (ms * 1e-3) / 1e6, "unit": "Mtok/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

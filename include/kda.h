@@ -1,0 +1,157 @@
+/*
+ * kda.h -- C ABI of libkda.so: Kimi Delta Attention (KDA) prefill and decode on one GB300 GPU.
+ *
+ * The operation (per sequence n and head h; "Kimi K3: the paper and proofs side by side",
+ * section 2.1.1, Equations 1 and 5; "Kimi K3: architecture, derivations and a pinned-source
+ * audit", section 4.3):
+ *
+ *   g_t     = g_min * sigmoid(exp(A_h) * z_t)           per key channel, g_min = -5 in K3
+ *   alpha_t = exp(g_t)                                   retention in (exp(g_min), 1)
+ *   S_t     = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *   o_t     = S_t^T q_t                                  read after the update
+ *
+ * S is d_k x d_v with rows = key channels and columns = value channels.  No 1/sqrt(d_k) scale is
+ * applied to q (the pages write o = S^T q); callers normalise q and k themselves.  o_t is the
+ * recurrence output before any head-wise norm or output gate.
+ *
+ * Conventions for every entry point
+ *   - Layouts are row-major and token-major packed:
+ *       q, k, z     [T_tot, H, d_k]      (io dtype)
+ *       v, out      [T_tot, H, d_v]      (io dtype)
+ *       beta        [T_tot, H]           fp32
+ *       A           [H]                  fp32
+ *       states      [N, H, d_k, d_v]     fp32
+ *       cu_seqlens  [N + 1]              int32, cu_seqlens[0] = 0, non-decreasing, last = T_tot
+ *   - All tensor pointers are DEVICE pointers (device or managed memory of the current device,
+ *     or mapped pinned host memory), 16-byte aligned.  The problem descriptor is a host pointer.
+ *   - The caller owns every buffer.  The library keeps no allocation between calls; forward's
+ *     scratch memory is the caller's `workspace`.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only enqueue work and
+ *     return without synchronising; launch failures are reported as KDA_ERR_CUDA, asynchronous
+ *     faults surface at the caller's next synchronisation.
+ *   - Argument errors are detected on the host before anything is launched, and nothing is
+ *     written in that case.  No C++ exception crosses this boundary.
+ *   - Supported sizes: d_k, d_v in {32, 64, 128}; 1 <= H <= 65535; io dtype fp32 or bf16.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,  /* null/misaligned/host-only pointer, bad descriptor, aliasing   */
+    KDA_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement (e.g. d_k = 96)  */
+    KDA_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed                   */
+    KDA_ERR_TIMEOUT = 4,      /* a bounded device-side wait gave up (reported via the status) */
+    KDA_ERR_WORKSPACE = 5,    /* workspace missing, misaligned or smaller than required        */
+    KDA_ERR_DEVICE_CHECK = 6  /* a device-side input check failed (e.g. bad cu_seqlens)       */
+} kda_status_t;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype_t;
+
+/* Problem descriptor (host memory). */
+typedef struct {
+    int32_t num_seqs;      /* N: number of packed sequences (batch size for equal lengths)      */
+    int64_t total_tokens;  /* T_tot = sum of sequence lengths (= N for a decode step)            */
+    int32_t max_seqlen;    /* host-known upper bound on any sequence length (grid sizing)       */
+    int32_t num_heads;     /* H                                                                  */
+    int32_t d_k;           /* key/query channels: 32, 64 or 128                                  */
+    int32_t d_v;           /* value channels: 32, 64 or 128                                      */
+    kda_dtype_t io_dtype;  /* dtype of q, k, v, z and out; A, beta and states are always fp32   */
+    float g_min;           /* log-decay floor, < 0 (-5 in K3)                                    */
+} kda_problem_t;
+
+/*
+ * Bytes of device workspace kda_forward needs for this problem (0 if the descriptor is invalid).
+ * The requirement depends only on the descriptor's sizes, never on the data.
+ */
+size_t kda_forward_workspace_bytes(const kda_problem_t* problem);
+
+/*
+ * Chunkwise-parallel prefill over packed sequences (Equation 1 for every token, in 16-token
+ * chunks; the chunk form is an exact regrouping of the token recurrence, "Kimi K3:
+ * architecture, derivations and a pinned-source audit", section 4.5, and the bounded gate keeps
+ * a chunk's accumulated log-decay in [16 g_min, 0], "Kimi K3" reading notes, section 2).
+ *
+ *   q, k, z, v, A, beta : inputs as laid out above.
+ *   initial_state : [N,H,d_k,d_v] fp32, or NULL for zero states.
+ *   cu_seqlens    : [N+1] int32 on the device, or NULL for N equal lengths T_tot / N
+ *                   (then T_tot must be a multiple of N).  Chunks restart at every sequence
+ *                   start; a zero-length sequence copies its initial state to its final state.
+ *                   Every length must be <= max_seqlen and the offsets must be non-decreasing
+ *                   and end at T_tot; violations are detected on the device, the offending
+ *                   sequence is skipped, and kda_workspace_status() reports KDA_ERR_DEVICE_CHECK.
+ *   out           : [T_tot,H,d_v] io dtype.  Must not overlap any input.
+ *   final_state   : [N,H,d_k,d_v] fp32, or NULL (not written).  May be the same pointer as
+ *                   initial_state (in-place carry); any other overlap is rejected.
+ *   workspace     : device scratch of at least kda_forward_workspace_bytes(problem) bytes,
+ *                   256-byte aligned, not shared with a concurrently running call.
+ *
+ * Returns KDA_OK once all kernels are enqueued on `stream`.
+ */
+kda_status_t kda_forward(const void* q, const void* k, const void* v, const void* z,
+                         const float* A, const float* beta, const float* initial_state,
+                         const int32_t* cu_seqlens, void* out, float* final_state,
+                         const kda_problem_t* problem, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/*
+ * One recurrent decode step: every one of the N sequences advances by exactly one token
+ * (KDA.step: update the state, then read it with the query; "Kimi K3: the paper and proofs side
+ * by side", section "A recurrent step and its return type").
+ *
+ *   q, k, z : [N,H,d_k] io dtype;  v : [N,H,d_v] io dtype;  beta : [N,H] fp32;  A : [H] fp32.
+ *   state   : [N,H,d_k,d_v] fp32, read and overwritten in place with the new state.
+ *   out     : [N,H,d_v] io dtype; must not overlap any input or the state.
+ *   problem : total_tokens must equal num_seqs (cu_seqlens is not used).
+ */
+kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const void* z,
+                             const float* A, const float* beta, float* state, void* out,
+                             const kda_problem_t* problem, void* stream);
+
+/*
+ * Synchronises `stream` and reads the device-side check word that kda_forward keeps in its
+ * workspace: KDA_OK, or KDA_ERR_DEVICE_CHECK if a sequence was skipped because its cu_seqlens
+ * entries were invalid, or KDA_ERR_TIMEOUT if a bounded device wait gave up.  The word is
+ * cleared by the next kda_forward on that workspace.
+ */
+kda_status_t kda_workspace_status(const void* workspace, size_t workspace_bytes, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* kda_status_string(kda_status_t status);
+
+/*
+ * Per-kernel device timing, for measurement tools.  While enabled, every kernel launched by
+ * kda_forward / kda_decode_step is bracketed by two CUDA events recorded on the call's stream;
+ * kda_profile_read synchronises on those events and returns, per kernel name, the number of
+ * launches and their summed device time.  Enabling (or disabling) discards earlier records.
+ * Events are host-side objects: no device memory is allocated.  Not thread-safe against
+ * concurrent calls on other threads while enabled.
+ */
+typedef struct {
+    char name[32];        /* kernel name, NUL-terminated                    */
+    int64_t launches;     /* launches recorded since the last enable        */
+    double total_ms;      /* summed device time of those launches (ms)      */
+} kda_kernel_time_t;
+
+kda_status_t kda_profile_enable(int enable);
+
+/* Fills up to max_entries records; returns the number of distinct kernels (or -1 on error). */
+int32_t kda_profile_read(kda_kernel_time_t* out, int32_t max_entries);
+
+/* ABI version of this header: (major << 16) | minor. */
+uint32_t kda_abi_version(void);
+
+#define KDA_ABI_VERSION ((1u << 16) | 0u)
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

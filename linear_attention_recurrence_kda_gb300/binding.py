@@ -1,0 +1,222 @@
+"""ctypes binding of libkda.so (the C ABI in include/kda.h), with the same entry-point names.
+
+Argument marshalling only: tensors are checked for device/dtype/shape/contiguity, their data
+pointers and the current CUDA stream are passed to the C ABI, and any non-OK status raises
+``KdaError``.  Every step of the computation runs in the library's CUDA kernels; there is no
+fallback path, and loading fails loudly if the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libkda.so")
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = 1
+KDA_ERR_UNSUPPORTED = 2
+KDA_ERR_CUDA = 3
+KDA_ERR_TIMEOUT = 4
+KDA_ERR_WORKSPACE = 5
+KDA_ERR_DEVICE_CHECK = 6
+
+KDA_F32 = 0
+KDA_BF16 = 1
+
+G_MIN = -5.0
+
+# Every symbol include/kda.h declares.
+EXPORTS = ("kda_forward_workspace_bytes", "kda_forward", "kda_decode_step", "kda_workspace_status",
+           "kda_status_string", "kda_profile_enable", "kda_profile_read", "kda_abi_version")
+
+
+class KdaProblem(ctypes.Structure):
+    """Mirror of kda_problem_t."""
+    _fields_ = [("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int64), ("max_seqlen", ctypes.c_int32),
+                ("num_heads", ctypes.c_int32), ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32),
+                ("io_dtype", ctypes.c_int), ("g_min", ctypes.c_float)]
+
+
+class KdaKernelTime(ctypes.Structure):
+    """Mirror of kda_kernel_time_t."""
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int64), ("total_ms", ctypes.c_double)]
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+_lock = threading.Lock()
+_lib = None
+_vp = ctypes.c_void_p
+
+
+def lib():
+    """The loaded libkda.so with argument types declared (raises if it is not built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libkda.so is not built ({LIB_PATH} missing); run "
+                                   "`python -m linear_attention_recurrence_kda_gb300.build`")
+            L = ctypes.CDLL(LIB_PATH)
+            P = ctypes.POINTER(KdaProblem)
+            L.kda_forward_workspace_bytes.restype = ctypes.c_size_t
+            L.kda_forward_workspace_bytes.argtypes = [P]
+            L.kda_forward.restype = ctypes.c_int
+            L.kda_forward.argtypes = [_vp] * 10 + [P, _vp, ctypes.c_size_t, _vp]
+            L.kda_decode_step.restype = ctypes.c_int
+            L.kda_decode_step.argtypes = [_vp] * 8 + [P, _vp]
+            L.kda_workspace_status.restype = ctypes.c_int
+            L.kda_workspace_status.argtypes = [_vp, ctypes.c_size_t, _vp]
+            L.kda_status_string.restype = ctypes.c_char_p
+            L.kda_status_string.argtypes = [ctypes.c_int]
+            L.kda_profile_enable.restype = ctypes.c_int
+            L.kda_profile_enable.argtypes = [ctypes.c_int]
+            L.kda_profile_read.restype = ctypes.c_int32
+            L.kda_profile_read.argtypes = [ctypes.POINTER(KdaKernelTime), ctypes.c_int32]
+            L.kda_abi_version.restype = ctypes.c_uint32
+            L.kda_abi_version.argtypes = []
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().kda_status_string(int(status)).decode()
+
+
+def make_problem(num_seqs: int, total_tokens: int, max_seqlen: int, num_heads: int, d_k: int, d_v: int,
+                 io_dtype, g_min: float = G_MIN) -> KdaProblem:
+    dt = io_dtype
+    if isinstance(dt, torch.dtype):
+        dt = {torch.float32: KDA_F32, torch.bfloat16: KDA_BF16}[dt]
+    return KdaProblem(int(num_seqs), int(total_tokens), int(max_seqlen), int(num_heads), int(d_k), int(d_v),
+                      int(dt), float(g_min))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype, shape, device):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def kda_forward_workspace_bytes(problem: KdaProblem) -> int:
+    return int(lib().kda_forward_workspace_bytes(ctypes.byref(problem)))
+
+
+def kda_forward(q, k, v, z, A, beta, initial_state=None, cu_seqlens=None, out=None, final_state=None,
+                max_seqlen: Optional[int] = None, workspace=None, g_min: float = G_MIN, stream=None,
+                want_final: bool = True):
+    """Chunkwise KDA prefill (see include/kda.h).  Shapes: q, k, z [T, H, d_k]; v [T, H, d_v];
+    A [H] fp32; beta [T, H] fp32; initial_state [N, H, d_k, d_v] fp32 or None; cu_seqlens [N+1]
+    int32 on the device or None (one sequence, or N = initial_state.shape[0] equal lengths).
+
+    ``max_seqlen`` must bound every sequence length when cu_seqlens is given (it is only used for
+    grid sizing; pass it to avoid a device->host read of cu_seqlens).  Returns (out, final_state).
+    """
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    dev = k.device
+    dt = k.dtype
+    if cu_seqlens is not None:
+        N = cu_seqlens.shape[0] - 1
+        _need(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,), dev)
+        if max_seqlen is None:
+            max_seqlen = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if N > 0 else 0
+    else:
+        N = initial_state.shape[0] if initial_state is not None else 1
+        max_seqlen = T // N
+    for name, t, shp in (("q", q, (T, H, dk)), ("k", k, (T, H, dk)), ("z", z, (T, H, dk)), ("v", v, (T, H, dv))):
+        _need(t, name, dt, shp, dev)
+    _need(A, "A", torch.float32, (H,), dev)
+    _need(beta, "beta", torch.float32, (T, H), dev)
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32, (N, H, dk, dv), dev)
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=dt, device=dev)
+    _need(out, "out", dt, (T, H, dv), dev)
+    if final_state is None and want_final:
+        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    if final_state is not None:
+        _need(final_state, "final_state", torch.float32, (N, H, dk, dv), dev)
+    prob = make_problem(N, T, max_seqlen, H, dk, dv, dt, g_min)
+    wsb = kda_forward_workspace_bytes(prob)
+    if wsb == 0:
+        raise KdaError(KDA_ERR_INVALID_ARG, "kda_forward_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    st = lib().kda_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(beta), _ptr(initial_state),
+                           _ptr(cu_seqlens), _ptr(out), _ptr(final_state), ctypes.byref(prob), _ptr(workspace),
+                           ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_forward")
+    return out, final_state
+
+
+def kda_decode_step(q, k, v, z, A, beta, state, out=None, g_min: float = G_MIN, stream=None):
+    """One decode token per sequence: q, k, z [N, H, d_k]; v [N, H, d_v]; beta [N, H] fp32;
+    state [N, H, d_k, d_v] fp32 (updated in place).  Returns out [N, H, d_v]."""
+    N, H, dk = k.shape
+    dv = v.shape[2]
+    dev = k.device
+    dt = k.dtype
+    for name, t, shp in (("q", q, (N, H, dk)), ("k", k, (N, H, dk)), ("z", z, (N, H, dk)), ("v", v, (N, H, dv))):
+        _need(t, name, dt, shp, dev)
+    _need(A, "A", torch.float32, (H,), dev)
+    _need(beta, "beta", torch.float32, (N, H), dev)
+    _need(state, "state", torch.float32, (N, H, dk, dv), dev)
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=dt, device=dev)
+    _need(out, "out", dt, (N, H, dv), dev)
+    prob = make_problem(N, N, 1, H, dk, dv, dt, g_min)
+    st = lib().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(beta), _ptr(state), _ptr(out),
+                               ctypes.byref(prob), _stream(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_decode_step")
+    return out
+
+
+def kda_workspace_status(workspace, stream=None) -> int:
+    """Synchronise and return the device-side check status of a forward workspace."""
+    return int(lib().kda_workspace_status(_ptr(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream)))
+
+
+def kda_abi_version() -> int:
+    return int(lib().kda_abi_version())
+
+
+def kda_profile_enable(enable: bool = True) -> None:
+    """Start (or stop) recording per-kernel device time for launches made through the C ABI."""
+    lib().kda_profile_enable(1 if enable else 0)
+
+
+def kda_profile_read() -> dict:
+    """{kernel name: (launches, total device ms)} since the last kda_profile_enable."""
+    buf = (KdaKernelTime * 64)()
+    n = lib().kda_profile_read(buf, 64)
+    if n < 0:
+        raise KdaError(KDA_ERR_CUDA, "kda_profile_read")
+    return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms)) for i in range(min(n, 64))}

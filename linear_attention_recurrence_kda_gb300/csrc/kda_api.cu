@@ -1,0 +1,249 @@
+// kda_api.cu -- the C ABI of libkda.so (declared in include/kda.h): argument checks and launches.
+//
+// Every check that can be made without the data runs on the host before anything is enqueued,
+// in this order: descriptor, required pointers, alignment, overlap, workspace, and finally the
+// CUDA pointer attributes (device-accessible memory of the current device).  The first four need
+// no GPU.  Nothing here synchronises except kda_workspace_status.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "kda_internal.cuh"
+
+using kda::ForwardLayout;
+
+namespace {
+
+bool supported_dim(int32_t d) { return d == 32 || d == 64 || d == 128; }
+
+size_t io_size(kda_dtype_t dt) { return dt == KDA_BF16 ? 2 : 4; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+Range range_of(const void* p, size_t bytes)
+{
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Range{lo, lo + bytes};
+}
+
+bool overlaps(Range a, Range b)
+{
+    if (a.lo == a.hi || b.lo == b.hi || a.lo == 0 || b.lo == 0) return false;
+    return a.lo < b.hi && b.lo < a.hi;
+}
+
+kda_status_t check_descriptor(const kda_problem_t* p, bool decode)
+{
+    if (p == nullptr) return KDA_ERR_INVALID_ARG;
+    if (p->num_seqs < 1 || p->total_tokens < 0 || p->num_heads < 1 || p->num_heads > 65535) return KDA_ERR_INVALID_ARG;
+    if (p->d_k <= 0 || p->d_v <= 0) return KDA_ERR_INVALID_ARG;
+    if (p->io_dtype != KDA_F32 && p->io_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
+    if (!(p->g_min < 0.f) || !std::isfinite(p->g_min)) return KDA_ERR_INVALID_ARG;
+    if (!supported_dim(p->d_k) || !supported_dim(p->d_v)) return KDA_ERR_UNSUPPORTED;
+    // element counts must stay far from overflow: T_tot * H * d <= 2^40
+    const double elems = (double)p->total_tokens * p->num_heads * (p->d_k > p->d_v ? p->d_k : p->d_v);
+    if (elems > 1099511627776.0) return KDA_ERR_UNSUPPORTED;
+    if ((double)p->num_seqs * p->num_heads * p->d_k * p->d_v > 1099511627776.0) return KDA_ERR_UNSUPPORTED;
+    if (decode) {
+        if (p->total_tokens != p->num_seqs) return KDA_ERR_INVALID_ARG;
+    } else {
+        if (p->max_seqlen < 0) return KDA_ERR_INVALID_ARG;
+    }
+    return KDA_OK;
+}
+
+// Device-accessible memory of the current device (or mapped pinned host memory).
+kda_status_t check_device_pointer(const void* p)
+{
+    if (p == nullptr) return KDA_OK;
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, p);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return e == cudaErrorInvalidValue ? KDA_ERR_INVALID_ARG : KDA_ERR_CUDA;
+    }
+    if (attr.devicePointer == nullptr) return KDA_ERR_INVALID_ARG;
+    if (attr.type == cudaMemoryTypeDevice) {
+        int dev = -1;
+        if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+        if (attr.device != dev) return KDA_ERR_INVALID_ARG;
+    }
+    return KDA_OK;
+}
+
+int32_t chunks_per_seq(const kda_problem_t& p, bool equal_lengths)
+{
+    int64_t L = equal_lengths ? p.total_tokens / p.num_seqs : p.max_seqlen;
+    if (L > p.total_tokens) L = p.total_tokens;
+    return (int32_t)((L + kda::kChunk - 1) / kda::kChunk);
+}
+
+}  // namespace
+
+extern "C" {
+
+uint32_t kda_abi_version(void) { return KDA_ABI_VERSION; }
+
+const char* kda_status_string(kda_status_t s)
+{
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: unsupported size or type";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA runtime error";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded device wait gave up";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+        case KDA_ERR_DEVICE_CHECK: return "KDA_ERR_DEVICE_CHECK: device-side input check failed";
+    }
+    return "KDA: unknown status";
+}
+
+size_t kda_forward_workspace_bytes(const kda_problem_t* problem)
+{
+    if (check_descriptor(problem, false) != KDA_OK) return 0;
+    return kda::forward_layout(*problem).total;
+}
+
+kda_status_t kda_forward(const void* q, const void* k, const void* v, const void* z, const float* A,
+                         const float* beta, const float* initial_state, const int32_t* cu_seqlens,
+                         void* out, float* final_state, const kda_problem_t* problem, void* workspace,
+                         size_t workspace_bytes, void* stream)
+{
+    kda_status_t st = check_descriptor(problem, false);
+    if (st != KDA_OK) return st;
+    const kda_problem_t& p = *problem;
+    const bool equal = cu_seqlens == nullptr;
+    if (equal && (p.total_tokens % p.num_seqs) != 0) return KDA_ERR_INVALID_ARG;
+    const int64_t cps = chunks_per_seq(p, equal);
+    if ((int64_t)p.num_seqs * (cps > 0 ? cps : 1) > 2147483647LL) return KDA_ERR_UNSUPPORTED;
+
+    const bool has_tokens = p.total_tokens > 0;
+    if (A == nullptr) return KDA_ERR_INVALID_ARG;
+    if (has_tokens && (!q || !k || !v || !z || !beta || !out)) return KDA_ERR_INVALID_ARG;
+
+    const size_t io = io_size(p.io_dtype);
+    const size_t tk = (size_t)p.total_tokens * p.num_heads * p.d_k;
+    const size_t tv = (size_t)p.total_tokens * p.num_heads * p.d_v;
+    const size_t sb = (size_t)p.num_seqs * p.num_heads * p.d_k * p.d_v * sizeof(float);
+    for (const void* ptr : {q, k, v, z, (const void*)out, (const void*)initial_state, (const void*)final_state}) {
+        if (!aligned(ptr, 16)) return KDA_ERR_INVALID_ARG;
+    }
+    if (!aligned(A, 4) || !aligned(beta, 4) || !aligned(cu_seqlens, 4)) return KDA_ERR_INVALID_ARG;
+
+    const Range rq = range_of(q, tk * io), rk = range_of(k, tk * io), rz = range_of(z, tk * io);
+    const Range rv = range_of(v, tv * io), ro = range_of(out, tv * io);
+    const Range ra = range_of(A, p.num_heads * sizeof(float));
+    const Range rb = range_of(beta, (size_t)p.total_tokens * p.num_heads * sizeof(float));
+    const Range ri = range_of(initial_state, sb), rf = range_of(final_state, sb);
+    const Range rc = range_of(cu_seqlens, cu_seqlens ? (size_t)(p.num_seqs + 1) * sizeof(int32_t) : 0);
+    for (Range r : {rq, rk, rz, rv, ra, rb, ri, rf, rc}) {
+        if (overlaps(ro, r)) return KDA_ERR_INVALID_ARG;
+    }
+    for (Range r : {rq, rk, rz, rv, ra, rb, rc}) {
+        if (overlaps(rf, r)) return KDA_ERR_INVALID_ARG;
+    }
+    if (overlaps(rf, ri) && final_state != initial_state) return KDA_ERR_INVALID_ARG;
+
+    const ForwardLayout L = kda::forward_layout(p);
+    if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < L.total) return KDA_ERR_WORKSPACE;
+    const Range rw = range_of(workspace, L.total);
+    for (Range r : {rq, rk, rz, rv, ra, rb, ri, rf, rc, ro}) {
+        if (overlaps(rw, r)) return KDA_ERR_INVALID_ARG;
+    }
+
+    for (const void* ptr : {q, k, v, z, (const void*)A, (const void*)beta, (const void*)initial_state,
+                            (const void*)cu_seqlens, (const void*)out, (const void*)final_state,
+                            (const void*)workspace}) {
+        st = check_device_pointer(ptr);
+        if (st != KDA_OK) return st;
+    }
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    kda::PrefillArgs a{};
+    a.q = q; a.k = k; a.v = v; a.z = z; a.A = A; a.beta = beta;
+    a.s0 = initial_state; a.cu = cu_seqlens; a.out = out; a.s_final = final_state;
+    a.check = reinterpret_cast<uint32_t*>(ws + L.status_off);
+    a.G = reinterpret_cast<float*>(ws + L.g_off);
+    a.W = reinterpret_cast<float*>(ws + L.w_off);
+    a.Ut = reinterpret_cast<float*>(ws + L.ut_off);
+    a.T_tot = p.total_tokens; a.N = p.num_seqs; a.H = p.num_heads; a.dk = p.d_k; a.dv = p.d_v;
+    a.max_seqlen = equal ? (int32_t)(p.total_tokens / p.num_seqs) : p.max_seqlen;
+    a.chunks_per_seq = (int32_t)cps;
+    a.g_min = p.g_min;
+
+    if (cudaMemsetAsync(a.check, 0, sizeof(uint32_t), s) != cudaSuccess) return KDA_ERR_CUDA;
+    cudaError_t e = cudaSuccess;
+    if (cps > 0) {
+        kda::prof_start("kda_gate", s);
+        e = kda::launch_gate(a, p.io_dtype, s);
+        kda::prof_stop(s);
+        if (e != cudaSuccess) return KDA_ERR_CUDA;
+        kda::prof_start("kda_ut_wy", s);
+        e = kda::launch_ut_wy(a, p.io_dtype, s);
+        kda::prof_stop(s);
+        if (e != cudaSuccess) return KDA_ERR_CUDA;
+    }
+    kda::prof_start("kda_chunk_fwd", s);
+    e = kda::launch_chunk_fwd(a, p.io_dtype, s);
+    kda::prof_stop(s);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const void* z, const float* A,
+                             const float* beta, float* state, void* out, const kda_problem_t* problem,
+                             void* stream)
+{
+    kda_status_t st = check_descriptor(problem, true);
+    if (st != KDA_OK) return st;
+    const kda_problem_t& p = *problem;
+    if (!q || !k || !v || !z || !A || !beta || !state || !out) return KDA_ERR_INVALID_ARG;
+    for (const void* ptr : {q, k, v, z, (const void*)state, (const void*)out}) {
+        if (!aligned(ptr, 16)) return KDA_ERR_INVALID_ARG;
+    }
+    if (!aligned(A, 4) || !aligned(beta, 4)) return KDA_ERR_INVALID_ARG;
+    if ((int64_t)p.num_seqs * p.num_heads > 2147483647LL) return KDA_ERR_UNSUPPORTED;
+    const size_t io = io_size(p.io_dtype);
+    const size_t nh = (size_t)p.num_seqs * p.num_heads;
+    const Range rq = range_of(q, nh * p.d_k * io), rk = range_of(k, nh * p.d_k * io);
+    const Range rz = range_of(z, nh * p.d_k * io), rv = range_of(v, nh * p.d_v * io);
+    const Range ra = range_of(A, p.num_heads * sizeof(float)), rb = range_of(beta, nh * sizeof(float));
+    const Range rs = range_of(state, nh * p.d_k * p.d_v * sizeof(float));
+    const Range ro = range_of(out, nh * p.d_v * io);
+    for (Range r : {rq, rk, rz, rv, ra, rb, rs}) {
+        if (overlaps(ro, r)) return KDA_ERR_INVALID_ARG;
+    }
+    for (Range r : {rq, rk, rz, rv, ra, rb}) {
+        if (overlaps(rs, r)) return KDA_ERR_INVALID_ARG;
+    }
+    for (const void* ptr : {q, k, v, z, (const void*)A, (const void*)beta, (const void*)state, (const void*)out}) {
+        st = check_device_pointer(ptr);
+        if (st != KDA_OK) return st;
+    }
+    kda::DecodeArgs a{};
+    a.q = q; a.k = k; a.v = v; a.z = z; a.A = A; a.beta = beta; a.state = state; a.out = out;
+    a.N = p.num_seqs; a.H = p.num_heads; a.g_min = p.g_min;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    kda::prof_start("kda_decode_step", s);
+    const cudaError_t e = kda::launch_decode(a, p.d_k, p.d_v, p.io_dtype, s);
+    kda::prof_stop(s);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_workspace_status(const void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < 256) return KDA_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return KDA_ERR_CUDA;
+    if (word & kda::kCheckTimeout) return KDA_ERR_TIMEOUT;
+    if (word & kda::kCheckBadSeqlens) return KDA_ERR_DEVICE_CHECK;
+    return KDA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,123 @@
+// kda_internal.cuh -- declarations shared by the libkda.so translation units (not installed).
+//
+// Workspace layout of kda_forward (every region 256-byte aligned, offsets from the base):
+//   [0, 256)   device check word (uint32) written by the kernels, read by kda_workspace_status
+//   G          fp32 [T_tot, H, d_k]   in-chunk inclusive cumulative log-decay (kda_gate)
+//   W          fp32 [T_tot, H, d_k]   WY-transformed keys T diag(beta) (K*Gamma)   (kda_ut_wy)
+//   Ut         fp32 [T_tot, H, d_v]   UT-transformed values T diag(beta) V         (kda_ut_wy)
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+constexpr int kChunk = 16;  // tokens per chunk: a chunk's log-decay stays in [16 g_min, 0]
+
+// Device check word bits.
+constexpr uint32_t kCheckBadSeqlens = 1u;
+constexpr uint32_t kCheckTimeout = 2u;
+
+struct ForwardLayout {
+    size_t status_off, g_off, w_off, ut_off, total;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline ForwardLayout forward_layout(const kda_problem_t& p)
+{
+    ForwardLayout L{};
+    const size_t th = (size_t)p.total_tokens * (size_t)p.num_heads;
+    L.status_off = 0;
+    L.g_off = 256;
+    L.w_off = align_up(L.g_off + th * p.d_k * sizeof(float), 256);
+    L.ut_off = align_up(L.w_off + th * p.d_k * sizeof(float), 256);
+    L.total = align_up(L.ut_off + th * p.d_v * sizeof(float), 256);
+    return L;
+}
+
+// Arguments common to the prefill kernels.
+struct PrefillArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* z;
+    const float* A;
+    const float* beta;
+    const float* s0;          // may be null
+    const int32_t* cu;        // may be null (equal lengths)
+    void* out;
+    float* s_final;           // may be null
+    float* G;                 // workspace
+    float* W;                 // workspace
+    float* Ut;                // workspace
+    uint32_t* check;          // workspace
+    int64_t T_tot;
+    int32_t N, H, dk, dv, max_seqlen, chunks_per_seq;
+    float g_min;
+};
+
+struct DecodeArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* z;
+    const float* A;
+    const float* beta;
+    float* state;
+    void* out;
+    int32_t N, H;
+    float g_min;
+};
+
+// Launchers (each returns the cudaError_t of its launch).
+cudaError_t launch_gate(const PrefillArgs& a, kda_dtype_t dt, cudaStream_t s);
+cudaError_t launch_ut_wy(const PrefillArgs& a, kda_dtype_t dt, cudaStream_t s);
+cudaError_t launch_chunk_fwd(const PrefillArgs& a, kda_dtype_t dt, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
+
+// Optional per-kernel timing around launches (no-ops unless kda_profile_enable(1)).
+void prof_start(const char* name, cudaStream_t s);
+void prof_stop(cudaStream_t s);
+
+// ---------------------------------------------------------------- device helpers
+
+__device__ __forceinline__ float ld_io(const float* p, int64_t i) { return p[i]; }
+__device__ __forceinline__ float ld_io(const __nv_bfloat16* p, int64_t i) { return __bfloat162float(p[i]); }
+__device__ __forceinline__ void st_io(float* p, int64_t i, float x) { p[i] = x; }
+__device__ __forceinline__ void st_io(__nv_bfloat16* p, int64_t i, float x) { p[i] = __float2bfloat16_rn(x); }
+
+// Token range [t0, t1) of sequence n.  Returns false (and raises the check bit) when the offsets
+// are inconsistent with the descriptor, in which case the sequence is skipped.
+__device__ __forceinline__ bool seq_range(const PrefillArgs& a, int n, int64_t& t0, int64_t& t1)
+{
+    if (a.cu == nullptr) {
+        const int64_t L = a.T_tot / a.N;
+        t0 = (int64_t)n * L;
+        t1 = t0 + L;
+        return true;
+    }
+    t0 = a.cu[n];
+    t1 = a.cu[n + 1];
+    const bool ok = (t0 >= 0) && (t1 >= t0) && (t1 <= a.T_tot) && (t1 - t0 <= (int64_t)a.max_seqlen) &&
+                    (n != 0 || t0 == 0) && (n != a.N - 1 || t1 == a.T_tot);
+    if (!ok) {
+        atomicOr(a.check, kCheckBadSeqlens);
+    }
+    return ok;
+}
+
+// Equation 5: log-decay for logit z with per-head scale e^{A_h}.  Uses the CUDA math library.
+__device__ __forceinline__ float log_decay(float z, float expA, float g_min)
+{
+    const float x = expA * z;
+    // logistic in the overflow-free form for both signs
+    const float e = expf(-fabsf(x));
+    const float sig = (x >= 0.f) ? 1.f / (1.f + e) : e / (1.f + e);
+    return g_min * sig;
+}
+
+}  // namespace kda

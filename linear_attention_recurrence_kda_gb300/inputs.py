@@ -69,16 +69,18 @@ def draw_tokens(gen: torch.Generator, shape_k, shape_v, io_dtype):
 
 
 def make_inputs(wl: int | Workload, lengths=None, num_heads=None, d=None, io_dtype=None, seed=None,
-                random_s0=None):
+                random_s0=None, d_k=None, d_v=None):
     """Inputs for a workload (or an override of its shape).  Returns a dict of CPU tensors:
 
-    q, k, z [T, H, d]; v [T, H, d]; A [H] fp32; beta [T, H] fp32; S0 [N, H, d, d] fp32 or None;
-    cu_seqlens [N+1] int32; lengths (list); and, for decode workloads, ``dec`` with per-step
-    q, k, v, z [steps, N, H, d] and beta [steps, N, H].
+    q, k, z [T, H, d_k]; v [T, H, d_v]; A [H] fp32; beta [T, H] fp32; S0 [N, H, d_k, d_v] fp32 or
+    None; cu_seqlens [N+1] int32; lengths (list); and, for decode workloads, ``dec`` with per-step
+    q, k, z [steps, N, H, d_k], v [steps, N, H, d_v] and beta [steps, N, H].
+    ``d`` overrides both d_k and d_v; ``d_k`` / ``d_v`` override one.
     """
     w = WORKLOADS[wl] if isinstance(wl, int) else wl
     H = num_heads or w.num_heads
-    dd = d or w.d
+    dk = d_k or d or w.d
+    dv = d_v or d or w.d
     dt = io_dtype or w.io_dtype
     sd = w.seed if seed is None else seed
     rs0 = w.random_s0 if random_s0 is None else random_s0
@@ -92,17 +94,17 @@ def make_inputs(wl: int | Workload, lengths=None, num_heads=None, d=None, io_dty
     lengths = [int(x) for x in lengths]
     N = len(lengths)
     T = sum(lengths)
-    q, k, v, z = draw_tokens(gen, (T, H, dd), (T, H, dd), dt)
+    q, k, v, z = draw_tokens(gen, (T, H, dk), (T, H, dv), dt)
     A = (torch.randn(H, generator=gen) * A_STD).float()
     beta = torch.sigmoid(torch.randn(T, H, generator=gen)).float().contiguous()
-    S0 = (torch.randn(N, H, dd, dd, generator=gen) * S0_STD).float().contiguous() if rs0 else None
+    S0 = (torch.randn(N, H, dk, dv, generator=gen) * S0_STD).float().contiguous() if rs0 else None
     cu = torch.zeros(N + 1, dtype=torch.int32)
     cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
     out = dict(q=q, k=k, v=v, z=z, A=A, beta=beta, S0=S0, cu_seqlens=cu, lengths=lengths,
-               num_heads=H, d=dd, io_dtype=dt)
+               num_heads=H, d_k=dk, d_v=dv, io_dtype=dt)
     if w.decode_steps:
         s = w.decode_steps
-        dq, dk_, dv_, dz = draw_tokens(gen, (s, N, H, dd), (s, N, H, dd), dt)
+        dq, dk_, dv_, dz = draw_tokens(gen, (s, N, H, dk), (s, N, H, dv), dt)
         db = torch.sigmoid(torch.randn(s, N, H, generator=gen)).float().contiguous()
         out["dec"] = dict(q=dq, k=dk_, v=dv_, z=dz, beta=db, steps=s)
     return out

@@ -115,6 +115,18 @@ def gate(z, A, g_min: float = -5.0):
     return g, al
 
 
+def _auto_col_block(col_block: int, units: int, dv: int, threads: int) -> int:
+    """Value columns per parallel unit: all of them unless there are fewer (sequence, head) units
+    than threads, in which case columns are split (they evolve independently)."""
+    if col_block > 0:
+        return col_block
+    nt = threads if threads > 0 else max_threads()
+    if units >= nt:
+        return dv
+    blocks = min(dv, -(-nt // max(units, 1)))
+    return max(1, -(-dv // blocks))
+
+
 def _check(rc: int):
     if rc == -1:
         raise ValueError("oracle: invalid arguments")
@@ -136,6 +148,7 @@ def recurrence(q, k, v, alpha, beta, S0=None, cu_seqlens=None, col_block: int = 
     N = cu.shape[0] - 1
     out = np.zeros((T, H, dv), dtype=np.float64) if want_out else None
     Sf = np.zeros((N, H, dk, dv), dtype=np.float64)
+    col_block = _auto_col_block(col_block, N * H, dv, threads)
     rc = _load().kda_oracle_recurrence(N, cu.ctypes.data_as(_i64p), H, dk, dv, _ptr(q), _ptr(k),
                                        _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0), _ptr(out),
                                        _ptr(Sf), int(col_block), int(threads))
@@ -156,6 +169,7 @@ def forward(q, k, v, z, A, beta, S0=None, cu_seqlens=None, g_min: float = -5.0, 
     N = cu.shape[0] - 1
     out = np.zeros((T, H, dv), dtype=np.float64) if want_out else None
     Sf = np.zeros((N, H, dk, dv), dtype=np.float64)
+    col_block = _auto_col_block(col_block, N * H, dv, threads)
     rc = _load().kda_oracle_forward(N, cu.ctypes.data_as(_i64p), H, dk, dv, _ptr(q), _ptr(k), _ptr(v),
                                     _ptr(z), _ptr(A), float(g_min), _ptr(beta), _ptr(S0), _ptr(out),
                                     _ptr(Sf), int(col_block), int(threads))

@@ -1,0 +1,150 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol include/kda.h declares,
+and rejects bad descriptors, pointers, aliasing and workspaces on the host before any launch.
+
+Every kda_forward / kda_decode_step call below is built to fail in a host-only check (the fake
+addresses are never dereferenced and nothing is launched)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from conftest import ROOT
+from linear_attention_recurrence_kda_gb300 import binding as B
+
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(B.LIB_PATH):
+        from linear_attention_recurrence_kda_gb300 import build
+        build.build()
+    return B.lib()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_exports():
+    assert set(_declared_functions()) == set(B.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True, text=True, check=True).stdout
+    syms = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in _declared_functions():
+        assert name in syms, name
+        assert hasattr(L, name)
+
+
+def test_abi_version_and_status_strings(L):
+    assert B.kda_abi_version() == (1 << 16)
+    for code in range(7):
+        s = B.status_string(code)
+        assert s.startswith("KDA_")
+    assert "unknown" in B.status_string(99)
+
+
+def _prob(**kw):
+    base = dict(num_seqs=1, total_tokens=64, max_seqlen=64, num_heads=2, d_k=32, d_v=32, io_dtype=B.KDA_F32, g_min=-5.0)
+    base.update(kw)
+    return B.make_problem(**base)
+
+
+def test_workspace_bytes(L):
+    p = _prob()
+    n = B.kda_forward_workspace_bytes(p)
+    # check word + G, W (d_k) and U~ (d_v) in fp32 for every token-head
+    assert n >= 256 + 64 * 2 * (32 + 32 + 32) * 4
+    assert n % 256 == 0
+    big = _prob(total_tokens=1 << 20, max_seqlen=1 << 20, num_heads=8, d_k=128, d_v=128, io_dtype=B.KDA_BF16)
+    assert B.kda_forward_workspace_bytes(big) > B.kda_forward_workspace_bytes(p)
+    for bad in (_prob(d_k=96), _prob(num_heads=0), _prob(g_min=0.0), _prob(g_min=float("nan")),
+                _prob(io_dtype=7), _prob(total_tokens=-1), _prob(num_seqs=0)):
+        assert B.kda_forward_workspace_bytes(bad) == 0
+
+
+# fake, 256-byte aligned, non-overlapping addresses; never dereferenced
+_BASE = 0x7000_0000_0000
+
+
+def _addr(i, size=1 << 24):
+    return _BASE + i * size
+
+
+def _fwd(L, prob, **over):
+    names = ["q", "k", "v", "z", "A", "beta", "s0", "cu", "out", "sf"]
+    ptr = {n: _addr(i) for i, n in enumerate(names)}
+    ptr["s0"] = None
+    ptr["cu"] = None
+    ptr["sf"] = None
+    ws = over.pop("ws", _addr(20))
+    wsb = over.pop("wsb", 1 << 30)
+    ptr.update(over)
+    args = [ctypes.c_void_p(ptr[n]) if ptr[n] is not None else None for n in names]
+    return L.kda_forward(*args, ctypes.byref(prob), ctypes.c_void_p(ws) if ws else None, ctypes.c_size_t(wsb), None)
+
+
+def test_forward_rejects_bad_descriptors(L):
+    assert L.kda_forward(None, None, None, None, None, None, None, None, None, None, None, None, 0, None) == B.KDA_ERR_INVALID_ARG
+    assert _fwd(L, _prob(d_k=48)) == B.KDA_ERR_UNSUPPORTED
+    assert _fwd(L, _prob(d_v=256)) == B.KDA_ERR_UNSUPPORTED
+    assert _fwd(L, _prob(g_min=1.0)) == B.KDA_ERR_INVALID_ARG
+    assert _fwd(L, _prob(num_heads=70000)) == B.KDA_ERR_INVALID_ARG
+    assert _fwd(L, _prob(max_seqlen=-1)) == B.KDA_ERR_INVALID_ARG
+    # equal lengths need T_tot divisible by N
+    assert _fwd(L, _prob(num_seqs=3, total_tokens=64)) == B.KDA_ERR_INVALID_ARG
+
+
+def test_forward_rejects_missing_and_misaligned_pointers(L):
+    p = _prob()
+    for name in ("q", "k", "v", "z", "A", "beta", "out"):
+        assert _fwd(L, p, **{name: None}) == B.KDA_ERR_INVALID_ARG, name
+    for name in ("q", "k", "v", "z", "out"):
+        assert _fwd(L, p, **{name: _addr(3) + 8}) == B.KDA_ERR_INVALID_ARG, name
+    assert _fwd(L, p, s0=_addr(11) + 4) == B.KDA_ERR_INVALID_ARG
+    assert _fwd(L, p, A=_addr(4) + 2) == B.KDA_ERR_INVALID_ARG
+
+
+def test_forward_rejects_overlap(L):
+    p = _prob()
+    assert _fwd(L, p, out=_addr(0)) == B.KDA_ERR_INVALID_ARG            # out == q
+    assert _fwd(L, p, out=_addr(3) + 256) == B.KDA_ERR_INVALID_ARG      # out inside z
+    assert _fwd(L, p, sf=_addr(1)) == B.KDA_ERR_INVALID_ARG             # final state on k
+    assert _fwd(L, p, s0=_addr(11), sf=_addr(11) + 256) == B.KDA_ERR_INVALID_ARG  # partial overlap
+    assert _fwd(L, p, ws=_addr(5)) == B.KDA_ERR_INVALID_ARG             # workspace on beta
+
+
+def test_forward_rejects_bad_workspace(L):
+    p = _prob()
+    need = B.kda_forward_workspace_bytes(p)
+    assert _fwd(L, p, ws=0) == B.KDA_ERR_WORKSPACE
+    assert _fwd(L, p, ws=_addr(20) + 16) == B.KDA_ERR_WORKSPACE
+    assert _fwd(L, p, wsb=need - 1) == B.KDA_ERR_WORKSPACE
+
+
+def test_decode_rejects_bad_arguments(L):
+    def dec(prob, **over):
+        names = ["q", "k", "v", "z", "A", "beta", "state", "out"]
+        ptr = {n: _addr(i) for i, n in enumerate(names)}
+        ptr.update(over)
+        args = [ctypes.c_void_p(ptr[n]) if ptr[n] is not None else None for n in names]
+        return L.kda_decode_step(*args, ctypes.byref(prob), None)
+
+    p = _prob(num_seqs=4, total_tokens=4, max_seqlen=1)
+    assert dec(_prob(num_seqs=4, total_tokens=5)) == B.KDA_ERR_INVALID_ARG
+    assert dec(_prob(num_seqs=4, total_tokens=4, d_k=16)) == B.KDA_ERR_UNSUPPORTED
+    for name in ("q", "k", "v", "z", "A", "beta", "state", "out"):
+        assert dec(p, **{name: None}) == B.KDA_ERR_INVALID_ARG, name
+    assert dec(p, state=_addr(6) + 4) == B.KDA_ERR_INVALID_ARG
+    assert dec(p, out=_addr(6)) == B.KDA_ERR_INVALID_ARG       # out on the state
+    assert dec(p, state=_addr(2)) == B.KDA_ERR_INVALID_ARG     # state on v
+
+
+def test_workspace_status_rejects_null(L):
+    assert L.kda_workspace_status(None, 0, None) == B.KDA_ERR_WORKSPACE

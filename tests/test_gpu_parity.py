@@ -1,0 +1,280 @@
+"""GPU parity: kda_forward / kda_decode_step through the C ABI against the fp64 oracle, element by
+element on the same seeded inputs, plus bit-exact pins, edge cases and invariants."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from linear_attention_recurrence_kda_gb300 import binding as B
+from linear_attention_recurrence_kda_gb300 import inputs as I
+from parity import check, gpu_forward, oracle_forward, to_dev, TOL_BF16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    B.lib()
+
+
+def _f64(t):
+    return t.detach().double().cpu().numpy()
+
+
+# ---------------------------------------------------------------- small shapes, both dtypes
+
+SMALL = [
+    ([1], 32, 32), ([15], 32, 32), ([16], 64, 64), ([17], 32, 64), ([33], 128, 128), ([64], 128, 64),
+    ([5, 0, 40, 16, 1], 64, 128), ([100, 3, 77], 128, 32), ([0], 32, 32), ([250], 128, 128),
+]
+
+
+@pytest.mark.parametrize("io", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("lengths,dk,dv", SMALL)
+@pytest.mark.parametrize("with_s0", [False, True], ids=["s0zero", "s0rand"])
+def test_forward_small(io, lengths, dk, dv, with_s0):
+    inp = I.make_inputs(1, lengths=lengths, num_heads=3, d_k=dk, d_v=dv, io_dtype=io,
+                        seed=sum(lengths) + dk + dv, random_s0=with_s0)
+    out, sf = gpu_forward(inp)
+    ref_o, ref_s = oracle_forward(inp)
+    check(_f64(out), ref_o, io, "out")
+    check(_f64(sf), ref_s, io, "final_state")
+
+
+def test_config0_full_fp32():
+    inp = I.make_inputs(0)
+    out, sf = gpu_forward(inp)
+    ref_o, ref_s = oracle_forward(inp)
+    e1 = check(_f64(out), ref_o, torch.float32, "out")
+    e2 = check(_f64(sf), ref_s, torch.float32, "final_state")
+    print(f"config 0: out max-rel {e1:.2e}, state max-rel {e2:.2e}")
+
+
+def test_config1_full_bf16():
+    inp = I.make_inputs(1)
+    out, sf = gpu_forward(inp)
+    ref_o, ref_s = oracle_forward(inp)
+    e1 = check(_f64(out), ref_o, torch.bfloat16, "out")
+    e2 = check(_f64(sf), ref_s, torch.bfloat16, "final_state")
+    print(f"config 1: out max/RMS {e1:.2e}, state max/RMS {e2:.2e}")
+
+
+def test_config2_varlen_full():
+    inp = I.make_inputs(2)
+    out, sf = gpu_forward(inp)
+    ref_o, ref_s = oracle_forward(inp)
+    e1 = check(_f64(out), ref_o, torch.bfloat16, "out")
+    e2 = check(_f64(sf), ref_s, torch.bfloat16, "final_state")
+    # per-sequence final states individually
+    for n in range(len(inp["lengths"])):
+        check(_f64(sf[n]), ref_s[n], torch.bfloat16, f"final_state[{n}]")
+    print(f"config 2 lengths {inp['lengths']}: out {e1:.2e}, state {e2:.2e}")
+
+
+@pytest.mark.slow
+def test_config3_long_context_sampled_and_split():
+    """1M tokens, 8 heads.  The oracle checks heads 0-1 over the first 65,536 tokens and the
+    final state of heads 0-1 after all 1,048,576 tokens; the chunk-carry invariant is checked by
+    running the GPU on [0, T/2) and [T/2, T) with the state carried."""
+    inp = I.make_inputs(3)
+    T = sum(inp["lengths"])
+    d = to_dev(inp)
+    out, sf = B.kda_forward(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], initial_state=d["S0"])
+    torch.cuda.synchronize()
+    P = 65536
+    ref_o, _ = oracle_forward(inp, heads=[0, 1], tokens=P)
+    check(_f64(out[:P, :2]), ref_o, torch.bfloat16, "out[:65536, heads 0-1]")
+    _, ref_s = oracle_forward(inp, heads=[0, 1], want_out=False)
+    check(_f64(sf[:, :2]), ref_s, torch.bfloat16, "final_state heads 0-1")
+    # split at T/2 with the state carried
+    h = T // 2
+    sl = lambda t, a, b: t[a:b].contiguous()
+    o1, s1 = B.kda_forward(*(sl(d[x], 0, h) for x in ("q", "k", "v", "z")), d["A"], sl(d["beta"], 0, h),
+                           initial_state=d["S0"])
+    o2, s2 = B.kda_forward(*(sl(d[x], h, T) for x in ("q", "k", "v", "z")), d["A"], sl(d["beta"], h, T),
+                           initial_state=s1)
+    torch.cuda.synchronize()
+    o12 = torch.cat([o1, o2])
+    check(_f64(o12[:P, :2]), ref_o, torch.bfloat16, "split out")
+    check(_f64(s2[:, :2]), ref_s, torch.bfloat16, "split final state")
+    diff = (o12.float() - out.float()).abs().max().item()
+    rms = out.float().pow(2).mean().sqrt().item()
+    assert diff <= TOL_BF16 * rms
+    del out, o1, o2, o12, d
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.slow
+def test_config4_decode_chain():
+    """256 sequences x 32 heads: 512-token varlen prefill from a random state, then 64 chained
+    decode steps; the oracle runs the 576 tokens of a sample of sequences."""
+    inp = I.make_inputs(4)
+    N, H = 256, 32
+    d = to_dev(inp)
+    _, state = B.kda_forward(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], initial_state=d["S0"],
+                             cu_seqlens=d["cu_seqlens"], max_seqlen=512)
+    dec = {k_: (v_.cuda() if torch.is_tensor(v_) else v_) for k_, v_ in inp["dec"].items()}
+    outs = []
+    for s in range(dec["steps"]):
+        outs.append(B.kda_decode_step(dec["q"][s], dec["k"][s], dec["v"][s], dec["z"][s], d["A"], dec["beta"][s],
+                                      state))
+    torch.cuda.synchronize()
+    outs = torch.stack(outs)  # [steps, N, H, d]
+    sample = list(range(0, N, 8))  # 32 sequences
+    L, S = 512, dec["steps"]
+    # token-major [576 * len(sample), H, d] per sampled sequence: 512 prefill tokens then 64 decode tokens
+    def seq_tokens(key):
+        pre = inp[key].view(N, L, H, -1)[sample]
+        de = inp["dec"][key].permute(1, 0, 2, 3)[sample]
+        return torch.cat([pre, de], dim=1).reshape(len(sample) * (L + S), H, -1)
+    q, k, v, z = (seq_tokens(x) for x in ("q", "k", "v", "z"))
+    beta = torch.cat([inp["beta"].view(N, L, H)[sample], inp["dec"]["beta"].permute(1, 0, 2)[sample]], 1)
+    beta = beta.reshape(-1, H)
+    cu = torch.arange(len(sample) + 1, dtype=torch.int64) * (L + S)
+    ref_o, ref_s = oracle.forward(q, k, v, z, inp["A"], beta, S0=inp["S0"][sample], cu_seqlens=cu)
+    ref_dec = ref_o.reshape(len(sample), L + S, H, -1)[:, L:]          # [n, steps, H, d]
+    gpu_dec = _f64(outs[:, sample].permute(1, 0, 2, 3))
+    check(gpu_dec, ref_dec, torch.bfloat16, "decode outputs (64 steps)")
+    check(_f64(state[sample]), ref_s, torch.bfloat16, "state after 64 steps")
+
+
+# ---------------------------------------------------------------- decode step alone
+
+@pytest.mark.parametrize("io", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("dk,dv", [(32, 32), (64, 128), (128, 64), (128, 128)])
+def test_decode_step_small(io, dk, dv):
+    N, H = 5, 3
+    inp = I.make_inputs(1, lengths=[1] * N, num_heads=H, d_k=dk, d_v=dv, io_dtype=io, seed=dk * 7 + dv)
+    S = inp["S0"] * 25.0  # a state of the size a prefill leaves behind
+    ref_o, ref_s = oracle.decode_step(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["beta"], S)
+    d = to_dev(inp)
+    st = S.cuda()
+    out = B.kda_decode_step(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], st)
+    torch.cuda.synchronize()
+    check(_f64(out), ref_o, io, "decode out")
+    check(_f64(st), ref_s, io, "decode state")
+
+
+def test_decode_after_prefill_equals_prefill_of_t_plus_1():
+    T, H, dk, dv = 37, 4, 128, 128
+    inp = I.make_inputs(1, lengths=[T + 1], num_heads=H, d_k=dk, d_v=dv, seed=5)
+    d = to_dev(inp)
+    o_full, s_full = B.kda_forward(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], initial_state=d["S0"])
+    _, s_pre = B.kda_forward(*(d[x][:T].contiguous() for x in ("q", "k", "v", "z")), d["A"],
+                             d["beta"][:T].contiguous(), initial_state=d["S0"])
+    o_dec = B.kda_decode_step(*(d[x][T:].contiguous() for x in ("q", "k", "v", "z")), d["A"],
+                              d["beta"][T:].contiguous(), s_pre)
+    torch.cuda.synchronize()
+    check(_f64(o_dec), _f64(o_full[T:]), torch.bfloat16, "decode vs prefill")
+    check(_f64(s_pre), _f64(s_full), torch.bfloat16, "state")
+
+
+# ---------------------------------------------------------------- exact pins, edge cases
+
+@pytest.mark.parametrize("io", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("T", [1, 16, 17, 100, 128])
+def test_bit_exact_identity_write_read(io, T):
+    """alpha = 1 (z = -1e4, A = 0 saturates the sigmoid to 0), beta = 1, q_t = k_t = distinct
+    standard basis vectors, zero state: every token writes its value into an empty row and the
+    query reads exactly that row back, so o_t = v_t bit for bit."""
+    H, d = 2, 128
+    g = torch.Generator().manual_seed(T)
+    perm = torch.stack([torch.randperm(d, generator=g)[:T] for _ in range(H)], 1)  # [T, H]
+    k = torch.zeros(T, H, d)
+    k.scatter_(2, perm.unsqueeze(-1), 1.0)
+    v = torch.randn(T, H, d, generator=g).to(io)
+    z = torch.full((T, H, d), -1e4)
+    A = torch.zeros(H)
+    beta = torch.ones(T, H)
+    out, sf = B.kda_forward(k.to(io).cuda(), k.to(io).cuda(), v.cuda(), z.to(io).cuda(), A.cuda(), beta.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu(), v)
+
+
+def test_beta_zero_pure_decay():
+    inp = I.make_inputs(1, lengths=[70], num_heads=2, d=64, io_dtype=torch.float32, seed=11)
+    inp["beta"] = torch.zeros_like(inp["beta"])
+    out, sf = gpu_forward(inp)
+    ref_o, ref_s = oracle_forward(inp)
+    check(_f64(out), ref_o, torch.float32, "out")
+    check(_f64(sf), ref_s, torch.float32, "state")
+
+
+def test_gate_floor_extreme_decay_fp32():
+    """Every log-decay at g_min (z large): a 16-token chunk spans exp(-80); stays finite and exact."""
+    inp = I.make_inputs(1, lengths=[48], num_heads=2, d=32, io_dtype=torch.float32, seed=12)
+    inp["z"] = torch.full_like(inp["z"], 60.0)
+    out, sf = gpu_forward(inp)
+    ref_o, ref_s = oracle_forward(inp)
+    check(_f64(out), ref_o, torch.float32, "out")
+    check(_f64(sf), ref_s, torch.float32, "state")
+
+
+def test_in_place_carry_and_no_final_state():
+    inp = I.make_inputs(1, lengths=[40, 24], num_heads=2, d=64, io_dtype=torch.float32, seed=13)
+    d = to_dev(inp)
+    ref_o, ref_s = oracle_forward(inp)
+    st = d["S0"].clone()
+    out, sf = B.kda_forward(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], initial_state=st,
+                            cu_seqlens=d["cu_seqlens"], final_state=st)
+    out2, none = B.kda_forward(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], initial_state=d["S0"],
+                               cu_seqlens=d["cu_seqlens"], want_final=False)
+    torch.cuda.synchronize()
+    assert none is None and sf.data_ptr() == st.data_ptr()
+    check(_f64(st), ref_s, torch.float32, "in-place state")
+    check(_f64(out), ref_o, torch.float32, "out")
+    assert torch.equal(out, out2)
+
+
+def test_equal_lengths_without_cu_seqlens():
+    inp = I.make_inputs(1, lengths=[48, 48, 48], num_heads=2, d=64, seed=14)
+    d = to_dev(inp)
+    out, sf = B.kda_forward(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], initial_state=d["S0"])
+    torch.cuda.synchronize()
+    ref_o, ref_s = oracle_forward(inp)
+    check(_f64(out), ref_o, torch.bfloat16, "out")
+    check(_f64(sf), ref_s, torch.bfloat16, "state")
+
+
+def test_deterministic():
+    inp = I.make_inputs(1, lengths=[300, 77], num_heads=4, d=128, seed=15)
+    o1, s1 = gpu_forward(inp)
+    o2, s2 = gpu_forward(inp)
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+
+
+def test_bad_cu_seqlens_is_reported_not_faulted():
+    """Offsets that violate the descriptor are caught on the device: the bad sequence is skipped,
+    the good ones are still computed, and the workspace status reports it."""
+    inp = I.make_inputs(1, lengths=[32, 32, 32], num_heads=2, d=32, io_dtype=torch.float32, seed=16)
+    d = to_dev(inp)
+    # sequence 1 has length -12, sequence 2 (76 tokens) exceeds max_seqlen = 64
+    bad = torch.tensor([0, 32, 20, 96], dtype=torch.int32, device="cuda")
+    prob = B.make_problem(3, 96, 64, 2, 32, 32, torch.float32)
+    ws = torch.empty(B.kda_forward_workspace_bytes(prob), dtype=torch.uint8, device="cuda")
+    out = torch.full((96, 2, 32), 7.0, device="cuda")
+    _, sf = B.kda_forward(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], cu_seqlens=bad, max_seqlen=64,
+                          out=out, workspace=ws)
+    assert B.kda_workspace_status(ws) == B.KDA_ERR_DEVICE_CHECK
+    ref_o, _ = oracle_forward(inp)
+    check(_f64(out[:32]), ref_o[:32], torch.float32, "sequence 0")
+    assert torch.all(out[32:] == 7.0)  # skipped sequences are not written
+    # a valid call on the same workspace clears the word
+    B.kda_forward(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], cu_seqlens=d["cu_seqlens"], max_seqlen=32,
+                  workspace=ws)
+    assert B.kda_workspace_status(ws) == B.KDA_OK
+
+
+def test_host_pointer_rejected():
+    """A pageable host pointer reaching the C ABI is rejected before any launch."""
+    import ctypes
+    inp = I.make_inputs(1, lengths=[16], num_heads=1, d=32, seed=17)
+    d = to_dev(inp)
+    prob = B.make_problem(1, 16, 16, 1, 32, 32, torch.bfloat16)
+    ws = torch.empty(B.kda_forward_workspace_bytes(prob), dtype=torch.uint8, device="cuda")
+    out = torch.empty(16, 1, 32, dtype=torch.bfloat16, device="cuda")
+    host_q = inp["q"].contiguous()  # CPU, pageable
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    st = B.lib().kda_forward(p(host_q), p(d["k"]), p(d["v"]), p(d["z"]), p(d["A"]), p(d["beta"]), None, None,
+                             p(out), None, ctypes.byref(prob), p(ws), ctypes.c_size_t(ws.numel()), None)
+    assert st == B.KDA_ERR_INVALID_ARG
