@@ -37,16 +37,16 @@ def test_forward_small(io, lengths, dk, dv, with_s0):
                         seed=sum(lengths) + dk + dv, random_s0=with_s0)
     out, sf = gpu_forward(inp)
     ref_o, ref_s = oracle_forward(inp)
-    check(_f64(out), ref_o, io, "out")
-    check(_f64(sf), ref_s, io, "final_state")
+    check(out, ref_o, io, "out")
+    check(sf, ref_s, io, "final_state")
 
 
 def test_config0_full_fp32():
     inp = I.make_inputs(0)
     out, sf = gpu_forward(inp)
     ref_o, ref_s = oracle_forward(inp)
-    e1 = check(_f64(out), ref_o, torch.float32, "out")
-    e2 = check(_f64(sf), ref_s, torch.float32, "final_state")
+    e1 = check(out, ref_o, torch.float32, "out")
+    e2 = check(sf, ref_s, torch.float32, "final_state")
     print(f"config 0: out max-rel {e1:.2e}, state max-rel {e2:.2e}")
 
 
@@ -54,8 +54,8 @@ def test_config1_full_bf16():
     inp = I.make_inputs(1)
     out, sf = gpu_forward(inp)
     ref_o, ref_s = oracle_forward(inp)
-    e1 = check(_f64(out), ref_o, torch.bfloat16, "out")
-    e2 = check(_f64(sf), ref_s, torch.bfloat16, "final_state")
+    e1 = check(out, ref_o, torch.bfloat16, "out")
+    e2 = check(sf, ref_s, torch.bfloat16, "final_state")
     print(f"config 1: out max/RMS {e1:.2e}, state max/RMS {e2:.2e}")
 
 
@@ -63,11 +63,11 @@ def test_config2_varlen_full():
     inp = I.make_inputs(2)
     out, sf = gpu_forward(inp)
     ref_o, ref_s = oracle_forward(inp)
-    e1 = check(_f64(out), ref_o, torch.bfloat16, "out")
-    e2 = check(_f64(sf), ref_s, torch.bfloat16, "final_state")
+    e1 = check(out, ref_o, torch.bfloat16, "out")
+    e2 = check(sf, ref_s, torch.bfloat16, "final_state")
     # per-sequence final states individually
     for n in range(len(inp["lengths"])):
-        check(_f64(sf[n]), ref_s[n], torch.bfloat16, f"final_state[{n}]")
+        check(sf[n], ref_s[n], torch.bfloat16, f"final_state[{n}]")
     print(f"config 2 lengths {inp['lengths']}: out {e1:.2e}, state {e2:.2e}")
 
 
@@ -83,9 +83,9 @@ def test_config3_long_context_sampled_and_split():
     torch.cuda.synchronize()
     P = 65536
     ref_o, _ = oracle_forward(inp, heads=[0, 1], tokens=P)
-    check(_f64(out[:P, :2]), ref_o, torch.bfloat16, "out[:65536, heads 0-1]")
+    check(out[:P, :2], ref_o, torch.bfloat16, "out[:65536, heads 0-1]")
     _, ref_s = oracle_forward(inp, heads=[0, 1], want_out=False)
-    check(_f64(sf[:, :2]), ref_s, torch.bfloat16, "final_state heads 0-1")
+    check(sf[:, :2], ref_s, torch.bfloat16, "final_state heads 0-1")
     # split at T/2 with the state carried
     h = T // 2
     sl = lambda t, a, b: t[a:b].contiguous()
@@ -95,8 +95,8 @@ def test_config3_long_context_sampled_and_split():
                            initial_state=s1)
     torch.cuda.synchronize()
     o12 = torch.cat([o1, o2])
-    check(_f64(o12[:P, :2]), ref_o, torch.bfloat16, "split out")
-    check(_f64(s2[:, :2]), ref_s, torch.bfloat16, "split final state")
+    check(o12[:P, :2], ref_o, torch.bfloat16, "split out")
+    check(s2[:, :2], ref_s, torch.bfloat16, "split final state")
     diff = (o12.float() - out.float()).abs().max().item()
     rms = out.float().pow(2).mean().sqrt().item()
     assert diff <= TOL_BF16 * rms
@@ -133,9 +133,9 @@ def test_config4_decode_chain():
     cu = torch.arange(len(sample) + 1, dtype=torch.int64) * (L + S)
     ref_o, ref_s = oracle.forward(q, k, v, z, inp["A"], beta, S0=inp["S0"][sample], cu_seqlens=cu)
     ref_dec = ref_o.reshape(len(sample), L + S, H, -1)[:, L:]          # [n, steps, H, d]
-    gpu_dec = _f64(outs[:, sample].permute(1, 0, 2, 3))
+    gpu_dec = outs[:, sample].permute(1, 0, 2, 3)
     check(gpu_dec, ref_dec, torch.bfloat16, "decode outputs (64 steps)")
-    check(_f64(state[sample]), ref_s, torch.bfloat16, "state after 64 steps")
+    check(state[sample], ref_s, torch.bfloat16, "state after 64 steps")
 
 
 # ---------------------------------------------------------------- decode step alone
@@ -151,8 +151,8 @@ def test_decode_step_small(io, dk, dv):
     st = S.cuda()
     out = B.kda_decode_step(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], st)
     torch.cuda.synchronize()
-    check(_f64(out), ref_o, io, "decode out")
-    check(_f64(st), ref_s, io, "decode state")
+    check(out, ref_o, io, "decode out")
+    check(st, ref_s, io, "decode state")
 
 
 def test_decode_after_prefill_equals_prefill_of_t_plus_1():
@@ -165,8 +165,8 @@ def test_decode_after_prefill_equals_prefill_of_t_plus_1():
     o_dec = B.kda_decode_step(*(d[x][T:].contiguous() for x in ("q", "k", "v", "z")), d["A"],
                               d["beta"][T:].contiguous(), s_pre)
     torch.cuda.synchronize()
-    check(_f64(o_dec), _f64(o_full[T:]), torch.bfloat16, "decode vs prefill")
-    check(_f64(s_pre), _f64(s_full), torch.bfloat16, "state")
+    check(o_dec, _f64(o_full[T:]), torch.bfloat16, "decode vs prefill")
+    check(s_pre, _f64(s_full), torch.bfloat16, "state")
 
 
 # ---------------------------------------------------------------- exact pins, edge cases
@@ -196,8 +196,8 @@ def test_beta_zero_pure_decay():
     inp["beta"] = torch.zeros_like(inp["beta"])
     out, sf = gpu_forward(inp)
     ref_o, ref_s = oracle_forward(inp)
-    check(_f64(out), ref_o, torch.float32, "out")
-    check(_f64(sf), ref_s, torch.float32, "state")
+    check(out, ref_o, torch.float32, "out")
+    check(sf, ref_s, torch.float32, "state")
 
 
 def test_gate_floor_extreme_decay_fp32():
@@ -206,8 +206,8 @@ def test_gate_floor_extreme_decay_fp32():
     inp["z"] = torch.full_like(inp["z"], 60.0)
     out, sf = gpu_forward(inp)
     ref_o, ref_s = oracle_forward(inp)
-    check(_f64(out), ref_o, torch.float32, "out")
-    check(_f64(sf), ref_s, torch.float32, "state")
+    check(out, ref_o, torch.float32, "out")
+    check(sf, ref_s, torch.float32, "state")
 
 
 def test_in_place_carry_and_no_final_state():
@@ -221,8 +221,8 @@ def test_in_place_carry_and_no_final_state():
                                cu_seqlens=d["cu_seqlens"], want_final=False)
     torch.cuda.synchronize()
     assert none is None and sf.data_ptr() == st.data_ptr()
-    check(_f64(st), ref_s, torch.float32, "in-place state")
-    check(_f64(out), ref_o, torch.float32, "out")
+    check(st, ref_s, torch.float32, "in-place state")
+    check(out, ref_o, torch.float32, "out")
     assert torch.equal(out, out2)
 
 
@@ -232,8 +232,8 @@ def test_equal_lengths_without_cu_seqlens():
     out, sf = B.kda_forward(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], initial_state=d["S0"])
     torch.cuda.synchronize()
     ref_o, ref_s = oracle_forward(inp)
-    check(_f64(out), ref_o, torch.bfloat16, "out")
-    check(_f64(sf), ref_s, torch.bfloat16, "state")
+    check(out, ref_o, torch.bfloat16, "out")
+    check(sf, ref_s, torch.bfloat16, "state")
 
 
 def test_deterministic():
@@ -253,11 +253,11 @@ def test_bad_cu_seqlens_is_reported_not_faulted():
     prob = B.make_problem(3, 96, 64, 2, 32, 32, torch.float32)
     ws = torch.empty(B.kda_forward_workspace_bytes(prob), dtype=torch.uint8, device="cuda")
     out = torch.full((96, 2, 32), 7.0, device="cuda")
-    _, sf = B.kda_forward(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], cu_seqlens=bad, max_seqlen=64,
-                          out=out, workspace=ws)
+    _, sf = B.kda_forward(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], initial_state=d["S0"],
+                          cu_seqlens=bad, max_seqlen=64, out=out, workspace=ws)
     assert B.kda_workspace_status(ws) == B.KDA_ERR_DEVICE_CHECK
     ref_o, _ = oracle_forward(inp)
-    check(_f64(out[:32]), ref_o[:32], torch.float32, "sequence 0")
+    check(out[:32], ref_o[:32], torch.float32, "sequence 0")
     assert torch.all(out[32:] == 7.0)  # skipped sequences are not written
     # a valid call on the same workspace clears the word
     B.kda_forward(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], cu_seqlens=d["cu_seqlens"], max_seqlen=32,
@@ -265,8 +265,10 @@ def test_bad_cu_seqlens_is_reported_not_faulted():
     assert B.kda_workspace_status(ws) == B.KDA_OK
 
 
-def test_host_pointer_rejected():
-    """A pageable host pointer reaching the C ABI is rejected before any launch."""
+def test_pageable_host_pointer():
+    """A pageable host pointer reaching the C ABI is either rejected before any launch (GPUs that
+    cannot address pageable memory) or, where the device reports it addressable (Grace-based
+    GB300: coherent access to system memory), accepted and computed correctly."""
     import ctypes
     inp = I.make_inputs(1, lengths=[16], num_heads=1, d=32, seed=17)
     d = to_dev(inp)
@@ -275,6 +277,11 @@ def test_host_pointer_rejected():
     out = torch.empty(16, 1, 32, dtype=torch.bfloat16, device="cuda")
     host_q = inp["q"].contiguous()  # CPU, pageable
     p = lambda t: ctypes.c_void_p(t.data_ptr())
-    st = B.lib().kda_forward(p(host_q), p(d["k"]), p(d["v"]), p(d["z"]), p(d["A"]), p(d["beta"]), None, None,
-                             p(out), None, ctypes.byref(prob), p(ws), ctypes.c_size_t(ws.numel()), None)
-    assert st == B.KDA_ERR_INVALID_ARG
+    st = B.lib().kda_forward(p(host_q), p(d["k"]), p(d["v"]), p(d["z"]), p(d["A"]), p(d["beta"]), p(d["S0"]),
+                             None, p(out), None, ctypes.byref(prob), p(ws), ctypes.c_size_t(ws.numel()), None)
+    torch.cuda.synchronize()
+    if st == B.KDA_OK:
+        ref, _ = gpu_forward(inp)
+        assert torch.equal(out, ref)
+    else:
+        assert st == B.KDA_ERR_INVALID_ARG
