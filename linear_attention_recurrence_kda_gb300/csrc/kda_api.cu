@@ -178,6 +178,12 @@ kda_status_t kda_forward(const void* q, const void* k, const void* v, const void
 
     if (cudaMemsetAsync(a.check, 0, sizeof(uint32_t), s) != cudaSuccess) return KDA_ERR_CUDA;
     cudaError_t e = cudaSuccess;
+    if (kda::use_tensor_core_path(p)) {
+        kda::prof_start("kda_chunk_fwd_tc", s);
+        e = kda::launch_chunk_fwd_tc(a, s);
+        kda::prof_stop(s);
+        return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    }
     if (cps > 0) {
         kda::prof_start("kda_gate", s);
         e = kda::launch_gate(a, p.io_dtype, s);

@@ -2,6 +2,7 @@
 //
 // Workspace layout of kda_forward (every region 256-byte aligned, offsets from the base):
 //   [0, 256)   device check word (uint32) written by the kernels, read by kda_workspace_status
+// and, for the fp32 SIMT path only (the fused tensor-core path keeps these on chip):
 //   G          fp32 [T_tot, H, d_k]   in-chunk inclusive cumulative log-decay (kda_gate)
 //   W          fp32 [T_tot, H, d_k]   WY-transformed keys T diag(beta) (K*Gamma)   (kda_ut_wy)
 //   Ut         fp32 [T_tot, H, d_v]   UT-transformed values T diag(beta) V         (kda_ut_wy)
@@ -27,10 +28,17 @@ struct ForwardLayout {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// bf16 inputs with d_k = d_v = 128 run on the fused tensor-core kernel (no per-token workspace).
+inline bool use_tensor_core_path(const kda_problem_t& p)
+{
+    return p.io_dtype == KDA_BF16 && p.d_k == 128 && p.d_v == 128 && p.total_tokens > 0 &&
+           p.total_tokens < (int64_t(1) << 31);
+}
+
 inline ForwardLayout forward_layout(const kda_problem_t& p)
 {
     ForwardLayout L{};
-    const size_t th = (size_t)p.total_tokens * (size_t)p.num_heads;
+    const size_t th = use_tensor_core_path(p) ? 0 : (size_t)p.total_tokens * (size_t)p.num_heads;
     L.status_off = 0;
     L.g_off = 256;
     L.w_off = align_up(L.g_off + th * p.d_k * sizeof(float), 256);
@@ -77,6 +85,7 @@ struct DecodeArgs {
 cudaError_t launch_gate(const PrefillArgs& a, kda_dtype_t dt, cudaStream_t s);
 cudaError_t launch_ut_wy(const PrefillArgs& a, kda_dtype_t dt, cudaStream_t s);
 cudaError_t launch_chunk_fwd(const PrefillArgs& a, kda_dtype_t dt, cudaStream_t s);
+cudaError_t launch_chunk_fwd_tc(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
 
 // Optional per-kernel timing around launches (no-ops unless kda_profile_enable(1)).

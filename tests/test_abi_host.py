@@ -62,8 +62,11 @@ def test_workspace_bytes(L):
     # check word + G, W (d_k) and U~ (d_v) in fp32 for every token-head
     assert n >= 256 + 64 * 2 * (32 + 32 + 32) * 4
     assert n % 256 == 0
+    # bf16 inputs with d_k = d_v = 128 take the fused tensor-core path: no per-token scratch
     big = _prob(total_tokens=1 << 20, max_seqlen=1 << 20, num_heads=8, d_k=128, d_v=128, io_dtype=B.KDA_BF16)
-    assert B.kda_forward_workspace_bytes(big) > B.kda_forward_workspace_bytes(p)
+    assert 256 <= B.kda_forward_workspace_bytes(big) < 1 << 30
+    simt_big = _prob(total_tokens=1 << 20, max_seqlen=1 << 20, num_heads=8, d_k=128, d_v=128)
+    assert B.kda_forward_workspace_bytes(simt_big) > B.kda_forward_workspace_bytes(p)
     for bad in (_prob(d_k=96), _prob(num_heads=0), _prob(g_min=0.0), _prob(g_min=float("nan")),
                 _prob(io_dtype=7), _prob(total_tokens=-1), _prob(num_seqs=0)):
         assert B.kda_forward_workspace_bytes(bad) == 0
