@@ -33,9 +33,11 @@
 // K/Gamma inside P, P and U in U P^T, U and K Gamma_C/Gamma in the state update, and T'.  The
 // remaining bf16 roundings (the state as the read operand, W, K Gamma) reach the outputs only
 // through products that the decay keeps small.
-// Two CTAs share an SM (256 TMEM columns and ~100 KB of shared memory each), so one CTA's SIMT
-// stages overlap the other's tensor-core work.  Every mbarrier wait is bounded; a wait that gives
-// up raises the timeout bit of the check word and the CTA stops cleanly.
+// The loop is software-pipelined across chunks: while the tensor core runs chunk n's state-read,
+// output and state-update products, all 256 threads prepare chunk n+1 (gate, factors, A, P, T')
+// into the other half of double-buffered operand tiles, and TMA fetches chunk n+2's inputs.
+// Every mbarrier wait is bounded; a wait that gives up raises the timeout bit of the check word
+// and the CTA stops cleanly.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -54,57 +56,58 @@ constexpr int NTHREADS = 256;
 constexpr int LROW = 136;         // padded row (elements) of the mma.sync operand tiles
 constexpr uint32_t WAIT_LIMIT = 1u << 24;
 
-// shared-memory map (bytes from a 1024-aligned base)
-constexpr uint32_t OFF_S = 0;         // S^T  [128 j][128 c] SW128          32768
-constexpr uint32_t OFF_WQ = 32768;    // [W ; Q Gamma] [32][128 c] SW128     8192
-constexpr uint32_t OFF_XT = 40960;    // (K Gamma)^T [128 c][16 i] NONE      4096
-constexpr uint32_t OFF_VT = 45056;    // V^T  [128 j][16 i] NONE             4096
-constexpr uint32_t OFF_UT = 49152;    // U^T hi [128 j][16 i] NONE           4096
-constexpr uint32_t OFF_UL = 53248;    // U^T lo                              4096
-constexpr uint32_t OFF_KT = 57344;    // (K Gamma_C/Gamma)^T hi [128 c][16 i] 4096
-constexpr uint32_t OFF_KTL = 61440;   // (K Gamma_C/Gamma)^T lo              4096
-constexpr uint32_t OFF_P = 65536;     // P hi [16 r][16 i] NONE              512
-constexpr uint32_t OFF_PL = 66048;    // P lo                                512
-constexpr uint32_t OFF_T = 66560;     // T' hi [16 r][16 i] NONE             512
-constexpr uint32_t OFF_TL = 67072;    // T' lo                               512
-constexpr uint32_t OFF_LL = 67584;    // K Gamma   [16][LROW] bf16           4352
-constexpr uint32_t OFF_QL = 71936;    // Q Gamma hi                          4352
-constexpr uint32_t OFF_QLL = 76288;   // Q Gamma lo                          4352
-constexpr uint32_t OFF_KD = 80640;    // K / Gamma hi                        4352
-constexpr uint32_t OFF_KDL = 84992;   // K / Gamma lo                        4352
-constexpr uint32_t OFF_A = 89344;     // A fp32 [16][16]                     1024
-constexpr uint32_t OFF_PF = 90368;    // P partial sums fp32 [2][16][16]     2048
-constexpr uint32_t OFF_GC = 92416;    // Gamma_C fp32 [128]                  512
-constexpr uint32_t OFF_BAR = 92928;   // mbarrier                            8
-constexpr uint32_t OFF_TSLOT = 92936; // TMEM base address                   4
-constexpr uint32_t OFF_ABORT = 92940; // stop flag                           4
-constexpr uint32_t OFF_STAGE = 93184; // q, k, v, z tiles [16][128] bf16 (TMA)  16384
-constexpr uint32_t OFF_BETA = 109568; // beta of the chunk                   64
-constexpr uint32_t OFF_BARLD = 109632;// mbarrier of the tile loads          8
-constexpr uint32_t SMEM_USED = 109640;
-constexpr uint32_t STAGE_TILE = C * D * 2;  // 4096 bytes per tensor and chunk
-// Two CTAs per SM fit (the number whose 256 TMEM columns fit in the SM's 512).
+// shared-memory map (bytes from a 1024-aligned base); "[2]" = double-buffered by chunk parity
+constexpr uint32_t OFF_S = 0;          // S^T [128 j][128 c] SW128                      32768
+constexpr uint32_t OFF_WQ = 32768;     // [2] [W ; Q Gamma] [32][128 c] SW128            2 x 8192
+constexpr uint32_t OFF_STAGE = 49152;  // q, k, v, z tiles [16][128] bf16 (TMA)         16384
+constexpr uint32_t OFF_KT = 65536;     // [2] (K Gamma_C/Gamma)^T hi, lo [128 c][16 i]   2 x 8192
+constexpr uint32_t OFF_XT = 81920;     // (K Gamma)^T [128 c][16 i] NONE                4096
+constexpr uint32_t OFF_VT = 86016;     // V^T [128 j][16 i] NONE                        4096
+constexpr uint32_t OFF_UT = 90112;     // U^T hi, lo [128 j][16 i] NONE                 8192
+constexpr uint32_t OFF_P = 98304;      // [2] P hi, lo [16 r][16 i] NONE                 2 x 1024
+constexpr uint32_t OFF_T = 100352;     // T' hi, lo [16 r][16 i] NONE                   1024
+constexpr uint32_t OFF_LL = 101376;    // K Gamma [16][LROW] bf16                       4352
+constexpr uint32_t OFF_QL = 105728;    // Q Gamma hi, lo                                2 x 4352
+constexpr uint32_t OFF_KD = 114432;    // K / Gamma hi, lo                              2 x 4352
+constexpr uint32_t OFF_A = 123136;     // A fp32 [16][16]                               1024
+constexpr uint32_t OFF_PF = 124160;    // P partial sums fp32 [2][16][16]               2048
+constexpr uint32_t OFF_GC = 126208;    // [2] Gamma_C fp32 [128]                         2 x 512
+constexpr uint32_t OFF_HS = 127232;    // per-channel half-chunk log-decay sums [2][128] 1024
+constexpr uint32_t OFF_BETA = 128256;  // [2] beta [16]                                  2 x 64
+constexpr uint32_t OFF_BAR = 128384;   // mbarrier of the tensor-core commits           8
+constexpr uint32_t OFF_BARLD = 128392; // mbarrier of the TMA tile loads                8
+constexpr uint32_t OFF_TSLOT = 128400; // TMEM base address                             4
+constexpr uint32_t OFF_ABORT = 128404; // stop flag                                     4
+constexpr uint32_t SMEM_USED = 128408;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
+constexpr uint32_t STAGE_TILE = C * D * 2;  // 4096 bytes per tensor and chunk
+constexpr uint32_t NONE_TILE = 4096;        // [128][16] bf16 NONE tile
+constexpr uint32_t SMALL_TILE = 512;        // [16][16] bf16 NONE tile
 
-// tensor-memory columns (256 allocated)
+// tensor-memory columns
 constexpr uint32_t TM_D1 = 0;    // [0,16): (W S)^T, [16,32): O^T
 constexpr uint32_t TM_W = 32;    // W^T  (lanes = c)
 constexpr uint32_t TM_U = 48;    // U~^T (lanes = j)
 constexpr uint32_t TM_D3 = 128;  // dS^T (lanes = j, columns = c)
 constexpr uint32_t TM_COLS = 256;
 
-__device__ __forceinline__ void st_bf16(unsigned char* base, uint32_t off, float x)
-{
-    *reinterpret_cast<__nv_bfloat16*>(base + off) = __float2bfloat16_rn(x);
-}
-
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+
+__device__ __forceinline__ void st_bf16(unsigned char* base, uint32_t off, __nv_bfloat16 x)
+{
+    *reinterpret_cast<__nv_bfloat16*>(base + off) = x;
+}
 
 // x = hi + lo with hi = bf16(x), lo = bf16(x - hi)
 __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bfloat16& lo)
 {
     hi = __float2bfloat16_rn(x);
     lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+}
+
+__device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b)
+{
+    return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
 }
 
 // acc[16 x 16] += L R^T over K = 128 (L, R: 16 rows of LROW bf16) with mma.sync m16n8k16.
@@ -129,7 +132,7 @@ __device__ __forceinline__ void mma_rows16(float (&acc)[2][4], const __nv_bfloat
     }
 }
 
-// Issue + commit + bounded wait by thread 0, then a CTA barrier.  Returns false if the CTA must stop.
+// Commit the issued tensor-core work, bounded wait by thread 0, CTA barrier.  False: stop.
 __device__ __forceinline__ bool tc_join(uint64_t* bar, uint32_t& phase, volatile uint32_t* abort_flag)
 {
     if (threadIdx.x == 0) {
@@ -151,33 +154,182 @@ __device__ __forceinline__ void tc_publish()
     tc::fence_after_sync();
 }
 
+struct Ctx {
+    unsigned char* sm;
+    int tid, w, lane;
+    int h, H;
+    float expA, g_min;
+};
+
+// Gate, in-chunk cumulative log-decay and every per-element factor of one chunk (all threads).
+// Thread (c, half) owns key/value channel c and tokens [8 half, 8 half + 8).
+// Writes: row-major K Gamma, Q Gamma (hi/lo), K/Gamma (hi/lo); WQ[b] rows 16..31 (Q Gamma hi);
+// (K Gamma)^T, V^T; KT[b] (K Gamma_C/Gamma hi/lo); GC[b] = Gamma_C.  Contains one CTA barrier.
+__device__ __forceinline__ void prep_factors(const Ctx& x, int len, int b)
+{
+    unsigned char* sm = x.sm;
+    const int c = x.tid & (D - 1);
+    const int half = x.tid >> 7;
+    const int r0 = 8 * half;
+    const __nv_bfloat16* tq = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_STAGE);
+    const __nv_bfloat16* tk = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_STAGE + STAGE_TILE);
+    const __nv_bfloat16* tv = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_STAGE + 2 * STAGE_TILE);
+    const __nv_bfloat16* tz = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_STAGE + 3 * STAGE_TILE);
+    float* hs = reinterpret_cast<float*>(sm + OFF_HS);
+
+    float Gl[8], kv[8], qv[8];
+    uint32_t vpk[4];
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const int r = r0 + e;
+        const bool ok = r < len;
+        const float g = ok ? log_decay(__bfloat162float(tz[r * D + c]), x.expA, x.g_min) : 0.f;
+        acc += g;
+        Gl[e] = acc;
+        kv[e] = ok ? __bfloat162float(tk[r * D + c]) : 0.f;
+        qv[e] = ok ? __bfloat162float(tq[r * D + c]) : 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+        const __nv_bfloat16 z0 = __float2bfloat16_rn(0.f);
+        vpk[e / 2] = pack2((r0 + e < len) ? tv[(r0 + e) * D + c] : z0, (r0 + e + 1 < len) ? tv[(r0 + e + 1) * D + c] : z0);
+    }
+    hs[half * D + c] = acc;
+    __syncthreads();
+    const float off = half ? hs[c] : 0.f;
+    const float GC = hs[c] + hs[D + c];
+    const float eGC = expf(GC);
+    if (half) reinterpret_cast<float*>(sm + OFF_GC + b * 512)[c] = eGC;
+
+    __nv_bfloat16* sLl = reinterpret_cast<__nv_bfloat16*>(sm + OFF_LL);
+    __nv_bfloat16* sQl = reinterpret_cast<__nv_bfloat16*>(sm + OFF_QL);
+    __nv_bfloat16* sQll = sQl + C * LROW;
+    __nv_bfloat16* sKd = reinterpret_cast<__nv_bfloat16*>(sm + OFF_KD);
+    __nv_bfloat16* sKdl = sKd + C * LROW;
+    unsigned char* wq = sm + OFF_WQ + b * 8192;
+    __nv_bfloat16 xt[8], kth[8], ktl[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const int r = r0 + e;
+        const float eG = expf(Gl[e] + off);      // Gamma_r in [e^-80, 1]
+        const float ieG = __frcp_rn(eG);          // 1 / Gamma_r in [1, e^80]
+        const float ll = kv[e] * eG;
+        __nv_bfloat16 hi, lo;
+        xt[e] = __float2bfloat16_rn(ll);
+        sLl[r * LROW + c] = xt[e];
+        split_bf16(qv[e] * eG, hi, lo);
+        sQl[r * LROW + c] = hi;
+        sQll[r * LROW + c] = lo;
+        st_bf16(wq, tc::sw128_off(C + r, c, 2 * C), hi);
+        split_bf16(kv[e] * ieG, hi, lo);
+        sKd[r * LROW + c] = hi;
+        sKdl[r * LROW + c] = lo;
+        split_bf16(kv[e] * (eGC * ieG), kth[e], ktl[e]);   // k Gamma_C / Gamma_r <= 1
+    }
+    *reinterpret_cast<uint4*>(sm + OFF_XT + tc::none_off(c, r0)) =
+        make_uint4(pack2(xt[0], xt[1]), pack2(xt[2], xt[3]), pack2(xt[4], xt[5]), pack2(xt[6], xt[7]));
+    *reinterpret_cast<uint4*>(sm + OFF_VT + tc::none_off(c, r0)) = make_uint4(vpk[0], vpk[1], vpk[2], vpk[3]);
+    unsigned char* kt = sm + OFF_KT + b * 8192;
+    *reinterpret_cast<uint4*>(kt + tc::none_off(c, r0)) =
+        make_uint4(pack2(kth[0], kth[1]), pack2(kth[2], kth[3]), pack2(kth[4], kth[5]), pack2(kth[6], kth[7]));
+    *reinterpret_cast<uint4*>(kt + NONE_TILE + tc::none_off(c, r0)) =
+        make_uint4(pack2(ktl[0], ktl[1]), pack2(ktl[2], ktl[3]), pack2(ktl[4], ktl[5]), pack2(ktl[6], ktl[7]));
+}
+
+// A, P (mma.sync), T = (I + A)^-1 and T' = T diag(beta) (hi/lo), P finalised into P[b] (hi/lo).
+// Contains one CTA barrier; the caller publishes afterwards.
+__device__ __forceinline__ void prep_solve(const Ctx& x, int b)
+{
+    unsigned char* sm = x.sm;
+    const int w = x.w, lane = x.lane, tid = x.tid;
+    float* sA = reinterpret_cast<float*>(sm + OFF_A);
+    float* sPf = reinterpret_cast<float*>(sm + OFF_PF);
+    const float* beta = reinterpret_cast<const float*>(sm + OFF_BETA + b * 64);
+    const __nv_bfloat16* sLl = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_LL);
+    const __nv_bfloat16* sQl = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_QL);
+    const __nv_bfloat16* sQll = sQl + C * LROW;
+    const __nv_bfloat16* sKd = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_KD);
+    const __nv_bfloat16* sKdl = sKd + C * LROW;
+    if (w < 3) {
+        const int g = lane >> 2, t = lane & 3;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        if (w == 0) {
+            mma_rows16(acc, sLl, sKd, lane);
+        } else if (w == 1) {
+            mma_rows16(acc, sQl, sKd, lane);
+            mma_rows16(acc, sQl, sKdl, lane);
+        } else {
+            mma_rows16(acc, sQll, sKd, lane);
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = g + ((e >> 1) << 3);
+                const int i = 8 * nt + 2 * t + (e & 1);
+                if (w == 0) {
+                    sA[r * C + i] = (i < r) ? beta[r] * acc[nt][e] : 0.f;
+                } else {
+                    sPf[(w - 1) * C * C + r * C + i] = acc[nt][e];
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (w == 0 && lane < C) {
+        // forward substitution, one lane per column j: T[r][j] = delta_rj - sum_{i<r} A[r][i] T[i][j]
+        const int j = lane;
+        float tcol[C];
+#pragma unroll
+        for (int r = 0; r < C; ++r) {
+            float p0 = (r == j) ? 1.f : 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+            for (int i = 0; i < r; i += 4) {
+                p0 -= sA[r * C + i] * tcol[i];
+                if (i + 1 < r) p1 -= sA[r * C + i + 1] * tcol[i + 1];
+                if (i + 2 < r) p2 -= sA[r * C + i + 2] * tcol[i + 2];
+                if (i + 3 < r) p3 -= sA[r * C + i + 3] * tcol[i + 3];
+            }
+            tcol[r] = (p0 + p1) + (p2 + p3);
+        }
+        const float bj = beta[j];
+#pragma unroll
+        for (int r = 0; r < C; ++r) {
+            __nv_bfloat16 hi, lo;
+            split_bf16(tcol[r] * bj, hi, lo);
+            st_bf16(sm, OFF_T + tc::none_off(r, j), hi);
+            st_bf16(sm, OFF_T + SMALL_TILE + tc::none_off(r, j), lo);
+        }
+    } else if (tid >= 128) {
+        unsigned char* pb = sm + OFF_P + b * 1024;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int idx = 2 * (tid - 128) + e;
+            const int r = idx >> 4, i = idx & 15;
+            const float pv = (i <= r) ? sPf[idx] + sPf[C * C + idx] : 0.f;
+            __nv_bfloat16 hi, lo;
+            split_bf16(pv, hi, lo);
+            st_bf16(pb, tc::none_off(r, i), hi);
+            st_bf16(pb, SMALL_TILE + tc::none_off(r, i), lo);
+        }
+    }
+}
+
 }  // namespace
 
 struct TileMaps {
     CUtensorMap q, k, v, z;  // 3-D views [T_tot][H][128] of the bf16 inputs, box [16][1][128]
 };
 
-__global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_fwd_tc_kernel(PrefillArgs a, const __grid_constant__ TileMaps maps)
+__global__ void __launch_bounds__(NTHREADS, 1) kda_chunk_fwd_tc_kernel(PrefillArgs a, const __grid_constant__ TileMaps maps)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+    uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + OFF_BARLD);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_TSLOT);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(sm + OFF_ABORT);
-    __nv_bfloat16* sLl = reinterpret_cast<__nv_bfloat16*>(sm + OFF_LL);
-    __nv_bfloat16* sQl = reinterpret_cast<__nv_bfloat16*>(sm + OFF_QL);
-    __nv_bfloat16* sQll = reinterpret_cast<__nv_bfloat16*>(sm + OFF_QLL);
-    __nv_bfloat16* sKd = reinterpret_cast<__nv_bfloat16*>(sm + OFF_KD);
-    __nv_bfloat16* sKdl = reinterpret_cast<__nv_bfloat16*>(sm + OFF_KDL);
-    float* sA = reinterpret_cast<float*>(sm + OFF_A);
-    float* sPf = reinterpret_cast<float*>(sm + OFF_PF);
-    float* sBeta = reinterpret_cast<float*>(sm + OFF_BETA);
-    uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + OFF_BARLD);
-    const __nv_bfloat16* tq = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_STAGE);
-    const __nv_bfloat16* tk = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_STAGE + STAGE_TILE);
-    const __nv_bfloat16* tv = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_STAGE + 2 * STAGE_TILE);
-    const __nv_bfloat16* tz = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_STAGE + 3 * STAGE_TILE);
-    float* sGC = reinterpret_cast<float*>(sm + OFF_GC);
 
     const int n = blockIdx.x;
     const int h = blockIdx.y;
@@ -190,29 +342,35 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_fwd_tc_kernel(PrefillAr
 
     int64_t s0, s1;
     if (!seq_range(a, n, s0, s1)) return;
-
-    __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.out);
     const int H = a.H;
-    const float expA = expf(a.A[h]);
-    const float g_min = a.g_min;
+    const Ctx x{sm, tid, w, lane, h, H, expf(a.A[h]), a.g_min};
+    __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.out);
+    const int nchunks = (int)((s1 - s0 + C - 1) / C);
+
+    auto issue_tiles = [&](int chunk) {  // thread 0
+        const int tn = (int)(s0 + (int64_t)chunk * C);
+        tc::fence_async_smem();
+        tc::mbar_arrive_expect_tx(bar_ld, 4 * STAGE_TILE);
+        tc::tma_load_3d(sm + OFF_STAGE, &maps.q, 0, h, tn, bar_ld);
+        tc::tma_load_3d(sm + OFF_STAGE + STAGE_TILE, &maps.k, 0, h, tn, bar_ld);
+        tc::tma_load_3d(sm + OFF_STAGE + 2 * STAGE_TILE, &maps.v, 0, h, tn, bar_ld);
+        tc::tma_load_3d(sm + OFF_STAGE + 3 * STAGE_TILE, &maps.z, 0, h, tn, bar_ld);
+    };
+    auto load_beta = [&](int chunk) -> float {  // threads 0..15
+        const int64_t t = s0 + (int64_t)chunk * C + tid;
+        return (chunk < nchunks && t < s1) ? a.beta[t * H + h] : 0.f;
+    };
+    auto chunk_len = [&](int chunk) -> int { return (int)min((int64_t)C, s1 - (s0 + (int64_t)chunk * C)); };
 
     if (w == 0) tc::tmem_alloc(tslot, TM_COLS);
+    float beta_next = 0.f;
     if (tid == 0) {
         tc::mbar_init(bar, 1);
         tc::mbar_init(bar_ld, 1);
         *abort_flag = 0u;
-        tc::fence_async_smem();
-        // first chunk's tiles
-        if (s0 < s1) {
-            tc::mbar_arrive_expect_tx(bar_ld, 4 * STAGE_TILE);
-            tc::tma_load_3d(sm + OFF_STAGE, &maps.q, 0, h, (int)s0, bar_ld);
-            tc::tma_load_3d(sm + OFF_STAGE + STAGE_TILE, &maps.k, 0, h, (int)s0, bar_ld);
-            tc::tma_load_3d(sm + OFF_STAGE + 2 * STAGE_TILE, &maps.v, 0, h, (int)s0, bar_ld);
-            tc::tma_load_3d(sm + OFF_STAGE + 3 * STAGE_TILE, &maps.z, 0, h, (int)s0, bar_ld);
-        }
+        if (nchunks > 0) issue_tiles(0);
     }
-    float beta_next = (tid < C && s0 + tid < s1) ? a.beta[(s0 + tid) * H + h] : 0.f;
-    uint32_t ld_phase = 0;
+    if (tid < C) beta_next = load_beta(0);
 
     // state slice: S[c][jrow] for c in [64*h2, 64*h2 + 64)
     float S[64];
@@ -221,216 +379,102 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_fwd_tc_kernel(PrefillAr
     for (int cc = 0; cc < 64; ++cc) {
         S[cc] = a.s0 ? a.s0[sbase + (int64_t)(64 * h2 + cc) * D + jrow] : 0.f;
     }
+    auto stage_state = [&]() {
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-        uint4 pk;
-        pk.x = tc::pack_bf16(S[8 * ch + 0], S[8 * ch + 1]);
-        pk.y = tc::pack_bf16(S[8 * ch + 2], S[8 * ch + 3]);
-        pk.z = tc::pack_bf16(S[8 * ch + 4], S[8 * ch + 5]);
-        pk.w = tc::pack_bf16(S[8 * ch + 6], S[8 * ch + 7]);
-        *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw128_chunk_off(jrow, 8 * h2 + ch, D)) = pk;
-    }
-    tc::fence_async_smem();
+        for (int ch = 0; ch < 8; ++ch) {
+            uint4 pk;
+            pk.x = tc::pack_bf16(S[8 * ch + 0], S[8 * ch + 1]);
+            pk.y = tc::pack_bf16(S[8 * ch + 2], S[8 * ch + 3]);
+            pk.z = tc::pack_bf16(S[8 * ch + 4], S[8 * ch + 5]);
+            pk.w = tc::pack_bf16(S[8 * ch + 6], S[8 * ch + 7]);
+            *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw128_chunk_off(jrow, 8 * h2 + ch, D)) = pk;
+        }
+    };
+    stage_state();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tbase = *tslot;
     const uint32_t lane_base = tbase + ((uint32_t)(32 * q4) << 16);
-    uint32_t phase = 0;
+    uint32_t phase = 0, ld_phase = 0;
 
-    for (int64_t t0 = s0; t0 < s1; t0 += C) {
-        const int len = (int)min((int64_t)C, s1 - t0);
-        if (tid < C) sBeta[tid] = beta_next;
+    // prepare chunk c into buffer (c & 1): wait for its tiles, factors, then prefetch chunk c+1
+    auto prepare_factors = [&](int chunk) -> bool {
+        const int b = chunk & 1;
+        if (tid < C) reinterpret_cast<float*>(sm + OFF_BETA + b * 64)[tid] = beta_next;
         if (tid == 0 && !tc::mbar_wait(bar_ld, ld_phase, WAIT_LIMIT)) *abort_flag = 1u;
         ld_phase ^= 1u;
         __syncthreads();
-        if (*abort_flag) break;
-
-        // ---------------- gate + per-token factors (kda_gate / kda_ut_wy prologue)
-        if (tid < D) {
-            const int c = tid;
-            float Gr[C];
-            float G = 0.f;
-#pragma unroll
-            for (int r = 0; r < C; ++r) {
-                float g = 0.f;
-                if (r < len) g = log_decay(__bfloat162float(tz[r * D + c]), expA, g_min);
-                G += g;
-                Gr[r] = G;
-            }
-            const float eGC = expf(G);
-            sGC[c] = eGC;
-            uint32_t xpk[C / 2], kpk[C / 2], kpl[C / 2];
-#pragma unroll
-            for (int r = 0; r < C; r += 2) {
-                float xv[2], kt[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int rr = r + e;
-                    float kv = 0.f, qv = 0.f;
-                    if (rr < len) {
-                        kv = __bfloat162float(tk[rr * D + c]);
-                        qv = __bfloat162float(tq[rr * D + c]);
-                    }
-                    const float eG = expf(Gr[rr]);       // Gamma_r in [e^-80, 1]
-                    const float ieG = __frcp_rn(eG);      // 1 / Gamma_r in [1, e^80]
-                    const float ll = kv * eG;
-                    __nv_bfloat16 hi, lo;
-                    sLl[rr * LROW + c] = __float2bfloat16_rn(ll);
-                    split_bf16(qv * eG, hi, lo);
-                    sQl[rr * LROW + c] = hi;
-                    sQll[rr * LROW + c] = lo;
-                    *reinterpret_cast<__nv_bfloat16*>(sm + OFF_WQ + tc::sw128_off(C + rr, c, 2 * C)) = hi;
-                    split_bf16(kv * ieG, hi, lo);
-                    sKd[rr * LROW + c] = hi;
-                    sKdl[rr * LROW + c] = lo;
-                    xv[e] = ll;
-                    kt[e] = kv * (eGC * ieG);            // k Gamma_C / Gamma_r <= 1
-                }
-                xpk[r / 2] = tc::pack_bf16(xv[0], xv[1]);
-                __nv_bfloat162 kh = __floats2bfloat162_rn(kt[0], kt[1]);
-                const float2 khf = __bfloat1622float2(kh);
-                __nv_bfloat162 kl = __floats2bfloat162_rn(kt[0] - khf.x, kt[1] - khf.y);
-                kpk[r / 2] = *reinterpret_cast<uint32_t*>(&kh);
-                kpl[r / 2] = *reinterpret_cast<uint32_t*>(&kl);
-            }
-            *reinterpret_cast<uint4*>(sm + OFF_XT + tc::none_off(c, 0)) = make_uint4(xpk[0], xpk[1], xpk[2], xpk[3]);
-            *reinterpret_cast<uint4*>(sm + OFF_XT + tc::none_off(c, 8)) = make_uint4(xpk[4], xpk[5], xpk[6], xpk[7]);
-            *reinterpret_cast<uint4*>(sm + OFF_KT + tc::none_off(c, 0)) = make_uint4(kpk[0], kpk[1], kpk[2], kpk[3]);
-            *reinterpret_cast<uint4*>(sm + OFF_KT + tc::none_off(c, 8)) = make_uint4(kpk[4], kpk[5], kpk[6], kpk[7]);
-            *reinterpret_cast<uint4*>(sm + OFF_KTL + tc::none_off(c, 0)) = make_uint4(kpl[0], kpl[1], kpl[2], kpl[3]);
-            *reinterpret_cast<uint4*>(sm + OFF_KTL + tc::none_off(c, 8)) = make_uint4(kpl[4], kpl[5], kpl[6], kpl[7]);
-        } else {
-            // V^T rows as given (beta is applied through T')
-            const int j = tid - D;
-            uint32_t vpk[C / 2];
-#pragma unroll
-            for (int r = 0; r < C; r += 2) {
-                const __nv_bfloat16 zero = __float2bfloat16_rn(0.f);
-                __nv_bfloat162 pr;
-                pr.x = (r < len) ? tv[r * D + j] : zero;
-                pr.y = (r + 1 < len) ? tv[(r + 1) * D + j] : zero;
-                vpk[r / 2] = *reinterpret_cast<uint32_t*>(&pr);
-            }
-            *reinterpret_cast<uint4*>(sm + OFF_VT + tc::none_off(j, 0)) = make_uint4(vpk[0], vpk[1], vpk[2], vpk[3]);
-            *reinterpret_cast<uint4*>(sm + OFF_VT + tc::none_off(j, 8)) = make_uint4(vpk[4], vpk[5], vpk[6], vpk[7]);
+        if (*abort_flag) return false;
+        prep_factors(x, chunk_len(chunk), b);
+        __syncthreads();  // stage consumed
+        if (chunk + 1 < nchunks) {
+            if (tid == 0) issue_tiles(chunk + 1);
+            if (tid < C) beta_next = load_beta(chunk + 1);
         }
-        __syncthreads();
-
-        // the staged tiles are consumed: fetch the next chunk's while this one computes
-        if (t0 + C < s1) {
-            if (tid == 0) {
-                tc::fence_async_smem();
-                tc::mbar_arrive_expect_tx(bar_ld, 4 * STAGE_TILE);
-                const int tn = (int)(t0 + C);
-                tc::tma_load_3d(sm + OFF_STAGE, &maps.q, 0, h, tn, bar_ld);
-                tc::tma_load_3d(sm + OFF_STAGE + STAGE_TILE, &maps.k, 0, h, tn, bar_ld);
-                tc::tma_load_3d(sm + OFF_STAGE + 2 * STAGE_TILE, &maps.v, 0, h, tn, bar_ld);
-                tc::tma_load_3d(sm + OFF_STAGE + 3 * STAGE_TILE, &maps.z, 0, h, tn, bar_ld);
-            }
-            if (tid < C) beta_next = (t0 + C + tid < s1) ? a.beta[(t0 + C + tid) * H + h] : 0.f;
+        return true;
+    };
+    auto issue_mw_mu = [&](int b) {  // thread 0: W^T = (K Gamma)^T T'^T, U~^T = V^T T'^T
+        (void)b;
+        const uint32_t id16 = tc::idesc_bf16(128, 16);
+        const uint64_t dT = tc::desc_none(tc::smem_u32(sm + OFF_T));
+        const uint64_t dTl = tc::desc_none(tc::smem_u32(sm + OFF_T + SMALL_TILE));
+        const uint64_t dX = tc::desc_none(tc::smem_u32(sm + OFF_XT));
+        const uint64_t dV = tc::desc_none(tc::smem_u32(sm + OFF_VT));
+        tc::umma(tbase + TM_W, dX, dT, id16, 0u);
+        tc::umma(tbase + TM_W, dX, dTl, id16, 1u);
+        tc::umma(tbase + TM_U, dV, dT, id16, 0u);
+        tc::umma(tbase + TM_U, dV, dTl, id16, 1u);
+    };
+    auto issue_m1 = [&](int b) {  // thread 0: D1 = S^T [W ; Q Gamma]^T (M = 128, N = 32, K = 128)
+        const uint32_t id32 = tc::idesc_bf16(128, 2 * C);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
+            tc::umma(tbase + TM_D1, tc::desc_sw128(tc::smem_u32(sm + OFF_S + kb * 16384 + off)),
+                     tc::desc_sw128(tc::smem_u32(sm + OFF_WQ + b * 8192 + kb * (2 * C * 128) + off)), id32,
+                     ks > 0 ? 1u : 0u);
         }
-
-        // ---------------- A (warp 0) and the two halves of P (warps 1, 2): 16x16, K = 128, mma.sync
-        if (w < 3) {
-            const int g = lane >> 2, t = lane & 3;
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            if (w == 0) {
-                mma_rows16(acc, sLl, sKd, lane);
-            } else if (w == 1) {
-                mma_rows16(acc, sQl, sKd, lane);
-                mma_rows16(acc, sQl, sKdl, lane);
-            } else {
-                mma_rows16(acc, sQll, sKd, lane);
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int r = g + ((e >> 1) << 3);
-                    const int i = 8 * nt + 2 * t + (e & 1);
-                    if (w == 0) {
-                        sA[r * C + i] = (i < r) ? sBeta[r] * acc[nt][e] : 0.f;
-                    } else {
-                        sPf[(w - 1) * C * C + r * C + i] = acc[nt][e];
-                    }
-                }
-            }
-        }
-        __syncthreads();
-
-        // ---------------- T = (I + A)^-1 by forward substitution (lane = column); T' = T diag(beta)
-        if (w == 0 && lane < C) {
-            const int j = lane;
-            const float bj = sBeta[j];
-            float tcol[C];
-#pragma unroll
-            for (int r = 0; r < C; ++r) {
-                float x = (r == j) ? 1.f : 0.f;
-#pragma unroll
-                for (int i = 0; i < r; ++i) x -= sA[r * C + i] * tcol[i];
-                tcol[r] = x;
-            }
-#pragma unroll
-            for (int r = 0; r < C; ++r) {
-                __nv_bfloat16 hi, lo;
-                split_bf16(tcol[r] * bj, hi, lo);
-                *reinterpret_cast<__nv_bfloat16*>(sm + OFF_T + tc::none_off(r, j)) = hi;
-                *reinterpret_cast<__nv_bfloat16*>(sm + OFF_TL + tc::none_off(r, j)) = lo;
-            }
-        } else if (tid >= 128) {
-            // P = tril_incl(sum of the partial products), as a hi/lo pair
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int idx = 2 * (tid - 128) + e;
-                const int r = idx >> 4, i = idx & 15;
-                const float pv = (i <= r) ? sPf[idx] + sPf[C * C + idx] : 0.f;
-                __nv_bfloat16 hi, lo;
-                split_bf16(pv, hi, lo);
-                *reinterpret_cast<__nv_bfloat16*>(sm + OFF_P + tc::none_off(r, i)) = hi;
-                *reinterpret_cast<__nv_bfloat16*>(sm + OFF_PL + tc::none_off(r, i)) = lo;
-            }
-        }
-        tc_publish();
-
-        // ---------------- W^T = (K Gamma)^T T'^T, U~^T = V^T T'^T  (T' = hi + lo)
-        if (tid == 0) {
-            const uint32_t id16 = tc::idesc_bf16(128, 16);
-            const uint64_t dT = tc::desc_none(tc::smem_u32(sm + OFF_T));
-            const uint64_t dTl = tc::desc_none(tc::smem_u32(sm + OFF_TL));
-            const uint64_t dX = tc::desc_none(tc::smem_u32(sm + OFF_XT));
-            const uint64_t dV = tc::desc_none(tc::smem_u32(sm + OFF_VT));
-            tc::umma(tbase + TM_W, dX, dT, id16, 0u);
-            tc::umma(tbase + TM_W, dX, dTl, id16, 1u);
-            tc::umma(tbase + TM_U, dV, dT, id16, 0u);
-            tc::umma(tbase + TM_U, dV, dTl, id16, 1u);
-        }
-        if (!tc_join(bar, phase, abort_flag)) break;
-
-        // ---------------- W -> rows 0..15 of the [W ; Q Gamma] operand
+    };
+    auto transpose_w = [&](int b) {  // warps 0..3: W^T (TMEM, lanes = c) -> rows 0..15 of WQ[b]
         if (w < 4) {
-            const int c = jrow;
             uint32_t v[16];
             KDA_TMEM_LD16(lane_base + TM_W, v);
             tc::tmem_wait_ld();
+            unsigned char* wq = sm + OFF_WQ + b * 8192;
 #pragma unroll
-            for (int r = 0; r < C; ++r) st_bf16(sm, OFF_WQ + tc::sw128_off(r, c, 2 * C), u2f(v[r]));
+            for (int r = 0; r < C; ++r) st_bf16(wq, tc::sw128_off(r, jrow, 2 * C), __float2bfloat16_rn(u2f(v[r])));
         }
-        tc_publish();
+    };
 
-        // ---------------- D1 = S^T [W ; Q Gamma]^T  (M = 128, N = 32, K = 128)
-        if (tid == 0) {
-            const uint32_t id32 = tc::idesc_bf16(128, 2 * C);
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
-                tc::umma(tbase + TM_D1, tc::desc_sw128(tc::smem_u32(sm + OFF_S + kb * 16384 + off)),
-                         tc::desc_sw128(tc::smem_u32(sm + OFF_WQ + kb * (2 * C * 128) + off)), id32, ks > 0 ? 1u : 0u);
-            }
+    bool ok = true;
+    if (nchunks > 0) {
+        // prologue: chunk 0 prepared and its state-read issued
+        ok = prepare_factors(0);
+        if (ok) {
+            prep_solve(x, 0);
+            tc_publish();
+            if (tid == 0) issue_mw_mu(0);
+            ok = tc_join(bar, phase, abort_flag);
         }
-        if (!tc_join(bar, phase, abort_flag)) break;
+        if (ok) {
+            transpose_w(0);
+            tc_publish();
+            if (tid == 0) issue_m1(0);
+        }
+    }
 
-        // ---------------- U^T = U~^T - (W S)^T  -> bf16 operand
+    for (int ch = 0; ok && ch < nchunks; ++ch) {
+        const int b = ch & 1, nb = b ^ 1;
+        const bool has_next = ch + 1 < nchunks;
+        const int64_t t0 = s0 + (int64_t)ch * C;
+        const int len = chunk_len(ch);
+
+        // (1) while the state-read of chunk ch runs: factors of chunk ch+1
+        if (has_next && !(ok = prepare_factors(ch + 1))) break;
+
+        // (2) U^T = U~^T - (W S)^T as a hi/lo pair
+        if (!(ok = tc_join(bar, phase, abort_flag))) break;
         {
             uint32_t dv[8], uv[8];
             KDA_TMEM_LD8(lane_base + TM_D1 + 8 * h2, dv);
@@ -448,51 +492,56 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_fwd_tc_kernel(PrefillAr
                 lo[e] = *reinterpret_cast<uint32_t*>(&l2v);
             }
             *reinterpret_cast<uint4*>(sm + OFF_UT + tc::none_off(jrow, 8 * h2)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(sm + OFF_UL + tc::none_off(jrow, 8 * h2)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<uint4*>(sm + OFF_UT + NONE_TILE + tc::none_off(jrow, 8 * h2)) =
+                make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
         tc_publish();
 
-        // ---------------- O^T += U^T P^T ;  dS^T = U^T (K Gamma_C / Gamma)  (hi/lo pairs)
+        // (3) O^T += U^T P^T and dS^T = U^T (K Gamma_C / Gamma), each as hi*hi + hi*lo + lo*hi
         if (tid == 0) {
             const uint32_t id16 = tc::idesc_bf16(128, 16);
+            const uint32_t id128 = tc::idesc_bf16(128, 128);
             const uint64_t dU = tc::desc_none(tc::smem_u32(sm + OFF_UT));
-            const uint64_t dUl = tc::desc_none(tc::smem_u32(sm + OFF_UL));
-            const uint64_t dP = tc::desc_none(tc::smem_u32(sm + OFF_P));
-            const uint64_t dPl = tc::desc_none(tc::smem_u32(sm + OFF_PL));
+            const uint64_t dUl = tc::desc_none(tc::smem_u32(sm + OFF_UT + NONE_TILE));
+            const uint64_t dP = tc::desc_none(tc::smem_u32(sm + OFF_P + b * 1024));
+            const uint64_t dPl = tc::desc_none(tc::smem_u32(sm + OFF_P + b * 1024 + SMALL_TILE));
+            const uint64_t dK = tc::desc_none(tc::smem_u32(sm + OFF_KT + b * 8192));
+            const uint64_t dKl = tc::desc_none(tc::smem_u32(sm + OFF_KT + b * 8192 + NONE_TILE));
             tc::umma(tbase + TM_D1 + C, dU, dP, id16, 1u);
             tc::umma(tbase + TM_D1 + C, dU, dPl, id16, 1u);
             tc::umma(tbase + TM_D1 + C, dUl, dP, id16, 1u);
-            const uint32_t id128 = tc::idesc_bf16(128, 128);
-            const uint64_t dK = tc::desc_none(tc::smem_u32(sm + OFF_KT));
-            const uint64_t dKl = tc::desc_none(tc::smem_u32(sm + OFF_KTL));
             tc::umma(tbase + TM_D3, dU, dK, id128, 0u);
             tc::umma(tbase + TM_D3, dU, dKl, id128, 1u);
             tc::umma(tbase + TM_D3, dUl, dK, id128, 1u);
         }
-        if (!tc_join(bar, phase, abort_flag)) break;
 
-        // ---------------- S <- Diag(Gamma_C) S + dS ; outputs
+        // (4) while those run: A, P, T' of chunk ch+1, then its W / U~ products
+        if (has_next) {
+            prep_solve(x, nb);
+            tc_publish();
+            if (tid == 0) issue_mw_mu(nb);
+        }
+        if (!(ok = tc_join(bar, phase, abort_flag))) break;
+
+        // (5) S <- Diag(Gamma_C) S + dS ; outputs of chunk ch ; W of chunk ch+1
         {
+            const float* gc = reinterpret_cast<const float*>(sm + OFF_GC + b * 512) + 64 * h2;
 #pragma unroll
             for (int blk = 0; blk < 4; ++blk) {
                 uint32_t v[16];
                 KDA_TMEM_LD16(lane_base + TM_D3 + 64 * h2 + 16 * blk, v);
                 tc::tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int cc = 16 * blk + e;
-                    S[cc] = sGC[64 * h2 + cc] * S[cc] + u2f(v[e]);
+                for (int e4 = 0; e4 < 4; ++e4) {
+                    const float4 g4 = *reinterpret_cast<const float4*>(gc + 16 * blk + 4 * e4);
+                    const int cc = 16 * blk + 4 * e4;
+                    S[cc + 0] = g4.x * S[cc + 0] + u2f(v[4 * e4 + 0]);
+                    S[cc + 1] = g4.y * S[cc + 1] + u2f(v[4 * e4 + 1]);
+                    S[cc + 2] = g4.z * S[cc + 2] + u2f(v[4 * e4 + 2]);
+                    S[cc + 3] = g4.w * S[cc + 3] + u2f(v[4 * e4 + 3]);
                 }
             }
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                uint4 pk;
-                pk.x = tc::pack_bf16(S[8 * ch + 0], S[8 * ch + 1]);
-                pk.y = tc::pack_bf16(S[8 * ch + 2], S[8 * ch + 3]);
-                pk.z = tc::pack_bf16(S[8 * ch + 4], S[8 * ch + 5]);
-                pk.w = tc::pack_bf16(S[8 * ch + 6], S[8 * ch + 7]);
-                *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw128_chunk_off(jrow, 8 * h2 + ch, D)) = pk;
-            }
+            stage_state();
             uint32_t ov[8];
             KDA_TMEM_LD8(lane_base + TM_D1 + C + 8 * h2, ov);
             tc::tmem_wait_ld();
@@ -502,10 +551,14 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_fwd_tc_kernel(PrefillAr
                 if (r < len) op[((t0 + r) * H + h) * D + jrow] = __float2bfloat16_rn(u2f(ov[e]));
             }
         }
-        tc_publish();
+        if (has_next) {
+            transpose_w(nb);
+            tc_publish();
+            if (tid == 0) issue_m1(nb);
+        }
     }
 
-    if (*abort_flag) {
+    if (!ok || *abort_flag) {
         if (tid == 0) atomicOr(a.check, kCheckTimeout);
     } else if (a.s_final) {
 #pragma unroll
