@@ -116,6 +116,35 @@ kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const 
                              const kda_problem_t* problem, void* stream);
 
 /*
+ * kda_forward for callers that cannot allocate device memory: a library or plugin that runs
+ * inside a host application which owns every device allocation (its own pool or arena) and gives
+ * the plugin no allocator, or a latency-critical path that must not enter the driver's allocator.
+ * Such callers still provide every input and output buffer; only the scratch is taken care of.
+ *
+ * The paper has no counterpart to this entry point: it is a memory-management convenience.
+ *
+ * Scratch comes from one array of KDA_STATIC_SCRATCH_BYTES that the library keeps in device
+ * memory of every GPU that loads it, for the life of the process.  The call allocates nothing and
+ * calls no allocating routine.  Arguments, layouts and results are those of kda_forward (same
+ * kernels), without `workspace` / `workspace_bytes`.
+ *   - A problem whose kda_forward_workspace_bytes() exceeds KDA_STATIC_SCRATCH_BYTES is rejected
+ *     on the host with KDA_ERR_WORKSPACE before anything is launched.  (bf16 problems with
+ *     d_k = d_v = 128 need only a few hundred bytes; the fp32 path needs 4 (2 d_k + d_v) bytes
+ *     per token and head.)
+ *   - The first call on each device looks up that device's copy of the array, with the device
+ *     current; make that first call before any stream capture.
+ *   - All calls on a device share the one array, and it keeps the last call's contents (the
+ *     check word is cleared at the start of every call).  Calls whose GPU work overlaps -- on
+ *     different streams, or from different host threads -- race on it; serialise them.
+ *   - kda_workspace_status() cannot be used with this entry point (there is no caller workspace).
+ */
+#define KDA_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
+kda_status_t kda_forward_static_scratch(const void* q, const void* k, const void* v, const void* z,
+                                        const float* A, const float* beta, const float* initial_state,
+                                        const int32_t* cu_seqlens, void* out, float* final_state,
+                                        const kda_problem_t* problem, void* stream);
+
+/*
  * Synchronises `stream` and reads the device-side check word that kda_forward keeps in its
  * workspace: KDA_OK, or KDA_ERR_DEVICE_CHECK if a sequence was skipped because its cu_seqlens
  * entries were invalid, or KDA_ERR_TIMEOUT if a bounded device wait gave up.  The word is

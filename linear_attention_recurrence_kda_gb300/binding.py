@@ -32,7 +32,11 @@ G_MIN = -5.0
 
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_forward_workspace_bytes", "kda_forward", "kda_decode_step", "kda_workspace_status",
-           "kda_status_string", "kda_profile_enable", "kda_profile_read", "kda_abi_version")
+           "kda_status_string", "kda_profile_enable", "kda_profile_read", "kda_abi_version",
+           "kda_forward_static_scratch")
+
+# Size of the library's own scratch array used by kda_forward_static_scratch.
+KDA_STATIC_SCRATCH_BYTES = 8 << 20
 
 
 class KdaProblem(ctypes.Structure):
@@ -82,6 +86,8 @@ def lib():
             L.kda_profile_enable.argtypes = [ctypes.c_int]
             L.kda_profile_read.restype = ctypes.c_int32
             L.kda_profile_read.argtypes = [ctypes.POINTER(KdaKernelTime), ctypes.c_int32]
+            L.kda_forward_static_scratch.restype = ctypes.c_int
+            L.kda_forward_static_scratch.argtypes = [_vp] * 10 + [P, _vp]
             L.kda_abi_version.restype = ctypes.c_uint32
             L.kda_abi_version.argtypes = []
             _lib = L
@@ -173,6 +179,47 @@ def kda_forward(q, k, v, z, A, beta, initial_state=None, cu_seqlens=None, out=No
                            ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream(stream))
     if st != KDA_OK:
         raise KdaError(st, "kda_forward")
+    return out, final_state
+
+
+def kda_forward_static_scratch(q, k, v, z, A, beta, initial_state=None, cu_seqlens=None, out=None,
+                               final_state=None, max_seqlen: Optional[int] = None, g_min: float = G_MIN,
+                               stream=None, want_final: bool = True):
+    """kda_forward without a workspace argument, for callers that cannot allocate device scratch
+    (see include/kda.h): the library's own fixed-size device array is used instead.  Arguments and
+    results as in :func:`kda_forward`; problems needing more than KDA_STATIC_SCRATCH_BYTES of
+    scratch raise KdaError(KDA_ERR_WORKSPACE).  Calls that overlap on the GPU race on the array."""
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    dev = k.device
+    dt = k.dtype
+    if cu_seqlens is not None:
+        N = cu_seqlens.shape[0] - 1
+        _need(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,), dev)
+        if max_seqlen is None:
+            max_seqlen = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if N > 0 else 0
+    else:
+        N = initial_state.shape[0] if initial_state is not None else 1
+        max_seqlen = T // N
+    for name, t, shp in (("q", q, (T, H, dk)), ("k", k, (T, H, dk)), ("z", z, (T, H, dk)), ("v", v, (T, H, dv))):
+        _need(t, name, dt, shp, dev)
+    _need(A, "A", torch.float32, (H,), dev)
+    _need(beta, "beta", torch.float32, (T, H), dev)
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32, (N, H, dk, dv), dev)
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=dt, device=dev)
+    _need(out, "out", dt, (T, H, dv), dev)
+    if final_state is None and want_final:
+        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    if final_state is not None:
+        _need(final_state, "final_state", torch.float32, (N, H, dk, dv), dev)
+    prob = make_problem(N, T, max_seqlen, H, dk, dv, dt, g_min)
+    st = lib().kda_forward_static_scratch(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(beta),
+                                          _ptr(initial_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+                                          ctypes.byref(prob), _stream(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_forward_static_scratch")
     return out, final_state
 
 
