@@ -90,8 +90,11 @@ size_t kda_forward_workspace_bytes(const kda_problem_t* problem);
  *   out           : [T_tot,H,d_v] io dtype.  Must not overlap any input.
  *   final_state   : [N,H,d_k,d_v] fp32, or NULL (not written).  May be the same pointer as
  *                   initial_state (in-place carry); any other overlap is rejected.
- *   workspace     : device scratch of at least kda_forward_workspace_bytes(problem) bytes,
- *                   256-byte aligned, not shared with a concurrently running call.
+ *   workspace     : device scratch, 256-byte aligned, not shared with a concurrently running
+ *                   call.  kda_forward_workspace_bytes(problem) bytes allow the fastest plan; a
+ *                   smaller workspace makes long sequences use fewer parallel segments (down to
+ *                   none), and one below the unsegmented minimum is rejected (KDA_ERR_WORKSPACE).
+ *                   Results do not depend on the plan beyond rounding.
  *
  * Returns KDA_OK once all kernels are enqueued on `stream`.
  */
@@ -127,10 +130,10 @@ kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const 
  * memory of every GPU that loads it, for the life of the process.  The call allocates nothing and
  * calls no allocating routine.  Arguments, layouts and results are those of kda_forward (same
  * kernels), without `workspace` / `workspace_bytes`.
- *   - A problem whose kda_forward_workspace_bytes() exceeds KDA_STATIC_SCRATCH_BYTES is rejected
- *     on the host with KDA_ERR_WORKSPACE before anything is launched.  (bf16 problems with
- *     d_k = d_v = 128 need only a few hundred bytes; the fp32 path needs 4 (2 d_k + d_v) bytes
- *     per token and head.)
+ *   - A problem whose smallest workspace exceeds KDA_STATIC_SCRATCH_BYTES is rejected on the host
+ *     with KDA_ERR_WORKSPACE before anything is launched.  (bf16 problems with d_k = d_v = 128
+ *     need only a few hundred bytes, and use as many parallel sequence segments as the array
+ *     holds; the fp32 path needs 4 (2 d_k + d_v) bytes per token and head.)
  *   - The first call on each device looks up that device's copy of the array, with the device
  *     current; make that first call before any stream capture.
  *   - All calls on a device share the one array, and it keeps the last call's contents (the

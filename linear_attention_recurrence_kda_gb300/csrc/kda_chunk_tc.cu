@@ -1,6 +1,6 @@
 // kda_chunk_tc.cu -- fused KDA prefill on the sm_103a tensor cores (bf16 inputs, d_k = d_v = 128).
 //
-// One CTA walks one sequence of one head in 16-token chunks and does, per chunk, every stage of
+// One CTA walks one sequence of one head in 16-token chunks and computes, per chunk, every stage of
 // the chunk form of Equation 1 ("Kimi K3: the paper and proofs side by side", section 2.1.1):
 //
 //   gate      g = g_min sigmoid(e^{A_h} z)  (Equation 5), G_r = in-chunk inclusive cumsum,
@@ -33,11 +33,15 @@
 // K/Gamma inside P, P and U in U P^T, U and K Gamma_C/Gamma in the state update, and T'.  The
 // remaining bf16 roundings (the state as the read operand, W, K Gamma) reach the outputs only
 // through products that the decay keeps small.
-// The loop is software-pipelined across chunks: while the tensor core runs chunk n's state-read,
-// output and state-update products, all 256 threads prepare chunk n+1 (gate, factors, A, P, T')
-// into the other half of double-buffered operand tiles, and TMA fetches chunk n+2's inputs.
-// Every mbarrier wait is bounded; a wait that gives up raises the timeout bit of the check word
-// and the CTA stops cleanly.
+//
+// Warp specialisation.  Warps 8..15 (producer) prepare chunk n+1 -- TMA tile loads, gate and
+// factors, A, P and T', the W / U~ products and W's transposition into the read operand -- while
+// warps 0..7 (consumer) run chunk n's state pass: the state read, U, the output and state-update
+// products, the state update and the outputs.  The per-chunk operands the consumer reads are
+// double-buffered by chunk parity; the two groups hand them over with named barriers (FULL[b]:
+// producer -> consumer, EMPTY[b]: consumer -> producer).  Every mbarrier wait is bounded; a wait
+// that gives up raises the timeout bit of the check word, and from then on both groups skip all
+// work but still walk the whole barrier protocol, so neither can be left waiting on the other.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -52,9 +56,16 @@ namespace {
 
 constexpr int D = 128;            // d_k = d_v
 constexpr int C = kChunk;         // 16
-constexpr int NTHREADS = 256;
+constexpr int NTHREADS = 512;     // 8 consumer + 8 producer warps
+constexpr int NGROUP = 256;       // threads per group
 constexpr int LROW = 136;         // padded row (elements) of the mma.sync operand tiles
-constexpr uint32_t WAIT_LIMIT = 1u << 24;
+constexpr uint32_t WAIT_LIMIT = 1u << 17;  // tries of up to 20 us each: ~2.6 s at most
+
+// named barriers (0 is __syncthreads)
+constexpr uint32_t NB_CONS = 1;   // consumer group only
+constexpr uint32_t NB_PROD = 2;   // producer group only
+constexpr uint32_t NB_FULL = 3;   // + b: chunk parity b's operands are ready (512 threads)
+constexpr uint32_t NB_EMPTY = 5;  // + b: chunk parity b's operands may be overwritten (512 threads)
 
 // shared-memory map (bytes from a 1024-aligned base); "[2]" = double-buffered by chunk parity
 constexpr uint32_t OFF_S = 0;          // S^T [128 j][128 c] SW128                      32768
@@ -70,28 +81,47 @@ constexpr uint32_t OFF_LL = 101376;    // K Gamma [16][LROW] bf16               
 constexpr uint32_t OFF_QL = 105728;    // Q Gamma hi, lo                                2 x 4352
 constexpr uint32_t OFF_KD = 114432;    // K / Gamma hi, lo                              2 x 4352
 constexpr uint32_t OFF_A = 123136;     // A fp32 [16][16]                               1024
-constexpr uint32_t OFF_PF = 124160;    // P partial sums fp32 [2][16][16]               2048
-constexpr uint32_t OFF_GC = 126208;    // [2] Gamma_C fp32 [128]                         2 x 512
-constexpr uint32_t OFF_HS = 127232;    // per-channel half-chunk log-decay sums [2][128] 1024
-constexpr uint32_t OFF_BETA = 128256;  // [2] beta [16]                                  2 x 64
-constexpr uint32_t OFF_BAR = 128384;   // mbarrier of the tensor-core commits           8
-constexpr uint32_t OFF_BARLD = 128392; // mbarrier of the TMA tile loads                8
-constexpr uint32_t OFF_TSLOT = 128400; // TMEM base address                             4
-constexpr uint32_t OFF_ABORT = 128404; // stop flag                                     4
-constexpr uint32_t SMEM_USED = 128408;
+constexpr uint32_t OFF_PART = 124160;  // k-step partial products fp32 [8 warps][16][16] 8192
+constexpr uint32_t OFF_GC = 132352;    // [2] Gamma_C fp32 [128]                         2 x 512
+constexpr uint32_t OFF_HS = 133376;    // per-channel half-chunk log-decay sums [2][128] 1024
+constexpr uint32_t OFF_BETA = 134400;  // beta [16]                                      64
+constexpr uint32_t OFF_BARC = 134464;  // mbarrier: consumer tensor-core commits        8
+constexpr uint32_t OFF_BARP = 134472;  // mbarrier: producer tensor-core commits        8
+constexpr uint32_t OFF_BARLD = 134480; // mbarrier: TMA tile loads                      8
+constexpr uint32_t OFF_TSLOT = 134488; // TMEM base address                             4
+constexpr uint32_t OFF_ABORT = 134492; // stop flag                                     4
+constexpr uint32_t SMEM_USED = 134496;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
 constexpr uint32_t STAGE_TILE = C * D * 2;  // 4096 bytes per tensor and chunk
 constexpr uint32_t NONE_TILE = 4096;        // [128][16] bf16 NONE tile
 constexpr uint32_t SMALL_TILE = 512;        // [16][16] bf16 NONE tile
 
 // tensor-memory columns
-constexpr uint32_t TM_D1 = 0;    // [0,16): (W S)^T, [16,32): O^T
-constexpr uint32_t TM_W = 32;    // W^T  (lanes = c)
-constexpr uint32_t TM_U = 48;    // U~^T (lanes = j)
-constexpr uint32_t TM_D3 = 128;  // dS^T (lanes = j, columns = c)
+constexpr uint32_t TM_D1 = 0;    // consumer: [0,16) (W S)^T, [16,32) O^T
+constexpr uint32_t TM_W = 32;    // producer: W^T  (lanes = c)
+constexpr uint32_t TM_U = 48;    // producer -> consumer: [2] U~^T (lanes = j), 16 columns each
+constexpr uint32_t TM_D3 = 128;  // consumer: dS^T (lanes = j, columns = c)
 constexpr uint32_t TM_COLS = 256;
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_arrive(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Equation 5 with the fast exponential and division (relative error ~1e-6, far below bf16).
+__device__ __forceinline__ float log_decay_fast(float z, float expA, float g_min)
+{
+    const float x = expA * z;
+    const float e = __expf(-fabsf(x));
+    const float sig = (x >= 0.f) ? __fdividef(1.f, 1.f + e) : __fdividef(e, 1.f + e);
+    return g_min * sig;
+}
 
 __device__ __forceinline__ void st_bf16(unsigned char* base, uint32_t off, __nv_bfloat16 x)
 {
@@ -110,66 +140,49 @@ __device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b)
     return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
 }
 
-// acc[16 x 16] += L R^T over K = 128 (L, R: 16 rows of LROW bf16) with mma.sync m16n8k16.
-__device__ __forceinline__ void mma_rows16(float (&acc)[2][4], const __nv_bfloat16* L, const __nv_bfloat16* R, int lane)
+// Abort flag, read identically by every lane of the warp (it guards warp-collective instructions).
+__device__ __forceinline__ bool read_dead(const volatile uint32_t* abort_flag)
+{
+    return __any_sync(0xffffffffu, *abort_flag != 0u);
+}
+
+// Thread 0 of a group: commit its issued tensor-core work and wait (bounded) for it.
+__device__ __forceinline__ void commit_wait(uint64_t* bar, uint32_t phase, volatile uint32_t* abort_flag)
+{
+    tc::umma_commit(bar);
+    if (!tc::mbar_wait(bar, phase, WAIT_LIMIT)) *abort_flag = 1u;
+}
+
+// 16x16 partial product over one k-step (16 channels): acc += L[:, k0:k0+16] R[:, k0:k0+16]^T.
+__device__ __forceinline__ void mma_kstep(float (&acc)[2][4], const __nv_bfloat16* L, const __nv_bfloat16* R, int k0,
+                                          int lane)
 {
     const int g = lane >> 2, t = lane & 3;
+    uint32_t af[4];
+    af[0] = *reinterpret_cast<const uint32_t*>(L + g * LROW + k0 + 2 * t);
+    af[1] = *reinterpret_cast<const uint32_t*>(L + (g + 8) * LROW + k0 + 2 * t);
+    af[2] = *reinterpret_cast<const uint32_t*>(L + g * LROW + k0 + 8 + 2 * t);
+    af[3] = *reinterpret_cast<const uint32_t*>(L + (g + 8) * LROW + k0 + 8 + 2 * t);
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-        const int k0 = 16 * ks;
-        uint32_t af[4];
-        af[0] = *reinterpret_cast<const uint32_t*>(L + g * LROW + k0 + 2 * t);
-        af[1] = *reinterpret_cast<const uint32_t*>(L + (g + 8) * LROW + k0 + 2 * t);
-        af[2] = *reinterpret_cast<const uint32_t*>(L + g * LROW + k0 + 8 + 2 * t);
-        af[3] = *reinterpret_cast<const uint32_t*>(L + (g + 8) * LROW + k0 + 8 + 2 * t);
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int n0 = 8 * nt;
-            const uint32_t b0 = *reinterpret_cast<const uint32_t*>(R + (n0 + g) * LROW + k0 + 2 * t);
-            const uint32_t b1 = *reinterpret_cast<const uint32_t*>(R + (n0 + g) * LROW + k0 + 8 + 2 * t);
-            tc::mma16816(acc[nt], af, b0, b1);
-        }
+    for (int nt = 0; nt < 2; ++nt) {
+        const int n0 = 8 * nt;
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(R + (n0 + g) * LROW + k0 + 2 * t);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(R + (n0 + g) * LROW + k0 + 8 + 2 * t);
+        tc::mma16816(acc[nt], af, b0, b1);
     }
 }
 
-// Commit the issued tensor-core work, bounded wait by thread 0, CTA barrier.  False: stop.
-__device__ __forceinline__ bool tc_join(uint64_t* bar, uint32_t& phase, volatile uint32_t* abort_flag)
-{
-    if (threadIdx.x == 0) {
-        tc::umma_commit(bar);
-        if (!tc::mbar_wait(bar, phase, WAIT_LIMIT)) *abort_flag = 1u;
-    }
-    phase ^= 1u;
-    __syncthreads();
-    tc::fence_after_sync();
-    return *abort_flag == 0u;
-}
+// ---------------------------------------------------------------------------- producer stages
 
-// Generic-proxy writes to operand tiles -> visible to the tensor core; CTA barrier.
-__device__ __forceinline__ void tc_publish()
-{
-    tc::fence_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-}
-
-struct Ctx {
-    unsigned char* sm;
-    int tid, w, lane;
-    int h, H;
-    float expA, g_min;
-};
-
-// Gate, in-chunk cumulative log-decay and every per-element factor of one chunk (all threads).
-// Thread (c, half) owns key/value channel c and tokens [8 half, 8 half + 8).
+// Gate, in-chunk cumulative log-decay and every per-element factor of one chunk (producer group).
+// Producer thread p owns key/value channel c = p % 128 and tokens [8 half, 8 half + 8), half = p / 128.
 // Writes: row-major K Gamma, Q Gamma (hi/lo), K/Gamma (hi/lo); WQ[b] rows 16..31 (Q Gamma hi);
-// (K Gamma)^T, V^T; KT[b] (K Gamma_C/Gamma hi/lo); GC[b] = Gamma_C.  Contains one CTA barrier.
-__device__ __forceinline__ void prep_factors(const Ctx& x, int len, int b)
+// (K Gamma)^T, V^T; KT[b] (K Gamma_C/Gamma hi/lo); GC[b] = Gamma_C.  One producer barrier inside.
+__device__ __forceinline__ void prep_factors(unsigned char* sm, int p, int len, int b, float expA, float g_min,
+                                             bool zero_v)
 {
-    unsigned char* sm = x.sm;
-    const int c = x.tid & (D - 1);
-    const int half = x.tid >> 7;
+    const int c = p & (D - 1);
+    const int half = p >> 7;
     const int r0 = 8 * half;
     const __nv_bfloat16* tq = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_STAGE);
     const __nv_bfloat16* tk = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_STAGE + STAGE_TILE);
@@ -178,28 +191,23 @@ __device__ __forceinline__ void prep_factors(const Ctx& x, int len, int b)
     float* hs = reinterpret_cast<float*>(sm + OFF_HS);
 
     float Gl[8], kv[8], qv[8];
-    uint32_t vpk[4];
+    __nv_bfloat16 vv[8];
     float acc = 0.f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
         const int r = r0 + e;
         const bool ok = r < len;
-        const float g = ok ? log_decay(__bfloat162float(tz[r * D + c]), x.expA, x.g_min) : 0.f;
+        const float g = ok ? log_decay_fast(__bfloat162float(tz[r * D + c]), expA, g_min) : 0.f;
         acc += g;
         Gl[e] = acc;
         kv[e] = ok ? __bfloat162float(tk[r * D + c]) : 0.f;
         qv[e] = ok ? __bfloat162float(tq[r * D + c]) : 0.f;
-    }
-#pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-        const __nv_bfloat16 z0 = __float2bfloat16_rn(0.f);
-        vpk[e / 2] = pack2((r0 + e < len) ? tv[(r0 + e) * D + c] : z0, (r0 + e + 1 < len) ? tv[(r0 + e + 1) * D + c] : z0);
+        vv[e] = (ok && !zero_v) ? tv[r * D + c] : __float2bfloat16_rn(0.f);
     }
     hs[half * D + c] = acc;
-    __syncthreads();
+    named_sync(NB_PROD, NGROUP);
     const float off = half ? hs[c] : 0.f;
-    const float GC = hs[c] + hs[D + c];
-    const float eGC = expf(GC);
+    const float eGC = __expf(hs[c] + hs[D + c]);
     if (half) reinterpret_cast<float*>(sm + OFF_GC + b * 512)[c] = eGC;
 
     __nv_bfloat16* sLl = reinterpret_cast<__nv_bfloat16*>(sm + OFF_LL);
@@ -212,8 +220,8 @@ __device__ __forceinline__ void prep_factors(const Ctx& x, int len, int b)
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
         const int r = r0 + e;
-        const float eG = expf(Gl[e] + off);      // Gamma_r in [e^-80, 1]
-        const float ieG = __frcp_rn(eG);          // 1 / Gamma_r in [1, e^80]
+        const float eG = __expf(Gl[e] + off);         // Gamma_r in [e^-80, 1]
+        const float ieG = __fdividef(1.f, eG);         // 1 / Gamma_r in [1, e^80]
         const float ll = kv[e] * eG;
         __nv_bfloat16 hi, lo;
         xt[e] = __float2bfloat16_rn(ll);
@@ -229,7 +237,8 @@ __device__ __forceinline__ void prep_factors(const Ctx& x, int len, int b)
     }
     *reinterpret_cast<uint4*>(sm + OFF_XT + tc::none_off(c, r0)) =
         make_uint4(pack2(xt[0], xt[1]), pack2(xt[2], xt[3]), pack2(xt[4], xt[5]), pack2(xt[6], xt[7]));
-    *reinterpret_cast<uint4*>(sm + OFF_VT + tc::none_off(c, r0)) = make_uint4(vpk[0], vpk[1], vpk[2], vpk[3]);
+    *reinterpret_cast<uint4*>(sm + OFF_VT + tc::none_off(c, r0)) =
+        make_uint4(pack2(vv[0], vv[1]), pack2(vv[2], vv[3]), pack2(vv[4], vv[5]), pack2(vv[6], vv[7]));
     unsigned char* kt = sm + OFF_KT + b * 8192;
     *reinterpret_cast<uint4*>(kt + tc::none_off(c, r0)) =
         make_uint4(pack2(kth[0], kth[1]), pack2(kth[2], kth[3]), pack2(kth[4], kth[5]), pack2(kth[6], kth[7]));
@@ -237,47 +246,61 @@ __device__ __forceinline__ void prep_factors(const Ctx& x, int len, int b)
         make_uint4(pack2(ktl[0], ktl[1]), pack2(ktl[2], ktl[3]), pack2(ktl[4], ktl[5]), pack2(ktl[6], ktl[7]));
 }
 
-// A, P (mma.sync), T = (I + A)^-1 and T' = T diag(beta) (hi/lo), P finalised into P[b] (hi/lo).
-// Contains one CTA barrier; the caller publishes afterwards.
-__device__ __forceinline__ void prep_solve(const Ctx& x, int b)
+// A and P over K = 128 with mma.sync, two k-steps per producer warp (warps 0..3: A, warps 4..7: P
+// as hi*hi + hi*lo + lo*hi), partial sums reduced in shared memory; then T = (I + A)^-1 by forward
+// substitution and T' = T diag(beta) (hi/lo), P finalised into P[b] (hi/lo).  Two producer barriers.
+__device__ __forceinline__ void prep_solve(unsigned char* sm, int p, int b)
 {
-    unsigned char* sm = x.sm;
-    const int w = x.w, lane = x.lane, tid = x.tid;
+    const int pw = p >> 5, lane = p & 31;
     float* sA = reinterpret_cast<float*>(sm + OFF_A);
-    float* sPf = reinterpret_cast<float*>(sm + OFF_PF);
-    const float* beta = reinterpret_cast<const float*>(sm + OFF_BETA + b * 64);
+    float* part = reinterpret_cast<float*>(sm + OFF_PART);
+    const float* beta = reinterpret_cast<const float*>(sm + OFF_BETA);
     const __nv_bfloat16* sLl = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_LL);
     const __nv_bfloat16* sQl = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_QL);
     const __nv_bfloat16* sQll = sQl + C * LROW;
     const __nv_bfloat16* sKd = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_KD);
     const __nv_bfloat16* sKdl = sKd + C * LROW;
-    if (w < 3) {
+    {
         const int g = lane >> 2, t = lane & 3;
+        const int k0 = 32 * (pw & 3);
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        if (w == 0) {
-            mma_rows16(acc, sLl, sKd, lane);
-        } else if (w == 1) {
-            mma_rows16(acc, sQl, sKd, lane);
-            mma_rows16(acc, sQl, sKdl, lane);
+        if (pw < 4) {
+            mma_kstep(acc, sLl, sKd, k0, lane);
+            mma_kstep(acc, sLl, sKd, k0 + 16, lane);
         } else {
-            mma_rows16(acc, sQll, sKd, lane);
-        }
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = g + ((e >> 1) << 3);
-                const int i = 8 * nt + 2 * t + (e & 1);
-                if (w == 0) {
-                    sA[r * C + i] = (i < r) ? beta[r] * acc[nt][e] : 0.f;
-                } else {
-                    sPf[(w - 1) * C * C + r * C + i] = acc[nt][e];
-                }
+            for (int kk = 0; kk < 32; kk += 16) {
+                mma_kstep(acc, sQl, sKd, k0 + kk, lane);
+                mma_kstep(acc, sQl, sKdl, k0 + kk, lane);
+                mma_kstep(acc, sQll, sKd, k0 + kk, lane);
             }
         }
+        float* pp = part + pw * C * C;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            *reinterpret_cast<float2*>(pp + g * C + 8 * nt + 2 * t) = make_float2(acc[nt][0], acc[nt][1]);
+            *reinterpret_cast<float2*>(pp + (g + 8) * C + 8 * nt + 2 * t) = make_float2(acc[nt][2], acc[nt][3]);
+        }
     }
-    __syncthreads();
-    if (w == 0 && lane < C) {
+    named_sync(NB_PROD, NGROUP);
+    {
+        const int idx = p;  // one entry of A and one of P per producer thread
+        const int r = idx >> 4, i = idx & 15;
+        float sa = 0.f, sp = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            sa += part[k * C * C + idx];
+            sp += part[(4 + k) * C * C + idx];
+        }
+        sA[idx] = (i < r) ? beta[r] * sa : 0.f;
+        __nv_bfloat16 hi, lo;
+        split_bf16((i <= r) ? sp : 0.f, hi, lo);
+        unsigned char* pb = sm + OFF_P + b * 1024;
+        st_bf16(pb, tc::none_off(r, i), hi);
+        st_bf16(pb, SMALL_TILE + tc::none_off(r, i), lo);
+    }
+    named_sync(NB_PROD, NGROUP);
+    if (pw == 0 && lane < C) {
         // forward substitution, one lane per column j: T[r][j] = delta_rj - sum_{i<r} A[r][i] T[i][j]
         const int j = lane;
         float tcol[C];
@@ -301,18 +324,6 @@ __device__ __forceinline__ void prep_solve(const Ctx& x, int b)
             st_bf16(sm, OFF_T + tc::none_off(r, j), hi);
             st_bf16(sm, OFF_T + SMALL_TILE + tc::none_off(r, j), lo);
         }
-    } else if (tid >= 128) {
-        unsigned char* pb = sm + OFF_P + b * 1024;
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int idx = 2 * (tid - 128) + e;
-            const int r = idx >> 4, i = idx & 15;
-            const float pv = (i <= r) ? sPf[idx] + sPf[C * C + idx] : 0.f;
-            __nv_bfloat16 hi, lo;
-            split_bf16(pv, hi, lo);
-            st_bf16(pb, tc::none_off(r, i), hi);
-            st_bf16(pb, SMALL_TILE + tc::none_off(r, i), lo);
-        }
     }
 }
 
@@ -324,9 +335,12 @@ struct TileMaps {
 
 __global__ void __launch_bounds__(NTHREADS, 1) kda_chunk_fwd_tc_kernel(PrefillArgs a, const __grid_constant__ TileMaps maps)
 {
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // 1024-byte aligned base (SW128 atoms), derived from the __shared__ array so that every access
+    // stays a shared-memory access
+    unsigned char* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bar_c = reinterpret_cast<uint64_t*>(sm + OFF_BARC);
+    uint64_t* bar_p = reinterpret_cast<uint64_t*>(sm + OFF_BARP);
     uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + OFF_BARLD);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_TSLOT);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(sm + OFF_ABORT);
@@ -336,233 +350,277 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_chunk_fwd_tc_kernel(PrefillAr
     const int tid = threadIdx.x;
     const int w = tid >> 5;
     const int lane = tid & 31;
-    const int q4 = w & 3;    // TMEM lane quarter
-    const int h2 = w >> 2;   // which half of the columns this warp handles
-    const int jrow = 32 * q4 + lane;
 
-    int64_t s0, s1;
-    if (!seq_range(a, n, s0, s1)) return;
+    int64_t q0, q1;
+    if (!seq_range(a, n, q0, q1)) return;
+    // segment k of the sequence, and what this CTA computes for it (mode 0: outputs and, for the
+    // last segment, the final state; 1: S~, the end state from a zero start; 2: M, the transition,
+    // as the end state from the identity with V = 0)
+    const int mode = a.seg_mode == 0 ? 0 : 1 + (int)(blockIdx.z & 1);
+    const int k = a.seg_mode == 0 ? (int)blockIdx.z : (int)(blockIdx.z >> 1);
+    const int64_t seq_chunks = (q1 - q0 + C - 1) / C;
+    const int64_t seg_c = a.seg_chunks > 0 ? (int64_t)a.seg_chunks : (seq_chunks > 0 ? seq_chunks : 1);
+    const int64_t nseg = seq_chunks > 0 ? (seq_chunks + seg_c - 1) / seg_c : 1;
+    if (mode == 0 ? (int64_t)k >= nseg : (int64_t)k >= nseg - 1) return;
+    const int64_t s0 = q0 + (int64_t)k * seg_c * C;
+    const int64_t s1 = min(q1, s0 + seg_c * C);
     const int H = a.H;
-    const Ctx x{sm, tid, w, lane, h, H, expf(a.A[h]), a.g_min};
-    __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.out);
     const int nchunks = (int)((s1 - s0 + C - 1) / C);
-
-    auto issue_tiles = [&](int chunk) {  // thread 0
-        const int tn = (int)(s0 + (int64_t)chunk * C);
-        tc::fence_async_smem();
-        tc::mbar_arrive_expect_tx(bar_ld, 4 * STAGE_TILE);
-        tc::tma_load_3d(sm + OFF_STAGE, &maps.q, 0, h, tn, bar_ld);
-        tc::tma_load_3d(sm + OFF_STAGE + STAGE_TILE, &maps.k, 0, h, tn, bar_ld);
-        tc::tma_load_3d(sm + OFF_STAGE + 2 * STAGE_TILE, &maps.v, 0, h, tn, bar_ld);
-        tc::tma_load_3d(sm + OFF_STAGE + 3 * STAGE_TILE, &maps.z, 0, h, tn, bar_ld);
-    };
-    auto load_beta = [&](int chunk) -> float {  // threads 0..15
-        const int64_t t = s0 + (int64_t)chunk * C + tid;
-        return (chunk < nchunks && t < s1) ? a.beta[t * H + h] : 0.f;
-    };
     auto chunk_len = [&](int chunk) -> int { return (int)min((int64_t)C, s1 - (s0 + (int64_t)chunk * C)); };
 
     if (w == 0) tc::tmem_alloc(tslot, TM_COLS);
-    float beta_next = 0.f;
     if (tid == 0) {
-        tc::mbar_init(bar, 1);
+        tc::mbar_init(bar_c, 1);
+        tc::mbar_init(bar_p, 1);
         tc::mbar_init(bar_ld, 1);
         *abort_flag = 0u;
-        if (nchunks > 0) issue_tiles(0);
     }
-    if (tid < C) beta_next = load_beta(0);
-
-    // state slice: S[c][jrow] for c in [64*h2, 64*h2 + 64)
-    float S[64];
-    const int64_t sbase = ((int64_t)n * H + h) * D * D;
-#pragma unroll
-    for (int cc = 0; cc < 64; ++cc) {
-        S[cc] = a.s0 ? a.s0[sbase + (int64_t)(64 * h2 + cc) * D + jrow] : 0.f;
-    }
-    auto stage_state = [&]() {
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-            uint4 pk;
-            pk.x = tc::pack_bf16(S[8 * ch + 0], S[8 * ch + 1]);
-            pk.y = tc::pack_bf16(S[8 * ch + 2], S[8 * ch + 3]);
-            pk.z = tc::pack_bf16(S[8 * ch + 4], S[8 * ch + 5]);
-            pk.w = tc::pack_bf16(S[8 * ch + 6], S[8 * ch + 7]);
-            *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw128_chunk_off(jrow, 8 * h2 + ch, D)) = pk;
-        }
-    };
-    stage_state();
+    tc::fence_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tbase = *tslot;
-    const uint32_t lane_base = tbase + ((uint32_t)(32 * q4) << 16);
-    uint32_t phase = 0, ld_phase = 0;
 
-    // prepare chunk c into buffer (c & 1): wait for its tiles, factors, then prefetch chunk c+1
-    auto prepare_factors = [&](int chunk) -> bool {
-        const int b = chunk & 1;
-        if (tid < C) reinterpret_cast<float*>(sm + OFF_BETA + b * 64)[tid] = beta_next;
-        if (tid == 0 && !tc::mbar_wait(bar_ld, ld_phase, WAIT_LIMIT)) *abort_flag = 1u;
-        ld_phase ^= 1u;
-        __syncthreads();
-        if (*abort_flag) return false;
-        prep_factors(x, chunk_len(chunk), b);
-        __syncthreads();  // stage consumed
-        if (chunk + 1 < nchunks) {
-            if (tid == 0) issue_tiles(chunk + 1);
-            if (tid < C) beta_next = load_beta(chunk + 1);
-        }
-        return true;
-    };
-    auto issue_mw_mu = [&](int b) {  // thread 0: W^T = (K Gamma)^T T'^T, U~^T = V^T T'^T
-        (void)b;
-        const uint32_t id16 = tc::idesc_bf16(128, 16);
-        const uint64_t dT = tc::desc_none(tc::smem_u32(sm + OFF_T));
-        const uint64_t dTl = tc::desc_none(tc::smem_u32(sm + OFF_T + SMALL_TILE));
-        const uint64_t dX = tc::desc_none(tc::smem_u32(sm + OFF_XT));
-        const uint64_t dV = tc::desc_none(tc::smem_u32(sm + OFF_VT));
-        tc::umma(tbase + TM_W, dX, dT, id16, 0u);
-        tc::umma(tbase + TM_W, dX, dTl, id16, 1u);
-        tc::umma(tbase + TM_U, dV, dT, id16, 0u);
-        tc::umma(tbase + TM_U, dV, dTl, id16, 1u);
-    };
-    auto issue_m1 = [&](int b) {  // thread 0: D1 = S^T [W ; Q Gamma]^T (M = 128, N = 32, K = 128)
-        const uint32_t id32 = tc::idesc_bf16(128, 2 * C);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
-            tc::umma(tbase + TM_D1, tc::desc_sw128(tc::smem_u32(sm + OFF_S + kb * 16384 + off)),
-                     tc::desc_sw128(tc::smem_u32(sm + OFF_WQ + b * 8192 + kb * (2 * C * 128) + off)), id32,
-                     ks > 0 ? 1u : 0u);
-        }
-    };
-    auto transpose_w = [&](int b) {  // warps 0..3: W^T (TMEM, lanes = c) -> rows 0..15 of WQ[b]
-        if (w < 4) {
-            uint32_t v[16];
-            KDA_TMEM_LD16(lane_base + TM_W, v);
-            tc::tmem_wait_ld();
-            unsigned char* wq = sm + OFF_WQ + b * 8192;
-#pragma unroll
-            for (int r = 0; r < C; ++r) st_bf16(wq, tc::sw128_off(r, jrow, 2 * C), __float2bfloat16_rn(u2f(v[r])));
-        }
-    };
+    if (w >= 8) {
+        // ======================================================================== producer
+        const int p = tid - NGROUP;
+        const int pw = w - 8;
+        const float expA = expf(a.A[h]);
+        const float g_min = a.g_min;
+        const uint32_t lane_base = tbase + ((uint32_t)(32 * (pw & 3)) << 16);
+        uint32_t ph_p = 0, ph_ld = 0;
+        auto issue_tiles = [&](int chunk) {  // producer thread 0
+            const int tn = (int)(s0 + (int64_t)chunk * C);
+            tc::fence_async_smem();
+            tc::mbar_arrive_expect_tx(bar_ld, 4 * STAGE_TILE);
+            tc::tma_load_3d(sm + OFF_STAGE, &maps.q, 0, h, tn, bar_ld);
+            tc::tma_load_3d(sm + OFF_STAGE + STAGE_TILE, &maps.k, 0, h, tn, bar_ld);
+            tc::tma_load_3d(sm + OFF_STAGE + 2 * STAGE_TILE, &maps.v, 0, h, tn, bar_ld);
+            tc::tma_load_3d(sm + OFF_STAGE + 3 * STAGE_TILE, &maps.z, 0, h, tn, bar_ld);
+        };
+        auto load_beta = [&](int chunk) -> float {  // producer threads 0..15
+            const int64_t t = s0 + (int64_t)chunk * C + p;
+            return (chunk < nchunks && t < s1) ? a.beta[t * H + h] : 0.f;
+        };
+        float beta_next = (p < C) ? load_beta(0) : 0.f;
+        if (p == 0 && nchunks > 0) issue_tiles(0);
 
-    bool ok = true;
-    if (nchunks > 0) {
-        // prologue: chunk 0 prepared and its state-read issued
-        ok = prepare_factors(0);
-        if (ok) {
-            prep_solve(x, 0);
-            tc_publish();
-            if (tid == 0) issue_mw_mu(0);
-            ok = tc_join(bar, phase, abort_flag);
-        }
-        if (ok) {
-            transpose_w(0);
-            tc_publish();
-            if (tid == 0) issue_m1(0);
-        }
-    }
-
-    for (int ch = 0; ok && ch < nchunks; ++ch) {
-        const int b = ch & 1, nb = b ^ 1;
-        const bool has_next = ch + 1 < nchunks;
-        const int64_t t0 = s0 + (int64_t)ch * C;
-        const int len = chunk_len(ch);
-
-        // (1) while the state-read of chunk ch runs: factors of chunk ch+1
-        if (has_next && !(ok = prepare_factors(ch + 1))) break;
-
-        // (2) U^T = U~^T - (W S)^T as a hi/lo pair
-        if (!(ok = tc_join(bar, phase, abort_flag))) break;
-        {
-            uint32_t dv[8], uv[8];
-            KDA_TMEM_LD8(lane_base + TM_D1 + 8 * h2, dv);
-            KDA_TMEM_LD8(lane_base + TM_U + 8 * h2, uv);
-            tc::tmem_wait_ld();
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float u0 = u2f(uv[2 * e]) - u2f(dv[2 * e]);
-                const float u1 = u2f(uv[2 * e + 1]) - u2f(dv[2 * e + 1]);
-                __nv_bfloat162 h2v = __floats2bfloat162_rn(u0, u1);
-                const float2 hf = __bfloat1622float2(h2v);
-                __nv_bfloat162 l2v = __floats2bfloat162_rn(u0 - hf.x, u1 - hf.y);
-                hi[e] = *reinterpret_cast<uint32_t*>(&h2v);
-                lo[e] = *reinterpret_cast<uint32_t*>(&l2v);
+        for (int ch = 0; ch < nchunks; ++ch) {
+            const int b = ch & 1;
+            if (ch >= 2) {
+                named_sync(NB_EMPTY + b, NTHREADS);  // the consumer is done with chunk ch-2
+                tc::fence_after_sync();
             }
-            *reinterpret_cast<uint4*>(sm + OFF_UT + tc::none_off(jrow, 8 * h2)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(sm + OFF_UT + NONE_TILE + tc::none_off(jrow, 8 * h2)) =
-                make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
-        tc_publish();
-
-        // (3) O^T += U^T P^T and dS^T = U^T (K Gamma_C / Gamma), each as hi*hi + hi*lo + lo*hi
-        if (tid == 0) {
-            const uint32_t id16 = tc::idesc_bf16(128, 16);
-            const uint32_t id128 = tc::idesc_bf16(128, 128);
-            const uint64_t dU = tc::desc_none(tc::smem_u32(sm + OFF_UT));
-            const uint64_t dUl = tc::desc_none(tc::smem_u32(sm + OFF_UT + NONE_TILE));
-            const uint64_t dP = tc::desc_none(tc::smem_u32(sm + OFF_P + b * 1024));
-            const uint64_t dPl = tc::desc_none(tc::smem_u32(sm + OFF_P + b * 1024 + SMALL_TILE));
-            const uint64_t dK = tc::desc_none(tc::smem_u32(sm + OFF_KT + b * 8192));
-            const uint64_t dKl = tc::desc_none(tc::smem_u32(sm + OFF_KT + b * 8192 + NONE_TILE));
-            tc::umma(tbase + TM_D1 + C, dU, dP, id16, 1u);
-            tc::umma(tbase + TM_D1 + C, dU, dPl, id16, 1u);
-            tc::umma(tbase + TM_D1 + C, dUl, dP, id16, 1u);
-            tc::umma(tbase + TM_D3, dU, dK, id128, 0u);
-            tc::umma(tbase + TM_D3, dU, dKl, id128, 1u);
-            tc::umma(tbase + TM_D3, dUl, dK, id128, 1u);
-        }
-
-        // (4) while those run: A, P, T' of chunk ch+1, then its W / U~ products
-        if (has_next) {
-            prep_solve(x, nb);
-            tc_publish();
-            if (tid == 0) issue_mw_mu(nb);
-        }
-        if (!(ok = tc_join(bar, phase, abort_flag))) break;
-
-        // (5) S <- Diag(Gamma_C) S + dS ; outputs of chunk ch ; W of chunk ch+1
-        {
-            const float* gc = reinterpret_cast<const float*>(sm + OFF_GC + b * 512) + 64 * h2;
-#pragma unroll
-            for (int blk = 0; blk < 4; ++blk) {
-                uint32_t v[16];
-                KDA_TMEM_LD16(lane_base + TM_D3 + 64 * h2 + 16 * blk, v);
+            bool dead = read_dead(abort_flag);
+            // tiles of chunk ch
+            if (p < C) reinterpret_cast<float*>(sm + OFF_BETA)[p] = beta_next;
+            if (p == 0 && !dead && !tc::mbar_wait(bar_ld, ph_ld, WAIT_LIMIT)) *abort_flag = 1u;
+            ph_ld ^= 1u;
+            named_sync(NB_PROD, NGROUP);
+            dead = read_dead(abort_flag);
+            if (!dead) prep_factors(sm, p, chunk_len(ch), b, expA, g_min, mode == 2);
+            else named_sync(NB_PROD, NGROUP);  // the barrier inside prep_factors
+            named_sync(NB_PROD, NGROUP);       // stage consumed
+            if (ch + 1 < nchunks) {
+                if (p == 0 && !dead) issue_tiles(ch + 1);
+                if (p < C) beta_next = load_beta(ch + 1);
+            }
+            if (!dead) {
+                prep_solve(sm, p, b);
+            } else {
+                named_sync(NB_PROD, NGROUP);
+                named_sync(NB_PROD, NGROUP);
+            }
+            tc::fence_async_smem();
+            tc::fence_before_sync();
+            named_sync(NB_PROD, NGROUP);
+            tc::fence_after_sync();
+            if (p == 0 && !dead) {
+                // W^T = (K Gamma)^T T'^T, U~^T = V^T T'^T (T' = hi + lo)
+                const uint32_t id16 = tc::idesc_bf16(128, 16);
+                const uint64_t dT = tc::desc_none(tc::smem_u32(sm + OFF_T));
+                const uint64_t dTl = tc::desc_none(tc::smem_u32(sm + OFF_T + SMALL_TILE));
+                const uint64_t dX = tc::desc_none(tc::smem_u32(sm + OFF_XT));
+                const uint64_t dV = tc::desc_none(tc::smem_u32(sm + OFF_VT));
+                const uint32_t du = tbase + TM_U + 16 * b;
+                tc::umma(tbase + TM_W, dX, dT, id16, 0u);
+                tc::umma(tbase + TM_W, dX, dTl, id16, 1u);
+                tc::umma(du, dV, dT, id16, 0u);
+                tc::umma(du, dV, dTl, id16, 1u);
+                commit_wait(bar_p, ph_p, abort_flag);
+            }
+            ph_p ^= 1u;
+            named_sync(NB_PROD, NGROUP);
+            tc::fence_after_sync();
+            dead = read_dead(abort_flag);
+            if (!dead) {
+                // W^T (lanes = c) -> rows 0..15 of WQ[b]; producer warp pw handles rows 8 (pw / 4) .. +8
+                uint32_t v[8];
+                KDA_TMEM_LD8(lane_base + TM_W + 8 * (pw >> 2), v);
                 tc::tmem_wait_ld();
+                unsigned char* wq = sm + OFF_WQ + b * 8192;
+                const int c = 32 * (pw & 3) + lane;
 #pragma unroll
-                for (int e4 = 0; e4 < 4; ++e4) {
-                    const float4 g4 = *reinterpret_cast<const float4*>(gc + 16 * blk + 4 * e4);
-                    const int cc = 16 * blk + 4 * e4;
-                    S[cc + 0] = g4.x * S[cc + 0] + u2f(v[4 * e4 + 0]);
-                    S[cc + 1] = g4.y * S[cc + 1] + u2f(v[4 * e4 + 1]);
-                    S[cc + 2] = g4.z * S[cc + 2] + u2f(v[4 * e4 + 2]);
-                    S[cc + 3] = g4.w * S[cc + 3] + u2f(v[4 * e4 + 3]);
+                for (int e = 0; e < 8; ++e) {
+                    st_bf16(wq, tc::sw128_off(8 * (pw >> 2) + e, c, 2 * C), __float2bfloat16_rn(u2f(v[e])));
                 }
             }
-            stage_state();
-            uint32_t ov[8];
-            KDA_TMEM_LD8(lane_base + TM_D1 + C + 8 * h2, ov);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int r = 8 * h2 + e;
-                if (r < len) op[((t0 + r) * H + h) * D + jrow] = __float2bfloat16_rn(u2f(ov[e]));
-            }
+            tc::fence_async_smem();
+            tc::fence_before_sync();
+            named_arrive(NB_FULL + b, NTHREADS);
         }
-        if (has_next) {
-            transpose_w(nb);
-            tc_publish();
-            if (tid == 0) issue_m1(nb);
-        }
-    }
+    } else {
+        // ======================================================================== consumer
+        const int q4 = w & 3;    // TMEM lane quarter
+        const int h2 = w >> 2;   // which half of the key channels this warp's state slice covers
+        const int jrow = 32 * q4 + lane;
+        const uint32_t lane_base = tbase + ((uint32_t)(32 * q4) << 16);
+        __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.out);
+        uint32_t ph_c = 0;
 
-    if (!ok || *abort_flag) {
-        if (tid == 0) atomicOr(a.check, kCheckTimeout);
-    } else if (a.s_final) {
+        // state slice: S[c][jrow] for c in [64*h2, 64*h2 + 64)
+        float S[64];
+        const int64_t sbase = ((int64_t)n * H + h) * D * D;
+        const int64_t segbase = (((int64_t)n * H + h) * a.max_seg + k) * D * D;
+        const float* init = nullptr;
+        if (mode == 0) init = (k == 0) ? (a.s0 ? a.s0 + sbase : nullptr) : a.seg_in + segbase;
 #pragma unroll
-        for (int cc = 0; cc < 64; ++cc) a.s_final[sbase + (int64_t)(64 * h2 + cc) * D + jrow] = S[cc];
+        for (int cc = 0; cc < 64; ++cc) {
+            const int c = 64 * h2 + cc;
+            S[cc] = init ? init[(int64_t)c * D + jrow] : ((mode == 2 && c == jrow) ? 1.f : 0.f);
+        }
+        auto stage_state = [&]() {
+#pragma unroll
+            for (int chn = 0; chn < 8; ++chn) {
+                uint4 pk;
+                pk.x = tc::pack_bf16(S[8 * chn + 0], S[8 * chn + 1]);
+                pk.y = tc::pack_bf16(S[8 * chn + 2], S[8 * chn + 3]);
+                pk.z = tc::pack_bf16(S[8 * chn + 4], S[8 * chn + 5]);
+                pk.w = tc::pack_bf16(S[8 * chn + 6], S[8 * chn + 7]);
+                *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw128_chunk_off(jrow, 8 * h2 + chn, D)) = pk;
+            }
+        };
+        stage_state();
+        tc::fence_async_smem();
+
+        for (int ch = 0; ch < nchunks; ++ch) {
+            const int b = ch & 1;
+            const int64_t t0 = s0 + (int64_t)ch * C;
+            const int len = chunk_len(ch);
+            named_sync(NB_FULL + b, NTHREADS);  // chunk ch's operands are ready; the state is staged
+            tc::fence_after_sync();
+            bool dead = read_dead(abort_flag);
+
+            // D1 = S^T [W ; Q Gamma]^T  (M = 128, N = 32, K = 128)
+            if (tid == 0 && !dead) {
+                const uint32_t id32 = tc::idesc_bf16(128, 2 * C);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
+                    tc::umma(tbase + TM_D1, tc::desc_sw128(tc::smem_u32(sm + OFF_S + kb * 16384 + off)),
+                             tc::desc_sw128(tc::smem_u32(sm + OFF_WQ + b * 8192 + kb * (2 * C * 128) + off)), id32,
+                             ks > 0 ? 1u : 0u);
+                }
+                commit_wait(bar_c, ph_c, abort_flag);
+            }
+            ph_c ^= 1u;
+            named_sync(NB_CONS, NGROUP);
+            tc::fence_after_sync();
+            dead = read_dead(abort_flag);
+
+            // U^T = U~^T - (W S)^T as a hi/lo pair; warp half h2 takes columns 8 h2 .. 8 h2 + 7
+            if (!dead) {
+                uint32_t dv[8], uv[8];
+                KDA_TMEM_LD8(lane_base + TM_D1 + 8 * h2, dv);
+                KDA_TMEM_LD8(lane_base + TM_U + 16 * b + 8 * h2, uv);
+                tc::tmem_wait_ld();
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float u0 = u2f(uv[2 * e]) - u2f(dv[2 * e]);
+                    const float u1 = u2f(uv[2 * e + 1]) - u2f(dv[2 * e + 1]);
+                    __nv_bfloat162 hv = __floats2bfloat162_rn(u0, u1);
+                    const float2 hf = __bfloat1622float2(hv);
+                    __nv_bfloat162 lv = __floats2bfloat162_rn(u0 - hf.x, u1 - hf.y);
+                    hi[e] = *reinterpret_cast<uint32_t*>(&hv);
+                    lo[e] = *reinterpret_cast<uint32_t*>(&lv);
+                }
+                *reinterpret_cast<uint4*>(sm + OFF_UT + tc::none_off(jrow, 8 * h2)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(sm + OFF_UT + NONE_TILE + tc::none_off(jrow, 8 * h2)) =
+                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+            tc::fence_async_smem();
+            tc::fence_before_sync();
+            named_sync(NB_CONS, NGROUP);
+            tc::fence_after_sync();
+
+            // O^T += U^T P^T and dS^T = U^T (K Gamma_C / Gamma), each as hi*hi + hi*lo + lo*hi
+            if (tid == 0 && !dead) {
+                const uint32_t id16 = tc::idesc_bf16(128, 16);
+                const uint32_t id128 = tc::idesc_bf16(128, 128);
+                const uint64_t dU = tc::desc_none(tc::smem_u32(sm + OFF_UT));
+                const uint64_t dUl = tc::desc_none(tc::smem_u32(sm + OFF_UT + NONE_TILE));
+                const uint64_t dP = tc::desc_none(tc::smem_u32(sm + OFF_P + b * 1024));
+                const uint64_t dPl = tc::desc_none(tc::smem_u32(sm + OFF_P + b * 1024 + SMALL_TILE));
+                const uint64_t dK = tc::desc_none(tc::smem_u32(sm + OFF_KT + b * 8192));
+                const uint64_t dKl = tc::desc_none(tc::smem_u32(sm + OFF_KT + b * 8192 + NONE_TILE));
+                tc::umma(tbase + TM_D1 + C, dU, dP, id16, 1u);
+                tc::umma(tbase + TM_D1 + C, dU, dPl, id16, 1u);
+                tc::umma(tbase + TM_D1 + C, dUl, dP, id16, 1u);
+                tc::umma(tbase + TM_D3, dU, dK, id128, 0u);
+                tc::umma(tbase + TM_D3, dU, dKl, id128, 1u);
+                tc::umma(tbase + TM_D3, dUl, dK, id128, 1u);
+                commit_wait(bar_c, ph_c, abort_flag);
+            }
+            ph_c ^= 1u;
+            named_sync(NB_CONS, NGROUP);
+            tc::fence_after_sync();
+            dead = read_dead(abort_flag);
+
+            // S <- Diag(Gamma_C) S + dS (staged for the next read), outputs of chunk ch
+            if (!dead) {
+                const float* gc = reinterpret_cast<const float*>(sm + OFF_GC + b * 512) + 64 * h2;
+#pragma unroll
+                for (int blk = 0; blk < 4; blk += 2) {
+                    uint32_t v0[16], v1[16];
+                    KDA_TMEM_LD16(lane_base + TM_D3 + 64 * h2 + 16 * blk, v0);
+                    KDA_TMEM_LD16(lane_base + TM_D3 + 64 * h2 + 16 * blk + 16, v1);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        const float4 g4 = *reinterpret_cast<const float4*>(gc + 16 * blk + 4 * e4);
+                        const int cc = 16 * blk + 4 * e4;
+                        const uint32_t* vv = (e4 < 4) ? v0 : v1;
+                        const int o = (e4 & 3) * 4;
+                        S[cc + 0] = g4.x * S[cc + 0] + u2f(vv[o + 0]);
+                        S[cc + 1] = g4.y * S[cc + 1] + u2f(vv[o + 1]);
+                        S[cc + 2] = g4.z * S[cc + 2] + u2f(vv[o + 2]);
+                        S[cc + 3] = g4.w * S[cc + 3] + u2f(vv[o + 3]);
+                    }
+                }
+                stage_state();
+                uint32_t ov[8];
+                KDA_TMEM_LD8(lane_base + TM_D1 + C + 8 * h2, ov);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int r = 8 * h2 + e;
+                    if (mode == 0 && r < len) op[((t0 + r) * H + h) * D + jrow] = __float2bfloat16_rn(u2f(ov[e]));
+                }
+            }
+            tc::fence_async_smem();
+            tc::fence_before_sync();
+            if (ch + 2 < nchunks) named_arrive(NB_EMPTY + b, NTHREADS);
+        }
+        float* dst = nullptr;
+        if (mode == 0) dst = ((int64_t)k == nseg - 1 && a.s_final) ? a.s_final + sbase : nullptr;
+        else dst = (mode == 1 ? a.seg_st : a.seg_mt) + segbase;
+        if (*abort_flag) {
+            if (tid == 0) atomicOr(a.check, kCheckTimeout);
+        } else if (dst) {
+#pragma unroll
+            for (int cc = 0; cc < 64; ++cc) dst[(int64_t)(64 * h2 + cc) * D + jrow] = S[cc];
+        }
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -612,9 +670,29 @@ cudaError_t launch_chunk_fwd_tc(const PrefillArgs& a, cudaStream_t s)
     cudaError_t e = cudaFuncSetAttribute(kda_chunk_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)a.N, (unsigned)a.H);
-    kda_chunk_fwd_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, s>>>(a, maps);
-    return cudaGetLastError();
+    if (a.seg_chunks > 0 && a.max_seg > 1) {
+        // pass 1: (S~, M) of every segment but the last; pass 2: scan; pass 3: outputs
+        PrefillArgs a1 = a;
+        a1.seg_mode = 1;
+        prof_start("kda_seg_summary_tc", s);
+        kda_chunk_fwd_tc_kernel<<<dim3((unsigned)a.N, (unsigned)a.H, (unsigned)(2 * (a.max_seg - 1))), NTHREADS,
+                                  SMEM_BYTES, s>>>(a1, maps);
+        e = cudaGetLastError();
+        prof_stop(s);
+        if (e != cudaSuccess) return e;
+        prof_start("kda_seg_scan", s);
+        e = launch_segment_scan(a, s);
+        prof_stop(s);
+        if (e != cudaSuccess) return e;
+    }
+    PrefillArgs a3 = a;
+    a3.seg_mode = 0;
+    prof_start("kda_chunk_fwd_tc", s);
+    kda_chunk_fwd_tc_kernel<<<dim3((unsigned)a.N, (unsigned)a.H, (unsigned)(a.max_seg > 1 ? a.max_seg : 1)), NTHREADS,
+                              SMEM_BYTES, s>>>(a3, maps);
+    e = cudaGetLastError();
+    prof_stop(s);
+    return e;
 }
 
 static_assert(SMEM_USED + 1024 <= SMEM_BYTES, "shared-memory map exceeds the request");

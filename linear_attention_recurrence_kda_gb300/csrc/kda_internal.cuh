@@ -23,7 +23,8 @@ constexpr uint32_t kCheckBadSeqlens = 1u;
 constexpr uint32_t kCheckTimeout = 2u;
 
 struct ForwardLayout {
-    size_t status_off, g_off, w_off, ut_off, total;
+    size_t status_off, g_off, w_off, ut_off, seg_in_off, seg_st_off, seg_mt_off, total;
+    int32_t seg_chunks, max_seg;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -35,7 +36,26 @@ inline bool use_tensor_core_path(const kda_problem_t& p)
            p.total_tokens < (int64_t(1) << 31);
 }
 
-inline ForwardLayout forward_layout(const kda_problem_t& p)
+// Chunks of the longest sequence allowed by the descriptor (max_seqlen, at most T_tot).
+inline int64_t max_chunks_of(const kda_problem_t& p)
+{
+    const int64_t L = p.max_seqlen < p.total_tokens ? p.max_seqlen : p.total_tokens;
+    return (L + kChunk - 1) / kChunk;
+}
+
+// Segmentation of the tensor-core path.  A sequence is cut into segments of seg_chunks chunks;
+// segment k's end state is S_end = M_k S_in + S~_k (its transition applied to the incoming state,
+// plus its end state from a zero start), so the segments' (M_k, S~_k) are computed in parallel,
+// scanned, and the segments re-run from their true incoming states.  The plan minimises a
+// wave-count model of the three passes for `sm_count` SMs (one CTA per SM).  The environment
+// variable KDA_SEGMENT_CHUNKS=<n> forces n chunks per segment (0: no segmentation).
+// Only plans whose per-segment state buffers fit in `budget_bytes` are considered.
+void segment_plan(const kda_problem_t& p, size_t budget_bytes, int32_t& seg_chunks, int32_t& max_seg);
+
+// Workspace layout for a problem given `available` bytes of workspace: the fastest segmentation
+// whose buffers fit (none if only the minimum fits).  forward_layout(p, SIZE_MAX).total is the
+// size kda_forward_workspace_bytes reports; forward_layout(p, 0).total is the minimum.
+inline ForwardLayout forward_layout(const kda_problem_t& p, size_t available)
 {
     ForwardLayout L{};
     const size_t th = use_tensor_core_path(p) ? 0 : (size_t)p.total_tokens * (size_t)p.num_heads;
@@ -43,7 +63,16 @@ inline ForwardLayout forward_layout(const kda_problem_t& p)
     L.g_off = 256;
     L.w_off = align_up(L.g_off + th * p.d_k * sizeof(float), 256);
     L.ut_off = align_up(L.w_off + th * p.d_k * sizeof(float), 256);
-    L.total = align_up(L.ut_off + th * p.d_v * sizeof(float), 256);
+    const size_t end = align_up(L.ut_off + th * p.d_v * sizeof(float), 256);
+    L.seg_chunks = 0;
+    L.max_seg = 1;
+    // segment buffers are whole multiples of 256 bytes, so a plan fits iff its three buffers do
+    if (use_tensor_core_path(p) && available > end) segment_plan(p, available - end, L.seg_chunks, L.max_seg);
+    const size_t seg_bytes = L.max_seg > 1 ? (size_t)p.num_seqs * p.num_heads * L.max_seg * p.d_k * p.d_v * sizeof(float) : 0;
+    L.seg_in_off = end;
+    L.seg_st_off = align_up(L.seg_in_off + seg_bytes, 256);
+    L.seg_mt_off = align_up(L.seg_st_off + seg_bytes, 256);
+    L.total = align_up(L.seg_mt_off + seg_bytes, 256);
     return L;
 }
 
@@ -66,6 +95,13 @@ struct PrefillArgs {
     int64_t T_tot;
     int32_t N, H, dk, dv, max_seqlen, chunks_per_seq;
     float g_min;
+    // sequence segmentation of the tensor-core path (seg_chunks == 0: one segment per sequence)
+    int32_t seg_chunks;       // chunks per segment
+    int32_t max_seg;          // segments of the longest sequence
+    int32_t seg_mode;         // 0: outputs; 1: end state from zero (S~); 2: transition (M)
+    float* seg_in;            // [N][H][max_seg][d][d] incoming state of every segment (scan output)
+    float* seg_st;            // [N][H][max_seg][d][d] S~ of every segment
+    float* seg_mt;            // [N][H][max_seg][d][d] M of every segment
 };
 
 struct DecodeArgs {
@@ -85,7 +121,8 @@ struct DecodeArgs {
 cudaError_t launch_gate(const PrefillArgs& a, kda_dtype_t dt, cudaStream_t s);
 cudaError_t launch_ut_wy(const PrefillArgs& a, kda_dtype_t dt, cudaStream_t s);
 cudaError_t launch_chunk_fwd(const PrefillArgs& a, kda_dtype_t dt, cudaStream_t s);
-cudaError_t launch_chunk_fwd_tc(const PrefillArgs& a, cudaStream_t s);
+cudaError_t launch_chunk_fwd_tc(const PrefillArgs& a, cudaStream_t s);  // all passes
+cudaError_t launch_segment_scan(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
 
 // Optional per-kernel timing around launches (no-ops unless kda_profile_enable(1)).

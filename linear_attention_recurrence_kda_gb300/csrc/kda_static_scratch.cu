@@ -45,8 +45,10 @@ extern "C" kda_status_t kda_forward_static_scratch(const void* q, const void* k,
                                                    const kda_problem_t* problem, void* stream)
 {
     if (problem == nullptr) return KDA_ERR_INVALID_ARG;
-    const size_t need = kda_forward_workspace_bytes(problem);
-    if (need > KDA_STATIC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE;
+    // the smallest workspace kda_forward can run with (it uses fewer sequence segments, or none,
+    // when the scratch is smaller than the fastest plan wants)
+    if (kda_forward_workspace_bytes(problem) == 0) return KDA_ERR_INVALID_ARG;
+    if (kda::forward_layout(*problem, 0).total > KDA_STATIC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE;
     void* scratch = nullptr;
     const kda_status_t st = scratch_for_current_device(&scratch);
     if (st != KDA_OK) return st;

@@ -131,14 +131,16 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
 }
 
 // Bounded wait for the phase with the given parity; returns false if the limit was reached.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t max_iters)
+// Each try parks the thread in hardware until the phase completes or `hint_ns` elapses, so a
+// waiting thread issues a handful of instructions instead of spinning; at most max_iters tries.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t max_iters, uint32_t hint_ns = 20000u)
 {
     uint32_t done = 0;
     for (uint32_t it = 0; it < max_iters && !done; ++it) {
         asm volatile(
-            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
             : "=r"(done)
-            : "r"(smem_u32(bar)), "r"(parity)
+            : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
             : "memory");
     }
     return done != 0;

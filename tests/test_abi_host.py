@@ -151,3 +151,4 @@ def test_decode_rejects_bad_arguments(L):
 
 def test_workspace_status_rejects_null(L):
     assert L.kda_workspace_status(None, 0, None) == B.KDA_ERR_WORKSPACE
+

@@ -285,3 +285,59 @@ def test_pageable_host_pointer():
         assert torch.equal(out, ref)
     else:
         assert st == B.KDA_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------- segmented prefill
+
+@pytest.mark.parametrize("seg", [1, 2, 3, 5])
+@pytest.mark.parametrize("lengths", [[250], [100, 3, 77, 0, 160], [33]])
+def test_segmented_prefill(monkeypatch, seg, lengths):
+    """Sequences cut into segments of `seg` chunks: segment summaries (S~, M), the fp32 scan of
+    incoming states and the re-run from them must reproduce the unsegmented result."""
+    monkeypatch.setenv("KDA_SEGMENT_CHUNKS", str(seg))
+    inp = I.make_inputs(1, lengths=lengths, num_heads=3, d=128, seed=seg * 100 + len(lengths))
+    out, sf = gpu_forward(inp)
+    ref_o, ref_s = oracle_forward(inp)
+    check(out, ref_o, torch.bfloat16, "out")
+    check(sf, ref_s, torch.bfloat16, "final_state")
+
+
+def test_segmented_prefill_identity_transition(monkeypatch):
+    """alpha = 1, beta = 0 keeps the state constant, so every segment's transition is the identity
+    and every incoming state equals the initial state: the scan must carry it exactly."""
+    monkeypatch.setenv("KDA_SEGMENT_CHUNKS", "2")
+    inp = I.make_inputs(1, lengths=[200], num_heads=2, d=128, seed=7)
+    inp["z"] = torch.full_like(inp["z"], -1e4)
+    inp["beta"] = torch.zeros_like(inp["beta"])
+    out, sf = gpu_forward(inp)
+    ref_o, ref_s = oracle_forward(inp)
+    check(out, ref_o, torch.bfloat16, "out")
+    check(sf, ref_s, torch.bfloat16, "final_state")
+    assert torch.allclose(sf.cpu(), inp["S0"], rtol=0, atol=1e-6)
+
+
+def test_workspace_smaller_than_the_fastest_plan():
+    """A workspace below kda_forward_workspace_bytes (here the 256-byte minimum of the
+    tensor-core path) makes kda_forward use fewer sequence segments; results are unchanged."""
+    inp = I.make_inputs(1, lengths=[700], num_heads=2, d=128, seed=21)
+    d = to_dev(inp)
+    prob = B.make_problem(1, 700, 700, 2, 128, 128, torch.bfloat16)
+    assert B.kda_forward_workspace_bytes(prob) > 256  # the fastest plan segments this sequence
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    out, sf = B.kda_forward(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], initial_state=d["S0"], workspace=small)
+    torch.cuda.synchronize()
+    ref_o, ref_s = oracle_forward(inp)
+    check(out, ref_o, torch.bfloat16, "out")
+    check(sf, ref_s, torch.bfloat16, "final_state")
+
+
+def test_reported_workspace_runs_the_segmented_plan():
+    """With exactly kda_forward_workspace_bytes of workspace, a 4096-token, 16-head prefill runs
+    the segmented plan (segment summaries, scan, outputs), one launch each."""
+    from linear_attention_recurrence_kda_gb300 import profile_cases as P
+    B.kda_profile_enable(True)
+    P.prefill(4096, 16, 0, torch.bfloat16)
+    prof = B.kda_profile_read()
+    B.kda_profile_enable(False)
+    assert set(prof) == {"kda_seg_summary_tc", "kda_seg_scan", "kda_chunk_fwd_tc"}
+    assert all(n == 1 for n, _ in prof.values())

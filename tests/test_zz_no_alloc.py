@@ -23,9 +23,6 @@ CASES = [
 
 @pytest.mark.parametrize("case", CASES, ids=["bf16-d128", "f32-d64"])
 def test_matches_kda_forward_on_two_calls_in_a_row(case):
-    prob = B.make_problem(len(case["lengths"]), sum(case["lengths"]), max(case["lengths"]), case["heads"],
-                          case["d"], case["d"], case["io"])
-    assert B.kda_forward_workspace_bytes(prob) <= B.KDA_STATIC_SCRATCH_BYTES
     for call in range(2):
         inp = I.make_inputs(1, lengths=case["lengths"], num_heads=case["heads"], d=case["d"], io_dtype=case["io"],
                             seed=100 + call)
