@@ -83,14 +83,14 @@ constexpr uint32_t OFF_KD = 114432;    // K / Gamma hi, lo                      
 constexpr uint32_t OFF_A = 123136;     // A fp32 [16][16]                               1024
 constexpr uint32_t OFF_PART = 124160;  // k-step partial products fp32 [8 warps][16][16] 8192
 constexpr uint32_t OFF_GC = 132352;    // [2] Gamma_C fp32 [128]                         2 x 512
-constexpr uint32_t OFF_HS = 133376;    // per-channel half-chunk log-decay sums [2][128] 1024
-constexpr uint32_t OFF_BETA = 134400;  // beta [16]                                      64
-constexpr uint32_t OFF_BARC = 134464;  // mbarrier: consumer tensor-core commits        8
-constexpr uint32_t OFF_BARP = 134472;  // mbarrier: producer tensor-core commits        8
-constexpr uint32_t OFF_BARLD = 134480; // mbarrier: TMA tile loads                      8
-constexpr uint32_t OFF_TSLOT = 134488; // TMEM base address                             4
-constexpr uint32_t OFF_ABORT = 134492; // stop flag                                     4
-constexpr uint32_t SMEM_USED = 134496;
+constexpr uint32_t OFF_HS = 133376;    // per-channel quarter-chunk log-decay sums [4][128] 2048
+constexpr uint32_t OFF_BETA = 135424;  // beta [16]                                      64
+constexpr uint32_t OFF_BARC = 135488;  // mbarrier: consumer tensor-core commits        8
+constexpr uint32_t OFF_BARP = 135496;  // mbarrier: producer tensor-core commits        8
+constexpr uint32_t OFF_BARLD = 135504; // mbarrier: TMA tile loads                      8
+constexpr uint32_t OFF_TSLOT = 135512; // TMEM base address                             4
+constexpr uint32_t OFF_ABORT = 135516; // stop flag                                     4
+constexpr uint32_t SMEM_USED = 135520;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
 constexpr uint32_t STAGE_TILE = C * D * 2;  // 4096 bytes per tensor and chunk
 constexpr uint32_t NONE_TILE = 4096;        // [128][16] bf16 NONE tile
@@ -135,11 +135,6 @@ __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bflo
     lo = __float2bfloat16_rn(x - __bfloat162float(hi));
 }
 
-__device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b)
-{
-    return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
-}
-
 // Abort flag, read identically by every lane of the warp (it guards warp-collective instructions).
 __device__ __forceinline__ bool read_dead(const volatile uint32_t* abort_flag)
 {
@@ -174,76 +169,133 @@ __device__ __forceinline__ void mma_kstep(float (&acc)[2][4], const __nv_bfloat1
 
 // ---------------------------------------------------------------------------- producer stages
 
+// (x0, x1) = hi + lo as bf16 pairs: hi = bf16(x), lo = bf16(x - hi); one packed conversion each.
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float2 hf = __bfloat1622float2(h);
+    __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<uint32_t*>(&h);
+    lo = *reinterpret_cast<uint32_t*>(&l);
+}
+
+__device__ __forceinline__ uint32_t pack_f2(float x0, float x1)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
 // Gate, in-chunk cumulative log-decay and every per-element factor of one chunk (producer group).
-// Producer thread p owns key/value channel c = p % 128 and tokens [8 half, 8 half + 8), half = p / 128.
+// Producer thread p owns the channel pair (2 cp, 2 cp + 1), cp = p % 64, and tokens
+// [4 tq, 4 tq + 4), tq = p / 64; pairs make every row-tile store a 32-bit word.
 // Writes: row-major K Gamma, Q Gamma (hi/lo), K/Gamma (hi/lo); WQ[b] rows 16..31 (Q Gamma hi);
 // (K Gamma)^T, V^T; KT[b] (K Gamma_C/Gamma hi/lo); GC[b] = Gamma_C.  One producer barrier inside.
 __device__ __forceinline__ void prep_factors(unsigned char* sm, int p, int len, int b, float expA, float g_min,
                                              bool zero_v)
 {
-    const int c = p & (D - 1);
-    const int half = p >> 7;
-    const int r0 = 8 * half;
-    const __nv_bfloat16* tq = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_STAGE);
-    const __nv_bfloat16* tk = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_STAGE + STAGE_TILE);
-    const __nv_bfloat16* tv = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_STAGE + 2 * STAGE_TILE);
-    const __nv_bfloat16* tz = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_STAGE + 3 * STAGE_TILE);
-    float* hs = reinterpret_cast<float*>(sm + OFF_HS);
+    const int cp = p & 63;
+    const int tq = p >> 6;
+    const int c0 = 2 * cp;
+    const int r0 = 4 * tq;
+    const uint32_t* tq32 = reinterpret_cast<const uint32_t*>(sm + OFF_STAGE);
+    const uint32_t* tk32 = reinterpret_cast<const uint32_t*>(sm + OFF_STAGE + STAGE_TILE);
+    const uint32_t* tv32 = reinterpret_cast<const uint32_t*>(sm + OFF_STAGE + 2 * STAGE_TILE);
+    const uint32_t* tz32 = reinterpret_cast<const uint32_t*>(sm + OFF_STAGE + 3 * STAGE_TILE);
+    float* hs = reinterpret_cast<float*>(sm + OFF_HS);  // [4 quarters][128 channels]
 
-    float Gl[8], kv[8], qv[8];
-    __nv_bfloat16 vv[8];
-    float acc = 0.f;
+    float G0[4], G1[4];
+    float2 kv[4], qv[4];
+    uint32_t vv[4];
+    float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
+    for (int e = 0; e < 4; ++e) {
         const int r = r0 + e;
         const bool ok = r < len;
-        const float g = ok ? log_decay_fast(__bfloat162float(tz[r * D + c]), expA, g_min) : 0.f;
-        acc += g;
-        Gl[e] = acc;
-        kv[e] = ok ? __bfloat162float(tk[r * D + c]) : 0.f;
-        qv[e] = ok ? __bfloat162float(tq[r * D + c]) : 0.f;
-        vv[e] = (ok && !zero_v) ? tv[r * D + c] : __float2bfloat16_rn(0.f);
+        const uint32_t zw = tz32[(r * D + c0) >> 1];
+        const float2 z2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&zw));
+        a0 += ok ? log_decay_fast(z2.x, expA, g_min) : 0.f;
+        a1 += ok ? log_decay_fast(z2.y, expA, g_min) : 0.f;
+        G0[e] = a0;
+        G1[e] = a1;
+        const uint32_t kw = ok ? tk32[(r * D + c0) >> 1] : 0u;
+        const uint32_t qw = ok ? tq32[(r * D + c0) >> 1] : 0u;
+        kv[e] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kw));
+        qv[e] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qw));
+        vv[e] = (ok && !zero_v) ? tv32[(r * D + c0) >> 1] : 0u;
     }
-    hs[half * D + c] = acc;
+    *reinterpret_cast<float2*>(hs + tq * D + c0) = make_float2(a0, a1);
     named_sync(NB_PROD, NGROUP);
-    const float off = half ? hs[c] : 0.f;
-    const float eGC = __expf(hs[c] + hs[D + c]);
-    if (half) reinterpret_cast<float*>(sm + OFF_GC + b * 512)[c] = eGC;
-
-    __nv_bfloat16* sLl = reinterpret_cast<__nv_bfloat16*>(sm + OFF_LL);
-    __nv_bfloat16* sQl = reinterpret_cast<__nv_bfloat16*>(sm + OFF_QL);
-    __nv_bfloat16* sQll = sQl + C * LROW;
-    __nv_bfloat16* sKd = reinterpret_cast<__nv_bfloat16*>(sm + OFF_KD);
-    __nv_bfloat16* sKdl = sKd + C * LROW;
-    unsigned char* wq = sm + OFF_WQ + b * 8192;
-    __nv_bfloat16 xt[8], kth[8], ktl[8];
+    float off0 = 0.f, off1 = 0.f, tot0 = 0.f, tot1 = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const int r = r0 + e;
-        const float eG = __expf(Gl[e] + off);         // Gamma_r in [e^-80, 1]
-        const float ieG = __fdividef(1.f, eG);         // 1 / Gamma_r in [1, e^80]
-        const float ll = kv[e] * eG;
-        __nv_bfloat16 hi, lo;
-        xt[e] = __float2bfloat16_rn(ll);
-        sLl[r * LROW + c] = xt[e];
-        split_bf16(qv[e] * eG, hi, lo);
-        sQl[r * LROW + c] = hi;
-        sQll[r * LROW + c] = lo;
-        st_bf16(wq, tc::sw128_off(C + r, c, 2 * C), hi);
-        split_bf16(kv[e] * ieG, hi, lo);
-        sKd[r * LROW + c] = hi;
-        sKdl[r * LROW + c] = lo;
-        split_bf16(kv[e] * (eGC * ieG), kth[e], ktl[e]);   // k Gamma_C / Gamma_r <= 1
+    for (int qq = 0; qq < 4; ++qq) {
+        const float2 hq = *reinterpret_cast<const float2*>(hs + qq * D + c0);
+        if (qq < tq) {
+            off0 += hq.x;
+            off1 += hq.y;
+        }
+        tot0 += hq.x;
+        tot1 += hq.y;
     }
-    *reinterpret_cast<uint4*>(sm + OFF_XT + tc::none_off(c, r0)) =
-        make_uint4(pack2(xt[0], xt[1]), pack2(xt[2], xt[3]), pack2(xt[4], xt[5]), pack2(xt[6], xt[7]));
-    *reinterpret_cast<uint4*>(sm + OFF_VT + tc::none_off(c, r0)) =
-        make_uint4(pack2(vv[0], vv[1]), pack2(vv[2], vv[3]), pack2(vv[4], vv[5]), pack2(vv[6], vv[7]));
+    const float eGC0 = __expf(tot0), eGC1 = __expf(tot1);
+    if (tq == 3) *reinterpret_cast<float2*>(sm + OFF_GC + b * 512 + 4 * c0) = make_float2(eGC0, eGC1);
+
+    uint32_t* sLl = reinterpret_cast<uint32_t*>(sm + OFF_LL);
+    uint32_t* sQl = reinterpret_cast<uint32_t*>(sm + OFF_QL);
+    uint32_t* sQll = sQl + C * LROW / 2;
+    uint32_t* sKd = reinterpret_cast<uint32_t*>(sm + OFF_KD);
+    uint32_t* sKdl = sKd + C * LROW / 2;
+    unsigned char* wq = sm + OFF_WQ + b * 8192;
+    // transposed tiles: 4 tokens of one channel = 8 bytes at none_off(c, 4 tq)
+    uint32_t xt0[2], xt1[2], kh0[2], kh1[2], kl0[2], kl1[2];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int r = r0 + e;
+        const float eG0 = __expf(G0[e] + off0), eG1 = __expf(G1[e] + off1);  // Gamma in [e^-80, 1]
+        const float iG0 = __fdividef(1.f, eG0), iG1 = __fdividef(1.f, eG1);  // 1/Gamma in [1, e^80]
+        const float ll0 = kv[e].x * eG0, ll1 = kv[e].y * eG1;
+        const uint32_t llw = pack_f2(ll0, ll1);
+        const int ri = (r * LROW + c0) >> 1;
+        sLl[ri] = llw;
+        uint32_t hi, lo;
+        split2(qv[e].x * eG0, qv[e].y * eG1, hi, lo);
+        sQl[ri] = hi;
+        sQll[ri] = lo;
+        *reinterpret_cast<uint32_t*>(wq + tc::sw128_off(C + r, c0, 2 * C)) = hi;
+        split2(kv[e].x * iG0, kv[e].y * iG1, hi, lo);
+        sKd[ri] = hi;
+        sKdl[ri] = lo;
+        uint32_t th, tl;
+        split2(kv[e].x * (eGC0 * iG0), kv[e].y * (eGC1 * iG1), th, tl);  // k Gamma_C / Gamma <= 1
+        // de-interleave the pairs into per-channel token runs
+        const int slot = e >> 1, sh = (e & 1) * 16;
+        if ((e & 1) == 0) {
+            xt0[slot] = llw & 0xffffu;
+            xt1[slot] = llw >> 16;
+            kh0[slot] = th & 0xffffu;
+            kh1[slot] = th >> 16;
+            kl0[slot] = tl & 0xffffu;
+            kl1[slot] = tl >> 16;
+        } else {
+            xt0[slot] |= (llw & 0xffffu) << sh;
+            xt1[slot] |= (llw >> 16) << sh;
+            kh0[slot] |= (th & 0xffffu) << sh;
+            kh1[slot] |= (th >> 16) << sh;
+            kl0[slot] |= (tl & 0xffffu) << sh;
+            kl1[slot] |= (tl >> 16) << sh;
+        }
+    }
+    const uint32_t v00 = (vv[0] & 0xffffu) | (vv[1] << 16), v01 = (vv[2] & 0xffffu) | (vv[3] << 16);
+    const uint32_t v10 = (vv[0] >> 16) | (vv[1] & 0xffff0000u), v11 = (vv[2] >> 16) | (vv[3] & 0xffff0000u);
     unsigned char* kt = sm + OFF_KT + b * 8192;
-    *reinterpret_cast<uint4*>(kt + tc::none_off(c, r0)) =
-        make_uint4(pack2(kth[0], kth[1]), pack2(kth[2], kth[3]), pack2(kth[4], kth[5]), pack2(kth[6], kth[7]));
-    *reinterpret_cast<uint4*>(kt + NONE_TILE + tc::none_off(c, r0)) =
-        make_uint4(pack2(ktl[0], ktl[1]), pack2(ktl[2], ktl[3]), pack2(ktl[4], ktl[5]), pack2(ktl[6], ktl[7]));
+    const uint32_t o0 = tc::none_off(c0, r0), o1 = tc::none_off(c0 + 1, r0);
+    *reinterpret_cast<uint2*>(sm + OFF_XT + o0) = make_uint2(xt0[0], xt0[1]);
+    *reinterpret_cast<uint2*>(sm + OFF_XT + o1) = make_uint2(xt1[0], xt1[1]);
+    *reinterpret_cast<uint2*>(sm + OFF_VT + o0) = make_uint2(v00, v01);
+    *reinterpret_cast<uint2*>(sm + OFF_VT + o1) = make_uint2(v10, v11);
+    *reinterpret_cast<uint2*>(kt + o0) = make_uint2(kh0[0], kh0[1]);
+    *reinterpret_cast<uint2*>(kt + o1) = make_uint2(kh1[0], kh1[1]);
+    *reinterpret_cast<uint2*>(kt + NONE_TILE + o0) = make_uint2(kl0[0], kl0[1]);
+    *reinterpret_cast<uint2*>(kt + NONE_TILE + o1) = make_uint2(kl1[0], kl1[1]);
 }
 
 // A and P over K = 128 with mma.sync, two k-steps per producer warp (warps 0..3: A, warps 4..7: P
