@@ -218,6 +218,7 @@ def main():
     __graft_entry__.build()
     from linear_attention_recurrence_kda_gb300 import binding as B
     from linear_attention_recurrence_kda_gb300 import inputs as I
+    from linear_attention_recurrence_kda_gb300 import sharding
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -233,11 +234,7 @@ def main():
             dist.barrier()
 
     def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return sharding.max_over_ranks(x, device=dev)
 
     # ---- CPU oracle baseline first (rank 0 only, before any timed GPU work)
     cpu = None

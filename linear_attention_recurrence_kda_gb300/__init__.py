@@ -4,4 +4,4 @@ The compute runs in ``libkda.so`` (hand-written sm_103a CUDA kernels behind a C 
 ``include/kda.h``).  ``binding`` marshals torch tensors to that ABI; it never computes anything
 itself and raises if the library is missing.
 """
-__all__ = ["binding", "inputs"]
+__all__ = ["binding", "inputs", "sharding"]
