@@ -101,7 +101,9 @@ class ClockSampler:
 def src_sha(kernel):
     name = {"kda_gate": "kda_gate.cu", "kda_ut_wy": "kda_ut_wy.cu", "kda_chunk_fwd": "kda_chunk_fwd.cu",
             "kda_decode_step": "kda_decode.cu", "kda_chunk_fwd_tc": "kda_chunk_tc.cu",
-            "kda_seg_summary_tc": "kda_chunk_tc.cu", "kda_seg_scan": "kda_segment_scan.cu"}.get(kernel)
+            "kda_seg_summary_tc": "kda_chunk_tc.cu", "kda_seg_scan": "kda_segment_scan.cu",
+            "kda_chunk_prep_tc": "kda_prep_tc.cu", "kda_state_summary_tc": "kda_state_tc.cu",
+            "kda_chunk_state_tc": "kda_state_tc.cu"}.get(kernel)
     if name is None:
         return None
     p = os.path.join(ROOT, "linear_attention_recurrence_kda_gb300", "csrc", name)
@@ -294,26 +296,29 @@ def main():
     value = tokens / (ms * 1e-3) / 1e6
     launches = sum(n for n, _ in prof.values())
 
-    # roofline of the kernel with the largest device time, each kernel against its own algorithmic
-    # bytes: the output pass reads q, k, v, z, beta and writes o for every token-head (plus the
-    # states); the segment-summary pass must read k, v, z, beta of the summarised tokens once and
-    # write two states per segment; the scan reads (M, S~) and writes S_in per segment.
+    # roofline of the kernel with the largest device time, each kernel against the bytes its design
+    # must move: the fused / output pass reads q, k, v, z, beta and writes o for every token-head
+    # (plus the states); the chunk preparation reads the same inputs and writes one operand block
+    # per chunk and head; the state passes read those blocks (the summary pass twice: S~ and M
+    # chains) and write states; the scan reads (M, S~) and writes S_in per segment step.
     pk, pk_src = peaks()
     th = T * H
-    n_seg = int(prof.get("kda_seg_scan", (0, 0))[0] > 0)
-    seg_tokens = 0
-    if "kda_seg_summary_tc" in prof:
-        prob_ws = B.kda_forward_workspace_bytes(prob)
-        max_seg = max(1, (prob_ws - 256) // (3 * H * dk * dv * 4))
-        seg_len = -(-T // (16 * max_seg)) * 16
-        seg_tokens = T - (T - seg_len * (max_seg - 1))  # all but the last segment
-        n_seg = max_seg
+    plan = B.kda_forward_plan(prob, ws.numel())
+    n_seg = plan["num_segments"]
+    seg_tokens = 16 * plan["seg_chunks"] * (n_seg - 1) if n_seg > 1 else 0  # tokens of all but the last segment
     state_bytes = H * dk * dv * 4
+    blk = 26112
+    chunk_heads = -(-T // 16) * H
+    seg_chunk_heads = (seg_tokens // 16) * H
+    in_bytes = th * ((2 * dk + dv + dk) * io_bytes + 4)
     alg = {
         "kda_chunk_fwd_tc": th * prefill_bytes_per_token_head(dk, dv, io_bytes) + 2 * state_bytes,
         "kda_chunk_fwd": th * prefill_bytes_per_token_head(dk, dv, io_bytes) + 2 * state_bytes,
         "kda_seg_summary_tc": seg_tokens * H * ((2 * dk + dv) * io_bytes + 4) + 2 * (n_seg - 1) * state_bytes,
         "kda_seg_scan": 3 * (n_seg - 1) * state_bytes,
+        "kda_chunk_prep_tc": in_bytes + chunk_heads * blk,
+        "kda_state_summary_tc": 2 * seg_chunk_heads * blk + 2 * (n_seg - 1) * state_bytes,
+        "kda_chunk_state_tc": chunk_heads * blk + th * dv * io_bytes + 2 * state_bytes,
     }
     kernels = {}
     for name, (cnt, tot_ms) in prof.items():

@@ -73,6 +73,26 @@ typedef struct {
  */
 size_t kda_forward_workspace_bytes(const kda_problem_t* problem);
 
+/* The execution plan kda_forward picks for a problem and a workspace size. */
+typedef struct {
+    int32_t split;         /* 1: parallel chunk preparation + state pass; 0: fused kernel or the
+                              fp32 three-kernel path                                              */
+    int32_t seg_chunks;    /* chunks per sequence segment, 0 when sequences are not segmented   */
+    int32_t num_segments;  /* segments of the longest sequence (1 when not segmented)           */
+    int32_t reserved;      /* 0                                                                  */
+} kda_plan_t;
+
+/*
+ * Fills *plan with the plan kda_forward would use for `problem` with `workspace_bytes` of
+ * workspace (SIZE_MAX: the plan of kda_forward_workspace_bytes(problem) bytes).  The plan depends
+ * only on the descriptor, the workspace size, the SM count of the current device and the
+ * environment overrides documented at kda_forward.  The library has no counterpart of this call
+ * on the pages; it exists so that callers can size workspaces and read measurements.
+ * Returns KDA_ERR_INVALID_ARG for a NULL plan or an invalid descriptor, KDA_ERR_WORKSPACE if the
+ * workspace is below the minimum, else KDA_OK.  Host only; launches nothing.
+ */
+kda_status_t kda_forward_plan(const kda_problem_t* problem, size_t workspace_bytes, kda_plan_t* plan);
+
 /*
  * Chunkwise-parallel prefill over packed sequences (Equation 1 for every token, in 16-token
  * chunks; the chunk form is an exact regrouping of the token recurrence, "Kimi K3:
@@ -91,10 +111,16 @@ size_t kda_forward_workspace_bytes(const kda_problem_t* problem);
  *   final_state   : [N,H,d_k,d_v] fp32, or NULL (not written).  May be the same pointer as
  *                   initial_state (in-place carry); any other overlap is rejected.
  *   workspace     : device scratch, 256-byte aligned, not shared with a concurrently running
- *                   call.  kda_forward_workspace_bytes(problem) bytes allow the fastest plan; a
- *                   smaller workspace makes long sequences use fewer parallel segments (down to
- *                   none), and one below the unsegmented minimum is rejected (KDA_ERR_WORKSPACE).
- *                   Results do not depend on the plan beyond rounding.
+ *                   call.  kda_forward_workspace_bytes(problem) bytes allow the fastest plan.  For
+ *                   bf16 inputs with d_k = d_v = 128 that plan first prepares every chunk's
+ *                   state-independent operands in parallel (about 26 KB per chunk and head, held
+ *                   in the workspace) and then runs the sequential state pass; a workspace too
+ *                   small for those blocks selects a fused kernel that prepares each chunk on the
+ *                   fly.  A smaller workspace also makes long sequences use fewer parallel
+ *                   segments (down to none); one below the unsegmented minimum is rejected
+ *                   (KDA_ERR_WORKSPACE).  Results do not depend on the plan beyond rounding.
+ *                   Environment overrides, read on every call: KDA_TC_PLAN=fused keeps the fused
+ *                   kernel; KDA_SEGMENT_CHUNKS=<n> forces n chunks per segment (0: unsegmented).
  *
  * Returns KDA_OK once all kernels are enqueued on `stream`.
  */

@@ -33,10 +33,16 @@ G_MIN = -5.0
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_forward_workspace_bytes", "kda_forward", "kda_decode_step", "kda_workspace_status",
            "kda_status_string", "kda_profile_enable", "kda_profile_read", "kda_abi_version",
-           "kda_forward_static_scratch")
+           "kda_forward_static_scratch", "kda_forward_plan")
 
 # Size of the library's own scratch array used by kda_forward_static_scratch.
 KDA_STATIC_SCRATCH_BYTES = 8 << 20
+
+
+class KdaPlan(ctypes.Structure):
+    """Mirror of kda_plan_t."""
+    _fields_ = [("split", ctypes.c_int32), ("seg_chunks", ctypes.c_int32), ("num_segments", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class KdaProblem(ctypes.Structure):
@@ -88,6 +94,8 @@ def lib():
             L.kda_profile_read.argtypes = [ctypes.POINTER(KdaKernelTime), ctypes.c_int32]
             L.kda_forward_static_scratch.restype = ctypes.c_int
             L.kda_forward_static_scratch.argtypes = [_vp] * 10 + [P, _vp]
+            L.kda_forward_plan.restype = ctypes.c_int
+            L.kda_forward_plan.argtypes = [P, ctypes.c_size_t, ctypes.POINTER(KdaPlan)]
             L.kda_abi_version.restype = ctypes.c_uint32
             L.kda_abi_version.argtypes = []
             _lib = L
@@ -131,6 +139,16 @@ def _need(t, name, dtype, shape, device):
 
 def kda_forward_workspace_bytes(problem: KdaProblem) -> int:
     return int(lib().kda_forward_workspace_bytes(ctypes.byref(problem)))
+
+
+def kda_forward_plan(problem: KdaProblem, workspace_bytes: Optional[int] = None) -> dict:
+    """The plan kda_forward picks for ``problem`` with ``workspace_bytes`` (None: the fastest)."""
+    plan = KdaPlan()
+    wb = ctypes.c_size_t(-1).value if workspace_bytes is None else int(workspace_bytes)
+    st = lib().kda_forward_plan(ctypes.byref(problem), wb, ctypes.byref(plan))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_forward_plan")
+    return {"split": bool(plan.split), "seg_chunks": int(plan.seg_chunks), "num_segments": int(plan.num_segments)}
 
 
 def kda_forward(q, k, v, z, A, beta, initial_state=None, cu_seqlens=None, out=None, final_state=None,

@@ -99,7 +99,7 @@ int sm_count_of_current_device()
 
 namespace kda {
 
-void segment_plan(const kda_problem_t& p, size_t budget_bytes, int32_t& seg_chunks, int32_t& max_seg)
+void segment_plan(const kda_problem_t& p, size_t budget_bytes, bool split, int32_t& seg_chunks, int32_t& max_seg)
 {
     const int64_t chunks = max_chunks_of(p);
     seg_chunks = 0;
@@ -115,10 +115,12 @@ void segment_plan(const kda_problem_t& p, size_t budget_bytes, int32_t& seg_chun
         }
         return;
     }
-    // one CTA per SM; cost in units of one chunk step: pass 3 runs nseg segments per (seq, head),
-    // pass 1 runs two summaries (S~ and M) of every segment but the last, and the scan costs about
-    // a quarter of a chunk step per segment
-    const double sms = (double)sm_count_of_current_device();
+    // cost in units of one chunk step of a chain: pass 3 runs nseg segments per (seq, head), pass 1
+    // two summaries (S~ and M) of every segment but the last, each in waves of `slots` concurrent
+    // chains (two state-pass CTAs per SM in the split plan, one fused CTA per SM otherwise); one
+    // step of the scan costs about scan_step chunk steps
+    const double sms = (double)sm_count_of_current_device() * (split ? 2.0 : 1.0);
+    const double scan_step = split ? 2.5 : 1.5;
     const double units = (double)p.num_seqs * p.num_heads;
     const double per_seg = units * p.d_k * p.d_v * 4.0 * 3.0;  // S_in, S~ and M of one segment
     double best = (double)chunks * std::ceil(units / sms);
@@ -128,7 +130,7 @@ void segment_plan(const kda_problem_t& p, size_t budget_bytes, int32_t& seg_chun
         if (ns < 2) continue;
         if (per_seg * (double)ns > (double)budget_bytes || per_seg * (double)ns > 2.0e9) continue;
         const double cost = (double)sc * (std::ceil(units * ns / sms) + std::ceil(2.0 * units * (ns - 1) / sms)) +
-                            0.25 * (double)(ns - 1);
+                            scan_step * (double)(ns - 1);
         if (cost < 0.9 * best) {
             best = cost;
             seg_chunks = (int32_t)sc;
@@ -167,6 +169,20 @@ size_t kda_forward_workspace_bytes(const kda_problem_t* problem)
 {
     if (check_descriptor(problem, false) != KDA_OK) return 0;
     return kda::forward_layout(*problem, SIZE_MAX).total;
+}
+
+kda_status_t kda_forward_plan(const kda_problem_t* problem, size_t workspace_bytes, kda_plan_t* plan)
+{
+    if (plan == nullptr) return KDA_ERR_INVALID_ARG;
+    const kda_status_t st = check_descriptor(problem, false);
+    if (st != KDA_OK) return st;
+    const ForwardLayout L = kda::forward_layout(*problem, workspace_bytes);
+    if (workspace_bytes < L.total) return KDA_ERR_WORKSPACE;
+    plan->split = L.split ? 1 : 0;
+    plan->seg_chunks = L.max_seg > 1 ? L.seg_chunks : 0;
+    plan->num_segments = L.max_seg > 1 ? L.max_seg : 1;
+    plan->reserved = 0;
+    return KDA_OK;
 }
 
 kda_status_t kda_forward(const void* q, const void* k, const void* v, const void* z, const float* A,
@@ -245,11 +261,13 @@ kda_status_t kda_forward(const void* q, const void* k, const void* v, const void
     a.seg_in = reinterpret_cast<float*>(ws + L.seg_in_off);
     a.seg_st = reinterpret_cast<float*>(ws + L.seg_st_off);
     a.seg_mt = reinterpret_cast<float*>(ws + L.seg_mt_off);
+    a.blocks = ws + L.blocks_off;
 
     if (cudaMemsetAsync(a.check, 0, sizeof(uint32_t), s) != cudaSuccess) return KDA_ERR_CUDA;
     cudaError_t e = cudaSuccess;
     if (kda::use_tensor_core_path(p)) {
-        e = kda::launch_chunk_fwd_tc(a, s);  // one to three passes, each timed by the profiling hooks
+        // every pass is timed by the profiling hooks inside the launchers
+        e = L.split ? kda::launch_prefill_split_tc(a, s) : kda::launch_chunk_fwd_tc(a, s);
         return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
     }
     if (cps > 0) {

@@ -49,16 +49,23 @@
 
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
+#include "kda_tc_chunk.cuh"
 
 namespace kda {
 
 namespace {
 
-constexpr int D = 128;            // d_k = d_v
-constexpr int C = kChunk;         // 16
+using tcc::C;
+using tcc::D;
+using tcc::NGROUP;
+using tcc::NONE_TILE;
+using tcc::SMALL_TILE;
+using tcc::STAGE_TILE;
+using tcc::named_arrive;
+using tcc::named_sync;
+using tcc::st_bf16;
+using tcc::u2f;
 constexpr int NTHREADS = 512;     // 8 consumer + 8 producer warps
-constexpr int NGROUP = 256;       // threads per group
-constexpr int LROW = 136;         // padded row (elements) of the mma.sync operand tiles
 constexpr uint32_t WAIT_LIMIT = 1u << 17;  // tries of up to 20 us each: ~2.6 s at most
 
 // named barriers (0 is __syncthreads)
@@ -92,9 +99,6 @@ constexpr uint32_t OFF_TSLOT = 135512; // TMEM base address                     
 constexpr uint32_t OFF_ABORT = 135516; // stop flag                                     4
 constexpr uint32_t SMEM_USED = 135520;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
-constexpr uint32_t STAGE_TILE = C * D * 2;  // 4096 bytes per tensor and chunk
-constexpr uint32_t NONE_TILE = 4096;        // [128][16] bf16 NONE tile
-constexpr uint32_t SMALL_TILE = 512;        // [16][16] bf16 NONE tile
 
 // tensor-memory columns
 constexpr uint32_t TM_D1 = 0;    // consumer: [0,16) (W S)^T, [16,32) O^T
@@ -103,37 +107,21 @@ constexpr uint32_t TM_U = 48;    // producer -> consumer: [2] U~^T (lanes = j), 
 constexpr uint32_t TM_D3 = 128;  // consumer: dS^T (lanes = j, columns = c)
 constexpr uint32_t TM_COLS = 256;
 
-__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
-
-__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-__device__ __forceinline__ void named_arrive(uint32_t id, uint32_t count)
-{
-    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// Equation 5 with the fast exponential and division (relative error ~1e-6, far below bf16).
-__device__ __forceinline__ float log_decay_fast(float z, float expA, float g_min)
-{
-    const float x = expA * z;
-    const float e = __expf(-fabsf(x));
-    const float sig = (x >= 0.f) ? __fdividef(1.f, 1.f + e) : __fdividef(e, 1.f + e);
-    return g_min * sig;
-}
-
-__device__ __forceinline__ void st_bf16(unsigned char* base, uint32_t off, __nv_bfloat16 x)
-{
-    *reinterpret_cast<__nv_bfloat16*>(base + off) = x;
-}
-
-// x = hi + lo with hi = bf16(x), lo = bf16(x - hi)
-__device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bfloat16& lo)
-{
-    hi = __float2bfloat16_rn(x);
-    lo = __float2bfloat16_rn(x - __bfloat162float(hi));
-}
+// Placement of the per-chunk preparation tiles in this kernel's shared memory.
+struct FusedMap {
+    static constexpr uint32_t OFF_STAGE = ::kda::OFF_STAGE;
+    static constexpr uint32_t OFF_HS = ::kda::OFF_HS;
+    static constexpr uint32_t OFF_LL = ::kda::OFF_LL;
+    static constexpr uint32_t OFF_QL = ::kda::OFF_QL;
+    static constexpr uint32_t OFF_KD = ::kda::OFF_KD;
+    static constexpr uint32_t OFF_XT = ::kda::OFF_XT;
+    static constexpr uint32_t OFF_VT = ::kda::OFF_VT;
+    static constexpr uint32_t OFF_A = ::kda::OFF_A;
+    static constexpr uint32_t OFF_PART = ::kda::OFF_PART;
+    static constexpr uint32_t OFF_BETA = ::kda::OFF_BETA;
+    static constexpr uint32_t OFF_T = ::kda::OFF_T;
+    static constexpr uint32_t NB = 2;  // producer-group barrier
+};
 
 // Abort flag, read identically by every lane of the warp (it guards warp-collective instructions).
 __device__ __forceinline__ bool read_dead(const volatile uint32_t* abort_flag)
@@ -148,242 +136,7 @@ __device__ __forceinline__ void commit_wait(uint64_t* bar, uint32_t phase, volat
     if (!tc::mbar_wait(bar, phase, WAIT_LIMIT)) *abort_flag = 1u;
 }
 
-// 16x16 partial product over one k-step (16 channels): acc += L[:, k0:k0+16] R[:, k0:k0+16]^T.
-__device__ __forceinline__ void mma_kstep(float (&acc)[2][4], const __nv_bfloat16* L, const __nv_bfloat16* R, int k0,
-                                          int lane)
-{
-    const int g = lane >> 2, t = lane & 3;
-    uint32_t af[4];
-    af[0] = *reinterpret_cast<const uint32_t*>(L + g * LROW + k0 + 2 * t);
-    af[1] = *reinterpret_cast<const uint32_t*>(L + (g + 8) * LROW + k0 + 2 * t);
-    af[2] = *reinterpret_cast<const uint32_t*>(L + g * LROW + k0 + 8 + 2 * t);
-    af[3] = *reinterpret_cast<const uint32_t*>(L + (g + 8) * LROW + k0 + 8 + 2 * t);
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-        const int n0 = 8 * nt;
-        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(R + (n0 + g) * LROW + k0 + 2 * t);
-        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(R + (n0 + g) * LROW + k0 + 8 + 2 * t);
-        tc::mma16816(acc[nt], af, b0, b1);
-    }
-}
-
-// ---------------------------------------------------------------------------- producer stages
-
-// (x0, x1) = hi + lo as bf16 pairs: hi = bf16(x), lo = bf16(x - hi); one packed conversion each.
-__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo)
-{
-    __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-    const float2 hf = __bfloat1622float2(h);
-    __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-    hi = *reinterpret_cast<uint32_t*>(&h);
-    lo = *reinterpret_cast<uint32_t*>(&l);
-}
-
-__device__ __forceinline__ uint32_t pack_f2(float x0, float x1)
-{
-    __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// Gate, in-chunk cumulative log-decay and every per-element factor of one chunk (producer group).
-// Producer thread p owns the channel pair (2 cp, 2 cp + 1), cp = p % 64, and tokens
-// [4 tq, 4 tq + 4), tq = p / 64; pairs make every row-tile store a 32-bit word.
-// Writes: row-major K Gamma, Q Gamma (hi/lo), K/Gamma (hi/lo); WQ[b] rows 16..31 (Q Gamma hi);
-// (K Gamma)^T, V^T; KT[b] (K Gamma_C/Gamma hi/lo); GC[b] = Gamma_C.  One producer barrier inside.
-__device__ __forceinline__ void prep_factors(unsigned char* sm, int p, int len, int b, float expA, float g_min,
-                                             bool zero_v)
-{
-    const int cp = p & 63;
-    const int tq = p >> 6;
-    const int c0 = 2 * cp;
-    const int r0 = 4 * tq;
-    const uint32_t* tq32 = reinterpret_cast<const uint32_t*>(sm + OFF_STAGE);
-    const uint32_t* tk32 = reinterpret_cast<const uint32_t*>(sm + OFF_STAGE + STAGE_TILE);
-    const uint32_t* tv32 = reinterpret_cast<const uint32_t*>(sm + OFF_STAGE + 2 * STAGE_TILE);
-    const uint32_t* tz32 = reinterpret_cast<const uint32_t*>(sm + OFF_STAGE + 3 * STAGE_TILE);
-    float* hs = reinterpret_cast<float*>(sm + OFF_HS);  // [4 quarters][128 channels]
-
-    float G0[4], G1[4];
-    float2 kv[4], qv[4];
-    uint32_t vv[4];
-    float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const int r = r0 + e;
-        const bool ok = r < len;
-        const uint32_t zw = tz32[(r * D + c0) >> 1];
-        const float2 z2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&zw));
-        a0 += ok ? log_decay_fast(z2.x, expA, g_min) : 0.f;
-        a1 += ok ? log_decay_fast(z2.y, expA, g_min) : 0.f;
-        G0[e] = a0;
-        G1[e] = a1;
-        const uint32_t kw = ok ? tk32[(r * D + c0) >> 1] : 0u;
-        const uint32_t qw = ok ? tq32[(r * D + c0) >> 1] : 0u;
-        kv[e] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kw));
-        qv[e] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qw));
-        vv[e] = (ok && !zero_v) ? tv32[(r * D + c0) >> 1] : 0u;
-    }
-    *reinterpret_cast<float2*>(hs + tq * D + c0) = make_float2(a0, a1);
-    named_sync(NB_PROD, NGROUP);
-    float off0 = 0.f, off1 = 0.f, tot0 = 0.f, tot1 = 0.f;
-#pragma unroll
-    for (int qq = 0; qq < 4; ++qq) {
-        const float2 hq = *reinterpret_cast<const float2*>(hs + qq * D + c0);
-        if (qq < tq) {
-            off0 += hq.x;
-            off1 += hq.y;
-        }
-        tot0 += hq.x;
-        tot1 += hq.y;
-    }
-    const float eGC0 = __expf(tot0), eGC1 = __expf(tot1);
-    if (tq == 3) *reinterpret_cast<float2*>(sm + OFF_GC + b * 512 + 4 * c0) = make_float2(eGC0, eGC1);
-
-    uint32_t* sLl = reinterpret_cast<uint32_t*>(sm + OFF_LL);
-    uint32_t* sQl = reinterpret_cast<uint32_t*>(sm + OFF_QL);
-    uint32_t* sQll = sQl + C * LROW / 2;
-    uint32_t* sKd = reinterpret_cast<uint32_t*>(sm + OFF_KD);
-    uint32_t* sKdl = sKd + C * LROW / 2;
-    unsigned char* wq = sm + OFF_WQ + b * 8192;
-    // transposed tiles: 4 tokens of one channel = 8 bytes at none_off(c, 4 tq)
-    uint32_t xt0[2], xt1[2], kh0[2], kh1[2], kl0[2], kl1[2];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const int r = r0 + e;
-        const float eG0 = __expf(G0[e] + off0), eG1 = __expf(G1[e] + off1);  // Gamma in [e^-80, 1]
-        const float iG0 = __fdividef(1.f, eG0), iG1 = __fdividef(1.f, eG1);  // 1/Gamma in [1, e^80]
-        const float ll0 = kv[e].x * eG0, ll1 = kv[e].y * eG1;
-        const uint32_t llw = pack_f2(ll0, ll1);
-        const int ri = (r * LROW + c0) >> 1;
-        sLl[ri] = llw;
-        uint32_t hi, lo;
-        split2(qv[e].x * eG0, qv[e].y * eG1, hi, lo);
-        sQl[ri] = hi;
-        sQll[ri] = lo;
-        *reinterpret_cast<uint32_t*>(wq + tc::sw128_off(C + r, c0, 2 * C)) = hi;
-        split2(kv[e].x * iG0, kv[e].y * iG1, hi, lo);
-        sKd[ri] = hi;
-        sKdl[ri] = lo;
-        uint32_t th, tl;
-        split2(kv[e].x * (eGC0 * iG0), kv[e].y * (eGC1 * iG1), th, tl);  // k Gamma_C / Gamma <= 1
-        // de-interleave the pairs into per-channel token runs
-        const int slot = e >> 1, sh = (e & 1) * 16;
-        if ((e & 1) == 0) {
-            xt0[slot] = llw & 0xffffu;
-            xt1[slot] = llw >> 16;
-            kh0[slot] = th & 0xffffu;
-            kh1[slot] = th >> 16;
-            kl0[slot] = tl & 0xffffu;
-            kl1[slot] = tl >> 16;
-        } else {
-            xt0[slot] |= (llw & 0xffffu) << sh;
-            xt1[slot] |= (llw >> 16) << sh;
-            kh0[slot] |= (th & 0xffffu) << sh;
-            kh1[slot] |= (th >> 16) << sh;
-            kl0[slot] |= (tl & 0xffffu) << sh;
-            kl1[slot] |= (tl >> 16) << sh;
-        }
-    }
-    const uint32_t v00 = (vv[0] & 0xffffu) | (vv[1] << 16), v01 = (vv[2] & 0xffffu) | (vv[3] << 16);
-    const uint32_t v10 = (vv[0] >> 16) | (vv[1] & 0xffff0000u), v11 = (vv[2] >> 16) | (vv[3] & 0xffff0000u);
-    unsigned char* kt = sm + OFF_KT + b * 8192;
-    const uint32_t o0 = tc::none_off(c0, r0), o1 = tc::none_off(c0 + 1, r0);
-    *reinterpret_cast<uint2*>(sm + OFF_XT + o0) = make_uint2(xt0[0], xt0[1]);
-    *reinterpret_cast<uint2*>(sm + OFF_XT + o1) = make_uint2(xt1[0], xt1[1]);
-    *reinterpret_cast<uint2*>(sm + OFF_VT + o0) = make_uint2(v00, v01);
-    *reinterpret_cast<uint2*>(sm + OFF_VT + o1) = make_uint2(v10, v11);
-    *reinterpret_cast<uint2*>(kt + o0) = make_uint2(kh0[0], kh0[1]);
-    *reinterpret_cast<uint2*>(kt + o1) = make_uint2(kh1[0], kh1[1]);
-    *reinterpret_cast<uint2*>(kt + NONE_TILE + o0) = make_uint2(kl0[0], kl0[1]);
-    *reinterpret_cast<uint2*>(kt + NONE_TILE + o1) = make_uint2(kl1[0], kl1[1]);
-}
-
-// A and P over K = 128 with mma.sync, two k-steps per producer warp (warps 0..3: A, warps 4..7: P
-// as hi*hi + hi*lo + lo*hi), partial sums reduced in shared memory; then T = (I + A)^-1 by forward
-// substitution and T' = T diag(beta) (hi/lo), P finalised into P[b] (hi/lo).  Two producer barriers.
-__device__ __forceinline__ void prep_solve(unsigned char* sm, int p, int b)
-{
-    const int pw = p >> 5, lane = p & 31;
-    float* sA = reinterpret_cast<float*>(sm + OFF_A);
-    float* part = reinterpret_cast<float*>(sm + OFF_PART);
-    const float* beta = reinterpret_cast<const float*>(sm + OFF_BETA);
-    const __nv_bfloat16* sLl = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_LL);
-    const __nv_bfloat16* sQl = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_QL);
-    const __nv_bfloat16* sQll = sQl + C * LROW;
-    const __nv_bfloat16* sKd = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_KD);
-    const __nv_bfloat16* sKdl = sKd + C * LROW;
-    {
-        const int g = lane >> 2, t = lane & 3;
-        const int k0 = 32 * (pw & 3);
-        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        if (pw < 4) {
-            mma_kstep(acc, sLl, sKd, k0, lane);
-            mma_kstep(acc, sLl, sKd, k0 + 16, lane);
-        } else {
-#pragma unroll
-            for (int kk = 0; kk < 32; kk += 16) {
-                mma_kstep(acc, sQl, sKd, k0 + kk, lane);
-                mma_kstep(acc, sQl, sKdl, k0 + kk, lane);
-                mma_kstep(acc, sQll, sKd, k0 + kk, lane);
-            }
-        }
-        float* pp = part + pw * C * C;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            *reinterpret_cast<float2*>(pp + g * C + 8 * nt + 2 * t) = make_float2(acc[nt][0], acc[nt][1]);
-            *reinterpret_cast<float2*>(pp + (g + 8) * C + 8 * nt + 2 * t) = make_float2(acc[nt][2], acc[nt][3]);
-        }
-    }
-    named_sync(NB_PROD, NGROUP);
-    {
-        const int idx = p;  // one entry of A and one of P per producer thread
-        const int r = idx >> 4, i = idx & 15;
-        float sa = 0.f, sp = 0.f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            sa += part[k * C * C + idx];
-            sp += part[(4 + k) * C * C + idx];
-        }
-        sA[idx] = (i < r) ? beta[r] * sa : 0.f;
-        __nv_bfloat16 hi, lo;
-        split_bf16((i <= r) ? sp : 0.f, hi, lo);
-        unsigned char* pb = sm + OFF_P + b * 1024;
-        st_bf16(pb, tc::none_off(r, i), hi);
-        st_bf16(pb, SMALL_TILE + tc::none_off(r, i), lo);
-    }
-    named_sync(NB_PROD, NGROUP);
-    if (pw == 0 && lane < C) {
-        // forward substitution, one lane per column j: T[r][j] = delta_rj - sum_{i<r} A[r][i] T[i][j]
-        const int j = lane;
-        float tcol[C];
-#pragma unroll
-        for (int r = 0; r < C; ++r) {
-            float p0 = (r == j) ? 1.f : 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
-#pragma unroll
-            for (int i = 0; i < r; i += 4) {
-                p0 -= sA[r * C + i] * tcol[i];
-                if (i + 1 < r) p1 -= sA[r * C + i + 1] * tcol[i + 1];
-                if (i + 2 < r) p2 -= sA[r * C + i + 2] * tcol[i + 2];
-                if (i + 3 < r) p3 -= sA[r * C + i + 3] * tcol[i + 3];
-            }
-            tcol[r] = (p0 + p1) + (p2 + p3);
-        }
-        const float bj = beta[j];
-#pragma unroll
-        for (int r = 0; r < C; ++r) {
-            __nv_bfloat16 hi, lo;
-            split_bf16(tcol[r] * bj, hi, lo);
-            st_bf16(sm, OFF_T + tc::none_off(r, j), hi);
-            st_bf16(sm, OFF_T + SMALL_TILE + tc::none_off(r, j), lo);
-        }
-    }
-}
-
 }  // namespace
-
-struct TileMaps {
-    CUtensorMap q, k, v, z;  // 3-D views [T_tot][H][128] of the bf16 inputs, box [16][1][128]
-};
 
 __global__ void __launch_bounds__(NTHREADS, 1) kda_chunk_fwd_tc_kernel(PrefillArgs a, const __grid_constant__ TileMaps maps)
 {
@@ -470,7 +223,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_chunk_fwd_tc_kernel(PrefillAr
             ph_ld ^= 1u;
             named_sync(NB_PROD, NGROUP);
             dead = read_dead(abort_flag);
-            if (!dead) prep_factors(sm, p, chunk_len(ch), b, expA, g_min, mode == 2);
+            if (!dead) tcc::prep_factors<FusedMap>(sm, p, chunk_len(ch), sm + OFF_WQ + b * 8192, sm + OFF_KT + b * 8192,
+                                                 reinterpret_cast<float*>(sm + OFF_GC + b * 512), expA, g_min, mode == 2);
             else named_sync(NB_PROD, NGROUP);  // the barrier inside prep_factors
             named_sync(NB_PROD, NGROUP);       // stage consumed
             if (ch + 1 < nchunks) {
@@ -478,7 +232,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_chunk_fwd_tc_kernel(PrefillAr
                 if (p < C) beta_next = load_beta(ch + 1);
             }
             if (!dead) {
-                prep_solve(sm, p, b);
+                tcc::prep_solve<FusedMap>(sm, p, sm + OFF_P + b * 1024);
             } else {
                 named_sync(NB_PROD, NGROUP);
                 named_sync(NB_PROD, NGROUP);
@@ -712,13 +466,16 @@ bool encode_tile_map(CUtensorMap* m, const void* base, int64_t T_tot, int H)
 
 }  // namespace
 
+bool encode_tile_maps(TileMaps& m, const PrefillArgs& a)
+{
+    return encode_tile_map(&m.q, a.q, a.T_tot, a.H) && encode_tile_map(&m.k, a.k, a.T_tot, a.H) &&
+           encode_tile_map(&m.v, a.v, a.T_tot, a.H) && encode_tile_map(&m.z, a.z, a.T_tot, a.H);
+}
+
 cudaError_t launch_chunk_fwd_tc(const PrefillArgs& a, cudaStream_t s)
 {
     TileMaps maps;
-    if (!encode_tile_map(&maps.q, a.q, a.T_tot, a.H) || !encode_tile_map(&maps.k, a.k, a.T_tot, a.H) ||
-        !encode_tile_map(&maps.v, a.v, a.T_tot, a.H) || !encode_tile_map(&maps.z, a.z, a.T_tot, a.H)) {
-        return cudaErrorInvalidValue;
-    }
+    if (!encode_tile_maps(maps, a)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(kda_chunk_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;

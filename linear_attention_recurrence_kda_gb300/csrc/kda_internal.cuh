@@ -6,11 +6,17 @@
 //   G          fp32 [T_tot, H, d_k]   in-chunk inclusive cumulative log-decay (kda_gate)
 //   W          fp32 [T_tot, H, d_k]   WY-transformed keys T diag(beta) (K*Gamma)   (kda_ut_wy)
 //   Ut         fp32 [T_tot, H, d_v]   UT-transformed values T diag(beta) V         (kda_ut_wy)
+// and, for the bf16 d = 128 tensor-core path:
+//   blocks     per-chunk operand blocks [T_tot / 16 + N + 1 slots][H][kBlockBytes] (kda_chunk_prep_tc),
+//              present when the workspace holds them ("split" plan; otherwise the fused kernel runs)
+//   seg_in, seg_st, seg_mt   fp32 [N][H][max_seg][d_k][d_v] per-segment states (segmented plans)
 #pragma once
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include "kda.h"
 
@@ -23,9 +29,13 @@ constexpr uint32_t kCheckBadSeqlens = 1u;
 constexpr uint32_t kCheckTimeout = 2u;
 
 struct ForwardLayout {
-    size_t status_off, g_off, w_off, ut_off, seg_in_off, seg_st_off, seg_mt_off, total;
+    size_t status_off, g_off, w_off, ut_off, blocks_off, seg_in_off, seg_st_off, seg_mt_off, total;
     int32_t seg_chunks, max_seg;
+    bool split;  // tensor-core path: parallel chunk preparation + state pass (else the fused kernel)
 };
+
+// Bytes of one chunk's operand block (the state pass's per-chunk input; see kda_tc_chunk.cuh).
+constexpr size_t kBlockBytes = 26112;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -43,22 +53,31 @@ inline int64_t max_chunks_of(const kda_problem_t& p)
     return (L + kChunk - 1) / kChunk;
 }
 
+// Operand-block slots of the split tensor-core plan: chunk c of sequence n uses slot cu[n] / 16 + n + c.
+inline size_t block_bytes_of(const kda_problem_t& p)
+{
+    const size_t slots = (size_t)(p.total_tokens / kChunk) + (size_t)p.num_seqs + 1;
+    return slots * (size_t)p.num_heads * kBlockBytes;
+}
+
 // Segmentation of the tensor-core path.  A sequence is cut into segments of seg_chunks chunks;
 // segment k's end state is S_end = M_k S_in + S~_k (its transition applied to the incoming state,
 // plus its end state from a zero start), so the segments' (M_k, S~_k) are computed in parallel,
 // scanned, and the segments re-run from their true incoming states.  The plan minimises a
-// wave-count model of the three passes for `sm_count` SMs (one CTA per SM).  The environment
-// variable KDA_SEGMENT_CHUNKS=<n> forces n chunks per segment (0: no segmentation).
-// Only plans whose per-segment state buffers fit in `budget_bytes` are considered.
-void segment_plan(const kda_problem_t& p, size_t budget_bytes, int32_t& seg_chunks, int32_t& max_seg);
+// wave-count model of the passes (`split`: two state-pass CTAs per SM, else the fused kernel's
+// one).  The environment variable KDA_SEGMENT_CHUNKS=<n> forces n chunks per segment
+// (0: no segmentation).  Only plans whose per-segment state buffers fit in `budget_bytes` count.
+void segment_plan(const kda_problem_t& p, size_t budget_bytes, bool split, int32_t& seg_chunks, int32_t& max_seg);
 
-// Workspace layout for a problem given `available` bytes of workspace: the fastest segmentation
-// whose buffers fit (none if only the minimum fits).  forward_layout(p, SIZE_MAX).total is the
-// size kda_forward_workspace_bytes reports; forward_layout(p, 0).total is the minimum.
+// Workspace layout for a problem given `available` bytes of workspace.  Tensor-core path: the split
+// plan (operand blocks) with the fastest segmentation that fits, else the fused kernel with the
+// fastest segmentation that fits (none if only the minimum fits).  forward_layout(p, SIZE_MAX).total
+// is the size kda_forward_workspace_bytes reports; forward_layout(p, 0).total is the minimum.
 inline ForwardLayout forward_layout(const kda_problem_t& p, size_t available)
 {
     ForwardLayout L{};
-    const size_t th = use_tensor_core_path(p) ? 0 : (size_t)p.total_tokens * (size_t)p.num_heads;
+    const bool tcp = use_tensor_core_path(p);
+    const size_t th = tcp ? 0 : (size_t)p.total_tokens * (size_t)p.num_heads;
     L.status_off = 0;
     L.g_off = 256;
     L.w_off = align_up(L.g_off + th * p.d_k * sizeof(float), 256);
@@ -66,10 +85,25 @@ inline ForwardLayout forward_layout(const kda_problem_t& p, size_t available)
     const size_t end = align_up(L.ut_off + th * p.d_v * sizeof(float), 256);
     L.seg_chunks = 0;
     L.max_seg = 1;
+    L.split = false;
+    L.blocks_off = end;
+    size_t seg_start = end;
     // segment buffers are whole multiples of 256 bytes, so a plan fits iff its three buffers do
-    if (use_tensor_core_path(p) && available > end) segment_plan(p, available - end, L.seg_chunks, L.max_seg);
+    if (tcp) {
+        const size_t bb = align_up(block_bytes_of(p), 256);
+        // KDA_TC_PLAN=fused keeps the fused kernel even when the operand blocks would fit
+        const char* plan = getenv("KDA_TC_PLAN");
+        const bool fused_only = plan != nullptr && strcmp(plan, "fused") == 0;
+        if (!fused_only && available >= end + bb) {
+            L.split = true;
+            seg_start = end + bb;
+            segment_plan(p, available - seg_start, true, L.seg_chunks, L.max_seg);
+        } else if (available > end) {
+            segment_plan(p, available - end, false, L.seg_chunks, L.max_seg);
+        }
+    }
     const size_t seg_bytes = L.max_seg > 1 ? (size_t)p.num_seqs * p.num_heads * L.max_seg * p.d_k * p.d_v * sizeof(float) : 0;
-    L.seg_in_off = end;
+    L.seg_in_off = seg_start;
     L.seg_st_off = align_up(L.seg_in_off + seg_bytes, 256);
     L.seg_mt_off = align_up(L.seg_st_off + seg_bytes, 256);
     L.total = align_up(L.seg_mt_off + seg_bytes, 256);
@@ -102,6 +136,7 @@ struct PrefillArgs {
     float* seg_in;            // [N][H][max_seg][d][d] incoming state of every segment (scan output)
     float* seg_st;            // [N][H][max_seg][d][d] S~ of every segment
     float* seg_mt;            // [N][H][max_seg][d][d] M of every segment
+    unsigned char* blocks;    // per-chunk operand blocks of the split tensor-core plan
 };
 
 struct DecodeArgs {
@@ -121,7 +156,9 @@ struct DecodeArgs {
 cudaError_t launch_gate(const PrefillArgs& a, kda_dtype_t dt, cudaStream_t s);
 cudaError_t launch_ut_wy(const PrefillArgs& a, kda_dtype_t dt, cudaStream_t s);
 cudaError_t launch_chunk_fwd(const PrefillArgs& a, kda_dtype_t dt, cudaStream_t s);
-cudaError_t launch_chunk_fwd_tc(const PrefillArgs& a, cudaStream_t s);  // all passes
+cudaError_t launch_chunk_fwd_tc(const PrefillArgs& a, cudaStream_t s);      // fused kernel, all passes
+cudaError_t launch_chunk_prep_tc(const PrefillArgs& a, cudaStream_t s);     // operand blocks
+cudaError_t launch_prefill_split_tc(const PrefillArgs& a, cudaStream_t s);  // blocks + state pass, all passes
 cudaError_t launch_segment_scan(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
 

@@ -56,15 +56,21 @@ def _prob(**kw):
     return B.make_problem(**base)
 
 
-def test_workspace_bytes(L):
+def test_workspace_bytes(L, monkeypatch):
     p = _prob()
     n = B.kda_forward_workspace_bytes(p)
     # check word + G, W (d_k) and U~ (d_v) in fp32 for every token-head
     assert n >= 256 + 64 * 2 * (32 + 32 + 32) * 4
     assert n % 256 == 0
-    # bf16 inputs with d_k = d_v = 128 take the fused tensor-core path: no per-token scratch
+    # bf16 inputs with d_k = d_v = 128: the fastest plan holds one 26,112-byte operand block per
+    # chunk slot (T_tot / 16 + N + 1 slots) and head, plus per-segment states
     big = _prob(total_tokens=1 << 20, max_seqlen=1 << 20, num_heads=8, d_k=128, d_v=128, io_dtype=B.KDA_BF16)
+    blocks = ((1 << 20) // 16 + 1 + 1) * 8 * 26112
+    assert blocks <= B.kda_forward_workspace_bytes(big) < blocks + (1 << 30)
+    # the fused kernel needs no per-token scratch
+    monkeypatch.setenv("KDA_TC_PLAN", "fused")
     assert 256 <= B.kda_forward_workspace_bytes(big) < 1 << 30
+    monkeypatch.delenv("KDA_TC_PLAN")
     simt_big = _prob(total_tokens=1 << 20, max_seqlen=1 << 20, num_heads=8, d_k=128, d_v=128)
     assert B.kda_forward_workspace_bytes(simt_big) > B.kda_forward_workspace_bytes(p)
     for bad in (_prob(d_k=96), _prob(num_heads=0), _prob(g_min=0.0), _prob(g_min=float("nan")),
@@ -152,3 +158,30 @@ def test_decode_rejects_bad_arguments(L):
 def test_workspace_status_rejects_null(L):
     assert L.kda_workspace_status(None, 0, None) == B.KDA_ERR_WORKSPACE
 
+
+
+def test_forward_plan(L, monkeypatch):
+    """kda_forward_plan reports the plan kda_forward would take for a workspace size."""
+    monkeypatch.delenv("KDA_TC_PLAN", raising=False)
+    monkeypatch.delenv("KDA_SEGMENT_CHUNKS", raising=False)
+    p = _prob(total_tokens=4096, max_seqlen=4096, num_heads=16, d_k=128, d_v=128, io_dtype=B.KDA_BF16)
+    fast = B.kda_forward_plan(p)
+    assert fast["split"] and fast["num_segments"] > 1 and fast["seg_chunks"] * fast["num_segments"] >= 256
+    assert B.kda_forward_plan(p, B.kda_forward_workspace_bytes(p)) == fast
+    # the 256-byte minimum: fused kernel, one segment
+    assert B.kda_forward_plan(p, 256) == {"split": False, "seg_chunks": 0, "num_segments": 1}
+    monkeypatch.setenv("KDA_TC_PLAN", "fused")
+    assert not B.kda_forward_plan(p)["split"]
+    monkeypatch.setenv("KDA_SEGMENT_CHUNKS", "0")
+    assert B.kda_forward_plan(p)["num_segments"] == 1
+    monkeypatch.delenv("KDA_TC_PLAN")
+    monkeypatch.setenv("KDA_SEGMENT_CHUNKS", "64")
+    assert B.kda_forward_plan(p) == {"split": True, "seg_chunks": 64, "num_segments": 4}
+    # the fp32 path needs per-token scratch: below it the call is refused
+    with pytest.raises(B.KdaError) as e:
+        B.kda_forward_plan(_prob(), 256)
+    assert e.value.status == B.KDA_ERR_WORKSPACE
+    with pytest.raises(B.KdaError) as e:
+        B.kda_forward_plan(_prob(d_k=96))
+    assert e.value.status == B.KDA_ERR_UNSUPPORTED
+    assert L.kda_forward_plan(ctypes.byref(p), ctypes.c_size_t(1 << 40), None) == B.KDA_ERR_INVALID_ARG

@@ -291,10 +291,13 @@ def test_pageable_host_pointer():
 
 @pytest.mark.parametrize("seg", [1, 2, 3, 5])
 @pytest.mark.parametrize("lengths", [[250], [100, 3, 77, 0, 160], [33]])
-def test_segmented_prefill(monkeypatch, seg, lengths):
+@pytest.mark.parametrize("plan", ["split", "fused"])
+def test_segmented_prefill(monkeypatch, seg, lengths, plan):
     """Sequences cut into segments of `seg` chunks: segment summaries (S~, M), the fp32 scan of
-    incoming states and the re-run from them must reproduce the unsegmented result."""
+    incoming states and the re-run from them must reproduce the unsegmented result, on both
+    tensor-core plans (parallel chunk preparation + state pass, and the fused kernel)."""
     monkeypatch.setenv("KDA_SEGMENT_CHUNKS", str(seg))
+    monkeypatch.setenv("KDA_TC_PLAN", plan)
     inp = I.make_inputs(1, lengths=lengths, num_heads=3, d=128, seed=seg * 100 + len(lengths))
     out, sf = gpu_forward(inp)
     ref_o, ref_s = oracle_forward(inp)
@@ -318,7 +321,8 @@ def test_segmented_prefill_identity_transition(monkeypatch):
 
 def test_workspace_smaller_than_the_fastest_plan():
     """A workspace below kda_forward_workspace_bytes (here the 256-byte minimum of the
-    tensor-core path) makes kda_forward use fewer sequence segments; results are unchanged."""
+    tensor-core path) makes kda_forward fall back to the fused kernel without sequence segments;
+    results are unchanged."""
     inp = I.make_inputs(1, lengths=[700], num_heads=2, d=128, seed=21)
     d = to_dev(inp)
     prob = B.make_problem(1, 700, 700, 2, 128, 128, torch.bfloat16)
@@ -333,11 +337,26 @@ def test_workspace_smaller_than_the_fastest_plan():
 
 def test_reported_workspace_runs_the_segmented_plan():
     """With exactly kda_forward_workspace_bytes of workspace, a 4096-token, 16-head prefill runs
-    the segmented plan (segment summaries, scan, outputs), one launch each."""
+    the split, segmented plan (operand blocks, segment summaries, scan, outputs), one launch each."""
     from linear_attention_recurrence_kda_gb300 import profile_cases as P
     B.kda_profile_enable(True)
     P.prefill(4096, 16, 0, torch.bfloat16)
     prof = B.kda_profile_read()
     B.kda_profile_enable(False)
-    assert set(prof) == {"kda_seg_summary_tc", "kda_seg_scan", "kda_chunk_fwd_tc"}
+    assert set(prof) == {"kda_chunk_prep_tc", "kda_state_summary_tc", "kda_seg_scan", "kda_chunk_state_tc"}
     assert all(n == 1 for n, _ in prof.values())
+
+
+def test_fused_plan_when_forced(monkeypatch):
+    """KDA_TC_PLAN=fused selects the fused kernel (its three segmented passes) for the same
+    prefill, with a correspondingly smaller reported workspace."""
+    from linear_attention_recurrence_kda_gb300 import profile_cases as P
+    prob = B.make_problem(1, 4096, 4096, 16, 128, 128, torch.bfloat16)
+    split_ws = B.kda_forward_workspace_bytes(prob)
+    monkeypatch.setenv("KDA_TC_PLAN", "fused")
+    assert B.kda_forward_workspace_bytes(prob) < split_ws
+    B.kda_profile_enable(True)
+    P.prefill(4096, 16, 0, torch.bfloat16)
+    prof = B.kda_profile_read()
+    B.kda_profile_enable(False)
+    assert set(prof) == {"kda_seg_summary_tc", "kda_seg_scan", "kda_chunk_fwd_tc"}
