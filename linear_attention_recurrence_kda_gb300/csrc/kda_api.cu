@@ -115,11 +115,13 @@ void segment_plan(const kda_problem_t& p, size_t budget_bytes, bool split, int32
         }
         return;
     }
-    // cost in units of one chunk step of a chain: pass 3 runs nseg segments per (seq, head), pass 1
-    // two summaries (S~ and M) of every segment but the last, each in waves of `slots` concurrent
-    // chains (two state-pass CTAs per SM in the split plan, one fused CTA per SM otherwise); one
-    // step of the scan costs about scan_step chunk steps
-    const double sms = (double)sm_count_of_current_device() * (split ? 2.0 : 1.0);
+    // cost in units of one chunk step of a chain running alone on an SM: pass 3 runs nseg segments
+    // per (seq, head) in waves of one chain per SM; pass 1 two summaries (S~ and M) of every
+    // segment but the last -- in the split plan two chains per SM, each about 1.3 times slower,
+    // in the fused plan one; one step of the scan costs about scan_step chunk steps
+    const double sms = (double)sm_count_of_current_device();
+    const double sum_slots = sms * (split ? 2.0 : 1.0);
+    const double sum_cost = split ? 1.3 : 1.0;
     const double scan_step = split ? 2.5 : 1.5;
     const double units = (double)p.num_seqs * p.num_heads;
     const double per_seg = units * p.d_k * p.d_v * 4.0 * 3.0;  // S_in, S~ and M of one segment
@@ -129,7 +131,8 @@ void segment_plan(const kda_problem_t& p, size_t budget_bytes, bool split, int32
         const int64_t ns = (chunks + sc - 1) / sc;
         if (ns < 2) continue;
         if (per_seg * (double)ns > (double)budget_bytes || per_seg * (double)ns > 2.0e9) continue;
-        const double cost = (double)sc * (std::ceil(units * ns / sms) + std::ceil(2.0 * units * (ns - 1) / sms)) +
+        const double cost = (double)sc * (std::ceil(units * ns / sms) +
+                                          sum_cost * std::ceil(2.0 * units * (ns - 1) / sum_slots)) +
                             scan_step * (double)(ns - 1);
         if (cost < 0.9 * best) {
             best = cost;

@@ -423,6 +423,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_chunk_fwd_tc_kernel(PrefillAr
         else dst = (mode == 1 ? a.seg_st : a.seg_mt) + segbase;
         if (*abort_flag) {
             if (tid == 0) atomicOr(a.check, kCheckTimeout);
+        } else if (dst && mode == 2) {
+            // the transition is stored transposed, M^T[j][c], for the scan
+            float4* d4 = reinterpret_cast<float4*>(dst + (int64_t)jrow * D + 64 * h2);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) d4[q] = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
         } else if (dst) {
 #pragma unroll
             for (int cc = 0; cc < 64; ++cc) dst[(int64_t)(64 * h2 + cc) * D + jrow] = S[cc];

@@ -7,10 +7,14 @@
 // entering segment k+1 is
 //     S_in[k+1] = M_k S_in[k] + S~_k,     S_in[0] = the sequence's initial state (or zero).
 // This kernel walks that short chain.  Value columns are independent (column j of S only meets
-// column j), so the grid splits them: one CTA per (sequence, head, block of 16 columns).  M_k is
-// staged through shared memory with asynchronous copies, the next one while the current step
-// computes (double buffer, padded rows); each thread produces a 4 x 2 tile of the 128 x 16 result
-// with fp32 FMAs.
+// column j), so the grid splits them: one CTA per (sequence, head, block of 16 columns).
+//
+// The summary pass stores every M_k transposed (M_k^T[c'][c], so that column c' of M_k -- the
+// coefficients of input row c' -- is contiguous).  M_k^T is staged through shared memory with
+// asynchronous copies, the next one while the current step computes.  Each of the 256 threads owns
+// a 4 x 4 tile of the 128 x 16 result over one half of the contraction (64 of the 128 input rows):
+// per input row one 16-byte load of M^T, one (broadcast) 16-byte load of S_in and 16 fp32 FMAs; the
+// two halves are added through shared memory.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -19,8 +23,7 @@ namespace {
 
 constexpr int D = 128;
 constexpr int COLS = 16;         // value columns per CTA
-constexpr int NTHREADS = 256;    // 32 row groups of 4 x 8 column pairs
-constexpr int MROW = D + 4;      // padded row of the staged M (floats; keeps 16-byte alignment)
+constexpr int NTHREADS = 256;    // 2 contraction halves x 4 column groups x 32 row groups
 
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src)
 {
@@ -31,30 +34,29 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src)
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all_but_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
-// Asynchronously stage M (row-major [128][128] fp32) into padded shared rows.
-__device__ __forceinline__ void stage_m(float* dst, const float* M, int tid)
+// Asynchronously stage M^T ([128][128] fp32, rows contiguous) into shared memory.
+__device__ __forceinline__ void stage_mt(float* dst, const float* Mt, int tid)
 {
 #pragma unroll 4
-    for (int e4 = tid; e4 < D * D / 4; e4 += NTHREADS) {
-        const int r = (4 * e4) / D, c = (4 * e4) % D;
-        cp_async16(dst + r * MROW + c, M + 4 * e4);
-    }
+    for (int e4 = tid; e4 < D * D / 4; e4 += NTHREADS) cp_async16(dst + 4 * e4, Mt + 4 * e4);
 }
 
 }  // namespace
 
-__global__ void __launch_bounds__(NTHREADS) kda_segment_scan_kernel(PrefillArgs a)
+__global__ void __launch_bounds__(NTHREADS, 1) kda_segment_scan_kernel(PrefillArgs a)
 {
     extern __shared__ __align__(16) float smem_f[];
-    float* sM = smem_f;                       // [2][D][MROW] double-buffered transition
-    float* sS = smem_f + 2 * D * MROW;        // [D][COLS] incoming state slice
+    float* sM = smem_f;                       // [2][D][D] double-buffered M^T
+    float* sS = smem_f + 2 * D * D;           // [D][COLS] incoming state slice
+    float* sP = sS + D * COLS;                // [128 threads][16] partial tiles of the upper half
 
     const int n = blockIdx.x;
     const int h = blockIdx.y;
     const int j0 = blockIdx.z * COLS;
     const int tid = threadIdx.x;
-    const int rg = tid >> 3;            // rows 4 rg .. 4 rg + 3
-    const int cp = tid & 7;             // columns j0 + 2 cp, j0 + 2 cp + 1
+    const int kh = tid >> 7;             // contraction half: input rows [64 kh, 64 kh + 64)
+    const int cg = (tid >> 5) & 3;       // columns j0 + 4 cg .. + 3
+    const int rg = tid & 31;             // rows 4 rg .. 4 rg + 3
 
     int64_t q0, q1;
     if (!seq_range(a, n, q0, q1)) return;
@@ -66,7 +68,7 @@ __global__ void __launch_bounds__(NTHREADS) kda_segment_scan_kernel(PrefillArgs 
     const int H = a.H;
     const int64_t sbase = ((int64_t)n * H + h) * D * D;
     const int64_t seg0 = ((int64_t)n * H + h) * a.max_seg * D * D;
-    stage_m(sM, a.seg_mt + seg0, tid);
+    stage_mt(sM, a.seg_mt + seg0, tid);
     cp_async_commit();
     for (int e = tid; e < D * COLS; e += NTHREADS) {
         const int c = e / COLS, jj = e % COLS;
@@ -75,44 +77,64 @@ __global__ void __launch_bounds__(NTHREADS) kda_segment_scan_kernel(PrefillArgs 
 
     for (int64_t k = 0; k + 1 < nseg; ++k) {
         const int64_t segk = seg0 + k * D * D;
-        float* Mk = sM + (k & 1) * D * MROW;
+        const float* Mt = sM + (k & 1) * D * D;
         // prefetch the next transition into the other buffer (an empty group on the last step)
-        if (k + 2 < nseg) stage_m(sM + ((k + 1) & 1) * D * MROW, a.seg_mt + segk + D * D, tid);
+        if (k + 2 < nseg) stage_mt(sM + ((k + 1) & 1) * D * D, a.seg_mt + segk + D * D, tid);
         cp_async_commit();
-        const float* St = a.seg_st + segk;
-        float acc[4][2];
+        float4 st[4];
+        if (kh == 0) {
+            const float* St = a.seg_st + segk;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 st = *reinterpret_cast<const float2*>(St + (int64_t)(4 * rg + i) * D + j0 + 2 * cp);
-            acc[i][0] = st.x;
-            acc[i][1] = st.y;
+            for (int i = 0; i < 4; ++i)
+                st[i] = *reinterpret_cast<const float4*>(St + (int64_t)(4 * rg + i) * D + j0 + 4 * cg);
         }
-        cp_async_wait_all_but_one();   // M_k has landed (this thread's part)
+        cp_async_wait_all_but_one();   // M_k^T has landed (this thread's part)
         __syncthreads();               // ... and every thread's part; sS of the previous step is written
-#pragma unroll 4
-        for (int c = 0; c < D; ++c) {
-            const float2 sv = *reinterpret_cast<const float2*>(sS + c * COLS + 2 * cp);
+        float acc[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) acc[i][jj] = 0.f;
+#pragma unroll 8
+        for (int cc = 0; cc < 64; ++cc) {
+            const int c = 64 * kh + cc;
+            const float4 m = *reinterpret_cast<const float4*>(Mt + c * D + 4 * rg);      // M_k[4 rg + i][c]
+            const float4 sv = *reinterpret_cast<const float4*>(sS + c * COLS + 4 * cg);  // S_in[c][j]
+            const float mi[4] = {m.x, m.y, m.z, m.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float m = Mk[(4 * rg + i) * MROW + c];
-                acc[i][0] = fmaf(m, sv.x, acc[i][0]);
-                acc[i][1] = fmaf(m, sv.y, acc[i][1]);
+                acc[i][0] = fmaf(mi[i], sv.x, acc[i][0]);
+                acc[i][1] = fmaf(mi[i], sv.y, acc[i][1]);
+                acc[i][2] = fmaf(mi[i], sv.z, acc[i][2]);
+                acc[i][3] = fmaf(mi[i], sv.w, acc[i][3]);
             }
         }
-        __syncthreads();               // every read of sS and Mk is done
-        float* out = a.seg_in + segk + D * D;
+        if (kh == 1) {
+            float* pp = sP + (tid - 128) * 16;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int r = 4 * rg + i;
-            *reinterpret_cast<float2*>(sS + r * COLS + 2 * cp) = make_float2(acc[i][0], acc[i][1]);
-            *reinterpret_cast<float2*>(out + (int64_t)r * D + j0 + 2 * cp) = make_float2(acc[i][0], acc[i][1]);
+            for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<float4*>(pp + 4 * i) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        }
+        __syncthreads();               // every read of sS and Mt is done; the upper half's partials are in
+        if (kh == 0) {
+            const float* pp = sP + tid * 16;
+            float* out = a.seg_in + segk + D * D;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 u = *reinterpret_cast<const float4*>(pp + 4 * i);
+                const float4 r = make_float4(acc[i][0] + u.x + st[i].x, acc[i][1] + u.y + st[i].y,
+                                             acc[i][2] + u.z + st[i].z, acc[i][3] + u.w + st[i].w);
+                const int row = 4 * rg + i;
+                *reinterpret_cast<float4*>(sS + row * COLS + 4 * cg) = r;
+                *reinterpret_cast<float4*>(out + (int64_t)row * D + j0 + 4 * cg) = r;
+            }
         }
     }
 }
 
 cudaError_t launch_segment_scan(const PrefillArgs& a, cudaStream_t s)
 {
-    const size_t smem = (size_t)(2 * D * MROW + D * COLS) * sizeof(float);
+    const size_t smem = (size_t)(2 * D * D + D * COLS + 128 * 16) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(kda_segment_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kda_segment_scan_kernel<<<dim3((unsigned)a.N, (unsigned)a.H, D / COLS), NTHREADS, smem, s>>>(a);

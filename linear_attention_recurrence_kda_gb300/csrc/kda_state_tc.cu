@@ -9,16 +9,20 @@
 // Value channels j are the 128 TMEM lanes.  Per chunk: D1 = S^T [W ; Q Gamma]^T (M = 128, N = 32,
 // K = 128) -> U^T = U~^T - D1[:, :16] as a bf16 hi/lo pair -> O^T += U^T P^T and
 // dS^T = U^T (K Gamma_C / Gamma) (hi*hi + hi*lo + lo*hi) -> S <- Diag(Gamma_C) S + dS in registers
-// (thread = one value channel x 64 key channels), re-staged as the bf16 SW128 operand of the next D1.
-// The blocks stream through a two-slot shared-memory ring by plain bulk copies, the next but one
-// issued as soon as a slot is free.  256 threads and ~93 KB of shared memory per CTA: two CTAs
-// (two independent chains) share an SM, hiding each other's latency.
+// (thread = one value channel x 64 key channels).  The A operands of these products -- the bf16 copy
+// of S^T and U^T hi/lo -- are written to tensor memory (tcgen05.st) rather than shared memory, so the
+// tensor core reads only the chunk's B operands (W, Q Gamma, K Gamma_C / Gamma, P) from shared memory.
+// The operand blocks stream through a four-slot shared-memory ring by plain bulk copies issued four
+// chunks ahead.  256 threads and ~105 KB of shared memory per CTA: two CTAs (two independent chains)
+// share an SM, hiding each other's latency.  Outputs are moved from tensor memory to registers with
+// the state update and stored while the next chunk's first product runs.
 //
 // Modes (segmented prefill, see the launcher): 0 writes outputs and (last segment) the final state;
 // 1 computes S~, the segment's end state from a zero start; 2 computes M, the segment's transition,
 // as the end state from the identity with V = 0 (columns of M evolve exactly like state columns).
 // Every mbarrier wait is bounded; a wait that gives up raises the timeout bit of the check word,
-// the CTA skips the remaining work, waits (bounded) for its copies in flight and frees its TMEM.
+// the CTA skips the remaining work, waits (bounded) for its copies and products in flight and frees
+// its tensor memory.
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
 #include "kda_tc_chunk.cuh"
@@ -35,25 +39,26 @@ using tcc::u2f;
 
 constexpr int NTHREADS = 256;
 constexpr uint32_t WAIT_LIMIT = 1u << 17;  // tries of up to 20 us each: ~2.6 s at most
+constexpr int NSLOT = 4;                   // ring depth (chunks in flight)
 constexpr uint32_t SLOT = 26624;           // ring slot stride (a multiple of 1024 >= BLK_BYTES)
 
 // shared-memory map (bytes from a 1024-aligned base)
-constexpr uint32_t OFF_S = 0;           // S^T [128 j][128 c] bf16 SW128                 32768
-constexpr uint32_t OFF_RING = 32768;    // [2] operand blocks                        2 x 26624
-constexpr uint32_t OFF_UT = 86016;      // U^T hi, lo [128 j][16 i] NONE                  8192
-constexpr uint32_t OFF_BARF = 94208;    // mbarriers: ring slot filled [2]                  16
-constexpr uint32_t OFF_BARC = 94224;    // mbarrier: tensor-core commits                     8
-constexpr uint32_t OFF_TSLOT = 94232;   // TMEM base address                                  4
-constexpr uint32_t OFF_ABORT = 94236;   // stop flag                                          4
-constexpr uint32_t SMEM_USED = 94240;
+constexpr uint32_t OFF_RING = 0;                         // [NSLOT] operand blocks
+constexpr uint32_t OFF_BARF = NSLOT * SLOT;              // mbarriers: ring slot filled [NSLOT]
+constexpr uint32_t OFF_BARC = OFF_BARF + 8 * NSLOT;      // mbarrier: tensor-core commits
+constexpr uint32_t OFF_TSLOT = OFF_BARC + 8;             // TMEM base address
+constexpr uint32_t OFF_ABORT = OFF_TSLOT + 4;            // stop flag
+constexpr uint32_t SMEM_USED = OFF_ABORT + 4;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
 
 static_assert(SLOT >= tcc::BLK_BYTES && SLOT % 1024 == 0, "ring slots must hold a block at 1024-byte alignment");
-static_assert(OFF_UT >= OFF_RING + 2 * SLOT, "shared-memory map overlaps");
+static_assert(2 * (SMEM_BYTES + 1024) <= 232448, "two CTAs must fit on an SM");
 
 // tensor-memory columns
-constexpr uint32_t TM_D1 = 0;    // [0, 16) (W S)^T, [16, 32) O^T
-constexpr uint32_t TM_D3 = 128;  // dS^T (lanes = j, columns = c)
+constexpr uint32_t TM_D1 = 0;     // [0, 16) (W S)^T, [16, 32) O^T
+constexpr uint32_t TM_D3 = 32;    // dS^T (lanes = j, columns = c), 128 columns
+constexpr uint32_t TM_SA = 160;   // bf16 S^T as the A operand of D1: c pairs, 64 columns
+constexpr uint32_t TM_UA = 224;   // bf16 U^T hi (8 columns), lo (8 columns): A operand of dS and O
 constexpr uint32_t TM_COLS = 256;
 
 __device__ __forceinline__ void sync_all() { tcc::named_sync(1, NTHREADS); }
@@ -66,7 +71,10 @@ __device__ __forceinline__ bool read_dead(const volatile uint32_t* abort_flag)
 
 }  // namespace
 
-__global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(PrefillArgs a)
+// MIN_BLOCKS = 2 caps registers at 128 so that two chains share an SM (segment summaries: many
+// chains); MIN_BLOCKS = 1 lets the compiler keep the state pass free of spills (one chain per SM).
+template <int MIN_BLOCKS>
+__global__ void __launch_bounds__(NTHREADS, MIN_BLOCKS) kda_chunk_state_tc_kernel(PrefillArgs a)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -102,8 +110,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
 
     if (w == 0) tc::tmem_alloc(tslot, TM_COLS);
     if (tid == 0) {
-        tc::mbar_init(&bar_f[0], 1);
-        tc::mbar_init(&bar_f[1], 1);
+        for (int sl = 0; sl < NSLOT; ++sl) tc::mbar_init(&bar_f[sl], 1);
         tc::mbar_init(bar_c, 1);
         *abort_flag = 0u;
     }
@@ -113,31 +120,22 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
     tc::fence_after_sync();
     const uint32_t tbase = *tslot;
 
-    // thread 0 owns the ring: pending loads per slot and the parity of each slot's next fill
-    uint32_t pend = 0, ph_f0 = 0, ph_f1 = 0, ph_c = 0;
-    bool pend_c = false;  // a tensor-core commit whose completion was not observed
+    // ring bookkeeping: every thread tracks each slot's fill parity; thread 0 also the loads it
+    // issued and has not seen complete, and an unobserved tensor-core commit
+    uint32_t phb = 0, pend = 0, ph_c = 0;
+    bool pend_c = false;
     auto issue_load = [&](int chunk) {
-        const int sl = chunk & 1;
+        const int sl = chunk % NSLOT;
         tc::mbar_arrive_expect_tx(&bar_f[sl], tcc::BLK_BYTES);
         tc::bulk_load(sm + OFF_RING + sl * SLOT, block_of(chunk), tcc::BLK_BYTES, &bar_f[sl]);
         pend |= 1u << sl;
     };
-    auto wait_slot = [&](int sl) -> bool {
-        const bool ok = tc::mbar_wait(&bar_f[sl], sl ? ph_f1 : ph_f0, WAIT_LIMIT);
-        if (ok) {
-            pend &= ~(1u << sl);
-            if (sl) ph_f1 ^= 1u;
-            else ph_f0 ^= 1u;
-        }
-        return ok;
-    };
     if (tid == 0) {
-        if (nchunks > 0) issue_load(0);
-        if (nchunks > 1) issue_load(1);
+        for (int c = 0; c < NSLOT && c < nchunks; ++c) issue_load(c);
     }
 
     const int q4 = w & 3;    // TMEM lane quarter
-    const int h2 = w >> 2;   // which half of the key channels this warp's state slice covers
+    const int h2 = w >> 2;   // which half of the key channels (and of the chunk's tokens) this warp covers
     const int jrow = 32 * q4 + lane;
     const uint32_t lane_base = tbase + ((uint32_t)(32 * q4) << 16);
     __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.out);
@@ -153,54 +151,79 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
         const int c = 64 * h2 + cc;
         S[cc] = init ? init[(int64_t)c * D + jrow] : ((mode == 2 && c == jrow) ? 1.f : 0.f);
     }
+    // bf16 S^T into the A operand of D1: this thread's 64 key channels are 32 columns
     auto stage_state = [&]() {
 #pragma unroll
-        for (int chn = 0; chn < 8; ++chn) {
-            uint4 pk;
-            pk.x = tc::pack_bf16(S[8 * chn + 0], S[8 * chn + 1]);
-            pk.y = tc::pack_bf16(S[8 * chn + 2], S[8 * chn + 3]);
-            pk.z = tc::pack_bf16(S[8 * chn + 4], S[8 * chn + 5]);
-            pk.w = tc::pack_bf16(S[8 * chn + 6], S[8 * chn + 7]);
-            *reinterpret_cast<uint4*>(sm + OFF_S + tc::sw128_chunk_off(jrow, 8 * h2 + chn, D)) = pk;
+        for (int half = 0; half < 2; ++half) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int m = 0; m < 16; ++m) pk[m] = tc::pack_bf16(S[32 * half + 2 * m], S[32 * half + 2 * m + 1]);
+            KDA_TMEM_ST16(lane_base + TM_SA + 32 * h2 + 16 * half, pk);
         }
+        tc::tmem_wait_st();
     };
     stage_state();
-    tc::fence_async_smem();
     tc::fence_before_sync();
     sync_all();
     tc::fence_after_sync();
 
+    // outputs of the previous chunk, held in registers until the next chunk's first product runs
+    uint32_t ovp[4];  // bf16 pairs
+    int64_t o_t0 = 0;
+    int o_len = 0;
+    bool o_have = false;
+    auto store_outputs = [&]() {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int r = 8 * h2 + e;
+            const unsigned short bits = (unsigned short)((e & 1) ? (ovp[e >> 1] >> 16) : (ovp[e >> 1] & 0xffffu));
+            if (r < o_len) op[((o_t0 + r) * H + h) * D + jrow] = __ushort_as_bfloat16(bits);
+        }
+        o_have = false;
+    };
+
     for (int ch = 0; ch < nchunks; ++ch) {
-        const int sl = ch & 1;
+        const int sl = ch % NSLOT;
         unsigned char* blk = sm + OFF_RING + sl * SLOT;
-        const int64_t t0 = s0 + (int64_t)ch * C;
-        const int len = chunk_len(ch);
         bool dead = read_dead(abort_flag);
 
-        // D1 = S^T [W ; Q Gamma]^T (M = 128, K = 128; N = 32 with outputs, else 16: W only)
-        if (tid == 0 && !dead) {
-            if (!wait_slot(sl)) {
-                *abort_flag = 1u;
+        // every thread waits for the block; thread 0 issues D1 = S^T [W ; Q Gamma]^T
+        // (M = 128, K = 128; N = 32 with outputs, else 16: W only)
+        bool got = false;
+        if (!dead) {
+            got = tc::mbar_wait(&bar_f[sl], (phb >> sl) & 1u, WAIT_LIMIT);
+            if (got) {
+                phb ^= 1u << sl;
+                if (tid == 0) pend &= ~(1u << sl);
             } else {
-                const uint32_t nq = (mode == 0) ? 2 * C : C;
-                const uint32_t idd = tc::idesc_bf16(128, (int)nq);
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
-                    tc::umma(tbase + TM_D1, tc::desc_sw128(tc::smem_u32(sm + OFF_S + kb * 16384 + off)),
-                             tc::desc_sw128(tc::smem_u32(blk + tcc::BLK_WQ + kb * (2 * C * 128) + off)), idd,
-                             ks > 0 ? 1u : 0u);
-                }
-                tc::umma_commit(bar_c);
-                if (tc::mbar_wait(bar_c, ph_c, WAIT_LIMIT)) ph_c ^= 1u;
-                else *abort_flag = 1u, pend_c = true;
+                *abort_flag = 1u;
             }
         }
+        bool issued = false;
+        if (tid == 0 && got) {
+            const uint32_t idd = tc::idesc_bf16(128, mode == 0 ? 2 * C : C);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
+                tc::umma_ts(tbase + TM_D1, tbase + TM_SA + 8 * ks,
+                            tc::desc_sw128(tc::smem_u32(blk + tcc::BLK_WQ + kb * (2 * C * 128) + off)), idd,
+                            ks > 0 ? 1u : 0u);
+            }
+            tc::umma_commit(bar_c);
+            issued = true;
+        }
+        if (o_have && w != 0) store_outputs();
+        if (issued) {
+            if (tc::mbar_wait(bar_c, ph_c, WAIT_LIMIT)) ph_c ^= 1u;
+            else *abort_flag = 1u, pend_c = true;
+        }
+        if (o_have) store_outputs();  // warp 0, after its thread 0 has issued and waited
+        tc::fence_before_sync();
         sync_all();
         tc::fence_after_sync();
         dead = read_dead(abort_flag);
 
-        // U^T = U~^T - (W S)^T as a hi/lo pair; warp half h2 takes tokens 8 h2 .. 8 h2 + 7
+        // U^T = U~^T - (W S)^T as a hi/lo pair into tensor memory; warp half h2 takes tokens 8 h2 .. + 7
         if (!dead) {
             uint32_t dv[8];
             KDA_TMEM_LD8(lane_base + TM_D1 + 8 * h2, dv);
@@ -214,11 +237,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
             for (int e = 0; e < 4; ++e) {
                 tcc::split2(uv[2 * e] - u2f(dv[2 * e]), uv[2 * e + 1] - u2f(dv[2 * e + 1]), hi[e], lo[e]);
             }
-            *reinterpret_cast<uint4*>(sm + OFF_UT + tc::none_off(jrow, 8 * h2)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(sm + OFF_UT + NONE_TILE + tc::none_off(jrow, 8 * h2)) =
-                make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            KDA_TMEM_ST4(lane_base + TM_UA + 4 * h2, hi);
+            KDA_TMEM_ST4(lane_base + TM_UA + 8 + 4 * h2, lo);
+            tc::tmem_wait_st();
         }
-        tc::fence_async_smem();
         tc::fence_before_sync();
         sync_all();
         tc::fence_after_sync();
@@ -227,20 +249,18 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
         if (tid == 0 && !dead) {
             const uint32_t id16 = tc::idesc_bf16(128, 16);
             const uint32_t id128 = tc::idesc_bf16(128, 128);
-            const uint64_t dU = tc::desc_none(tc::smem_u32(sm + OFF_UT));
-            const uint64_t dUl = tc::desc_none(tc::smem_u32(sm + OFF_UT + NONE_TILE));
             const uint64_t dK = tc::desc_none(tc::smem_u32(blk + tcc::BLK_KT));
             const uint64_t dKl = tc::desc_none(tc::smem_u32(blk + tcc::BLK_KT + NONE_TILE));
+            tc::umma_ts(tbase + TM_D3, tbase + TM_UA, dK, id128, 0u);
+            tc::umma_ts(tbase + TM_D3, tbase + TM_UA, dKl, id128, 1u);
+            tc::umma_ts(tbase + TM_D3, tbase + TM_UA + 8, dK, id128, 1u);
             if (mode == 0) {
                 const uint64_t dP = tc::desc_none(tc::smem_u32(blk + tcc::BLK_P));
                 const uint64_t dPl = tc::desc_none(tc::smem_u32(blk + tcc::BLK_P + SMALL_TILE));
-                tc::umma(tbase + TM_D1 + C, dU, dP, id16, 1u);
-                tc::umma(tbase + TM_D1 + C, dU, dPl, id16, 1u);
-                tc::umma(tbase + TM_D1 + C, dUl, dP, id16, 1u);
+                tc::umma_ts(tbase + TM_D1 + C, tbase + TM_UA, dP, id16, 1u);
+                tc::umma_ts(tbase + TM_D1 + C, tbase + TM_UA, dPl, id16, 1u);
+                tc::umma_ts(tbase + TM_D1 + C, tbase + TM_UA + 8, dP, id16, 1u);
             }
-            tc::umma(tbase + TM_D3, dU, dK, id128, 0u);
-            tc::umma(tbase + TM_D3, dU, dKl, id128, 1u);
-            tc::umma(tbase + TM_D3, dUl, dK, id128, 1u);
             tc::umma_commit(bar_c);
             if (tc::mbar_wait(bar_c, ph_c, WAIT_LIMIT)) ph_c ^= 1u;
             else *abort_flag = 1u, pend_c = true;
@@ -249,7 +269,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
         tc::fence_after_sync();
         dead = read_dead(abort_flag);
 
-        // S <- Diag(Gamma_C) S + dS (staged for the next read), outputs of the chunk
+        // S <- Diag(Gamma_C) S + dS, staged as the next chunk's A operand; outputs to registers
         if (!dead) {
             const float* gc = reinterpret_cast<const float*>(blk + tcc::BLK_GC) + 64 * h2;
 #pragma unroll
@@ -272,22 +292,22 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
             }
             stage_state();
             if (mode == 0) {
-                uint32_t ov[8];
-                KDA_TMEM_LD8(lane_base + TM_D1 + C + 8 * h2, ov);
+                uint32_t ob[8];
+                KDA_TMEM_LD8(lane_base + TM_D1 + C + 8 * h2, ob);
                 tc::tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int r = 8 * h2 + e;
-                    if (r < len) op[((t0 + r) * H + h) * D + jrow] = __float2bfloat16_rn(u2f(ov[e]));
-                }
+                for (int e = 0; e < 4; ++e) ovp[e] = tc::pack_bf16(u2f(ob[2 * e]), u2f(ob[2 * e + 1]));
+                o_t0 = s0 + (int64_t)ch * C;
+                o_len = chunk_len(ch);
+                o_have = true;
             }
         }
-        tc::fence_async_smem();
         tc::fence_before_sync();
         sync_all();  // every read of this slot is done; the next state is staged
         tc::fence_after_sync();
-        if (tid == 0 && ch + 2 < nchunks && *abort_flag == 0u) issue_load(ch + 2);
+        if (tid == 0 && *abort_flag == 0u && ch + NSLOT < nchunks) issue_load(ch + NSLOT);
     }
+    if (o_have) store_outputs();
 
     float* dst = nullptr;
     if (mode == 0) dst = ((int64_t)k == nseg - 1 && a.s_final) ? a.s_final + sbase : nullptr;
@@ -297,14 +317,21 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
             atomicOr(a.check, kCheckTimeout);
             // copies and tensor-core work still in flight must finish before the shared and tensor
             // memory are released
-            for (int sl = 0; sl < 2; ++sl) {
-                if (pend & (1u << sl)) (void)wait_slot(sl);
+            for (int sl = 0; sl < NSLOT; ++sl) {
+                if (pend & (1u << sl)) (void)tc::mbar_wait(&bar_f[sl], (phb >> sl) & 1u, WAIT_LIMIT);
             }
             if (pend_c) (void)tc::mbar_wait(bar_c, ph_c, WAIT_LIMIT);
         }
     } else if (dst) {
+        if (mode == 2) {
+            // the transition is stored transposed, M^T[j][c], for the scan
+            float4* d4 = reinterpret_cast<float4*>(dst + (int64_t)jrow * D + 64 * h2);
 #pragma unroll
-        for (int cc = 0; cc < 64; ++cc) dst[(int64_t)(64 * h2 + cc) * D + jrow] = S[cc];
+            for (int q = 0; q < 16; ++q) d4[q] = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
+        } else {
+#pragma unroll
+            for (int cc = 0; cc < 64; ++cc) dst[(int64_t)(64 * h2 + cc) * D + jrow] = S[cc];
+        }
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -315,14 +342,15 @@ namespace {
 
 cudaError_t launch_chunk_state_tc(const PrefillArgs& a, int seg_mode, cudaStream_t s)
 {
-    cudaError_t e = cudaFuncSetAttribute(kda_chunk_state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+    // summaries (two chains per summarised segment) pack two CTAs per SM; the output pass runs one
+    auto kern = seg_mode == 0 ? kda_chunk_state_tc_kernel<1> : kda_chunk_state_tc_kernel<2>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     PrefillArgs b = a;
     b.seg_mode = seg_mode;
     const unsigned gz = seg_mode == 0 ? (unsigned)(a.max_seg > 1 ? a.max_seg : 1) : (unsigned)(2 * (a.max_seg - 1));
     if (gz == 0) return cudaSuccess;
-    kda_chunk_state_tc_kernel<<<dim3((unsigned)a.N, (unsigned)a.H, gz), NTHREADS, SMEM_BYTES, s>>>(b);
+    kern<<<dim3((unsigned)a.N, (unsigned)a.H, gz), NTHREADS, SMEM_BYTES, s>>>(b);
     return cudaGetLastError();
 }
 

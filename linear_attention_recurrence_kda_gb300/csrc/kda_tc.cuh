@@ -96,6 +96,19 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a_desc, uint64_t 
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T, issued by one thread.  A (M = 128 rows) sits in tensor memory
+// with row m in lane m and its 16-bit K elements packed in pairs (even k in the low half) along
+// the columns: one K = 16 step occupies 8 columns.
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive on an mbarrier once all previously issued tcgen05 operations of this thread complete.
 __device__ __forceinline__ void umma_commit(uint64_t* bar)
 {
@@ -122,6 +135,21 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
                  : "r"(taddr))
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Store 32-bit registers to this warp's 32 lanes of tensor memory, consecutive columns.
+#define KDA_TMEM_ST4(taddr, v)                                                                     \
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(v[0]), \
+                 "r"(v[1]), "r"(v[2]), "r"(v[3])                                                    \
+                 : "memory")
+
+#define KDA_TMEM_ST16(taddr, v)                                                                             \
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14," \
+                 "%15,%16};" ::"r"(taddr),                                                                   \
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),      \
+                 "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])  \
+                 : "memory")
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------- mbarrier
 
@@ -175,6 +203,12 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                      smem_u32(dst)),
                  "l"(src), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
+}
+
+// Hint: bring `bytes` (multiple of 16) of global memory at `src` (16-byte aligned) into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // Contiguous shared -> global copy, tracked in this thread's bulk async-group.
