@@ -76,7 +76,7 @@ kda_status_t check_device_pointer(const void* p)
     return KDA_OK;
 }
 
-int sm_count_of_current_device()
+int sm_count_cached()
 {
     static int cached[64] = {};
     int dev = 0;
@@ -98,6 +98,8 @@ int sm_count_of_current_device()
 }  // namespace
 
 namespace kda {
+
+int sm_count_of_current_device() { return sm_count_cached(); }
 
 void segment_plan(const kda_problem_t& p, size_t budget_bytes, bool split, int32_t& seg_chunks, int32_t& max_seg)
 {

@@ -120,7 +120,8 @@ struct FusedMap {
     static constexpr uint32_t OFF_PART = ::kda::OFF_PART;
     static constexpr uint32_t OFF_BETA = ::kda::OFF_BETA;
     static constexpr uint32_t OFF_T = ::kda::OFF_T;
-    static constexpr uint32_t NB = 2;  // producer-group barrier
+    static constexpr uint32_t NB = 2;       // producer-group barrier
+    static constexpr uint32_t XT_RG = 256;  // (K Gamma)^T and V^T are tensor-core operands here
 };
 
 // Abort flag, read identically by every lane of the warp (it guards warp-collective instructions).

@@ -162,6 +162,9 @@ cudaError_t launch_prefill_split_tc(const PrefillArgs& a, cudaStream_t s);  // b
 cudaError_t launch_segment_scan(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
 
+// SM count of the current device (cached per device; 152 if it cannot be queried).
+int sm_count_of_current_device();
+
 // Optional per-kernel timing around launches (no-ops unless kda_profile_enable(1)).
 void prof_start(const char* name, cudaStream_t s);
 void prof_stop(cudaStream_t s);

@@ -4,14 +4,14 @@
 // (Equation 5), the in-chunk decays, the WY/UT transform and the in-chunk output product -- is
 // computed here for every chunk of every (sequence, head) at once, and written as one contiguous
 // operand block per chunk (layout: tcc::BLK_*):
-//   [W ; Q Gamma] SW128, (K Gamma_C / Gamma)^T hi/lo, U~ = T' V (fp32), P hi/lo, Gamma_C
+//   [W ; Q Gamma] SW128, [P ; (K Gamma_C / Gamma)^T] hi/lo, U~ = T' V (fp32), Gamma_C
 // with W = T diag(beta) (K Gamma), U~ = T diag(beta) V, T = (I + A)^-1 (the chunk form of Equation 1,
 // "Kimi K3: the paper and proofs side by side", section 2.1.1; "Kimi K3: architecture, derivations
 // and a pinned-source audit", section 4.5).  The sequential state pass (kda_state_tc.cu) then
 // only streams these blocks.
 //
-// One CTA of 256 threads walks a run of up to kRun chunks of one (sequence, head): the q, k, v, z
-// tiles arrive by TMA one chunk ahead, the factors, A, P and T come from the shared preparation
+// One CTA of 256 threads (three per SM) walks a run of up to kRun chunks of one (sequence, head):
+// the q, k, v, z tiles arrive by TMA one chunk ahead, the factors, A, P and T come from the shared preparation
 // functions, W and U~ from warp-level mma.sync (T' hi/lo against (K Gamma)^T and V^T), and the
 // assembled block leaves shared memory as one bulk copy.  Block slot of chunk c of sequence n:
 // cu[n] / 16 + n + c, so the slots of consecutive sequences never overlap
@@ -31,22 +31,23 @@ using tcc::NGROUP;
 constexpr int kRun = 4;                      // chunks per CTA
 constexpr uint32_t WAIT_LIMIT = 1u << 17;    // tries of up to 20 us each
 
-// shared-memory map (bytes from a 1024-aligned base)
+// shared-memory map (bytes from a 1024-aligned base); the operand block itself is written straight
+// to global memory
+constexpr uint32_t XT_RG = 272;          // padded 8-row-group stride of the transposed tiles
 constexpr uint32_t OFF_STAGE = 0;        // q, k, v, z tiles [16][128] bf16 (TMA)     16384
-constexpr uint32_t OFF_BLK = 16384;      // the operand block being assembled        26112
-constexpr uint32_t OFF_LL = 42496;       // K Gamma [16][LROW] bf16                     4352
-constexpr uint32_t OFF_QL = 46848;       // Q Gamma hi, lo                          2 x 4352
-constexpr uint32_t OFF_KD = 55552;       // K / Gamma hi, lo                        2 x 4352
-constexpr uint32_t OFF_XT = 64256;       // (K Gamma)^T [128 c][16 i] NONE              4096
-constexpr uint32_t OFF_VT = 68352;       // V^T [128 j][16 i] NONE                      4096
-constexpr uint32_t OFF_A = 72448;        // A fp32 [16][16]                             1024
-constexpr uint32_t OFF_PART = 73472;     // partial products fp32 [8][16][16]           8192
-constexpr uint32_t OFF_T = 81664;        // T' hi, lo [16][16] NONE                     1024
-constexpr uint32_t OFF_HS = 82688;       // quarter-chunk log-decay sums [4][128]       2048
-constexpr uint32_t OFF_BETA = 84736;     // beta [16]                                     64
-constexpr uint32_t OFF_BAR = 84800;      // mbarrier: TMA tile loads                       8
-constexpr uint32_t OFF_ABORT = 84808;    // stop flag                                      4
-constexpr uint32_t SMEM_USED = 84816;
+constexpr uint32_t OFF_LL = 16384;       // K Gamma [16][LROW] bf16                     4352
+constexpr uint32_t OFF_QL = 20736;       // Q Gamma hi, lo                          2 x 4352
+constexpr uint32_t OFF_KD = 29440;       // K / Gamma hi, lo                        2 x 4352
+constexpr uint32_t OFF_XT = 38144;       // (K Gamma)^T [128 c][16 i], padded           4352
+constexpr uint32_t OFF_VT = 42496;       // V^T [128 j][16 i], padded                   4352
+constexpr uint32_t OFF_A = 46848;        // A fp32 [16][16]                             1024
+constexpr uint32_t OFF_PART = 47872;     // partial products fp32 [8][16][16]           8192
+constexpr uint32_t OFF_T = 56064;        // T' hi, lo [16][16] NONE                     1024
+constexpr uint32_t OFF_HS = 57088;       // quarter-chunk log-decay sums [4][128]       2048
+constexpr uint32_t OFF_BETA = 59136;     // beta [16]                                     64
+constexpr uint32_t OFF_BAR = 59200;      // mbarrier: TMA tile loads                       8
+constexpr uint32_t OFF_ABORT = 59208;    // stop flag                                      4
+constexpr uint32_t SMEM_USED = 59212;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
 
 struct PrepMap {
@@ -62,42 +63,37 @@ struct PrepMap {
     static constexpr uint32_t OFF_BETA = ::kda::OFF_BETA;
     static constexpr uint32_t OFF_T = ::kda::OFF_T;
     static constexpr uint32_t NB = 1;
+    static constexpr uint32_t XT_RG = ::kda::XT_RG;
 };
 
-static_assert(OFF_BLK % 1024 == 0, "the SW128 part of the block needs 1024-byte alignment");
-static_assert(OFF_LL == OFF_BLK + tcc::BLK_BYTES, "shared-memory map out of order");
+static_assert(OFF_XT + 16 * XT_RG <= OFF_VT && OFF_VT + 16 * XT_RG <= OFF_A, "shared-memory map overlaps");
+static_assert(3 * (SMEM_BYTES + 1024) <= 232448, "three CTAs must fit on an SM");
 
 __device__ __forceinline__ void sync_all() { tcc::named_sync(1, NGROUP); }
 
 // W = T' (K Gamma) and U~ = T' V for the 16 channels [16 w, 16 w + 16) of warp w, by mma.sync
 // (M = 16 tokens, N = 8 channels per tile, K = 16 tokens; T' = hi + lo, two products each).
 // W goes to rows 0..15 of the block's SW128 [W ; Q Gamma] tile (bf16), U~ to its fp32 tile.
-__device__ __forceinline__ void wy_products(unsigned char* sm, int w, int lane)
+__device__ __forceinline__ void wy_products(const unsigned char* sm, unsigned char* blk, int w, int lane)
 {
     const int g = lane >> 2, t = lane & 3;
     const unsigned char* tt = sm + OFF_T;
     uint32_t th[4], tl[4];
-    th[0] = *reinterpret_cast<const uint32_t*>(tt + tc::none_off(g, 2 * t));
-    th[1] = *reinterpret_cast<const uint32_t*>(tt + tc::none_off(g + 8, 2 * t));
-    th[2] = *reinterpret_cast<const uint32_t*>(tt + tc::none_off(g, 2 * t + 8));
-    th[3] = *reinterpret_cast<const uint32_t*>(tt + tc::none_off(g + 8, 2 * t + 8));
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const uint32_t o = (e == 0)   ? tc::none_off(g, 2 * t)
-                           : (e == 1) ? tc::none_off(g + 8, 2 * t)
-                           : (e == 2) ? tc::none_off(g, 2 * t + 8)
-                                      : tc::none_off(g + 8, 2 * t + 8);
+        const uint32_t o = tc::none_off(g + 8 * (e & 1), 2 * t + 8 * (e >> 1));
+        th[e] = *reinterpret_cast<const uint32_t*>(tt + o);
         tl[e] = *reinterpret_cast<const uint32_t*>(tt + tcc::SMALL_TILE + o);
     }
-    unsigned char* blk = sm + OFF_BLK;
     float* ut = reinterpret_cast<float*>(blk + tcc::BLK_UT);
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
         const int n0 = 16 * w + 8 * nt;
-        const uint32_t xb0 = *reinterpret_cast<const uint32_t*>(sm + OFF_XT + tc::none_off(n0 + g, 2 * t));
-        const uint32_t xb1 = *reinterpret_cast<const uint32_t*>(sm + OFF_XT + tc::none_off(n0 + g, 2 * t + 8));
-        const uint32_t vb0 = *reinterpret_cast<const uint32_t*>(sm + OFF_VT + tc::none_off(n0 + g, 2 * t));
-        const uint32_t vb1 = *reinterpret_cast<const uint32_t*>(sm + OFF_VT + tc::none_off(n0 + g, 2 * t + 8));
+        const uint32_t o0 = tcc::none_off_rg<XT_RG>(n0 + g, 2 * t), o1 = tcc::none_off_rg<XT_RG>(n0 + g, 2 * t + 8);
+        const uint32_t xb0 = *reinterpret_cast<const uint32_t*>(sm + OFF_XT + o0);
+        const uint32_t xb1 = *reinterpret_cast<const uint32_t*>(sm + OFF_XT + o1);
+        const uint32_t vb0 = *reinterpret_cast<const uint32_t*>(sm + OFF_VT + o0);
+        const uint32_t vb1 = *reinterpret_cast<const uint32_t*>(sm + OFF_VT + o1);
         float wa[4] = {0.f, 0.f, 0.f, 0.f}, ua[4] = {0.f, 0.f, 0.f, 0.f};
         tc::mma16816(wa, th, xb0, xb1);
         tc::mma16816(wa, tl, xb0, xb1);
@@ -113,7 +109,7 @@ __device__ __forceinline__ void wy_products(unsigned char* sm, int w, int lane)
 
 }  // namespace
 
-__global__ void __launch_bounds__(NGROUP, 2) kda_chunk_prep_tc_kernel(PrefillArgs a, const __grid_constant__ TileMaps maps)
+__global__ void __launch_bounds__(NGROUP, 3) kda_chunk_prep_tc_kernel(PrefillArgs a, const __grid_constant__ TileMaps maps)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -169,19 +165,17 @@ __global__ void __launch_bounds__(NGROUP, 2) kda_chunk_prep_tc_kernel(PrefillArg
     for (int64_t c = cb; c < ce; ++c) {
         const int len = (int)min((int64_t)C, q1 - (q0 + c * C));
         if (tid < C) sbeta[tid] = beta_next;
-        if (tid == 0) {
-            if (pend_ld) {
-                if (tc::mbar_wait(bar, ph, WAIT_LIMIT)) pend_ld = false, ph ^= 1u;
-                else *abort_flag = 1u;
-            }
-            tc::bulk_wait_read_all();  // the previous block has left shared memory
+        if (tid == 0 && pend_ld) {
+            if (tc::mbar_wait(bar, ph, WAIT_LIMIT)) pend_ld = false, ph ^= 1u;
+            else *abort_flag = 1u;
         }
         sync_all();
         const bool dead = *abort_flag != 0u;
-        unsigned char* blk = sm + OFF_BLK;
+        unsigned char* blk = a.blocks + ((slot0 + c) * H + h) * (int64_t)tcc::BLK_BYTES;  // global
         if (!dead) {
             tcc::prep_factors<PrepMap>(sm, tid, len, blk + tcc::BLK_WQ, blk + tcc::BLK_KT,
-                                       reinterpret_cast<float*>(blk + tcc::BLK_GC), expA, g_min, false);
+                                       reinterpret_cast<float*>(blk + tcc::BLK_GC), expA, g_min, false,
+                                       tcc::BLK_PK_LO);
         } else {
             sync_all();  // the barrier inside prep_factors
         }
@@ -195,23 +189,15 @@ __global__ void __launch_bounds__(NGROUP, 2) kda_chunk_prep_tc_kernel(PrefillArg
             if (tid < C) beta_next = load_beta(c + 1);
         }
         if (!dead) {
-            tcc::prep_solve<PrepMap>(sm, tid, blk + tcc::BLK_P);
+            tcc::prep_solve<PrepMap>(sm, tid, blk + tcc::BLK_PK, tcc::BLK_PK_LO);
         } else {
             sync_all();
             sync_all();
         }
         sync_all();  // T' is complete
-        if (!dead) wy_products(sm, w, lane);
-        tc::fence_async_smem();
-        sync_all();  // the block is assembled
-        if (tid == 0 && !dead) {
-            unsigned char* dst = a.blocks + ((slot0 + c) * H + h) * (int64_t)tcc::BLK_BYTES;
-            tc::bulk_store(dst, blk, tcc::BLK_BYTES);
-            tc::bulk_commit();
-        }
+        if (!dead) wy_products(sm, blk, w, lane);
     }
     if (tid == 0) {
-        tc::bulk_wait_all();
         if (*abort_flag) {
             atomicOr(a.check, kCheckTimeout);
             if (pend_ld) (void)tc::mbar_wait(bar, ph, WAIT_LIMIT);  // a load in flight must land first

@@ -6,23 +6,26 @@
 // (the chunk form of Equation 1, "Kimi K3: the paper and proofs side by side", section 2.1.1;
 // "Kimi K3: architecture, derivations and a pinned-source audit", section 4.5).
 //
-// Value channels j are the 128 TMEM lanes.  Per chunk: D1 = S^T [W ; Q Gamma]^T (M = 128, N = 32,
-// K = 128) -> U^T = U~^T - D1[:, :16] as a bf16 hi/lo pair -> O^T += U^T P^T and
-// dS^T = U^T (K Gamma_C / Gamma) (hi*hi + hi*lo + lo*hi) -> S <- Diag(Gamma_C) S + dS in registers
-// (thread = one value channel x 64 key channels).  The A operands of these products -- the bf16 copy
-// of S^T and U^T hi/lo -- are written to tensor memory (tcgen05.st) rather than shared memory, so the
-// tensor core reads only the chunk's B operands (W, Q Gamma, K Gamma_C / Gamma, P) from shared memory.
-// The operand blocks stream through a four-slot shared-memory ring by plain bulk copies issued four
-// chunks ahead.  256 threads and ~105 KB of shared memory per CTA: two CTAs (two independent chains)
-// share an SM, hiding each other's latency.  Outputs are moved from tensor memory to registers with
-// the state update and stored while the next chunk's first product runs.
+// Value channels j are the 128 TMEM lanes; the fp32 state S^T [j][c] itself lives in tensor memory.
+// Per chunk:
+//   D1 = bf16(S)^T [W ; Q Gamma]^T      (M = 128, N = 32, K = 128: (W S)^T and (Q Gamma S)^T)
+//   S^T <- S^T Diag(Gamma_C)            (threads scale the state in tensor memory while D1 runs)
+//   U^T = U~^T - (W S)^T                (a bf16 hi/lo pair, written to tensor memory)
+//   [O^T | S^T] += U^T [P ; (K Gamma_C / Gamma)^T]^T   (one N = 144 product per hi/lo term: the
+//                                        output update and the state update share an instruction)
+//   bf16(S)^T                            (the next D1's A operand, written to tensor memory)
+// A tcgen05.mma costs about the same whatever N is, so the chunk is organised around few
+// instructions: 8 for D1 and 3 for the fused update.  The operand blocks stream through a four-slot
+// shared-memory ring by plain bulk copies issued four chunks ahead.  256 threads, ~105 KB of shared
+// memory and 256 TMEM columns per CTA: two CTAs (two independent chains) share an SM.  Outputs are
+// moved from tensor memory to registers after the update and stored while the next chunk's D1 runs.
 //
 // Modes (segmented prefill, see the launcher): 0 writes outputs and (last segment) the final state;
 // 1 computes S~, the segment's end state from a zero start; 2 computes M, the segment's transition,
-// as the end state from the identity with V = 0 (columns of M evolve exactly like state columns).
-// Every mbarrier wait is bounded; a wait that gives up raises the timeout bit of the check word,
-// the CTA skips the remaining work, waits (bounded) for its copies and products in flight and frees
-// its tensor memory.
+// as the end state from the identity with V = 0 (columns of M evolve exactly like state columns),
+// stored transposed.  Every mbarrier wait is bounded; a wait that gives up raises the timeout bit of
+// the check word, the CTA skips the remaining work, waits (bounded) for its copies and products in
+// flight and frees its tensor memory.
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
 #include "kda_tc_chunk.cuh"
@@ -33,8 +36,6 @@ namespace {
 
 using tcc::C;
 using tcc::D;
-using tcc::NONE_TILE;
-using tcc::SMALL_TILE;
 using tcc::u2f;
 
 constexpr int NTHREADS = 256;
@@ -55,10 +56,11 @@ static_assert(SLOT >= tcc::BLK_BYTES && SLOT % 1024 == 0, "ring slots must hold 
 static_assert(2 * (SMEM_BYTES + 1024) <= 232448, "two CTAs must fit on an SM");
 
 // tensor-memory columns
-constexpr uint32_t TM_D1 = 0;     // [0, 16) (W S)^T, [16, 32) O^T
-constexpr uint32_t TM_D3 = 32;    // dS^T (lanes = j, columns = c), 128 columns
+constexpr uint32_t TM_WQ = 0;     // D1: [0, 16) (W S)^T; [16, 32) (Q Gamma S)^T, then O^T
+constexpr uint32_t TM_O = 16;     // O^T, immediately followed by the state: the fused update's D
+constexpr uint32_t TM_S = 32;     // S^T fp32 (lanes = j, columns = c), 128 columns
 constexpr uint32_t TM_SA = 160;   // bf16 S^T as the A operand of D1: c pairs, 64 columns
-constexpr uint32_t TM_UA = 224;   // bf16 U^T hi (8 columns), lo (8 columns): A operand of dS and O
+constexpr uint32_t TM_UA = 224;   // bf16 U^T hi (8 columns), lo (8 columns)
 constexpr uint32_t TM_COLS = 256;
 
 __device__ __forceinline__ void sync_all() { tcc::named_sync(1, NTHREADS); }
@@ -71,10 +73,7 @@ __device__ __forceinline__ bool read_dead(const volatile uint32_t* abort_flag)
 
 }  // namespace
 
-// MIN_BLOCKS = 2 caps registers at 128 so that two chains share an SM (segment summaries: many
-// chains); MIN_BLOCKS = 1 lets the compiler keep the state pass free of spills (one chain per SM).
-template <int MIN_BLOCKS>
-__global__ void __launch_bounds__(NTHREADS, MIN_BLOCKS) kda_chunk_state_tc_kernel(PrefillArgs a)
+__global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(PrefillArgs a)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -138,36 +137,44 @@ __global__ void __launch_bounds__(NTHREADS, MIN_BLOCKS) kda_chunk_state_tc_kerne
     const int h2 = w >> 2;   // which half of the key channels (and of the chunk's tokens) this warp covers
     const int jrow = 32 * q4 + lane;
     const uint32_t lane_base = tbase + ((uint32_t)(32 * q4) << 16);
+    const uint32_t my_s = lane_base + TM_S + 64 * h2;    // this thread's 64 state columns
+    const uint32_t my_sa = lane_base + TM_SA + 32 * h2;  // ... and their 32 bf16-pair columns
     __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.out);
 
-    // state slice: S[c][jrow] for c in [64*h2, 64*h2 + 64)
-    float S[64];
-    const int64_t sbase = ((int64_t)n * H + h) * D * D;
-    const int64_t segbase = (((int64_t)n * H + h) * a.max_seg + k) * D * D;
-    const float* init = nullptr;
-    if (mode == 0) init = (k == 0) ? (a.s0 ? a.s0 + sbase : nullptr) : a.seg_in + segbase;
+    // bf16 copy of this thread's 64 state values (16 of them per call) into the A operand
+    auto stage16 = [&](int q, const uint32_t (&v)[16]) {
+        uint32_t pk[8];
 #pragma unroll
-    for (int cc = 0; cc < 64; ++cc) {
-        const int c = 64 * h2 + cc;
-        S[cc] = init ? init[(int64_t)c * D + jrow] : ((mode == 2 && c == jrow) ? 1.f : 0.f);
-    }
-    // bf16 S^T into the A operand of D1: this thread's 64 key channels are 32 columns
-    auto stage_state = [&]() {
+        for (int m = 0; m < 8; ++m) pk[m] = tc::pack_bf16(u2f(v[2 * m]), u2f(v[2 * m + 1]));
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(my_sa + 8 * q),
+                     "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]), "r"(pk[6]), "r"(pk[7])
+                     : "memory");
+    };
+
+    // initial state S[c][jrow], c in [64 h2, 64 h2 + 64), into tensor memory (fp32 and bf16)
+    {
+        const int64_t sbase = ((int64_t)n * H + h) * D * D;
+        const int64_t segbase = (((int64_t)n * H + h) * a.max_seg + k) * D * D;
+        const float* init = nullptr;
+        if (mode == 0) init = (k == 0) ? (a.s0 ? a.s0 + sbase : nullptr) : a.seg_in + segbase;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            uint32_t pk[16];
+        for (int q = 0; q < 4; ++q) {
+            uint32_t v[16];
 #pragma unroll
-            for (int m = 0; m < 16; ++m) pk[m] = tc::pack_bf16(S[32 * half + 2 * m], S[32 * half + 2 * m + 1]);
-            KDA_TMEM_ST16(lane_base + TM_SA + 32 * h2 + 16 * half, pk);
+            for (int e = 0; e < 16; ++e) {
+                const int c = 64 * h2 + 16 * q + e;
+                v[e] = __float_as_uint(init ? init[(int64_t)c * D + jrow] : ((mode == 2 && c == jrow) ? 1.f : 0.f));
+            }
+            KDA_TMEM_ST16(my_s + 16 * q, v);
+            stage16(q, v);
         }
         tc::tmem_wait_st();
-    };
-    stage_state();
+    }
     tc::fence_before_sync();
     sync_all();
     tc::fence_after_sync();
 
-    // outputs of the previous chunk, held in registers until the next chunk's first product runs
+    // outputs of the previous chunk, held in registers until the next chunk's D1 runs
     uint32_t ovp[4];  // bf16 pairs
     int64_t o_t0 = 0;
     int o_len = 0;
@@ -187,8 +194,7 @@ __global__ void __launch_bounds__(NTHREADS, MIN_BLOCKS) kda_chunk_state_tc_kerne
         unsigned char* blk = sm + OFF_RING + sl * SLOT;
         bool dead = read_dead(abort_flag);
 
-        // every thread waits for the block; thread 0 issues D1 = S^T [W ; Q Gamma]^T
-        // (M = 128, K = 128; N = 32 with outputs, else 16: W only)
+        // every thread waits for the block; thread 0 issues D1 (N = 32 with outputs, else 16: W only)
         bool got = false;
         if (!dead) {
             got = tc::mbar_wait(&bar_f[sl], (phb >> sl) & 1u, WAIT_LIMIT);
@@ -205,12 +211,34 @@ __global__ void __launch_bounds__(NTHREADS, MIN_BLOCKS) kda_chunk_state_tc_kerne
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
                 const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
-                tc::umma_ts(tbase + TM_D1, tbase + TM_SA + 8 * ks,
+                tc::umma_ts(tbase + TM_WQ, tbase + TM_SA + 8 * ks,
                             tc::desc_sw128(tc::smem_u32(blk + tcc::BLK_WQ + kb * (2 * C * 128) + off)), idd,
                             ks > 0 ? 1u : 0u);
             }
             tc::umma_commit(bar_c);
             issued = true;
+        }
+        // meanwhile: S <- S Diag(Gamma_C) in tensor memory (D1 reads only the bf16 copy)
+        dead = read_dead(abort_flag);
+        if (!dead) {
+            const float* gc = reinterpret_cast<const float*>(blk + tcc::BLK_GC) + 64 * h2;
+            uint32_t v[4][16];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) KDA_TMEM_LD16(my_s + 16 * q, v[q]);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                for (int e4 = 0; e4 < 4; ++e4) {
+                    const float4 g4 = *reinterpret_cast<const float4*>(gc + 16 * q + 4 * e4);
+                    v[q][4 * e4 + 0] = __float_as_uint(u2f(v[q][4 * e4 + 0]) * g4.x);
+                    v[q][4 * e4 + 1] = __float_as_uint(u2f(v[q][4 * e4 + 1]) * g4.y);
+                    v[q][4 * e4 + 2] = __float_as_uint(u2f(v[q][4 * e4 + 2]) * g4.z);
+                    v[q][4 * e4 + 3] = __float_as_uint(u2f(v[q][4 * e4 + 3]) * g4.w);
+                }
+                KDA_TMEM_ST16(my_s + 16 * q, v[q]);
+            }
+            tc::tmem_wait_st();
         }
         if (o_have && w != 0) store_outputs();
         if (issued) {
@@ -226,7 +254,7 @@ __global__ void __launch_bounds__(NTHREADS, MIN_BLOCKS) kda_chunk_state_tc_kerne
         // U^T = U~^T - (W S)^T as a hi/lo pair into tensor memory; warp half h2 takes tokens 8 h2 .. + 7
         if (!dead) {
             uint32_t dv[8];
-            KDA_TMEM_LD8(lane_base + TM_D1 + 8 * h2, dv);
+            KDA_TMEM_LD8(lane_base + TM_WQ + 8 * h2, dv);
             float uv[8];
             const float* ut = reinterpret_cast<const float*>(blk + tcc::BLK_UT);
 #pragma unroll
@@ -245,22 +273,17 @@ __global__ void __launch_bounds__(NTHREADS, MIN_BLOCKS) kda_chunk_state_tc_kerne
         sync_all();
         tc::fence_after_sync();
 
-        // O^T += U^T P^T (outputs only) and dS^T = U^T (K Gamma_C / Gamma), each hi*hi + hi*lo + lo*hi
+        // [O^T | S^T] += U^T [P ; (K Gamma_C / Gamma)^T]^T as hi*hi + hi*lo + lo*hi (without outputs:
+        // S^T += U^T (K Gamma_C / Gamma) alone)
         if (tid == 0 && !dead) {
-            const uint32_t id16 = tc::idesc_bf16(128, 16);
-            const uint32_t id128 = tc::idesc_bf16(128, 128);
-            const uint64_t dK = tc::desc_none(tc::smem_u32(blk + tcc::BLK_KT));
-            const uint64_t dKl = tc::desc_none(tc::smem_u32(blk + tcc::BLK_KT + NONE_TILE));
-            tc::umma_ts(tbase + TM_D3, tbase + TM_UA, dK, id128, 0u);
-            tc::umma_ts(tbase + TM_D3, tbase + TM_UA, dKl, id128, 1u);
-            tc::umma_ts(tbase + TM_D3, tbase + TM_UA + 8, dK, id128, 1u);
-            if (mode == 0) {
-                const uint64_t dP = tc::desc_none(tc::smem_u32(blk + tcc::BLK_P));
-                const uint64_t dPl = tc::desc_none(tc::smem_u32(blk + tcc::BLK_P + SMALL_TILE));
-                tc::umma_ts(tbase + TM_D1 + C, tbase + TM_UA, dP, id16, 1u);
-                tc::umma_ts(tbase + TM_D1 + C, tbase + TM_UA, dPl, id16, 1u);
-                tc::umma_ts(tbase + TM_D1 + C, tbase + TM_UA + 8, dP, id16, 1u);
-            }
+            const uint32_t dst = mode == 0 ? TM_O : TM_S;
+            const uint32_t idd = tc::idesc_bf16(128, mode == 0 ? C + D : D);
+            const uint32_t boff = mode == 0 ? tcc::BLK_PK : tcc::BLK_KT;
+            const uint64_t dB = tc::desc_none(tc::smem_u32(blk + boff));
+            const uint64_t dBl = tc::desc_none(tc::smem_u32(blk + boff + tcc::BLK_PK_LO));
+            tc::umma_ts(tbase + dst, tbase + TM_UA, dB, idd, 1u);
+            tc::umma_ts(tbase + dst, tbase + TM_UA, dBl, idd, 1u);
+            tc::umma_ts(tbase + dst, tbase + TM_UA + 8, dB, idd, 1u);
             tc::umma_commit(bar_c);
             if (tc::mbar_wait(bar_c, ph_c, WAIT_LIMIT)) ph_c ^= 1u;
             else *abort_flag = 1u, pend_c = true;
@@ -269,38 +292,23 @@ __global__ void __launch_bounds__(NTHREADS, MIN_BLOCKS) kda_chunk_state_tc_kerne
         tc::fence_after_sync();
         dead = read_dead(abort_flag);
 
-        // S <- Diag(Gamma_C) S + dS, staged as the next chunk's A operand; outputs to registers
+        // the new state's bf16 copy for the next D1; outputs to registers
         if (!dead) {
-            const float* gc = reinterpret_cast<const float*>(blk + tcc::BLK_GC) + 64 * h2;
+            uint32_t v[4][16], ob[8];
 #pragma unroll
-            for (int b4 = 0; b4 < 4; b4 += 2) {
-                uint32_t v0[16], v1[16];
-                KDA_TMEM_LD16(lane_base + TM_D3 + 64 * h2 + 16 * b4, v0);
-                KDA_TMEM_LD16(lane_base + TM_D3 + 64 * h2 + 16 * b4 + 16, v1);
-                tc::tmem_wait_ld();
+            for (int q = 0; q < 4; ++q) KDA_TMEM_LD16(my_s + 16 * q, v[q]);
+            if (mode == 0) KDA_TMEM_LD8(lane_base + TM_O + 8 * h2, ob);
+            tc::tmem_wait_ld();
 #pragma unroll
-                for (int e4 = 0; e4 < 8; ++e4) {
-                    const float4 g4 = *reinterpret_cast<const float4*>(gc + 16 * b4 + 4 * e4);
-                    const int cc = 16 * b4 + 4 * e4;
-                    const uint32_t* vv = (e4 < 4) ? v0 : v1;
-                    const int o = (e4 & 3) * 4;
-                    S[cc + 0] = g4.x * S[cc + 0] + u2f(vv[o + 0]);
-                    S[cc + 1] = g4.y * S[cc + 1] + u2f(vv[o + 1]);
-                    S[cc + 2] = g4.z * S[cc + 2] + u2f(vv[o + 2]);
-                    S[cc + 3] = g4.w * S[cc + 3] + u2f(vv[o + 3]);
-                }
-            }
-            stage_state();
+            for (int q = 0; q < 4; ++q) stage16(q, v[q]);
             if (mode == 0) {
-                uint32_t ob[8];
-                KDA_TMEM_LD8(lane_base + TM_D1 + C + 8 * h2, ob);
-                tc::tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 4; ++e) ovp[e] = tc::pack_bf16(u2f(ob[2 * e]), u2f(ob[2 * e + 1]));
                 o_t0 = s0 + (int64_t)ch * C;
                 o_len = chunk_len(ch);
                 o_have = true;
             }
+            tc::tmem_wait_st();
         }
         tc::fence_before_sync();
         sync_all();  // every read of this slot is done; the next state is staged
@@ -309,10 +317,12 @@ __global__ void __launch_bounds__(NTHREADS, MIN_BLOCKS) kda_chunk_state_tc_kerne
     }
     if (o_have) store_outputs();
 
+    const int64_t sbase = ((int64_t)n * H + h) * D * D;
+    const int64_t segbase = (((int64_t)n * H + h) * a.max_seg + k) * D * D;
     float* dst = nullptr;
     if (mode == 0) dst = ((int64_t)k == nseg - 1 && a.s_final) ? a.s_final + sbase : nullptr;
     else dst = (mode == 1 ? a.seg_st : a.seg_mt) + segbase;
-    if (*abort_flag) {
+    if (read_dead(abort_flag)) {
         if (tid == 0) {
             atomicOr(a.check, kCheckTimeout);
             // copies and tensor-core work still in flight must finish before the shared and tensor
@@ -323,14 +333,21 @@ __global__ void __launch_bounds__(NTHREADS, MIN_BLOCKS) kda_chunk_state_tc_kerne
             if (pend_c) (void)tc::mbar_wait(bar_c, ph_c, WAIT_LIMIT);
         }
     } else if (dst) {
-        if (mode == 2) {
-            // the transition is stored transposed, M^T[j][c], for the scan
-            float4* d4 = reinterpret_cast<float4*>(dst + (int64_t)jrow * D + 64 * h2);
 #pragma unroll
-            for (int q = 0; q < 16; ++q) d4[q] = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
-        } else {
+        for (int q = 0; q < 4; ++q) {
+            uint32_t v[16];
+            KDA_TMEM_LD16(my_s + 16 * q, v);
+            tc::tmem_wait_ld();
+            if (mode == 2) {
+                // the transition is stored transposed, M^T[j][c], for the scan
+                float4* d4 = reinterpret_cast<float4*>(dst + (int64_t)jrow * D + 64 * h2 + 16 * q);
 #pragma unroll
-            for (int cc = 0; cc < 64; ++cc) dst[(int64_t)(64 * h2 + cc) * D + jrow] = S[cc];
+                for (int e = 0; e < 4; ++e)
+                    d4[e] = make_float4(u2f(v[4 * e]), u2f(v[4 * e + 1]), u2f(v[4 * e + 2]), u2f(v[4 * e + 3]));
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) dst[(int64_t)(64 * h2 + 16 * q + e) * D + jrow] = u2f(v[e]);
+            }
         }
     }
     tc::fence_before_sync();
@@ -342,15 +359,14 @@ namespace {
 
 cudaError_t launch_chunk_state_tc(const PrefillArgs& a, int seg_mode, cudaStream_t s)
 {
-    // summaries (two chains per summarised segment) pack two CTAs per SM; the output pass runs one
-    auto kern = seg_mode == 0 ? kda_chunk_state_tc_kernel<1> : kda_chunk_state_tc_kernel<2>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(kda_chunk_state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     PrefillArgs b = a;
     b.seg_mode = seg_mode;
     const unsigned gz = seg_mode == 0 ? (unsigned)(a.max_seg > 1 ? a.max_seg : 1) : (unsigned)(2 * (a.max_seg - 1));
     if (gz == 0) return cudaSuccess;
-    kern<<<dim3((unsigned)a.N, (unsigned)a.H, gz), NTHREADS, SMEM_BYTES, s>>>(b);
+    kda_chunk_state_tc_kernel<<<dim3((unsigned)a.N, (unsigned)a.H, gz), NTHREADS, SMEM_BYTES, s>>>(b);
     return cudaGetLastError();
 }
 

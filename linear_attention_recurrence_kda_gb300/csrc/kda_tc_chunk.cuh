@@ -41,11 +41,15 @@ constexpr uint32_t SMALL_TILE = 512;        // [16][16] bf16 NONE tile
 constexpr uint32_t ROW_TILE = C * LROW * 2; // [16][LROW] bf16 row-major tile: 4352 bytes
 
 // Per-chunk operand block: everything the state pass needs for one chunk of one head, laid out
-// exactly as the state pass stages it in shared memory (one contiguous bulk copy).
+// exactly as the state pass stages it in shared memory (one contiguous bulk copy).  P and
+// (K Gamma_C / Gamma)^T are stored as one NONE-layout operand [P ; (K Gamma_C / Gamma)^T]
+// (16 + 128 rows of 16 tokens), so that the output and state-update products of a chunk share one
+// tensor-core instruction (N = 144); hi and lo parts are two such operands.
 constexpr uint32_t BLK_WQ = 0;        // [W ; Q Gamma (hi)] [32][128 c] bf16 SW128           8192
-constexpr uint32_t BLK_KT = 8192;     // (K Gamma_C / Gamma)^T hi, lo [128 c][16 i] NONE      8192
-constexpr uint32_t BLK_UT = 16384;    // U~ = T' V fp32 [16 r][128 j]                         8192
-constexpr uint32_t BLK_P = 24576;     // P hi, lo [16 r][16 i] NONE                           1024
+constexpr uint32_t BLK_PK = 8192;     // [P ; (K Gamma_C / Gamma)^T] hi [144][16] NONE         4608
+constexpr uint32_t BLK_PK_LO = 4608;  //   ... and its lo part at BLK_PK + BLK_PK_LO          4608
+constexpr uint32_t BLK_KT = BLK_PK + SMALL_TILE;  // (K Gamma_C / Gamma)^T hi (lo: + BLK_PK_LO)
+constexpr uint32_t BLK_UT = 17408;    // U~ = T' V fp32 [16 r][128 j]                         8192
 constexpr uint32_t BLK_GC = 25600;    // Gamma_C fp32 [128]                                    512
 constexpr uint32_t BLK_BYTES = 26112;
 
@@ -59,6 +63,15 @@ __device__ __forceinline__ void named_arrive(uint32_t id, uint32_t count)
 }
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+
+// NONE-style tile [rows][16] with an 8-row-group stride of RG bytes (256: the tensor-core operand
+// layout; 272: padded, so that the transposed per-channel stores of prep_factors spread over the
+// shared-memory banks).
+template <uint32_t RG>
+__host__ __device__ __forceinline__ uint32_t none_off_rg(int r, int k)
+{
+    return (uint32_t)((r >> 3) * RG + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2);
+}
 
 // Equation 5 with the fast exponential and division (relative error ~1e-6, far below bf16).
 __device__ __forceinline__ float log_decay_fast(float z, float expA, float g_min)
@@ -123,10 +136,12 @@ __device__ __forceinline__ void mma_kstep(float (&acc)[2][4], const __nv_bfloat1
 // bf16, row-major) are at Map::OFF_STAGE; tokens r >= len are treated as absent (zero).
 // Writes: row-major K Gamma (OFF_LL), Q Gamma hi/lo (OFF_QL), K/Gamma hi/lo (OFF_KD); rows 16..31
 // of the SW128 [W ; Q Gamma] tile at `wq` (Q Gamma hi); (K Gamma)^T and V^T (NONE, OFF_XT / OFF_VT);
-// (K Gamma_C / Gamma)^T hi/lo at `kt` (NONE); Gamma_C at `gc`.  One barrier (Map::NB) inside.
+// (K Gamma_C / Gamma)^T hi/lo at `kt` and `kt + kt_lo` (NONE); Gamma_C at `gc`.  One barrier
+// (Map::NB) inside.
 template <class Map>
 __device__ __forceinline__ void prep_factors(unsigned char* sm, int p, int len, unsigned char* wq, unsigned char* kt,
-                                             float* gc, float expA, float g_min, bool zero_v)
+                                             float* gc, float expA, float g_min, bool zero_v,
+                                             uint32_t kt_lo = NONE_TILE)
 {
     const int cp = p & 63;
     const int tq = p >> 6;
@@ -220,23 +235,24 @@ __device__ __forceinline__ void prep_factors(unsigned char* sm, int p, int len, 
     }
     const uint32_t v00 = (vv[0] & 0xffffu) | (vv[1] << 16), v01 = (vv[2] & 0xffffu) | (vv[3] << 16);
     const uint32_t v10 = (vv[0] >> 16) | (vv[1] & 0xffff0000u), v11 = (vv[2] >> 16) | (vv[3] & 0xffff0000u);
+    const uint32_t p0 = none_off_rg<Map::XT_RG>(c0, r0), p1 = none_off_rg<Map::XT_RG>(c0 + 1, r0);
+    *reinterpret_cast<uint2*>(sm + Map::OFF_XT + p0) = make_uint2(xt0[0], xt0[1]);
+    *reinterpret_cast<uint2*>(sm + Map::OFF_XT + p1) = make_uint2(xt1[0], xt1[1]);
+    *reinterpret_cast<uint2*>(sm + Map::OFF_VT + p0) = make_uint2(v00, v01);
+    *reinterpret_cast<uint2*>(sm + Map::OFF_VT + p1) = make_uint2(v10, v11);
     const uint32_t o0 = tc::none_off(c0, r0), o1 = tc::none_off(c0 + 1, r0);
-    *reinterpret_cast<uint2*>(sm + Map::OFF_XT + o0) = make_uint2(xt0[0], xt0[1]);
-    *reinterpret_cast<uint2*>(sm + Map::OFF_XT + o1) = make_uint2(xt1[0], xt1[1]);
-    *reinterpret_cast<uint2*>(sm + Map::OFF_VT + o0) = make_uint2(v00, v01);
-    *reinterpret_cast<uint2*>(sm + Map::OFF_VT + o1) = make_uint2(v10, v11);
     *reinterpret_cast<uint2*>(kt + o0) = make_uint2(kh0[0], kh0[1]);
     *reinterpret_cast<uint2*>(kt + o1) = make_uint2(kh1[0], kh1[1]);
-    *reinterpret_cast<uint2*>(kt + NONE_TILE + o0) = make_uint2(kl0[0], kl0[1]);
-    *reinterpret_cast<uint2*>(kt + NONE_TILE + o1) = make_uint2(kl1[0], kl1[1]);
+    *reinterpret_cast<uint2*>(kt + kt_lo + o0) = make_uint2(kl0[0], kl0[1]);
+    *reinterpret_cast<uint2*>(kt + kt_lo + o1) = make_uint2(kl1[0], kl1[1]);
 }
 
 // A and P over K = 128 with mma.sync, two k-steps per warp (warps 0..3: A, warps 4..7: P as
 // hi*hi + hi*lo + lo*hi), partial sums reduced in shared memory (OFF_PART, 8 KB); then
 // T = (I + A)^-1 by forward substitution and T' = T diag(beta) (hi/lo, OFF_T), P finalised into
-// `pb` (hi/lo NONE).  beta of the chunk is read from OFF_BETA.  Two barriers (Map::NB) inside.
+// `pb` and `pb + p_lo` (hi/lo NONE).  beta of the chunk is read from OFF_BETA.  Two barriers (Map::NB) inside.
 template <class Map>
-__device__ __forceinline__ void prep_solve(unsigned char* sm, int p, unsigned char* pb)
+__device__ __forceinline__ void prep_solve(unsigned char* sm, int p, unsigned char* pb, uint32_t p_lo = SMALL_TILE)
 {
     const int pw = p >> 5, lane = p & 31;
     float* sA = reinterpret_cast<float*>(sm + Map::OFF_A);
@@ -283,30 +299,28 @@ __device__ __forceinline__ void prep_solve(unsigned char* sm, int p, unsigned ch
         __nv_bfloat16 hi, lo;
         split_bf16((i <= r) ? sp : 0.f, hi, lo);
         st_bf16(pb, tc::none_off(r, i), hi);
-        st_bf16(pb, SMALL_TILE + tc::none_off(r, i), lo);
+        st_bf16(pb, p_lo + tc::none_off(r, i), lo);
     }
     named_sync(Map::NB, NGROUP);
     if (pw == 0 && lane < C) {
-        // forward substitution, one lane per column j: T[r][j] = delta_rj - sum_{i<r} A[r][i] T[i][j]
+        // forward substitution, one lane per column j, column-oriented: once T[i][j] is final it is
+        // eliminated from every later row, p_r -= A[r][i] T[i][j] (r > i), so each step adds one
+        // dependent multiply-add instead of a length-r dot product
         const int j = lane;
-        float tcol[C];
+        float p[C];
 #pragma unroll
-        for (int r = 0; r < C; ++r) {
-            float p0 = (r == j) ? 1.f : 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+        for (int r = 0; r < C; ++r) p[r] = (r == j) ? 1.f : 0.f;
 #pragma unroll
-            for (int i = 0; i < r; i += 4) {
-                p0 -= sA[r * C + i] * tcol[i];
-                if (i + 1 < r) p1 -= sA[r * C + i + 1] * tcol[i + 1];
-                if (i + 2 < r) p2 -= sA[r * C + i + 2] * tcol[i + 2];
-                if (i + 3 < r) p3 -= sA[r * C + i + 3] * tcol[i + 3];
-            }
-            tcol[r] = (p0 + p1) + (p2 + p3);
+        for (int i = 0; i < C; ++i) {
+            const float ti = p[i];
+#pragma unroll
+            for (int r = i + 1; r < C; ++r) p[r] = fmaf(-sA[r * C + i], ti, p[r]);
         }
         const float bj = beta[j];
 #pragma unroll
         for (int r = 0; r < C; ++r) {
             __nv_bfloat16 hi, lo;
-            split_bf16(tcol[r] * bj, hi, lo);
+            split_bf16(p[r] * bj, hi, lo);
             st_bf16(sm, Map::OFF_T + tc::none_off(r, j), hi);
             st_bf16(sm, Map::OFF_T + SMALL_TILE + tc::none_off(r, j), lo);
         }
