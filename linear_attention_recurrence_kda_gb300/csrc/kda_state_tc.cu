@@ -9,11 +9,12 @@
 // Value channels j are the 128 TMEM lanes; the fp32 state S^T [j][c] itself lives in tensor memory.
 // Per chunk:
 //   D1 = bf16(S)^T [W ; Q Gamma]^T      (M = 128, N = 32, K = 128: (W S)^T and (Q Gamma S)^T)
-//   S^T <- S^T Diag(Gamma_C)            (threads scale the state in tensor memory while D1 runs)
 //   U^T = U~^T - (W S)^T                (a bf16 hi/lo pair, written to tensor memory)
 //   [O^T | S^T] += U^T [P ; (K Gamma_C / Gamma)^T]^T   (one N = 144 product per hi/lo term: the
-//                                        output update and the state update share an instruction)
-//   bf16(S)^T                            (the next D1's A operand, written to tensor memory)
+//                                        output update and the state update share an instruction;
+//                                        S^T already holds S^T Diag(Gamma_C))
+//   bf16(S)^T and S^T Diag(Gamma_C of the next chunk)  (one read of the new state writes the next
+//                                        D1's A operand and the next update's decayed state)
 // A tcgen05.mma costs about the same whatever N is, so the chunk is organised around few
 // instructions: 8 for D1 and 3 for the fused update.  The operand blocks stream through a four-slot
 // shared-memory ring by plain bulk copies issued four chunks ahead.  256 threads, ~105 KB of shared
@@ -151,8 +152,20 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
                      : "memory");
     };
 
-    // initial state S[c][jrow], c in [64 h2, 64 h2 + 64), into tensor memory (fp32 and bf16)
+    // initial state S[c][jrow], c in [64 h2, 64 h2 + 64), into tensor memory: the bf16 copy as is, the
+    // fp32 state already multiplied by the first chunk's Gamma_C (the decay the first update applies)
+    bool init_ok = true;
+    if (nchunks > 0) {
+        init_ok = tc::mbar_wait(&bar_f[0], 0u, WAIT_LIMIT);
+        if (init_ok) {
+            phb ^= 1u;
+            if (tid == 0) pend &= ~1u;
+        } else {
+            *abort_flag = 1u;
+        }
+    }
     {
+        const float* gc0 = reinterpret_cast<const float*>(sm + OFF_RING + tcc::BLK_GC) + 64 * h2;
         const int64_t sbase = ((int64_t)n * H + h) * D * D;
         const int64_t segbase = (((int64_t)n * H + h) * a.max_seg + k) * D * D;
         const float* init = nullptr;
@@ -165,8 +178,12 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
                 const int c = 64 * h2 + 16 * q + e;
                 v[e] = __float_as_uint(init ? init[(int64_t)c * D + jrow] : ((mode == 2 && c == jrow) ? 1.f : 0.f));
             }
-            KDA_TMEM_ST16(my_s + 16 * q, v);
             stage16(q, v);
+            if (nchunks > 0 && init_ok) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(u2f(v[e]) * gc0[16 * q + e]);
+            }
+            KDA_TMEM_ST16(my_s + 16 * q, v);
         }
         tc::tmem_wait_st();
     }
@@ -194,17 +211,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
         unsigned char* blk = sm + OFF_RING + sl * SLOT;
         bool dead = read_dead(abort_flag);
 
-        // every thread waits for the block; thread 0 issues D1 (N = 32 with outputs, else 16: W only)
-        bool got = false;
-        if (!dead) {
-            got = tc::mbar_wait(&bar_f[sl], (phb >> sl) & 1u, WAIT_LIMIT);
-            if (got) {
-                phb ^= 1u << sl;
-                if (tid == 0) pend &= ~(1u << sl);
-            } else {
-                *abort_flag = 1u;
-            }
-        }
+        // chunk ch's block has landed: every thread waited for it in the previous chunk's re-staging
+        // (or before the initial state was written).  Thread 0 issues D1 (N = 32 with outputs, else
+        // 16: W only) while the other warps store the previous chunk's outputs.
+        const bool got = !dead;
         bool issued = false;
         if (tid == 0 && got) {
             const uint32_t idd = tc::idesc_bf16(128, mode == 0 ? 2 * C : C);
@@ -217,28 +227,6 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
             }
             tc::umma_commit(bar_c);
             issued = true;
-        }
-        // meanwhile: S <- S Diag(Gamma_C) in tensor memory (D1 reads only the bf16 copy)
-        dead = read_dead(abort_flag);
-        if (!dead) {
-            const float* gc = reinterpret_cast<const float*>(blk + tcc::BLK_GC) + 64 * h2;
-            uint32_t v[4][16];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) KDA_TMEM_LD16(my_s + 16 * q, v[q]);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-#pragma unroll
-                for (int e4 = 0; e4 < 4; ++e4) {
-                    const float4 g4 = *reinterpret_cast<const float4*>(gc + 16 * q + 4 * e4);
-                    v[q][4 * e4 + 0] = __float_as_uint(u2f(v[q][4 * e4 + 0]) * g4.x);
-                    v[q][4 * e4 + 1] = __float_as_uint(u2f(v[q][4 * e4 + 1]) * g4.y);
-                    v[q][4 * e4 + 2] = __float_as_uint(u2f(v[q][4 * e4 + 2]) * g4.z);
-                    v[q][4 * e4 + 3] = __float_as_uint(u2f(v[q][4 * e4 + 3]) * g4.w);
-                }
-                KDA_TMEM_ST16(my_s + 16 * q, v[q]);
-            }
-            tc::tmem_wait_st();
         }
         if (o_have && w != 0) store_outputs();
         if (issued) {
@@ -292,8 +280,20 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
         tc::fence_after_sync();
         dead = read_dead(abort_flag);
 
-        // the new state's bf16 copy for the next D1; outputs to registers
+        // the new state's bf16 copy for the next D1, and the state multiplied by the next chunk's
+        // Gamma_C (the decay its update applies; its block is in the ring already); outputs to registers
         if (!dead) {
+            bool next_ok = false;
+            if (ch + 1 < nchunks) {
+                const int sn = (ch + 1) % NSLOT;
+                next_ok = tc::mbar_wait(&bar_f[sn], (phb >> sn) & 1u, WAIT_LIMIT);
+                if (next_ok) {
+                    phb ^= 1u << sn;
+                    if (tid == 0) pend &= ~(1u << sn);
+                } else {
+                    *abort_flag = 1u;
+                }
+            }
             uint32_t v[4][16], ob[8];
 #pragma unroll
             for (int q = 0; q < 4; ++q) KDA_TMEM_LD16(my_s + 16 * q, v[q]);
@@ -301,6 +301,21 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
             tc::tmem_wait_ld();
 #pragma unroll
             for (int q = 0; q < 4; ++q) stage16(q, v[q]);
+            if (next_ok) {
+                const float* gcn = reinterpret_cast<const float*>(sm + OFF_RING + ((ch + 1) % NSLOT) * SLOT + tcc::BLK_GC) + 64 * h2;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                    for (int e4 = 0; e4 < 4; ++e4) {
+                        const float4 g4 = *reinterpret_cast<const float4*>(gcn + 16 * q + 4 * e4);
+                        v[q][4 * e4 + 0] = __float_as_uint(u2f(v[q][4 * e4 + 0]) * g4.x);
+                        v[q][4 * e4 + 1] = __float_as_uint(u2f(v[q][4 * e4 + 1]) * g4.y);
+                        v[q][4 * e4 + 2] = __float_as_uint(u2f(v[q][4 * e4 + 2]) * g4.z);
+                        v[q][4 * e4 + 3] = __float_as_uint(u2f(v[q][4 * e4 + 3]) * g4.w);
+                    }
+                    KDA_TMEM_ST16(my_s + 16 * q, v[q]);
+                }
+            }
             if (mode == 0) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) ovp[e] = tc::pack_bf16(u2f(ob[2 * e]), u2f(ob[2 * e + 1]));
