@@ -277,7 +277,6 @@ def main():
     time.sleep(0.3)
 
     # ---- timed prefill: K steps, L2 flushed before each, per-step events on the launching stream
-    B.kda_profile_enable(True)
     barrier()
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -288,12 +287,21 @@ def main():
         evs[i][1].record(stream)
     torch.cuda.synchronize()
     barrier()
-    prof = B.kda_profile_read()
-    B.kda_profile_enable(False)
     step_ms = [a.elapsed_time(b) for a, b in evs]
     ms = max_over_ranks(sum(step_ms) / len(step_ms))
     tokens = T * world
     value = tokens / (ms * 1e-3) / 1e6
+
+    # ---- the same K steps again with the library's per-kernel event hooks on (they sit between the
+    # kernels of a step and stop one kernel's launch from overlapping the previous one's tail, so the
+    # step time above is taken without them)
+    B.kda_profile_enable(True)
+    for i in range(args.steps):
+        flush.zero_()
+        fwd()
+    torch.cuda.synchronize()
+    prof = B.kda_profile_read()
+    B.kda_profile_enable(False)
     launches = sum(n for n, _ in prof.values())
 
     # roofline of the kernel with the largest device time, each kernel against the bytes its design
@@ -425,44 +433,71 @@ def bench_decode(args, B, I, dev, stream, max_over_ranks, barrier, pk, pk_src):
             "gpu_launches": kn}
 
 
-def bench_e2e(args, B, inp, dev, stream, max_over_ranks, barrier, world):
+def bench_e2e(args, B, inp, dev, stream, max_over_ranks, barrier, world, depth=2):
+    """The prefill end to end through kda_forward with host buffers: every step copies its inputs
+    from pinned host memory to the device, runs the prefill and copies the outputs and final state
+    back to pinned host memory.  Steps stream through three CUDA streams with `depth` sets of device
+    buffers, so step i+1's inputs travel while step i computes and step i-1's outputs travel back
+    (a stream of independent prefill requests); the time per step is the steady-state spacing."""
     import torch
     keys = ("q", "k", "v", "z", "A", "beta", "S0")
     host = {k: inp[k].pin_memory() for k in keys}
-    dbuf = {k: torch.empty_like(host[k], device=dev) for k in keys}
     T, H, dk = inp["k"].shape
     dv = inp["v"].shape[2]
-    out = torch.empty(T, H, dv, dtype=inp["k"].dtype, device=dev)
-    fin = torch.empty(1, H, dk, dv, dtype=torch.float32, device=dev)
-    h_out = torch.empty_like(out, device="cpu").pin_memory()
-    h_fin = torch.empty_like(fin, device="cpu").pin_memory()
+    dbuf = [{k: torch.empty_like(host[k], device=dev) for k in keys} for _ in range(depth)]
+    dout = [(torch.empty(T, H, dv, dtype=inp["k"].dtype, device=dev),
+             torch.empty(1, H, dk, dv, dtype=torch.float32, device=dev)) for _ in range(depth)]
+    h_out = torch.empty(T, H, dv, dtype=inp["k"].dtype).pin_memory()
+    h_fin = torch.empty(1, H, dk, dv, dtype=torch.float32).pin_memory()
     prob = B.make_problem(1, T, T, H, dk, dv, inp["k"].dtype)
     ws = torch.empty(B.kda_forward_workspace_bytes(prob), dtype=torch.uint8, device=dev)
     h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
     d2h = h_out.numel() * h_out.element_size() + h_fin.numel() * h_fin.element_size()
+    s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(depth)]
+    ev_cmp = [torch.cuda.Event() for _ in range(depth)]
+    ev_out = [torch.cuda.Event() for _ in range(depth)]
+    count = [0]
 
     def step():
-        for k in keys:
-            dbuf[k].copy_(host[k], non_blocking=True)
-        B.kda_forward(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["z"], dbuf["A"], dbuf["beta"], initial_state=dbuf["S0"],
-                      out=out, final_state=fin, workspace=ws)
-        h_out.copy_(out, non_blocking=True)
-        h_fin.copy_(fin, non_blocking=True)
+        i = count[0]
+        b = i % depth
+        with torch.cuda.stream(s_in):
+            if i >= depth:
+                s_in.wait_event(ev_cmp[b])   # the compute of step i - depth has read these inputs
+            for k in keys:
+                dbuf[b][k].copy_(host[k], non_blocking=True)
+            ev_in[b].record(s_in)
+        with torch.cuda.stream(s_cmp):
+            s_cmp.wait_event(ev_in[b])
+            if i >= depth:
+                s_cmp.wait_event(ev_out[b])  # the outputs of step i - depth have left
+            d = dbuf[b]
+            B.kda_forward(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], initial_state=d["S0"],
+                          out=dout[b][0], final_state=dout[b][1], workspace=ws, stream=s_cmp)
+            ev_cmp[b].record(s_cmp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_cmp[b])
+            h_out.copy_(dout[b][0], non_blocking=True)
+            h_fin.copy_(dout[b][1], non_blocking=True)
+            ev_out[b].record(s_out)
+        count[0] += 1
 
     for _ in range(3):
         step()
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    e0.record(s_in)
     for _ in range(args.steps):
         step()
-    e1.record(stream)
+    e1.record(s_out)
     torch.cuda.synchronize()
     barrier()
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
     return {"value": T * world / (ms * 1e-3) / 1e6, "unit": "Mtok/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "pipeline": f"{depth} device buffer sets over H2D / compute / D2H streams"}
 
 
 if __name__ == "__main__":

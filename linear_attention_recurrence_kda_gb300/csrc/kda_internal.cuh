@@ -18,6 +18,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <utility>
+
 #include "kda.h"
 
 namespace kda {
@@ -168,6 +170,33 @@ int sm_count_of_current_device();
 // Optional per-kernel timing around launches (no-ops unless kda_profile_enable(1)).
 void prof_start(const char* name, cudaStream_t s);
 void prof_stop(cudaStream_t s);
+
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// The kernels of one prefill run back to back on one stream.  Each signals at its start that the
+// next kernel may be scheduled (it can then only start once every CTA of this grid has started, so
+// it never takes resources this grid still needs); a kernel launched with launch_dependent() waits
+// in griddep_wait() until the previous grid has completed and its writes are visible, and does its
+// set-up (tensor-memory allocation, barrier initialisation) before that.
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                    Args&&... args)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------- device helpers
 

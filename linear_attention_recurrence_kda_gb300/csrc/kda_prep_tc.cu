@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(NGROUP, 3) kda_chunk_prep_tc_kernel(PrefillArg
     const int h = blockIdx.y;
     const int tid = threadIdx.x;
     const int w = tid >> 5, lane = tid & 31;
+    griddep_launch_dependents();
 
     int64_t q0, q1;
     if (!seq_range(a, n, q0, q1)) return;

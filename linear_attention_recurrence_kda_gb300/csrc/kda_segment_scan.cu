@@ -11,10 +11,11 @@
 //
 // The summary pass stores every M_k transposed (M_k^T[c'][c], so that column c' of M_k -- the
 // coefficients of input row c' -- is contiguous).  M_k^T is staged through shared memory with
-// asynchronous copies, the next one while the current step computes.  Each of the 256 threads owns
-// a 4 x 4 tile of the 128 x 16 result over one half of the contraction (64 of the 128 input rows):
+// asynchronous copies, the next one while the current step computes.  Each of the 512 threads owns
+// a 4 x 4 tile of the 128 x 16 result over one quarter of the contraction (32 of the 128 input rows):
 // per input row one 16-byte load of M^T, one (broadcast) 16-byte load of S_in and 16 fp32 FMAs; the
-// two halves are added through shared memory.
+// four quarters are added through shared memory.  512 threads keep enough warps in flight to hide
+// the shared-memory latency of the short inner loop.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -23,7 +24,8 @@ namespace {
 
 constexpr int D = 128;
 constexpr int COLS = 16;         // value columns per CTA
-constexpr int NTHREADS = 256;    // 2 contraction halves x 4 column groups x 32 row groups
+constexpr int KSPLIT = 4;        // contraction quarters
+constexpr int NTHREADS = 128 * KSPLIT;  // quarters x 4 column groups x 32 row groups
 
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src)
 {
@@ -48,15 +50,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_segment_scan_kernel(PrefillAr
     extern __shared__ __align__(16) float smem_f[];
     float* sM = smem_f;                       // [2][D][D] double-buffered M^T
     float* sS = smem_f + 2 * D * D;           // [D][COLS] incoming state slice
-    float* sP = sS + D * COLS;                // [128 threads][16] partial tiles of the upper half
+    float* sP = sS + D * COLS;                // [3][128 threads][16] partial tiles of quarters 1..3
 
     const int n = blockIdx.x;
     const int h = blockIdx.y;
     const int j0 = blockIdx.z * COLS;
     const int tid = threadIdx.x;
-    const int kh = tid >> 7;             // contraction half: input rows [64 kh, 64 kh + 64)
+    const int kh = tid >> 7;             // contraction quarter: input rows [32 kh, 32 kh + 32)
     const int cg = (tid >> 5) & 3;       // columns j0 + 4 cg .. + 3
     const int rg = tid & 31;             // rows 4 rg .. 4 rg + 3
+    griddep_launch_dependents();
 
     int64_t q0, q1;
     if (!seq_range(a, n, q0, q1)) return;
@@ -68,6 +71,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_segment_scan_kernel(PrefillAr
     const int H = a.H;
     const int64_t sbase = ((int64_t)n * H + h) * D * D;
     const int64_t seg0 = ((int64_t)n * H + h) * a.max_seg * D * D;
+    griddep_wait();  // the segment summaries come from the previous kernel
     stage_mt(sM, a.seg_mt + seg0, tid);
     cp_async_commit();
     for (int e = tid; e < D * COLS; e += NTHREADS) {
@@ -96,8 +100,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_segment_scan_kernel(PrefillAr
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) acc[i][jj] = 0.f;
 #pragma unroll 8
-        for (int cc = 0; cc < 64; ++cc) {
-            const int c = 64 * kh + cc;
+        for (int cc = 0; cc < D / KSPLIT; ++cc) {
+            const int c = (D / KSPLIT) * kh + cc;
             const float4 m = *reinterpret_cast<const float4*>(Mt + c * D + 4 * rg);      // M_k[4 rg + i][c]
             const float4 sv = *reinterpret_cast<const float4*>(sS + c * COLS + 4 * cg);  // S_in[c][j]
             const float mi[4] = {m.x, m.y, m.z, m.w};
@@ -109,19 +113,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_segment_scan_kernel(PrefillAr
                 acc[i][3] = fmaf(mi[i], sv.w, acc[i][3]);
             }
         }
-        if (kh == 1) {
-            float* pp = sP + (tid - 128) * 16;
+        if (kh > 0) {
+            // partials laid out [quarter][i][thread] so that a warp's float4 stores are contiguous
+            float4* pp = reinterpret_cast<float4*>(sP) + (kh - 1) * 4 * 128;
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                *reinterpret_cast<float4*>(pp + 4 * i) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+            for (int i = 0; i < 4; ++i) pp[i * 128 + (tid & 127)] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
         }
-        __syncthreads();               // every read of sS and Mt is done; the upper half's partials are in
+        __syncthreads();               // every read of sS and Mt is done; the other quarters' partials are in
         if (kh == 0) {
-            const float* pp = sP + tid * 16;
+            const float4* pp = reinterpret_cast<const float4*>(sP);
             float* out = a.seg_in + segk + D * D;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float4 u = *reinterpret_cast<const float4*>(pp + 4 * i);
+                float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int q = 0; q < KSPLIT - 1; ++q) {
+                    const float4 p4 = pp[(q * 4 + i) * 128 + tid];
+                    u.x += p4.x;
+                    u.y += p4.y;
+                    u.z += p4.z;
+                    u.w += p4.w;
+                }
                 const float4 r = make_float4(acc[i][0] + u.x + st[i].x, acc[i][1] + u.y + st[i].y,
                                              acc[i][2] + u.z + st[i].z, acc[i][3] + u.w + st[i].w);
                 const int row = 4 * rg + i;
@@ -134,11 +146,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_segment_scan_kernel(PrefillAr
 
 cudaError_t launch_segment_scan(const PrefillArgs& a, cudaStream_t s)
 {
-    const size_t smem = (size_t)(2 * D * D + D * COLS + 128 * 16) * sizeof(float);
+    const size_t smem = (size_t)(2 * D * D + D * COLS + (KSPLIT - 1) * 128 * 16) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(kda_segment_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kda_segment_scan_kernel<<<dim3((unsigned)a.N, (unsigned)a.H, D / COLS), NTHREADS, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(kda_segment_scan_kernel, dim3((unsigned)a.N, (unsigned)a.H, D / COLS), dim3(NTHREADS), smem,
+                            s, a);
 }
 
 }  // namespace kda

@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
     const int tid = threadIdx.x;
     const int w = tid >> 5;
     const int lane = tid & 31;
+    griddep_launch_dependents();
 
     int64_t q0, q1;
     if (!seq_range(a, n, q0, q1)) return;
@@ -119,6 +120,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tbase = *tslot;
+    griddep_wait();  // the operand blocks and incoming states come from the previous kernels
 
     // ring bookkeeping: every thread tracks each slot's fill parity; thread 0 also the loads it
     // issued and has not seen complete, and an unobserved tensor-core commit
@@ -381,8 +383,8 @@ cudaError_t launch_chunk_state_tc(const PrefillArgs& a, int seg_mode, cudaStream
     b.seg_mode = seg_mode;
     const unsigned gz = seg_mode == 0 ? (unsigned)(a.max_seg > 1 ? a.max_seg : 1) : (unsigned)(2 * (a.max_seg - 1));
     if (gz == 0) return cudaSuccess;
-    kda_chunk_state_tc_kernel<<<dim3((unsigned)a.N, (unsigned)a.H, gz), NTHREADS, SMEM_BYTES, s>>>(b);
-    return cudaGetLastError();
+    return launch_dependent(kda_chunk_state_tc_kernel, dim3((unsigned)a.N, (unsigned)a.H, gz), dim3(NTHREADS), SMEM_BYTES,
+                            s, b);
 }
 
 }  // namespace
