@@ -307,17 +307,17 @@ def main():
     # roofline of the kernel with the largest device time, each kernel against the bytes its design
     # must move: the fused / output pass reads q, k, v, z, beta and writes o for every token-head
     # (plus the states); the chunk preparation reads the same inputs and writes one operand block
-    # per chunk and head; the state passes read those blocks (the summary pass twice: S~ and M
-    # chains) and write states; the scan reads (M, S~) and writes S_in per segment step.
+    # per 32-token step and head; the state passes read those blocks (the summary pass twice: S~ and
+    # M chains) and write states; the scan reads (M, S~) and writes S_in per segment step.
     pk, pk_src = peaks()
     th = T * H
     plan = B.kda_forward_plan(prob, ws.numel())
     n_seg = plan["num_segments"]
     seg_tokens = 16 * plan["seg_chunks"] * (n_seg - 1) if n_seg > 1 else 0  # tokens of all but the last segment
     state_bytes = H * dk * dv * 4
-    blk = 26112
-    chunk_heads = -(-T // 16) * H
-    seg_chunk_heads = (seg_tokens // 16) * H
+    blk = 53760  # operand block of one 32-token step and head
+    chunk_heads = -(-T // 32) * H  # step-heads
+    seg_chunk_heads = (seg_tokens // 32) * H
     in_bytes = th * ((2 * dk + dv + dk) * io_bytes + 4)
     alg = {
         "kda_chunk_fwd_tc": th * prefill_bytes_per_token_head(dk, dv, io_bytes) + 2 * state_bytes,

@@ -112,15 +112,17 @@ kda_status_t kda_forward_plan(const kda_problem_t* problem, size_t workspace_byt
  *                   initial_state (in-place carry); any other overlap is rejected.
  *   workspace     : device scratch, 256-byte aligned, not shared with a concurrently running
  *                   call.  kda_forward_workspace_bytes(problem) bytes allow the fastest plan.  For
- *                   bf16 inputs with d_k = d_v = 128 that plan first prepares every chunk's
- *                   state-independent operands in parallel (about 26 KB per chunk and head, held
- *                   in the workspace) and then runs the sequential state pass; a workspace too
+ *                   bf16 inputs with d_k = d_v = 128 that plan first prepares the
+ *                   state-independent operands of every pair of chunks in parallel (52.5 KB per
+ *                   32 tokens and head, held in the workspace) and then runs the sequential state
+ *                   pass in 32-token steps; a workspace too
  *                   small for those blocks selects a fused kernel that prepares each chunk on the
  *                   fly.  A smaller workspace also makes long sequences use fewer parallel
  *                   segments (down to none); one below the unsegmented minimum is rejected
  *                   (KDA_ERR_WORKSPACE).  Results do not depend on the plan beyond rounding.
  *                   Environment overrides, read on every call: KDA_TC_PLAN=fused keeps the fused
- *                   kernel; KDA_SEGMENT_CHUNKS=<n> forces n chunks per segment (0: unsegmented).
+ *                   kernel; KDA_SEGMENT_CHUNKS=<n> forces n chunks per segment (0: unsegmented;
+ *                   the pair-step plan rounds n up to an even count).
  *
  * Returns KDA_OK once all kernels are enqueued on `stream`.
  */

@@ -104,11 +104,14 @@ int sm_count_of_current_device() { return sm_count_cached(); }
 void segment_plan(const kda_problem_t& p, size_t budget_bytes, bool split, int32_t& seg_chunks, int32_t& max_seg)
 {
     const int64_t chunks = max_chunks_of(p);
+    // the split plan advances the state by pairs of chunks, so its segments hold an even number
+    const int64_t gran = split ? 2 : 1;
     seg_chunks = 0;
     max_seg = 1;
-    if (chunks <= 1) return;
+    if (chunks <= gran) return;
     if (const char* env = std::getenv("KDA_SEGMENT_CHUNKS")) {
-        const long v = std::strtol(env, nullptr, 10);
+        long v = std::strtol(env, nullptr, 10);
+        if (v > 0) v = (long)(((int64_t)v + gran - 1) / gran * gran);
         const int64_t ns = v > 0 ? (chunks + v - 1) / v : 1;
         const double need = (double)p.num_seqs * p.num_heads * p.d_k * p.d_v * 12.0 * (double)ns;
         if (v > 0 && v < chunks && need <= (double)budget_bytes) {
@@ -117,20 +120,22 @@ void segment_plan(const kda_problem_t& p, size_t budget_bytes, bool split, int32
         }
         return;
     }
-    // cost in units of one chunk step of a chain running alone on an SM: pass 3 runs nseg segments
-    // per (seq, head) in waves of one chain per SM; pass 1 two summaries (S~ and M) of every
-    // segment but the last -- in the split plan two chains per SM, each about 1.3 times slower,
-    // in the fused plan one; one step of the scan costs about scan_step chunk steps
+    // cost in units of one state step of a chain running alone on an SM (a chunk, or a pair of
+    // chunks in the split plan): pass 3 runs nseg segments per (seq, head) in waves of one chain per
+    // SM; pass 1 two summaries (S~ and M) of every segment but the last -- in the split plan two
+    // chains per SM, each about 1.3 times slower, in the fused plan one; one step of the scan costs
+    // about scan_step state steps
+    const int64_t steps = (chunks + gran - 1) / gran;
     const double sms = (double)sm_count_of_current_device();
     const double sum_slots = sms * (split ? 2.0 : 1.0);
     const double sum_cost = split ? 1.3 : 1.0;
-    const double scan_step = split ? 2.5 : 1.5;
+    const double scan_step = split ? 0.6 : 0.8;
     const double units = (double)p.num_seqs * p.num_heads;
     const double per_seg = units * p.d_k * p.d_v * 4.0 * 3.0;  // S_in, S~ and M of one segment
-    double best = (double)chunks * std::ceil(units / sms);
-    for (int64_t nseg = 2; nseg <= 64 && nseg <= chunks; ++nseg) {
-        const int64_t sc = (chunks + nseg - 1) / nseg;
-        const int64_t ns = (chunks + sc - 1) / sc;
+    double best = (double)steps * std::ceil(units / sms);
+    for (int64_t nseg = 2; nseg <= 64 && nseg <= steps; ++nseg) {
+        const int64_t sc = (steps + nseg - 1) / nseg;  // steps per segment
+        const int64_t ns = (steps + sc - 1) / sc;
         if (ns < 2) continue;
         if (per_seg * (double)ns > (double)budget_bytes || per_seg * (double)ns > 2.0e9) continue;
         const double cost = (double)sc * (std::ceil(units * ns / sms) +
@@ -138,7 +143,7 @@ void segment_plan(const kda_problem_t& p, size_t budget_bytes, bool split, int32
                             scan_step * (double)(ns - 1);
         if (cost < 0.9 * best) {
             best = cost;
-            seg_chunks = (int32_t)sc;
+            seg_chunks = (int32_t)(sc * gran);
             max_seg = (int32_t)ns;
         }
     }

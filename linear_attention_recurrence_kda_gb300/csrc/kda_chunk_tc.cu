@@ -425,10 +425,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_chunk_fwd_tc_kernel(PrefillAr
         if (*abort_flag) {
             if (tid == 0) atomicOr(a.check, kCheckTimeout);
         } else if (dst && mode == 2) {
-            // the transition is stored transposed, M^T[j][c], for the scan
-            float4* d4 = reinterpret_cast<float4*>(dst + (int64_t)jrow * D + 64 * h2);
+            // the transition M[c][j] (this lane holds column j = jrow) in the scan's operand format
 #pragma unroll
-            for (int q = 0; q < 16; ++q) d4[q] = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
+            for (int cc = 0; cc < 64; ++cc) store_seg_m(dst, 64 * h2 + cc, jrow, S[cc]);
         } else if (dst) {
 #pragma unroll
             for (int cc = 0; cc < 64; ++cc) dst[(int64_t)(64 * h2 + cc) * D + jrow] = S[cc];

@@ -7,9 +7,11 @@
 //   W          fp32 [T_tot, H, d_k]   WY-transformed keys T diag(beta) (K*Gamma)   (kda_ut_wy)
 //   Ut         fp32 [T_tot, H, d_v]   UT-transformed values T diag(beta) V         (kda_ut_wy)
 // and, for the bf16 d = 128 tensor-core path:
-//   blocks     per-chunk operand blocks [T_tot / 16 + N + 1 slots][H][kBlockBytes] (kda_chunk_prep_tc),
+//   blocks     per-step operand blocks [T_tot / 32 + N + 1 slots][H][kBlockBytes] (kda_chunk_prep_tc),
 //              present when the workspace holds them ("split" plan; otherwise the fused kernel runs)
-//   seg_in, seg_st, seg_mt   fp32 [N][H][max_seg][d_k][d_v] per-segment states (segmented plans)
+//   seg_in, seg_st           fp32 [N][H][max_seg][d_k][d_v] per-segment states (segmented plans)
+//   seg_mt                   [N][H][max_seg] transitions M, 64 KB each in the scan's operand format
+//                            (seg_m_off below)
 #pragma once
 
 #include <cuda_bf16.h>
@@ -36,8 +38,9 @@ struct ForwardLayout {
     bool split;  // tensor-core path: parallel chunk preparation + state pass (else the fused kernel)
 };
 
-// Bytes of one chunk's operand block (the state pass's per-chunk input; see kda_tc_chunk.cuh).
-constexpr size_t kBlockBytes = 26112;
+// Bytes of one operand block (the state pass's input for one 32-token step; see kda_tc_chunk.cuh).
+constexpr size_t kBlockBytes = 53760;
+constexpr int kPair = 2 * kChunk;  // tokens per state step of the split tensor-core plan
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -55,10 +58,11 @@ inline int64_t max_chunks_of(const kda_problem_t& p)
     return (L + kChunk - 1) / kChunk;
 }
 
-// Operand-block slots of the split tensor-core plan: chunk c of sequence n uses slot cu[n] / 16 + n + c.
+// Operand-block slots of the split tensor-core plan: 32-token step s of sequence n uses slot
+// cu[n] / 32 + n + s.
 inline size_t block_bytes_of(const kda_problem_t& p)
 {
-    const size_t slots = (size_t)(p.total_tokens / kChunk) + (size_t)p.num_seqs + 1;
+    const size_t slots = (size_t)(p.total_tokens / kPair) + (size_t)p.num_seqs + 1;
     return slots * (size_t)p.num_heads * kBlockBytes;
 }
 
@@ -68,7 +72,8 @@ inline size_t block_bytes_of(const kda_problem_t& p)
 // scanned, and the segments re-run from their true incoming states.  The plan minimises a
 // wave-count model of the passes (`split`: two state-pass CTAs per SM, else the fused kernel's
 // one).  The environment variable KDA_SEGMENT_CHUNKS=<n> forces n chunks per segment
-// (0: no segmentation).  Only plans whose per-segment state buffers fit in `budget_bytes` count.
+// (0: no segmentation; the split plan rounds n up to an even count, its state steps being
+// pairs of chunks).  Only plans whose per-segment state buffers fit in `budget_bytes` count.
 void segment_plan(const kda_problem_t& p, size_t budget_bytes, bool split, int32_t& seg_chunks, int32_t& max_seg);
 
 // Workspace layout for a problem given `available` bytes of workspace.  Tensor-core path: the split
@@ -137,9 +142,27 @@ struct PrefillArgs {
     int32_t seg_mode;         // 0: outputs; 1: end state from zero (S~); 2: transition (M)
     float* seg_in;            // [N][H][max_seg][d][d] incoming state of every segment (scan output)
     float* seg_st;            // [N][H][max_seg][d][d] S~ of every segment
-    float* seg_mt;            // [N][H][max_seg][d][d] M of every segment
+    float* seg_mt;            // [N][H][max_seg] M of every segment, seg_m_off format (64 KB each)
     unsigned char* blocks;    // per-chunk operand blocks of the split tensor-core plan
 };
+
+// A segment's transition M (d = 128; M[c][j]: the coefficient of incoming state row j in outgoing
+// row c) as the scan's mma.sync A operand: bf16 hi and lo planes of the row-major [c][j] matrix,
+// lo = bf16(M - hi), 32 KB each, the 16-byte chunks of every 256-byte row permuted by XOR with
+// c mod 8 so that the rows of an 8 x 8 ldmatrix tile fall on distinct banks.
+constexpr uint32_t kSegMPlane = 128 * 128 * 2;
+__host__ __device__ __forceinline__ uint32_t seg_m_off(int c, int j)
+{
+    return (uint32_t)(c * 256 + ((((j >> 3) ^ (c & 7))) << 4) + (j & 7) * 2);
+}
+__device__ __forceinline__ void store_seg_m(float* seg, int c, int j, float x)
+{
+    const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+    unsigned char* base = reinterpret_cast<unsigned char*>(seg);
+    *reinterpret_cast<__nv_bfloat16*>(base + seg_m_off(c, j)) = hi;
+    *reinterpret_cast<__nv_bfloat16*>(base + kSegMPlane + seg_m_off(c, j)) = lo;
+}
 
 struct DecodeArgs {
     const void* q;

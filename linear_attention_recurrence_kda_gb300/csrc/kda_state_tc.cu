@@ -1,32 +1,32 @@
 // kda_state_tc.cu -- the sequential state pass of the bf16, d = 128 prefill on the tensor cores.
 //
-// Per chunk of one (sequence, head[, segment]), with the chunk's operand block prepared by
-// kda_prep_tc.cu (W, Q Gamma, (K Gamma_C / Gamma)^T, U~, P, Gamma_C):
+// The state advances in 32-token steps (two 16-token chunks fused by the preparation kernel,
+// kda_prep_tc.cu, into one operand block: W, Q Gamma, [P ; (K Gamma_C / Gamma)^T], U~, Gamma_C):
 //   U = U~ - W S,   O = (Q Gamma) S + P U,   S <- Diag(Gamma_C) S + (K Gamma_C / Gamma)^T U
 // (the chunk form of Equation 1, "Kimi K3: the paper and proofs side by side", section 2.1.1;
 // "Kimi K3: architecture, derivations and a pinned-source audit", section 4.5).
 //
 // Value channels j are the 128 TMEM lanes; the fp32 state S^T [j][c] itself lives in tensor memory.
-// Per chunk:
-//   D1 = bf16(S)^T [W ; Q Gamma]^T      (M = 128, N = 32, K = 128: (W S)^T and (Q Gamma S)^T)
-//   U^T = U~^T - (W S)^T                (a bf16 hi/lo pair, written to tensor memory)
-//   [O^T | S^T] += U^T [P ; (K Gamma_C / Gamma)^T]^T   (one N = 144 product per hi/lo term: the
-//                                        output update and the state update share an instruction;
+// Per step:
+//   D1 = bf16(S)^T [W ; Q Gamma]^T      (M = 128, N = 64, K = 128: (W S)^T and (Q Gamma S)^T)
+//   U^T = U~^T - (W S)^T                (a bf16 hi/lo pair, written to tensor memory over (W S)^T)
+//   [O^T | S^T] += U^T [P ; (K Gamma_C / Gamma)^T]^T   (N = 160, K = 32: per hi/lo term two
+//                                        instructions update the outputs and the state together;
 //                                        S^T already holds S^T Diag(Gamma_C))
-//   bf16(S)^T and S^T Diag(Gamma_C of the next chunk)  (one read of the new state writes the next
+//   bf16(S)^T and S^T Diag(Gamma_C of the next step)   (one read of the new state writes the next
 //                                        D1's A operand and the next update's decayed state)
-// A tcgen05.mma costs about the same whatever N is, so the chunk is organised around few
-// instructions: 8 for D1 and 3 for the fused update.  The operand blocks stream through a four-slot
-// shared-memory ring by plain bulk copies issued four chunks ahead.  256 threads, ~105 KB of shared
+// A tcgen05.mma costs about the same whatever N is, so a step is organised around few
+// instructions: 8 for D1 and 6 for the fused update, for 32 tokens.  The operand blocks stream
+// through a two-slot shared-memory ring by plain bulk copies.  256 threads, ~107 KB of shared
 // memory and 256 TMEM columns per CTA: two CTAs (two independent chains) share an SM.  Outputs are
-// moved from tensor memory to registers after the update and stored while the next chunk's D1 runs.
+// moved from tensor memory to registers after the update and stored while the next step's D1 runs.
 //
 // Modes (segmented prefill, see the launcher): 0 writes outputs and (last segment) the final state;
 // 1 computes S~, the segment's end state from a zero start; 2 computes M, the segment's transition,
 // as the end state from the identity with V = 0 (columns of M evolve exactly like state columns),
-// stored transposed.  Every mbarrier wait is bounded; a wait that gives up raises the timeout bit of
-// the check word, the CTA skips the remaining work, waits (bounded) for its copies and products in
-// flight and frees its tensor memory.
+// stored as the scan's bf16 hi/lo operand (seg_m_off).  Every mbarrier wait is bounded; a wait
+// that gives up raises the timeout bit of the check word, the CTA skips the remaining work, waits
+// (bounded) for its copies and products in flight and frees its tensor memory.
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
 #include "kda_tc_chunk.cuh"
@@ -41,8 +41,9 @@ using tcc::u2f;
 
 constexpr int NTHREADS = 256;
 constexpr uint32_t WAIT_LIMIT = 1u << 17;  // tries of up to 20 us each: ~2.6 s at most
-constexpr int NSLOT = 4;                   // ring depth (chunks in flight)
-constexpr uint32_t SLOT = 26624;           // ring slot stride (a multiple of 1024 >= BLK_BYTES)
+constexpr int CT = tcc::PAIR;              // tokens per step (32)
+constexpr int NSLOT = 2;                   // ring depth (steps in flight)
+constexpr uint32_t SLOT = 54272;           // ring slot stride (a multiple of 1024 >= BLK_BYTES)
 
 // shared-memory map (bytes from a 1024-aligned base)
 constexpr uint32_t OFF_RING = 0;                         // [NSLOT] operand blocks
@@ -57,11 +58,11 @@ static_assert(SLOT >= tcc::BLK_BYTES && SLOT % 1024 == 0, "ring slots must hold 
 static_assert(2 * (SMEM_BYTES + 1024) <= 232448, "two CTAs must fit on an SM");
 
 // tensor-memory columns
-constexpr uint32_t TM_WQ = 0;     // D1: [0, 16) (W S)^T; [16, 32) (Q Gamma S)^T, then O^T
-constexpr uint32_t TM_O = 16;     // O^T, immediately followed by the state: the fused update's D
-constexpr uint32_t TM_S = 32;     // S^T fp32 (lanes = j, columns = c), 128 columns
-constexpr uint32_t TM_SA = 160;   // bf16 S^T as the A operand of D1: c pairs, 64 columns
-constexpr uint32_t TM_UA = 224;   // bf16 U^T hi (8 columns), lo (8 columns)
+constexpr uint32_t TM_WU = 0;     // D1's (W S)^T [32 tokens], then U^T hi/lo: tokens 16 h .. 16 h + 15 hi at
+                                  // columns 16 h .. 16 h + 7, lo at 16 h + 8 .. 16 h + 15 (h = 0, 1)
+constexpr uint32_t TM_O = 32;     // D1's (Q Gamma S)^T, then O^T; immediately followed by the state
+constexpr uint32_t TM_S = 64;     // S^T fp32 (lanes = j, columns = c), 128 columns
+constexpr uint32_t TM_SA = 192;   // bf16 S^T as the A operand of D1: c pairs, 64 columns
 constexpr uint32_t TM_COLS = 256;
 
 __device__ __forceinline__ void sync_all() { tcc::named_sync(1, NTHREADS); }
@@ -102,9 +103,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
     const int64_t s0 = q0 + (int64_t)k * seg_c * C;
     const int64_t s1 = min(q1, s0 + seg_c * C);
     const int H = a.H;
-    const int nchunks = (int)((s1 - s0 + C - 1) / C);
-    const int64_t cbase = q0 / C + n + (int64_t)k * seg_c;  // block slot of the segment's first chunk
-    auto chunk_len = [&](int chunk) -> int { return (int)min((int64_t)C, s1 - (s0 + (int64_t)chunk * C)); };
+    const int nchunks = (int)((s1 - s0 + CT - 1) / CT);  // 32-token steps of the segment
+    // block slot of the segment's first step (segments hold an even number of 16-token chunks)
+    const int64_t cbase = q0 / CT + n + (int64_t)k * (seg_c / 2);
+    auto chunk_len = [&](int chunk) -> int { return (int)min((int64_t)CT, s1 - (s0 + (int64_t)chunk * CT)); };
     auto block_of = [&](int chunk) -> const unsigned char* {
         return a.blocks + ((cbase + chunk) * H + h) * (int64_t)tcc::BLK_BYTES;
     };
@@ -194,14 +196,14 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
     tc::fence_after_sync();
 
     // outputs of the previous chunk, held in registers until the next chunk's D1 runs
-    uint32_t ovp[4];  // bf16 pairs
+    uint32_t ovp[8];  // bf16 pairs: tokens 16 h2 .. 16 h2 + 15
     int64_t o_t0 = 0;
     int o_len = 0;
     bool o_have = false;
     auto store_outputs = [&]() {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int r = 8 * h2 + e;
+        for (int e = 0; e < 16; ++e) {
+            const int r = 16 * h2 + e;
             const unsigned short bits = (unsigned short)((e & 1) ? (ovp[e >> 1] >> 16) : (ovp[e >> 1] & 0xffffu));
             if (r < o_len) op[((o_t0 + r) * H + h) * D + jrow] = __ushort_as_bfloat16(bits);
         }
@@ -213,18 +215,18 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
         unsigned char* blk = sm + OFF_RING + sl * SLOT;
         bool dead = read_dead(abort_flag);
 
-        // chunk ch's block has landed: every thread waited for it in the previous chunk's re-staging
-        // (or before the initial state was written).  Thread 0 issues D1 (N = 32 with outputs, else
-        // 16: W only) while the other warps store the previous chunk's outputs.
+        // step ch's block has landed: every thread waited for it in the previous step's re-staging
+        // (or before the initial state was written).  Thread 0 issues D1 (N = 64 with outputs, else
+        // 32: W only) while the other warps store the previous step's outputs.
         const bool got = !dead;
         bool issued = false;
         if (tid == 0 && got) {
-            const uint32_t idd = tc::idesc_bf16(128, mode == 0 ? 2 * C : C);
+            const uint32_t idd = tc::idesc_bf16(128, mode == 0 ? 2 * CT : CT);
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
                 const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
-                tc::umma_ts(tbase + TM_WQ, tbase + TM_SA + 8 * ks,
-                            tc::desc_sw128(tc::smem_u32(blk + tcc::BLK_WQ + kb * (2 * C * 128) + off)), idd,
+                tc::umma_ts(tbase + TM_WU, tbase + TM_SA + 8 * ks,
+                            tc::desc_sw128(tc::smem_u32(blk + tcc::BLK_WQ + kb * (2 * CT * 128) + off)), idd,
                             ks > 0 ? 1u : 0u);
             }
             tc::umma_commit(bar_c);
@@ -241,39 +243,45 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
         tc::fence_after_sync();
         dead = read_dead(abort_flag);
 
-        // U^T = U~^T - (W S)^T as a hi/lo pair into tensor memory; warp half h2 takes tokens 8 h2 .. + 7
+        // U^T = U~^T - (W S)^T as a hi/lo pair into tensor memory; warp half h2 takes tokens
+        // 16 h2 .. 16 h2 + 15 and overwrites exactly the (W S)^T columns it has read
         if (!dead) {
-            uint32_t dv[8];
-            KDA_TMEM_LD8(lane_base + TM_WQ + 8 * h2, dv);
-            float uv[8];
+            uint32_t dv[16];
+            KDA_TMEM_LD16(lane_base + TM_WU + 16 * h2, dv);
+            float uv[16];
             const float* ut = reinterpret_cast<const float*>(blk + tcc::BLK_UT);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) uv[e] = (mode == 2) ? 0.f : ut[(8 * h2 + e) * D + jrow];
+            for (int e = 0; e < 16; ++e) uv[e] = (mode == 2) ? 0.f : ut[(16 * h2 + e) * D + jrow];
             tc::tmem_wait_ld();
-            uint32_t hi[4], lo[4];
+            uint32_t hi[8], lo[8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
+            for (int e = 0; e < 8; ++e) {
                 tcc::split2(uv[2 * e] - u2f(dv[2 * e]), uv[2 * e + 1] - u2f(dv[2 * e + 1]), hi[e], lo[e]);
             }
-            KDA_TMEM_ST4(lane_base + TM_UA + 4 * h2, hi);
-            KDA_TMEM_ST4(lane_base + TM_UA + 8 + 4 * h2, lo);
+            KDA_TMEM_ST8(lane_base + TM_WU + 16 * h2, hi);
+            KDA_TMEM_ST8(lane_base + TM_WU + 16 * h2 + 8, lo);
             tc::tmem_wait_st();
         }
         tc::fence_before_sync();
         sync_all();
         tc::fence_after_sync();
 
-        // [O^T | S^T] += U^T [P ; (K Gamma_C / Gamma)^T]^T as hi*hi + hi*lo + lo*hi (without outputs:
-        // S^T += U^T (K Gamma_C / Gamma) alone)
+        // [O^T | S^T] += U^T [P ; (K Gamma_C / Gamma)^T]^T as hi*hi + hi*lo + lo*hi, one K = 16 half of
+        // the step's tokens at a time (without outputs: S^T += U^T (K Gamma_C / Gamma) alone)
         if (tid == 0 && !dead) {
             const uint32_t dst = mode == 0 ? TM_O : TM_S;
-            const uint32_t idd = tc::idesc_bf16(128, mode == 0 ? C + D : D);
+            const uint32_t idd = tc::idesc_bf16(128, mode == 0 ? CT + D : D);
             const uint32_t boff = mode == 0 ? tcc::BLK_PK : tcc::BLK_KT;
-            const uint64_t dB = tc::desc_none(tc::smem_u32(blk + boff));
-            const uint64_t dBl = tc::desc_none(tc::smem_u32(blk + boff + tcc::BLK_PK_LO));
-            tc::umma_ts(tbase + dst, tbase + TM_UA, dB, idd, 1u);
-            tc::umma_ts(tbase + dst, tbase + TM_UA, dBl, idd, 1u);
-            tc::umma_ts(tbase + dst, tbase + TM_UA + 8, dB, idd, 1u);
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const uint64_t dB = tc::desc_none_strided(tc::smem_u32(blk + boff + 256 * ks), 128, tcc::PK_RG);
+                const uint64_t dBl =
+                    tc::desc_none_strided(tc::smem_u32(blk + boff + tcc::BLK_PK_LO + 256 * ks), 128, tcc::PK_RG);
+                const uint32_t ahi = tbase + TM_WU + 16 * ks, alo = ahi + 8;
+                tc::umma_ts(tbase + dst, ahi, dB, idd, 1u);
+                tc::umma_ts(tbase + dst, ahi, dBl, idd, 1u);
+                tc::umma_ts(tbase + dst, alo, dB, idd, 1u);
+            }
             tc::umma_commit(bar_c);
             if (tc::mbar_wait(bar_c, ph_c, WAIT_LIMIT)) ph_c ^= 1u;
             else *abort_flag = 1u, pend_c = true;
@@ -296,10 +304,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
                     *abort_flag = 1u;
                 }
             }
-            uint32_t v[4][16], ob[8];
+            uint32_t v[4][16], ob[16];
 #pragma unroll
             for (int q = 0; q < 4; ++q) KDA_TMEM_LD16(my_s + 16 * q, v[q]);
-            if (mode == 0) KDA_TMEM_LD8(lane_base + TM_O + 8 * h2, ob);
+            if (mode == 0) KDA_TMEM_LD16(lane_base + TM_O + 16 * h2, ob);
             tc::tmem_wait_ld();
 #pragma unroll
             for (int q = 0; q < 4; ++q) stage16(q, v[q]);
@@ -320,8 +328,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
             }
             if (mode == 0) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) ovp[e] = tc::pack_bf16(u2f(ob[2 * e]), u2f(ob[2 * e + 1]));
-                o_t0 = s0 + (int64_t)ch * C;
+                for (int e = 0; e < 8; ++e) ovp[e] = tc::pack_bf16(u2f(ob[2 * e]), u2f(ob[2 * e + 1]));
+                o_t0 = s0 + (int64_t)ch * CT;
                 o_len = chunk_len(ch);
                 o_have = true;
             }
@@ -356,11 +364,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
             KDA_TMEM_LD16(my_s + 16 * q, v);
             tc::tmem_wait_ld();
             if (mode == 2) {
-                // the transition is stored transposed, M^T[j][c], for the scan
-                float4* d4 = reinterpret_cast<float4*>(dst + (int64_t)jrow * D + 64 * h2 + 16 * q);
+                // the transition M[c][j] (this lane holds column j = jrow) in the scan's operand format
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    d4[e] = make_float4(u2f(v[4 * e]), u2f(v[4 * e + 1]), u2f(v[4 * e + 2]), u2f(v[4 * e + 3]));
+                for (int e = 0; e < 16; ++e) store_seg_m(dst, 64 * h2 + 16 * q + e, jrow, u2f(v[e]));
             } else {
 #pragma unroll
                 for (int e = 0; e < 16; ++e) dst[(int64_t)(64 * h2 + 16 * q + e) * D + jrow] = u2f(v[e]);
@@ -374,17 +380,25 @@ __global__ void __launch_bounds__(NTHREADS, 2) kda_chunk_state_tc_kernel(Prefill
 
 namespace {
 
+// Shared memory requested by a grid that fits on the SMs one CTA each: more than half of an SM's,
+// so that two chains never share an SM.  (A CTA launched early, next to the previous kernel's
+// CTAs, is placed wherever there is room; without this it could land on an SM that already holds
+// a chain and run at the shared speed.)
+constexpr uint32_t SMEM_EXCLUSIVE = 120 * 1024;
+static_assert(SMEM_EXCLUSIVE >= SMEM_BYTES && 2 * (SMEM_EXCLUSIVE + 1024) > 233472, "one CTA per SM");
+
 cudaError_t launch_chunk_state_tc(const PrefillArgs& a, int seg_mode, cudaStream_t s)
 {
     cudaError_t e = cudaFuncSetAttribute(kda_chunk_state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+                                         (int)SMEM_EXCLUSIVE);
     if (e != cudaSuccess) return e;
     PrefillArgs b = a;
     b.seg_mode = seg_mode;
     const unsigned gz = seg_mode == 0 ? (unsigned)(a.max_seg > 1 ? a.max_seg : 1) : (unsigned)(2 * (a.max_seg - 1));
     if (gz == 0) return cudaSuccess;
-    return launch_dependent(kda_chunk_state_tc_kernel, dim3((unsigned)a.N, (unsigned)a.H, gz), dim3(NTHREADS), SMEM_BYTES,
-                            s, b);
+    const int64_t ctas = (int64_t)a.N * a.H * gz;
+    const uint32_t smem = ctas <= (int64_t)sm_count_of_current_device() ? SMEM_EXCLUSIVE : SMEM_BYTES;
+    return launch_dependent(kda_chunk_state_tc_kernel, dim3((unsigned)a.N, (unsigned)a.H, gz), dim3(NTHREADS), smem, s, b);
 }
 
 }  // namespace

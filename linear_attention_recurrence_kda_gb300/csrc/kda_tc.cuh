@@ -67,6 +67,18 @@ __device__ __forceinline__ uint64_t desc_none(uint32_t addr)
     return d;                          // layout type 0: no swizzle
 }
 
+// No-swizzle K-major operand with a K-direction core-matrix stride of `lbo` bytes and an
+// 8-row-group stride of `sbo` bytes (rows of 32 elements: lbo = 128, sbo = 512).
+__device__ __forceinline__ uint64_t desc_none_strided(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
 // kind::f16 instruction descriptor: bf16 A and B (K-major), fp32 accumulator, M x N.
 __host__ __device__ __forceinline__ uint32_t idesc_bf16(int M, int N)
 {
@@ -140,6 +152,11 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 #define KDA_TMEM_ST4(taddr, v)                                                                     \
     asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(v[0]), \
                  "r"(v[1]), "r"(v[2]), "r"(v[3])                                                    \
+                 : "memory")
+
+#define KDA_TMEM_ST8(taddr, v)                                                                       \
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), \
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])  \
                  : "memory")
 
 #define KDA_TMEM_ST16(taddr, v)                                                                             \

@@ -40,18 +40,31 @@ constexpr uint32_t NONE_TILE = 4096;        // [128][16] bf16 NONE tile
 constexpr uint32_t SMALL_TILE = 512;        // [16][16] bf16 NONE tile
 constexpr uint32_t ROW_TILE = C * LROW * 2; // [16][LROW] bf16 row-major tile: 4352 bytes
 
-// Per-chunk operand block: everything the state pass needs for one chunk of one head, laid out
-// exactly as the state pass stages it in shared memory (one contiguous bulk copy).  P and
-// (K Gamma_C / Gamma)^T are stored as one NONE-layout operand [P ; (K Gamma_C / Gamma)^T]
-// (16 + 128 rows of 16 tokens), so that the output and state-update products of a chunk share one
-// tensor-core instruction (N = 144); hi and lo parts are two such operands.
-constexpr uint32_t BLK_WQ = 0;        // [W ; Q Gamma (hi)] [32][128 c] bf16 SW128           8192
-constexpr uint32_t BLK_PK = 8192;     // [P ; (K Gamma_C / Gamma)^T] hi [144][16] NONE         4608
-constexpr uint32_t BLK_PK_LO = 4608;  //   ... and its lo part at BLK_PK + BLK_PK_LO          4608
-constexpr uint32_t BLK_KT = BLK_PK + SMALL_TILE;  // (K Gamma_C / Gamma)^T hi (lo: + BLK_PK_LO)
-constexpr uint32_t BLK_UT = 17408;    // U~ = T' V fp32 [16 r][128 j]                         8192
-constexpr uint32_t BLK_GC = 25600;    // Gamma_C fp32 [128]                                    512
-constexpr uint32_t BLK_BYTES = 26112;
+// Per-pair operand block: everything the state pass needs for one 32-token step (two consecutive
+// 16-token chunks a, b of one head), laid out exactly as the state pass stages it in shared memory
+// (one contiguous bulk copy).  With X = W_b K~_a^T and Z = (Q Gamma)_b K~_a^T (K~ = K Gamma_C /
+// Gamma), the pair acts on the state like one chunk of 32 tokens:
+//   W = [W_a ; W_b Gamma_Ca - X W_a],  U~ = [U~_a ; U~_b - X U~_a],  Q = [(Q Gamma)_a ; (Q Gamma)_b Gamma_Ca],
+//   K~ = [K~_a Gamma_Cb ; K~_b],       P = [[P_a, 0] ; [Z, P_b]],     Gamma_C = Gamma_Ca Gamma_Cb
+// (substitute chunk a's end state into chunk b's equations), and every factor stays bounded by one
+// in magnitude as in the 16-token form.  P and K~^T are stored as one no-swizzle operand
+// [P ; K~^T] (32 + 128 rows of 32 tokens), so that the output and state-update products of a step
+// share one tensor-core instruction (N = 160); hi and lo parts are two such operands.
+constexpr int PAIR = 2 * C;                          // tokens per state step
+constexpr uint32_t PK_RG = 512;                      // 8-row-group stride of the [P ; K~^T] operand
+constexpr uint32_t BLK_WQ = 0;        // [W ; Q Gamma (hi)] [64][128 c] bf16 SW128               16384
+constexpr uint32_t BLK_PK = 16384;    // [P ; K~^T] hi [160][32] no-swizzle (LBO 128, SBO 512)    10240
+constexpr uint32_t BLK_PK_LO = 10240; //   ... and its lo part at BLK_PK + BLK_PK_LO              10240
+constexpr uint32_t BLK_KT = BLK_PK + 4 * PK_RG;  // the K~^T rows (from row 32)
+constexpr uint32_t BLK_UT = 36864;    // U~ fp32 [32 r][128 j]                                    16384
+constexpr uint32_t BLK_GC = 53248;    // Gamma_C fp32 [128]                                         512
+constexpr uint32_t BLK_BYTES = 53760;
+
+// Byte offset of element (row, k) of the [P ; K~^T] operand (k < 32 tokens).
+__host__ __device__ __forceinline__ uint32_t pk_off(int row, int k)
+{
+    return (uint32_t)((row >> 3) * PK_RG + (k >> 3) * 128 + (row & 7) * 16 + (k & 7) * 2);
+}
 
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count)
 {
@@ -72,6 +85,18 @@ __host__ __device__ __forceinline__ uint32_t none_off_rg(int r, int k)
 {
     return (uint32_t)((r >> 3) * RG + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2);
 }
+
+// Placement of a no-swizzle K-major tile inside a larger operand: element (r, k) of the tile is
+// element (r + row0, k + k0) of an operand whose 8-row groups are `rg` bytes apart.
+struct NonePlace {
+    uint32_t rg, row0, k0;
+    __device__ __forceinline__ uint32_t off(int r, int k) const
+    {
+        const int rr = r + (int)row0, kk = k + (int)k0;
+        return (uint32_t)((rr >> 3) * (int)rg + (kk >> 3) * 128 + (rr & 7) * 16 + (kk & 7) * 2);
+    }
+};
+constexpr NonePlace kNoneTile{256u, 0u, 0u};  // a standalone [rows][16] tile
 
 // Equation 5 with the fast exponential and division (relative error ~1e-6, far below bf16).
 __device__ __forceinline__ float log_decay_fast(float z, float expA, float g_min)
@@ -138,10 +163,16 @@ __device__ __forceinline__ void mma_kstep(float (&acc)[2][4], const __nv_bfloat1
 // of the SW128 [W ; Q Gamma] tile at `wq` (Q Gamma hi); (K Gamma)^T and V^T (NONE, OFF_XT / OFF_VT);
 // (K Gamma_C / Gamma)^T hi/lo at `kt` and `kt + kt_lo` (NONE); Gamma_C at `gc`.  One barrier
 // (Map::NB) inside.
+// Optional outputs: `wq` (Q Gamma hi into rows wq_row0 + r of an SW128 tile of wq_rows rows,
+// multiplied per channel by `wq_scale` if that is not null) and `kt` may be null; `kt_place` /
+// `kt_lo` place the transposed (K Gamma_C / Gamma) hi/lo tiles inside a larger operand; `kr`, if
+// not null, receives (K Gamma_C / Gamma) row-major hi/lo ([16][LROW] each).
 template <class Map>
 __device__ __forceinline__ void prep_factors(unsigned char* sm, int p, int len, unsigned char* wq, unsigned char* kt,
                                              float* gc, float expA, float g_min, bool zero_v,
-                                             uint32_t kt_lo = NONE_TILE)
+                                             uint32_t kt_lo = NONE_TILE, NonePlace kt_place = kNoneTile,
+                                             int wq_row0 = C, int wq_rows = 2 * C, unsigned char* kr = nullptr,
+                                             const float* wq_scale = nullptr)
 {
     const int cp = p & 63;
     const int tq = p >> 6;
@@ -196,6 +227,7 @@ __device__ __forceinline__ void prep_factors(unsigned char* sm, int p, int len, 
     uint32_t* sKdl = sKd + C * LROW / 2;
     // transposed tiles: 4 tokens of one channel = 8 bytes at none_off(c, 4 tq)
     uint32_t xt0[2], xt1[2], kh0[2], kh1[2], kl0[2], kl1[2];
+    const float2 wsc = wq_scale ? *reinterpret_cast<const float2*>(wq_scale + c0) : make_float2(1.f, 1.f);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
         const int r = r0 + e;
@@ -209,12 +241,19 @@ __device__ __forceinline__ void prep_factors(unsigned char* sm, int p, int len, 
         split2(qv[e].x * eG0, qv[e].y * eG1, hi, lo);
         sQl[ri] = hi;
         sQll[ri] = lo;
-        *reinterpret_cast<uint32_t*>(wq + tc::sw128_off(C + r, c0, 2 * C)) = hi;
+        if (wq) {
+            const uint32_t wv = wq_scale ? pack_f2(qv[e].x * eG0 * wsc.x, qv[e].y * eG1 * wsc.y) : hi;
+            *reinterpret_cast<uint32_t*>(wq + tc::sw128_off(wq_row0 + r, c0, wq_rows)) = wv;
+        }
         split2(kv[e].x * iG0, kv[e].y * iG1, hi, lo);
         sKd[ri] = hi;
         sKdl[ri] = lo;
         uint32_t th, tl;
         split2(kv[e].x * (eGC0 * iG0), kv[e].y * (eGC1 * iG1), th, tl);  // k Gamma_C / Gamma <= 1
+        if (kr) {
+            reinterpret_cast<uint32_t*>(kr)[ri] = th;
+            reinterpret_cast<uint32_t*>(kr)[C * LROW / 2 + ri] = tl;
+        }
         // de-interleave the pairs into per-channel token runs
         const int slot = e >> 1, sh = (e & 1) * 16;
         if ((e & 1) == 0) {
@@ -240,19 +279,34 @@ __device__ __forceinline__ void prep_factors(unsigned char* sm, int p, int len, 
     *reinterpret_cast<uint2*>(sm + Map::OFF_XT + p1) = make_uint2(xt1[0], xt1[1]);
     *reinterpret_cast<uint2*>(sm + Map::OFF_VT + p0) = make_uint2(v00, v01);
     *reinterpret_cast<uint2*>(sm + Map::OFF_VT + p1) = make_uint2(v10, v11);
-    const uint32_t o0 = tc::none_off(c0, r0), o1 = tc::none_off(c0 + 1, r0);
-    *reinterpret_cast<uint2*>(kt + o0) = make_uint2(kh0[0], kh0[1]);
-    *reinterpret_cast<uint2*>(kt + o1) = make_uint2(kh1[0], kh1[1]);
-    *reinterpret_cast<uint2*>(kt + kt_lo + o0) = make_uint2(kl0[0], kl0[1]);
-    *reinterpret_cast<uint2*>(kt + kt_lo + o1) = make_uint2(kl1[0], kl1[1]);
+    if (kt) {
+        const uint32_t o0 = kt_place.off(c0, r0), o1 = kt_place.off(c0 + 1, r0);
+        *reinterpret_cast<uint2*>(kt + o0) = make_uint2(kh0[0], kh0[1]);
+        *reinterpret_cast<uint2*>(kt + o1) = make_uint2(kh1[0], kh1[1]);
+        *reinterpret_cast<uint2*>(kt + kt_lo + o0) = make_uint2(kl0[0], kl0[1]);
+        *reinterpret_cast<uint2*>(kt + kt_lo + o1) = make_uint2(kl1[0], kl1[1]);
+    }
 }
 
-// A and P over K = 128 with mma.sync, two k-steps per warp (warps 0..3: A, warps 4..7: P as
-// hi*hi + hi*lo + lo*hi), partial sums reduced in shared memory (OFF_PART, 8 KB); then
-// T = (I + A)^-1 by forward substitution and T' = T diag(beta) (hi/lo, OFF_T), P finalised into
-// `pb` and `pb + p_lo` (hi/lo NONE).  beta of the chunk is read from OFF_BETA.  Two barriers (Map::NB) inside.
-template <class Map>
-__device__ __forceinline__ void prep_solve(unsigned char* sm, int p, unsigned char* pb, uint32_t p_lo = SMALL_TILE)
+// Variants of the per-chunk solve (template argument of prep_solve).
+enum SolveVariant : int {
+    SOLVE_ONE = 0,    // a chunk on its own
+    SOLVE_FIRST = 1,  // chunk a of a pair: also zeroes the upper-right block of the pair's P
+    SOLVE_SECOND = 2  // chunk b of a pair: also the cross products with chunk a's K~ (below)
+};
+
+// A and P over K = 128 with mma.sync, partial sums reduced in shared memory (OFF_PART, 8 KB);
+// then T = (I + A)^-1 by forward substitution and T' = T diag(beta) (hi/lo, OFF_T), P finalised
+// into `pb` and `pb + p_lo` (hi/lo, placed by p_place).  beta of the chunk is read from OFF_BETA.
+// SOLVE_ONE / SOLVE_FIRST: warps 0..3 A, warps 4..7 P as hi*hi + hi*lo + lo*hi, two k-steps each.
+// SOLVE_SECOND: chunk a's K~ = K Gamma_C / Gamma (row-major hi/lo at Map::OFF_KRA) also enters
+//   Y = (K Gamma) K~_a^T  (so that X = W K~_a^T = T' Y)   -> bf16 hi/lo B operand at Map::OFF_YT
+//   Z = (Q Gamma) K~_a^T  (the pair's lower-left output block) -> `pb` rows 16..31, tokens 0..15
+// with warp 0: A, warps 1, 2: Y (K~ hi, lo), warps 3..5: P, warps 6, 7: Z (k-steps 0..3, 4..7).
+// Two barriers (Map::NB) inside.
+template <class Map, int VAR = SOLVE_ONE>
+__device__ __forceinline__ void prep_solve(unsigned char* sm, int p, unsigned char* pb, uint32_t p_lo = SMALL_TILE,
+                                           NonePlace p_place = kNoneTile)
 {
     const int pw = p >> 5, lane = p & 31;
     float* sA = reinterpret_cast<float*>(sm + Map::OFF_A);
@@ -265,17 +319,43 @@ __device__ __forceinline__ void prep_solve(unsigned char* sm, int p, unsigned ch
     const __nv_bfloat16* sKdl = sKd + C * LROW;
     {
         const int g = lane >> 2, t = lane & 3;
-        const int k0 = 32 * (pw & 3);
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        if (pw < 4) {
-            mma_kstep(acc, sLl, sKd, k0, lane);
-            mma_kstep(acc, sLl, sKd, k0 + 16, lane);
-        } else {
+        if constexpr (VAR != SOLVE_SECOND) {
+            const int k0 = 32 * (pw & 3);
+            if (pw < 4) {
+                mma_kstep(acc, sLl, sKd, k0, lane);
+                mma_kstep(acc, sLl, sKd, k0 + 16, lane);
+            } else {
 #pragma unroll
-            for (int kk = 0; kk < 32; kk += 16) {
-                mma_kstep(acc, sQl, sKd, k0 + kk, lane);
-                mma_kstep(acc, sQl, sKdl, k0 + kk, lane);
-                mma_kstep(acc, sQll, sKd, k0 + kk, lane);
+                for (int kk = 0; kk < 32; kk += 16) {
+                    mma_kstep(acc, sQl, sKd, k0 + kk, lane);
+                    mma_kstep(acc, sQl, sKdl, k0 + kk, lane);
+                    mma_kstep(acc, sQll, sKd, k0 + kk, lane);
+                }
+            }
+        } else {
+            const __nv_bfloat16* sKa = reinterpret_cast<const __nv_bfloat16*>(sm + Map::OFF_KRA);
+            const __nv_bfloat16* sKal = sKa + C * LROW;
+            // one product over all eight k-steps per warp (two half-ranges of three for Z)
+            const __nv_bfloat16* L = (pw < 3) ? sLl : (pw == 4 ? sQl : (pw == 5 ? sQll : sQl));
+            const __nv_bfloat16* R = (pw == 0)   ? sKd
+                                     : (pw == 1) ? sKa
+                                     : (pw == 2) ? sKal
+                                     : (pw == 3) ? sKd
+                                     : (pw == 4) ? sKdl
+                                     : (pw == 5) ? sKd
+                                                 : sKa;
+            if (pw < 6) {
+#pragma unroll 4
+                for (int k0 = 0; k0 < D; k0 += 16) mma_kstep(acc, L, R, k0, lane);
+            } else {
+                const int kb = 64 * (pw - 6);
+#pragma unroll 2
+                for (int k0 = kb; k0 < kb + 64; k0 += 16) {
+                    mma_kstep(acc, sQl, sKa, k0, lane);
+                    mma_kstep(acc, sQl, sKal, k0, lane);
+                    mma_kstep(acc, sQll, sKa, k0, lane);
+                }
             }
         }
         float* pp = part + pw * C * C;
@@ -287,19 +367,42 @@ __device__ __forceinline__ void prep_solve(unsigned char* sm, int p, unsigned ch
     }
     named_sync(Map::NB, NGROUP);
     {
-        const int idx = p;  // one entry of A and one of P per thread
+        const int idx = p;  // one entry of each 16 x 16 result per thread
         const int r = idx >> 4, i = idx & 15;
-        float sa = 0.f, sp = 0.f;
+        float sa, sp;
+        if constexpr (VAR != SOLVE_SECOND) {
+            sa = 0.f;
+            sp = 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            sa += part[k * C * C + idx];
-            sp += part[(4 + k) * C * C + idx];
+            for (int k = 0; k < 4; ++k) {
+                sa += part[k * C * C + idx];
+                sp += part[(4 + k) * C * C + idx];
+            }
+        } else {
+            sa = part[idx];
+            sp = part[3 * C * C + idx] + part[4 * C * C + idx] + part[5 * C * C + idx];
+            const float sy = part[1 * C * C + idx] + part[2 * C * C + idx];
+            const float sz = part[6 * C * C + idx] + part[7 * C * C + idx];
+            __nv_bfloat16 hi, lo;
+            // Y[r][i] as the B operand of T' Y: element (k = r, n = i) of a no-swizzle [16 n][16 k] tile
+            split_bf16(sy, hi, lo);
+            st_bf16(sm, Map::OFF_YT + tc::none_off(i, r), hi);
+            st_bf16(sm, Map::OFF_YT + SMALL_TILE + tc::none_off(i, r), lo);
+            split_bf16(sz, hi, lo);
+            const NonePlace zp{p_place.rg, p_place.row0, p_place.k0 - C};
+            st_bf16(pb, zp.off(r, i), hi);
+            st_bf16(pb, p_lo + zp.off(r, i), lo);
         }
         sA[idx] = (i < r) ? beta[r] * sa : 0.f;
         __nv_bfloat16 hi, lo;
         split_bf16((i <= r) ? sp : 0.f, hi, lo);
-        st_bf16(pb, tc::none_off(r, i), hi);
-        st_bf16(pb, p_lo + tc::none_off(r, i), lo);
+        st_bf16(pb, p_place.off(r, i), hi);
+        st_bf16(pb, p_lo + p_place.off(r, i), lo);
+        if constexpr (VAR == SOLVE_FIRST) {
+            const NonePlace up{p_place.rg, p_place.row0, p_place.k0 + C};
+            st_bf16(pb, up.off(r, i), __float2bfloat16_rn(0.f));
+            st_bf16(pb, p_lo + up.off(r, i), __float2bfloat16_rn(0.f));
+        }
     }
     named_sync(Map::NB, NGROUP);
     if (pw == 0 && lane < C) {

@@ -62,10 +62,10 @@ def test_workspace_bytes(L, monkeypatch):
     # check word + G, W (d_k) and U~ (d_v) in fp32 for every token-head
     assert n >= 256 + 64 * 2 * (32 + 32 + 32) * 4
     assert n % 256 == 0
-    # bf16 inputs with d_k = d_v = 128: the fastest plan holds one 26,112-byte operand block per
-    # chunk slot (T_tot / 16 + N + 1 slots) and head, plus per-segment states
+    # bf16 inputs with d_k = d_v = 128: the fastest plan holds one 53,760-byte operand block per
+    # 32-token step slot (T_tot / 32 + N + 1 slots) and head, plus per-segment states
     big = _prob(total_tokens=1 << 20, max_seqlen=1 << 20, num_heads=8, d_k=128, d_v=128, io_dtype=B.KDA_BF16)
-    blocks = ((1 << 20) // 16 + 1 + 1) * 8 * 26112
+    blocks = ((1 << 20) // 32 + 1 + 1) * 8 * 53760
     assert blocks <= B.kda_forward_workspace_bytes(big) < blocks + (1 << 30)
     # the fused kernel needs no per-token scratch
     monkeypatch.setenv("KDA_TC_PLAN", "fused")
@@ -177,6 +177,18 @@ def test_forward_plan(L, monkeypatch):
     monkeypatch.delenv("KDA_TC_PLAN")
     monkeypatch.setenv("KDA_SEGMENT_CHUNKS", "64")
     assert B.kda_forward_plan(p) == {"split": True, "seg_chunks": 64, "num_segments": 4}
+    # the split plan steps the state by pairs of chunks: an odd count is rounded up
+    monkeypatch.setenv("KDA_SEGMENT_CHUNKS", "3")
+    assert B.kda_forward_plan(p) == {"split": True, "seg_chunks": 4, "num_segments": 64}
+    monkeypatch.setenv("KDA_TC_PLAN", "fused")
+    assert B.kda_forward_plan(p) == {"split": False, "seg_chunks": 3, "num_segments": 86}
+    monkeypatch.delenv("KDA_TC_PLAN")
+    monkeypatch.delenv("KDA_SEGMENT_CHUNKS")
+    # the planner's own choice for the split plan is a whole number of pairs
+    for T in (4096, 3000, 65536):
+        pl = B.kda_forward_plan(_prob(total_tokens=T, max_seqlen=T, num_heads=16, d_k=128, d_v=128,
+                                      io_dtype=B.KDA_BF16))
+        assert pl["split"] and pl["seg_chunks"] % 2 == 0
     # the fp32 path needs per-token scratch: below it the call is refused
     with pytest.raises(B.KdaError) as e:
         B.kda_forward_plan(_prob(), 256)
