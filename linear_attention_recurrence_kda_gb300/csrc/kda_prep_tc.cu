@@ -36,7 +36,8 @@ constexpr int kRunPairs = 2;                 // 32-token steps per CTA
 constexpr uint32_t WAIT_LIMIT = 1u << 17;    // tries of up to 20 us each
 
 // shared-memory map (bytes from a 1024-aligned base)
-constexpr uint32_t XT_RG = 272;          // padded 8-row-group stride of the transposed tiles
+constexpr uint32_t XT_RG = 264;          // padded 8-row-group stride of the transposed tiles (the
+                                         // 8-byte per-channel stores of a half-warp cover all banks)
 constexpr uint32_t OFF_STAGE = 0;        // q, k, v, z tiles [16][128] bf16 (TMA)     16384
 constexpr uint32_t OFF_LL = 16384;       // K Gamma [16][LROW] bf16                     4352
 constexpr uint32_t OFF_QL = 20736;       // Q Gamma hi, lo                          2 x 4352
@@ -92,16 +93,14 @@ __device__ __forceinline__ uint32_t transpose8x8(uint32_t x)
     return y;
 }
 
-// T' hi/lo as mma.sync A fragments (M = 16 tokens, K = 16 tokens)
-__device__ __forceinline__ void load_tprime(const unsigned char* sm, int g, int t, uint32_t (&th)[4], uint32_t (&tl)[4])
+// T' hi/lo as mma.sync A fragments (M = 16 tokens, K = 16 tokens): the four 8 x 8 core matrices
+// of the no-swizzle tile, rows 0..7 / 8..15 at +0 / +256 bytes, tokens 8..15 at +128
+__device__ __forceinline__ void load_tprime(const unsigned char* sm, int lane, uint32_t (&th)[4], uint32_t (&tl)[4])
 {
-    const unsigned char* tt = sm + OFF_T;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const uint32_t o = tc::none_off(g + 8 * (e & 1), 2 * t + 8 * (e >> 1));
-        th[e] = *reinterpret_cast<const uint32_t*>(tt + o);
-        tl[e] = *reinterpret_cast<const uint32_t*>(tt + tcc::SMALL_TILE + o);
-    }
+    const int mi = lane >> 3;
+    const unsigned char* row = sm + OFF_T + (mi & 1) * 256 + (mi >> 1) * 128 + (lane & 7) * 16;
+    tcc::ldsm4(row, th);
+    tcc::ldsm4(row + tcc::SMALL_TILE, tl);
 }
 
 // W = T' (K Gamma) and U~ = T' V of the current chunk for the 8 channels [n0, n0 + 8) (N = 8 per
@@ -129,7 +128,7 @@ __device__ __forceinline__ void wy_first(unsigned char* sm, unsigned char* blk, 
 {
     const int g = lane >> 2, t = lane & 3;
     uint32_t th[4], tl[4];
-    load_tprime(sm, g, t, th, tl);
+    load_tprime(sm, lane, th, tl);
     float* ut = reinterpret_cast<float*>(blk + tcc::BLK_UT);
     uint32_t* fragw = reinterpret_cast<uint32_t*>(sm + OFF_FRAGW);
 #pragma unroll
@@ -165,7 +164,7 @@ __device__ __forceinline__ void wy_second(unsigned char* sm, unsigned char* blk,
         ur[nt][3] = ut[(2 * t + 9) * D + j];
     }
     uint32_t th[4], tl[4];
-    load_tprime(sm, g, t, th, tl);
+    load_tprime(sm, lane, th, tl);
     // X = T' Y, every warp the whole 16 x 16 (its accumulator fragments are the A fragments of X W_a)
     float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     const unsigned char* yt = sm + OFF_YT;

@@ -78,7 +78,7 @@ __device__ __forceinline__ void named_arrive(uint32_t id, uint32_t count)
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 
 // NONE-style tile [rows][16] with an 8-row-group stride of RG bytes (256: the tensor-core operand
-// layout; 272: padded, so that the transposed per-channel stores of prep_factors spread over the
+// layout; 264: padded, so that the transposed per-channel stores of prep_factors spread over the
 // shared-memory banks).
 template <uint32_t RG>
 __host__ __device__ __forceinline__ uint32_t none_off_rg(int r, int k)
@@ -98,13 +98,26 @@ struct NonePlace {
 };
 constexpr NonePlace kNoneTile{256u, 0u, 0u};  // a standalone [rows][16] tile
 
-// Equation 5 with the fast exponential and division (relative error ~1e-6, far below bf16).
-__device__ __forceinline__ float log_decay_fast(float z, float expA, float g_min)
+constexpr float kLog2e = 1.4426950408889634f;
+
+// 2^x and 1/x by the hardware approximations (relative errors ~2^-22, far below bf16)
+__device__ __forceinline__ float ex2_fast(float x)
 {
-    const float x = expA * z;
-    const float e = __expf(-fabsf(x));
-    const float sig = (x >= 0.f) ? __fdividef(1.f, 1.f + e) : __fdividef(e, 1.f + e);
-    return g_min * sig;
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_fast(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// a packed pair of bf16 as two floats (low half first)
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t w)
+{
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
 __device__ __forceinline__ void st_bf16(unsigned char* base, uint32_t off, __nv_bfloat16 x)
@@ -134,24 +147,52 @@ __device__ __forceinline__ uint32_t pack_f2(float x0, float x1)
     __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
     return *reinterpret_cast<uint32_t*>(&h);
 }
+__device__ __forceinline__ uint32_t pack_f2(float2 x) { return pack_f2(x.x, x.y); }
 
-// 16x16 partial product over one k-step (16 channels): acc += L[:, k0:k0+16] R[:, k0:k0+16]^T,
-// L and R row-major [16][LROW] bf16.
-__device__ __forceinline__ void mma_kstep(float (&acc)[2][4], const __nv_bfloat16* L, const __nv_bfloat16* R, int k0,
-                                          int lane)
+// x = hi + lo as bf16 pairs, the residual by one packed subtraction
+__device__ __forceinline__ void split2v(float2 x, uint32_t& hi, uint32_t& lo)
 {
-    const int g = lane >> 2, t = lane & 3;
-    uint32_t af[4];
-    af[0] = *reinterpret_cast<const uint32_t*>(L + g * LROW + k0 + 2 * t);
-    af[1] = *reinterpret_cast<const uint32_t*>(L + (g + 8) * LROW + k0 + 2 * t);
-    af[2] = *reinterpret_cast<const uint32_t*>(L + g * LROW + k0 + 8 + 2 * t);
-    af[3] = *reinterpret_cast<const uint32_t*>(L + (g + 8) * LROW + k0 + 8 + 2 * t);
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-        const int n0 = 8 * nt;
-        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(R + (n0 + g) * LROW + k0 + 2 * t);
-        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(R + (n0 + g) * LROW + k0 + 8 + 2 * t);
-        tc::mma16816(acc[nt], af, b0, b1);
+    hi = pack_f2(x);
+    lo = pack_f2(__fadd2_rn(x, make_float2(-__uint_as_float(hi << 16), -__uint_as_float(hi & 0xffff0000u))));
+}
+
+// mma.sync operands of row-major [16][LROW] bf16 tiles by ldmatrix (rows 272 bytes apart, so the
+// eight rows of each 8 x 8 matrix fall on distinct banks)
+__device__ __forceinline__ void ldsm4(const void* p, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(tc::smem_u32(p)));
+}
+// A fragment: rows 0..15 of L, columns k0 .. k0 + 15
+__device__ __forceinline__ void frag_a(const __nv_bfloat16* L, int k0, int lane, uint32_t (&a)[4])
+{
+    ldsm4(L + ((lane & 7) + 8 * ((lane >> 3) & 1)) * LROW + k0 + 8 * (lane >> 4), a);
+}
+// B fragments of the two n-tiles (rows 0..7 and 8..15 of R: b[0..1] and b[2..3]), columns k0 .. k0 + 15
+__device__ __forceinline__ void frag_b(const __nv_bfloat16* R, int k0, int lane, uint32_t (&b)[4])
+{
+    ldsm4(R + ((lane & 7) + 8 * (lane >> 4)) * LROW + k0 + 8 * ((lane >> 3) & 1), b);
+}
+// acc += A B^T over one k-step for both n-tiles
+__device__ __forceinline__ void mma2(float (&acc)[2][4], const uint32_t (&a)[4], const uint32_t (&b)[4])
+{
+    tc::mma16816(acc[0], a, b[0], b[1]);
+    tc::mma16816(acc[1], a, b[2], b[3]);
+}
+// acc += (Lh + Ll)(Rh + Rl)^T without the lo*lo term, over k-steps [k0, k1)
+__device__ __forceinline__ void mma_hilo(float (&acc)[2][4], const __nv_bfloat16* Lh, const __nv_bfloat16* Ll,
+                                         const __nv_bfloat16* Rh, const __nv_bfloat16* Rl, int k0, int k1, int lane)
+{
+    for (int k = k0; k < k1; k += 16) {
+        uint32_t ah[4], al[4], bh[4], bl[4];
+        frag_a(Lh, k, lane, ah);
+        frag_a(Ll, k, lane, al);
+        frag_b(Rh, k, lane, bh);
+        frag_b(Rl, k, lane, bl);
+        mma2(acc, ah, bh);
+        mma2(acc, ah, bl);
+        mma2(acc, al, bh);
     }
 }
 
@@ -184,41 +225,41 @@ __device__ __forceinline__ void prep_factors(unsigned char* sm, int p, int len, 
     const uint32_t* tz32 = reinterpret_cast<const uint32_t*>(sm + Map::OFF_STAGE + 3 * STAGE_TILE);
     float* hs = reinterpret_cast<float*>(sm + Map::OFF_HS);  // [4 quarters][128 channels]
 
-    float G0[4], G1[4];
-    float2 kv[4], qv[4];
+    // Both channels of the pair go through packed fp32 arithmetic.  Decays are kept in base 2:
+    // the gate g log2(e) = g_min log2(e) / (1 + 2^(-log2(e) e^{A_h} z)) (Equation 5), G its in-chunk
+    // cumulative sum, Gamma = 2^G and 1/Gamma = 2^-G.
+    const float2 zs = make_float2(-kLog2e * expA, -kLog2e * expA);
+    const float2 gm = make_float2(kLog2e * g_min, kLog2e * g_min);
+    const float2 one = make_float2(1.f, 1.f);
+    float2 G[4], kv[4], qv[4];
     uint32_t vv[4];
-    float a0 = 0.f, a1 = 0.f;
+    float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
         const int r = r0 + e;
         const bool ok = r < len;
         const uint32_t zw = tz32[(r * D + c0) >> 1];
-        const float2 z2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&zw));
-        a0 += ok ? log_decay_fast(z2.x, expA, g_min) : 0.f;
-        a1 += ok ? log_decay_fast(z2.y, expA, g_min) : 0.f;
-        G0[e] = a0;
-        G1[e] = a1;
-        const uint32_t kw = ok ? tk32[(r * D + c0) >> 1] : 0u;
-        const uint32_t qw = ok ? tq32[(r * D + c0) >> 1] : 0u;
-        kv[e] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kw));
-        qv[e] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qw));
+        const float2 y = __fmul2_rn(zs, bf2_to_f2(zw));
+        const float2 den = __fadd2_rn(one, make_float2(ex2_fast(y.x), ex2_fast(y.y)));
+        const float2 g = __fmul2_rn(gm, make_float2(rcp_fast(den.x), rcp_fast(den.y)));
+        acc = ok ? __fadd2_rn(acc, g) : acc;
+        G[e] = acc;
+        kv[e] = bf2_to_f2(ok ? tk32[(r * D + c0) >> 1] : 0u);
+        qv[e] = bf2_to_f2(ok ? tq32[(r * D + c0) >> 1] : 0u);
         vv[e] = (ok && !zero_v) ? tv32[(r * D + c0) >> 1] : 0u;
     }
-    *reinterpret_cast<float2*>(hs + tq * D + c0) = make_float2(a0, a1);
+    *reinterpret_cast<float2*>(hs + tq * D + c0) = acc;
     named_sync(Map::NB, NGROUP);
-    float off0 = 0.f, off1 = 0.f, tot0 = 0.f, tot1 = 0.f;
+    float2 off = make_float2(0.f, 0.f), tot = make_float2(0.f, 0.f);
 #pragma unroll
     for (int qq = 0; qq < 4; ++qq) {
         const float2 hq = *reinterpret_cast<const float2*>(hs + qq * D + c0);
-        if (qq < tq) {
-            off0 += hq.x;
-            off1 += hq.y;
-        }
-        tot0 += hq.x;
-        tot1 += hq.y;
+        if (qq < tq) off = __fadd2_rn(off, hq);
+        tot = __fadd2_rn(tot, hq);
     }
-    const float eGC0 = __expf(tot0), eGC1 = __expf(tot1);
-    if (tq == 3) *reinterpret_cast<float2*>(gc + c0) = make_float2(eGC0, eGC1);
+    const float2 eGC = make_float2(ex2_fast(tot.x), ex2_fast(tot.y));
+    if (tq == 3) *reinterpret_cast<float2*>(gc + c0) = eGC;
+    const float2 wsc = wq_scale ? *reinterpret_cast<const float2*>(wq_scale + c0) : one;
 
     uint32_t* sLl = reinterpret_cast<uint32_t*>(sm + Map::OFF_LL);
     uint32_t* sQl = reinterpret_cast<uint32_t*>(sm + Map::OFF_QL);
@@ -227,35 +268,35 @@ __device__ __forceinline__ void prep_factors(unsigned char* sm, int p, int len, 
     uint32_t* sKdl = sKd + C * LROW / 2;
     // transposed tiles: 4 tokens of one channel = 8 bytes at none_off(c, 4 tq)
     uint32_t xt0[2], xt1[2], kh0[2], kh1[2], kl0[2], kl1[2];
-    const float2 wsc = wq_scale ? *reinterpret_cast<const float2*>(wq_scale + c0) : make_float2(1.f, 1.f);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
         const int r = r0 + e;
-        const float eG0 = __expf(G0[e] + off0), eG1 = __expf(G1[e] + off1);  // Gamma in [e^-80, 1]
-        const float iG0 = __fdividef(1.f, eG0), iG1 = __fdividef(1.f, eG1);  // 1/Gamma in [1, e^80]
-        const float ll0 = kv[e].x * eG0, ll1 = kv[e].y * eG1;
-        const uint32_t llw = pack_f2(ll0, ll1);
+        const float2 Gs = __fadd2_rn(G[e], off);
+        const float2 eG = make_float2(ex2_fast(Gs.x), ex2_fast(Gs.y));     // Gamma in [e^-80, 1]
+        const float2 iG = make_float2(ex2_fast(-Gs.x), ex2_fast(-Gs.y));   // 1/Gamma in [1, e^80]
+        const uint32_t llw = pack_f2(__fmul2_rn(kv[e], eG));
         const int ri = (r * LROW + c0) >> 1;
         sLl[ri] = llw;
+        const float2 qg = __fmul2_rn(qv[e], eG);
         uint32_t hi, lo;
-        split2(qv[e].x * eG0, qv[e].y * eG1, hi, lo);
+        split2v(qg, hi, lo);
         sQl[ri] = hi;
         sQll[ri] = lo;
         if (wq) {
-            const uint32_t wv = wq_scale ? pack_f2(qv[e].x * eG0 * wsc.x, qv[e].y * eG1 * wsc.y) : hi;
+            const uint32_t wv = wq_scale ? pack_f2(__fmul2_rn(qg, wsc)) : hi;
             *reinterpret_cast<uint32_t*>(wq + tc::sw128_off(wq_row0 + r, c0, wq_rows)) = wv;
         }
-        split2(kv[e].x * iG0, kv[e].y * iG1, hi, lo);
+        split2v(__fmul2_rn(kv[e], iG), hi, lo);
         sKd[ri] = hi;
         sKdl[ri] = lo;
         uint32_t th, tl;
-        split2(kv[e].x * (eGC0 * iG0), kv[e].y * (eGC1 * iG1), th, tl);  // k Gamma_C / Gamma <= 1
+        split2v(__fmul2_rn(kv[e], __fmul2_rn(eGC, iG)), th, tl);  // k Gamma_C / Gamma <= 1
         if (kr) {
             reinterpret_cast<uint32_t*>(kr)[ri] = th;
             reinterpret_cast<uint32_t*>(kr)[C * LROW / 2 + ri] = tl;
         }
         // de-interleave the pairs into per-channel token runs
-        const int slot = e >> 1, sh = (e & 1) * 16;
+        const int slot = e >> 1;
         if ((e & 1) == 0) {
             xt0[slot] = llw & 0xffffu;
             xt1[slot] = llw >> 16;
@@ -264,16 +305,16 @@ __device__ __forceinline__ void prep_factors(unsigned char* sm, int p, int len, 
             kl0[slot] = tl & 0xffffu;
             kl1[slot] = tl >> 16;
         } else {
-            xt0[slot] |= (llw & 0xffffu) << sh;
-            xt1[slot] |= (llw >> 16) << sh;
-            kh0[slot] |= (th & 0xffffu) << sh;
-            kh1[slot] |= (th >> 16) << sh;
-            kl0[slot] |= (tl & 0xffffu) << sh;
-            kl1[slot] |= (tl >> 16) << sh;
+            xt0[slot] = __byte_perm(xt0[slot], llw, 0x5410);
+            xt1[slot] = __byte_perm(xt1[slot], llw, 0x7610);
+            kh0[slot] = __byte_perm(kh0[slot], th, 0x5410);
+            kh1[slot] = __byte_perm(kh1[slot], th, 0x7610);
+            kl0[slot] = __byte_perm(kl0[slot], tl, 0x5410);
+            kl1[slot] = __byte_perm(kl1[slot], tl, 0x7610);
         }
     }
-    const uint32_t v00 = (vv[0] & 0xffffu) | (vv[1] << 16), v01 = (vv[2] & 0xffffu) | (vv[3] << 16);
-    const uint32_t v10 = (vv[0] >> 16) | (vv[1] & 0xffff0000u), v11 = (vv[2] >> 16) | (vv[3] & 0xffff0000u);
+    const uint32_t v00 = __byte_perm(vv[0], vv[1], 0x5410), v01 = __byte_perm(vv[2], vv[3], 0x5410);
+    const uint32_t v10 = __byte_perm(vv[0], vv[1], 0x7632), v11 = __byte_perm(vv[2], vv[3], 0x7632);
     const uint32_t p0 = none_off_rg<Map::XT_RG>(c0, r0), p1 = none_off_rg<Map::XT_RG>(c0 + 1, r0);
     *reinterpret_cast<uint2*>(sm + Map::OFF_XT + p0) = make_uint2(xt0[0], xt0[1]);
     *reinterpret_cast<uint2*>(sm + Map::OFF_XT + p1) = make_uint2(xt1[0], xt1[1]);
@@ -288,12 +329,17 @@ __device__ __forceinline__ void prep_factors(unsigned char* sm, int p, int len, 
     }
 }
 
+
 // Variants of the per-chunk solve (template argument of prep_solve).
 enum SolveVariant : int {
     SOLVE_ONE = 0,    // a chunk on its own
     SOLVE_FIRST = 1,  // chunk a of a pair: also zeroes the upper-right block of the pair's P
     SOLVE_SECOND = 2  // chunk b of a pair: also the cross products with chunk a's K~ (below)
 };
+
+// Index of element (r, c) of a 16 x 16 fp32 partial tile: rows with bit 1 set hold their two
+// column halves swapped.
+__device__ __forceinline__ int part_idx(int r, int c) { return r * C + (c ^ (((r >> 1) & 1) << 3)); }
 
 // A and P over K = 128 with mma.sync, partial sums reduced in shared memory (OFF_PART, 8 KB);
 // then T = (I + A)^-1 by forward substitution and T' = T diag(beta) (hi/lo, OFF_T), P finalised
@@ -302,7 +348,8 @@ enum SolveVariant : int {
 // SOLVE_SECOND: chunk a's K~ = K Gamma_C / Gamma (row-major hi/lo at Map::OFF_KRA) also enters
 //   Y = (K Gamma) K~_a^T  (so that X = W K~_a^T = T' Y)   -> bf16 hi/lo B operand at Map::OFF_YT
 //   Z = (Q Gamma) K~_a^T  (the pair's lower-left output block) -> `pb` rows 16..31, tokens 0..15
-// with warp 0: A, warps 1, 2: Y (K~ hi, lo), warps 3..5: P, warps 6, 7: Z (k-steps 0..3, 4..7).
+// with warp 0: A, warps 1, 2: Y (k-steps 0..3, 4..7), warps 3..5: P (k-steps 0..2, 3..5, 6..7),
+// warps 6, 7: Z (k-steps 0..3, 4..7).
 // Two barriers (Map::NB) inside.
 template <class Map, int VAR = SOLVE_ONE>
 __device__ __forceinline__ void prep_solve(unsigned char* sm, int p, unsigned char* pb, uint32_t p_lo = SMALL_TILE,
@@ -323,52 +370,57 @@ __device__ __forceinline__ void prep_solve(unsigned char* sm, int p, unsigned ch
         if constexpr (VAR != SOLVE_SECOND) {
             const int k0 = 32 * (pw & 3);
             if (pw < 4) {
-                mma_kstep(acc, sLl, sKd, k0, lane);
-                mma_kstep(acc, sLl, sKd, k0 + 16, lane);
-            } else {
 #pragma unroll
-                for (int kk = 0; kk < 32; kk += 16) {
-                    mma_kstep(acc, sQl, sKd, k0 + kk, lane);
-                    mma_kstep(acc, sQl, sKdl, k0 + kk, lane);
-                    mma_kstep(acc, sQll, sKd, k0 + kk, lane);
+                for (int k = k0; k < k0 + 32; k += 16) {
+                    uint32_t a[4], b[4];
+                    frag_a(sLl, k, lane, a);
+                    frag_b(sKd, k, lane, b);
+                    mma2(acc, a, b);
                 }
+            } else {
+                mma_hilo(acc, sQl, sQll, sKd, sKdl, k0, k0 + 32, lane);
             }
         } else {
             const __nv_bfloat16* sKa = reinterpret_cast<const __nv_bfloat16*>(sm + Map::OFF_KRA);
             const __nv_bfloat16* sKal = sKa + C * LROW;
-            // one product over all eight k-steps per warp (two half-ranges of three for Z)
-            const __nv_bfloat16* L = (pw < 3) ? sLl : (pw == 4 ? sQl : (pw == 5 ? sQll : sQl));
-            const __nv_bfloat16* R = (pw == 0)   ? sKd
-                                     : (pw == 1) ? sKa
-                                     : (pw == 2) ? sKal
-                                     : (pw == 3) ? sKd
-                                     : (pw == 4) ? sKdl
-                                     : (pw == 5) ? sKd
-                                                 : sKa;
-            if (pw < 6) {
+            if (pw == 0) {  // A over all k-steps
 #pragma unroll 4
-                for (int k0 = 0; k0 < D; k0 += 16) mma_kstep(acc, L, R, k0, lane);
-            } else {
-                const int kb = 64 * (pw - 6);
-#pragma unroll 2
-                for (int k0 = kb; k0 < kb + 64; k0 += 16) {
-                    mma_kstep(acc, sQl, sKa, k0, lane);
-                    mma_kstep(acc, sQl, sKal, k0, lane);
-                    mma_kstep(acc, sQll, sKa, k0, lane);
+                for (int k = 0; k < D; k += 16) {
+                    uint32_t a[4], b[4];
+                    frag_a(sLl, k, lane, a);
+                    frag_b(sKd, k, lane, b);
+                    mma2(acc, a, b);
                 }
+            } else if (pw < 3) {  // Y = (K Gamma) (K~hi + K~lo)^T over one half of the k-steps
+#pragma unroll 2
+                for (int k = 64 * (pw - 1); k < 64 * pw; k += 16) {
+                    uint32_t a[4], bh[4], bl[4];
+                    frag_a(sLl, k, lane, a);
+                    frag_b(sKa, k, lane, bh);
+                    frag_b(sKal, k, lane, bl);
+                    mma2(acc, a, bh);
+                    mma2(acc, a, bl);
+                }
+            } else if (pw < 6) {  // P over k-steps [0, 3), [3, 6), [6, 8)
+                const int kb = 48 * (pw - 3);
+                mma_hilo(acc, sQl, sQll, sKd, sKdl, kb, min(kb + 48, D), lane);
+            } else {  // Z over one half of the k-steps
+                mma_hilo(acc, sQl, sQll, sKa, sKal, 64 * (pw - 6), 64 * (pw - 5), lane);
             }
         }
+        // partial tiles [16][16] with the column halves of rows 2, 3 (mod 4) swapped, so that each
+        // half-warp's 8-byte stores cover all 32 banks (part_idx)
         float* pp = part + pw * C * C;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            *reinterpret_cast<float2*>(pp + g * C + 8 * nt + 2 * t) = make_float2(acc[nt][0], acc[nt][1]);
-            *reinterpret_cast<float2*>(pp + (g + 8) * C + 8 * nt + 2 * t) = make_float2(acc[nt][2], acc[nt][3]);
+            *reinterpret_cast<float2*>(pp + part_idx(g, 8 * nt + 2 * t)) = make_float2(acc[nt][0], acc[nt][1]);
+            *reinterpret_cast<float2*>(pp + part_idx(g + 8, 8 * nt + 2 * t)) = make_float2(acc[nt][2], acc[nt][3]);
         }
     }
     named_sync(Map::NB, NGROUP);
     {
-        const int idx = p;  // one entry of each 16 x 16 result per thread
-        const int r = idx >> 4, i = idx & 15;
+        const int r = p >> 4, i = p & 15;  // one entry of each 16 x 16 result per thread
+        const int idx = part_idx(r, i);
         float sa, sp;
         if constexpr (VAR != SOLVE_SECOND) {
             sa = 0.f;
@@ -393,7 +445,7 @@ __device__ __forceinline__ void prep_solve(unsigned char* sm, int p, unsigned ch
             st_bf16(pb, zp.off(r, i), hi);
             st_bf16(pb, p_lo + zp.off(r, i), lo);
         }
-        sA[idx] = (i < r) ? beta[r] * sa : 0.f;
+        sA[p] = (i < r) ? beta[r] * sa : 0.f;
         __nv_bfloat16 hi, lo;
         split_bf16((i <= r) ? sp : 0.f, hi, lo);
         st_bf16(pb, p_place.off(r, i), hi);
