@@ -121,25 +121,26 @@ void segment_plan(const kda_problem_t& p, size_t budget_bytes, bool split, int32
         return;
     }
     // cost in units of one state step of a chain running alone on an SM (a chunk, or a pair of
-    // chunks in the split plan): pass 3 runs nseg segments per (seq, head) in waves of one chain per
-    // SM; pass 1 two summaries (S~ and M) of every segment but the last -- in the split plan two
-    // chains per SM, each about 1.3 times slower, in the fused plan one; one step of the scan costs
-    // about scan_step state steps
+    // chunks in the split plan).  A pass of c chains takes ceil(c / slots) waves, where the split
+    // plan's state pass fits two chains per SM at about 1.1 times the time per step (the fused
+    // kernel: one chain per SM); pass 3 runs one chain per segment, pass 1 two (S~ and M) per
+    // segment but the last; one step of the scan costs about scan_step state steps
     const int64_t steps = (chunks + gran - 1) / gran;
     const double sms = (double)sm_count_of_current_device();
-    const double sum_slots = sms * (split ? 2.0 : 1.0);
-    const double sum_cost = split ? 1.3 : 1.0;
     const double scan_step = split ? 0.6 : 0.8;
     const double units = (double)p.num_seqs * p.num_heads;
     const double per_seg = units * p.d_k * p.d_v * 4.0 * 3.0;  // S_in, S~ and M of one segment
-    double best = (double)steps * std::ceil(units / sms);
+    auto waves = [&](double ctas) -> double {
+        if (ctas <= sms) return 1.0;
+        return split ? 1.1 * std::ceil(ctas / (2.0 * sms)) : std::ceil(ctas / sms);
+    };
+    double best = (double)steps * waves(units);
     for (int64_t nseg = 2; nseg <= 64 && nseg <= steps; ++nseg) {
         const int64_t sc = (steps + nseg - 1) / nseg;  // steps per segment
         const int64_t ns = (steps + sc - 1) / sc;
         if (ns < 2) continue;
         if (per_seg * (double)ns > (double)budget_bytes || per_seg * (double)ns > 2.0e9) continue;
-        const double cost = (double)sc * (std::ceil(units * ns / sms) +
-                                          sum_cost * std::ceil(2.0 * units * (ns - 1) / sum_slots)) +
+        const double cost = (double)sc * (waves(units * ns) + waves(2.0 * units * (ns - 1))) +
                             scan_step * (double)(ns - 1);
         if (cost < 0.9 * best) {
             best = cost;

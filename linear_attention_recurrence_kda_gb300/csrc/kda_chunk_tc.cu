@@ -290,7 +290,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_chunk_fwd_tc_kernel(PrefillAr
         const int64_t sbase = ((int64_t)n * H + h) * D * D;
         const int64_t segbase = (((int64_t)n * H + h) * a.max_seg + k) * D * D;
         const float* init = nullptr;
-        if (mode == 0) init = (k == 0) ? (a.s0 ? a.s0 + sbase : nullptr) : a.seg_in + segbase;
+        // with several segments every segment, the first included, starts from the scan's copy: the
+        // final state may overwrite the caller's initial state (in-place carry) while the first
+        // segment's CTA has not read it yet
+        if (mode == 0) init = (nseg == 1) ? (a.s0 ? a.s0 + sbase : nullptr) : a.seg_in + segbase;
 #pragma unroll
         for (int cc = 0; cc < 64; ++cc) {
             const int c = 64 * h2 + cc;

@@ -5,7 +5,8 @@
 // the KDA context-parallel decomposition of the "Kimi K3" reading notes, section 7:
 // S_t = S~_t + M_{t<-1} S_in).  With (M_k, S~_k) of every segment computed in parallel, the state
 // entering segment k+1 is
-//     S_in[k+1] = M_k S_in[k] + S~_k,     S_in[0] = the sequence's initial state (or zero).
+//     S_in[k+1] = M_k S_in[k] + S~_k,     S_in[0] = the sequence's initial state (or zero),
+// S_in[0] included in what it writes.
 // This kernel walks that short chain.  Value columns are independent (column j of S only meets
 // column j), so the grid splits them: one CTA per (sequence, head, block of 16 columns).
 //
@@ -87,6 +88,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_segment_scan_kernel(PrefillAr
         tc::mbar_init(&bar[1], 1);
         *abort_flag = 0u;
     }
+    // the caller's initial state is an input of the call (no kernel of this call writes it before
+    // the output pass): stage it while the summaries finish, and copy it to the first segment's
+    // incoming state, which the output pass reads instead of the caller's buffer (that buffer may
+    // receive the final state while the first segment is still starting)
+    for (int e = tid; e < D * COLS; e += NTHREADS) {
+        const int c = e / COLS, jj = e % COLS;
+        const float x = a.s0 ? a.s0[sbase + (int64_t)c * D + j0 + jj] : 0.f;
+        put_s(smem_raw + OFF_S, c, jj, x);
+        a.seg_in[seg0 + (int64_t)c * D + j0 + jj] = x;
+    }
     tc::fence_async_smem();
     __syncthreads();
     griddep_wait();  // the segment summaries come from the previous kernel
@@ -99,10 +110,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_segment_scan_kernel(PrefillAr
         pend |= 1u << b;
     };
     if (tid == 0) issue(0);
-    for (int e = tid; e < D * COLS; e += NTHREADS) {
-        const int c = e / COLS, jj = e % COLS;
-        put_s(smem_raw + OFF_S, c, jj, a.s0 ? a.s0[sbase + (int64_t)c * D + j0 + jj] : 0.f);
-    }
 
     // this thread's accumulator positions: rows c0, c0 + 8; columns jj, jj + 1 of n-tiles 0 and 1
     const int c0 = 16 * w + g;

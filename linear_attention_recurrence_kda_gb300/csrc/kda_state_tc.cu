@@ -252,7 +252,10 @@ __device__ __forceinline__ void state_pass(const PrefillArgs& a)
             const int64_t sbase = ((int64_t)n * H + h) * D * D;
             const int64_t segbase = (((int64_t)n * H + h) * a.max_seg + k) * D * D;
             const float* init = nullptr;
-            if (mode == 0) init = (k == 0) ? (a.s0 ? a.s0 + sbase : nullptr) : a.seg_in + segbase;
+            // with several segments every segment, the first included, starts from the scan's copy: the
+            // final state may overwrite the caller's initial state (in-place carry) while the first
+            // segment's CTA has not read it yet
+            if (mode == 0) init = (nseg == 1) ? (a.s0 ? a.s0 + sbase : nullptr) : a.seg_in + segbase;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 uint32_t v[16];
