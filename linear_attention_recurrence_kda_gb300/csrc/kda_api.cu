@@ -121,28 +121,37 @@ void segment_plan(const kda_problem_t& p, size_t budget_bytes, bool split, int32
         return;
     }
     // cost in units of one state step of a chain running alone on an SM (a chunk, or a pair of
-    // chunks in the split plan).  A pass of c chains takes ceil(c / slots) waves, where the split
+    // chunks in the split plan).  A pass of c chains of sc steps takes sc steps per wave plus a
+    // start-up of about OVH steps per wave (launch, first operand block, initial state); the split
     // plan's state pass fits two chains per SM at about 1.1 times the time per step (the fused
-    // kernel: one chain per SM); pass 3 runs one chain per segment, pass 1 two (S~ and M) per
-    // segment but the last; one step of the scan costs about scan_step state steps
+    // kernel: one chain per SM).  Pass 3 runs one chain per segment, pass 1 two (S~ and M) per
+    // segment but the last; one step of the scan costs about scan_step state steps.
     const int64_t steps = (chunks + gran - 1) / gran;
     const double sms = (double)sm_count_of_current_device();
     const double scan_step = split ? 0.6 : 0.8;
+    constexpr double OVH = 4.0;
     const double units = (double)p.num_seqs * p.num_heads;
     const double per_seg = units * p.d_k * p.d_v * 4.0 * 3.0;  // S_in, S~ and M of one segment
-    auto waves = [&](double ctas) -> double {
-        if (ctas <= sms) return 1.0;
-        return split ? 1.1 * std::ceil(ctas / (2.0 * sms)) : std::ceil(ctas / sms);
+    auto pass = [&](double ctas, double sc) -> double {
+        if (ctas <= sms) return sc + OVH;
+        const double nw = split ? std::ceil(ctas / (2.0 * sms)) : std::ceil(ctas / sms);
+        return nw * ((split ? 1.1 : 1.0) * sc + OVH);
     };
-    double best = (double)steps * waves(units);
-    for (int64_t nseg = 2; nseg <= 64 && nseg <= steps; ++nseg) {
-        const int64_t sc = (steps + nseg - 1) / nseg;  // steps per segment
+    const double unsegmented = pass(units, (double)steps);
+    double best = unsegmented;
+    for (int64_t sc = 1; sc < steps; ++sc) {  // steps per segment
         const int64_t ns = (steps + sc - 1) / sc;
-        if (ns < 2) continue;
+        if (ns < 2 || ns > 64) continue;
         if (per_seg * (double)ns > (double)budget_bytes || per_seg * (double)ns > 2.0e9) continue;
-        const double cost = (double)sc * (waves(units * ns) + waves(2.0 * units * (ns - 1))) +
-                            scan_step * (double)(ns - 1);
-        if (cost < 0.9 * best) {
+        // pass 3: when only the last segment's chains overflow the SMs, they share SMs with full
+        // chains, which run about 20 % slower while both run (the last segment's steps)
+        const int64_t last = steps - (ns - 1) * sc;
+        const double ctas3 = units * ns;
+        const double pass3 = (split && ctas3 > sms && units * (ns - 1) <= sms && ctas3 <= 2.0 * sms)
+                                 ? (double)sc + 0.2 * (double)last + OVH
+                                 : pass(ctas3, (double)sc);
+        const double cost = pass3 + pass(2.0 * units * (ns - 1), (double)sc) + scan_step * (double)(ns - 1);
+        if (cost < best && cost < 0.9 * unsegmented) {
             best = cost;
             seg_chunks = (int32_t)(sc * gran);
             max_seg = (int32_t)ns;

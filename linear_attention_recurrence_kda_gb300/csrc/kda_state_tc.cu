@@ -293,8 +293,15 @@ __device__ __forceinline__ void state_pass(const PrefillArgs& a)
 
         for (int s = 0; s < nsteps; ++s) {
             const unsigned char* blk = slot_ptr(s);
+            // this block's U~ (in the ring since D1 was issued) into registers while D1 runs
+            if (!wait_warp(&bar_f[s % NSLOT], fill_parity(s))) break;
+            float uv[16];
+            {
+                const float* ut = reinterpret_cast<const float*>(blk + tcc::BLK_UT);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) uv[e] = (mode == 2) ? 0.f : ut[(16 * h2 + e) * D + jrow];
+            }
             if (!wait_warp(bar_d1, (uint32_t)(s & 1))) break;
-            if (!wait_warp(&bar_f[s % NSLOT], fill_parity(s))) break;  // this block's U~ is visible
             tc::fence_after_sync();
 
             // U^T = U~^T - (W S)^T as a hi/lo pair into tensor memory; warp half h2 takes tokens
@@ -302,10 +309,6 @@ __device__ __forceinline__ void state_pass(const PrefillArgs& a)
             {
                 uint32_t dv[16];
                 KDA_TMEM_LD16(lane_base + TM_WU + 16 * h2, dv);
-                float uv[16];
-                const float* ut = reinterpret_cast<const float*>(blk + tcc::BLK_UT);
-#pragma unroll
-                for (int e = 0; e < 16; ++e) uv[e] = (mode == 2) ? 0.f : ut[(16 * h2 + e) * D + jrow];
                 tc::tmem_wait_ld();
                 uint32_t hi[8], lo[8];
 #pragma unroll
@@ -325,14 +328,17 @@ __device__ __forceinline__ void state_pass(const PrefillArgs& a)
             // the new state's bf16 copy for the next D1 first (32 values at a time), then -- while that D1
             // runs -- the state multiplied by the next step's Gamma_C (the decay its update applies),
             // read again 16 columns at a time; outputs to registers
+            {
+                constexpr int NR = SHARED ? 2 : 4;  // 16-column groups per tensor-memory round trip
 #pragma unroll
-            for (int hq = 0; hq < 2; ++hq) {
-                uint32_t v0[16], v1[16];
-                KDA_TMEM_LD16(my_s + 32 * hq, v0);
-                KDA_TMEM_LD16(my_s + 32 * hq + 16, v1);
-                tc::tmem_wait_ld();
-                stage16(2 * hq, v0);
-                stage16(2 * hq + 1, v1);
+                for (int hq = 0; hq < 4 / NR; ++hq) {
+                    uint32_t v[NR][16];
+#pragma unroll
+                    for (int qq = 0; qq < NR; ++qq) KDA_TMEM_LD16(my_s + 16 * (NR * hq + qq), v[qq]);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int qq = 0; qq < NR; ++qq) stage16(NR * hq + qq, v[qq]);
+                }
             }
             if (mode == 0) {
                 uint32_t ob[16];
