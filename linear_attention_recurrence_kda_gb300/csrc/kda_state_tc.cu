@@ -281,12 +281,14 @@ __device__ __forceinline__ void state_pass(const PrefillArgs& a)
         int64_t o_t0 = 0;
         int o_len = 0;
         bool o_have = false;
+        const int64_t o_stride = (int64_t)H * D;  // between consecutive tokens of one head
         auto store_outputs = [&]() {
+            __nv_bfloat16* base = op + ((o_t0 + 16 * h2) * H + h) * D + jrow;
+            const int n_valid = o_len - 16 * h2;
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-                const int r = 16 * h2 + e;
                 const unsigned short bits = (unsigned short)((e & 1) ? (ovp[e >> 1] >> 16) : (ovp[e >> 1] & 0xffffu));
-                if (r < o_len) op[((o_t0 + r) * H + h) * D + jrow] = __ushort_as_bfloat16(bits);
+                if (e < n_valid) base[e * o_stride] = __ushort_as_bfloat16(bits);
             }
             o_have = false;
         };

@@ -293,7 +293,7 @@ def test_pageable_host_pointer():
 @pytest.mark.parametrize("lengths", [[250], [100, 3, 77, 0, 160], [33]])
 @pytest.mark.parametrize("plan", ["split", "fused"])
 def test_segmented_prefill(monkeypatch, seg, lengths, plan):
-    """Sequences cut into segments of `seg` chunks: segment summaries (S~, M), the fp32 scan of
+    """Sequences cut into segments of `seg` chunks: segment summaries (S~, M), the scan of
     incoming states and the re-run from them must reproduce the unsegmented result, on both
     tensor-core plans (parallel chunk preparation + state pass, and the fused kernel)."""
     monkeypatch.setenv("KDA_SEGMENT_CHUNKS", str(seg))
@@ -303,6 +303,26 @@ def test_segmented_prefill(monkeypatch, seg, lengths, plan):
     ref_o, ref_s = oracle_forward(inp)
     check(out, ref_o, torch.bfloat16, "out")
     check(sf, ref_s, torch.bfloat16, "final_state")
+
+
+@pytest.mark.parametrize("plan", ["split", "fused"])
+def test_segmented_in_place_carry(monkeypatch, plan):
+    """Final state written over the initial state with many segments: every segment must start
+    from the state the call was given, although the last segment's CTAs write the final state
+    into the same buffer (the first segment reads the scan's copy)."""
+    monkeypatch.setenv("KDA_SEGMENT_CHUNKS", "2")
+    monkeypatch.setenv("KDA_TC_PLAN", plan)
+    inp = I.make_inputs(1, lengths=[250, 96, 33], num_heads=3, d=128, seed=77)
+    d = to_dev(inp)
+    ref_o, ref_s = oracle_forward(inp)
+    for _ in range(3):
+        st = d["S0"].clone()
+        out, sf = B.kda_forward(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], initial_state=st,
+                                cu_seqlens=d["cu_seqlens"], final_state=st)
+        torch.cuda.synchronize()
+        assert sf.data_ptr() == st.data_ptr()
+        check(out, ref_o, torch.bfloat16, "out")
+        check(st, ref_s, torch.bfloat16, "in-place state")
 
 
 def test_segmented_prefill_identity_transition(monkeypatch):
