@@ -210,6 +210,7 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-shapes", action="store_true", help="skip the varlen and long-context prefill shapes")
     args = ap.parse_args()
     if args.impl == "reference":
         return reference_arm(args)
@@ -289,6 +290,20 @@ def main():
     barrier()
     step_ms = [a.elapsed_time(b) for a, b in evs]
     ms = max_over_ranks(sum(step_ms) / len(step_ms))
+    srt = sorted(step_ms)
+    step_stats = {"median_ms": max_over_ranks(srt[len(srt) // 2]),
+                  "p90_ms": max_over_ranks(srt[min(len(srt) - 1, int(0.9 * len(srt)))])}
+    # the same steps with the inputs left in L2 (no flush between steps)
+    barrier()
+    torch.cuda.synchronize()
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0.record(stream)
+    for _ in range(args.steps):
+        fwd()
+    w1.record(stream)
+    torch.cuda.synchronize()
+    warm_ms = max_over_ranks(w0.elapsed_time(w1) / args.steps)
+    step_stats.update({"warm_l2_ms_per_step": warm_ms, "warm_l2_value": T * world / (warm_ms * 1e-3) / 1e6})
     tokens = T * world
     value = tokens / (ms * 1e-3) / 1e6
 
@@ -344,6 +359,16 @@ def main():
                 "path_achieved_gbs": (th * prefill_bytes_per_token_head(dk, dv, io_bytes) + 2 * state_bytes)
                 / (ms * 1e-3) / 1e9, "kernels": kernels}
     roofline["path_frac"] = roofline["path_achieved_gbs"] / pk["hbm_gbs"]
+    # the path's own roofline: min(tensor peak, arithmetic intensity x HBM); at d = 128 and 16-token
+    # chunks the intensity is below the ridge point, so the bound is HBM
+    ai = prefill_flops_per_token_head(dk, dv) / prefill_bytes_per_token_head(dk, dv, io_bytes)
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    path_bytes = th * prefill_bytes_per_token_head(dk, dv, io_bytes) + 2 * state_bytes
+    roofline["path_roofline"] = {"bound": "hbm" if ai < ridge else "tensor", "flop_per_byte": ai,
+                                 "ridge_flop_per_byte": ridge,
+                                 "floor_ms": path_bytes / (pk["hbm_gbs"] * 1e9) * 1e3 if ai < ridge
+                                 else th * prefill_flops_per_token_head(dk, dv) / (pk["bf16_tflops"] * 1e12) * 1e3,
+                                 "frac": roofline["path_frac"]}
     flops = th * prefill_flops_per_token_head(dk, dv)
     tensor = {"achieved_tflops": flops / (ms * 1e-3) / 1e12,
               "frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"],
@@ -357,6 +382,9 @@ def main():
     # ---- e2e through the public call with pinned host buffers
     e2e = bench_e2e(args, B, inp, dev, stream, max_over_ranks, barrier, world)
 
+    # ---- the other prefill shapes of the pages' workloads (varlen batch, 1M-token context)
+    shapes = None if args.no_shapes else bench_shapes(B, I, dev, stream, max_over_ranks, barrier, world)
+
     clk = clocks.stop() if clocks else None
     line = {
         "metric": METRIC, "value": value, "unit": "Mtok/s", "n_gpus": world, "steps": args.steps,
@@ -367,14 +395,71 @@ def main():
                    "arithmetic": "bf16 tensor-core products (split hi/lo where precision needs it) with fp32 "
                                  "accumulation; fp32 state",
                    "l2": "flushed by a 512 MiB write before every timed step"},
-        "roofline": roofline, "tensor": tensor, "decode": decode, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": launches, "clocks": clk,
+        "step_stats": step_stats, "roofline": roofline, "tensor": tensor, "decode": decode,
+        "cpu_baseline": cpu, "e2e": e2e, "shapes": shapes, "gpu_launches": launches, "clocks": clk,
     }
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def bench_shapes(B, I, dev, stream, max_over_ranks, barrier, world, ids_reps=((2, 10), (3, 4))):
+    """Prefill throughput at the varlen (8 sequences x 32 heads) and long-context (1,048,576 tokens x
+    8 heads) shapes: inputs drawn on the device with the workloads' distributions (larger than L2,
+    so no flush), two warm-up calls, then `reps` calls timed one by one with CUDA events."""
+    import torch
+    res = []
+    for wid, reps in ids_reps:
+        w = I.WORKLOADS[wid]
+        if w.varlen_range is not None:
+            lo, hi = w.varlen_range
+            lengths = torch.randint(lo, hi + 1, (w.num_varlen,), generator=torch.Generator().manual_seed(w.seed)).tolist()
+        else:
+            lengths = list(w.lengths)
+        N, T, H, d = len(lengths), int(sum(lengths)), w.num_heads, w.d
+        gen = torch.Generator(device=dev).manual_seed(w.seed)
+
+        def tok(normalise):
+            x = torch.randn(T, H, d, generator=gen, device=dev)
+            if normalise:
+                x = x / torch.sqrt((x * x).sum(dim=-1, keepdim=True) + I.L2_EPS)
+            return x.to(torch.bfloat16)
+        q, k, v, z = tok(True), tok(True), tok(False), tok(False)
+        A = torch.randn(H, generator=gen, device=dev) * I.A_STD
+        beta = torch.sigmoid(torch.randn(T, H, generator=gen, device=dev))
+        S0 = torch.randn(N, H, d, d, generator=gen, device=dev) * I.S0_STD
+        cu = torch.zeros(N + 1, dtype=torch.int32)
+        cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
+        cu = cu.to(dev)
+        out = torch.empty(T, H, d, dtype=torch.bfloat16, device=dev)
+        fin = torch.empty(N, H, d, d, dtype=torch.float32, device=dev)
+        prob = B.make_problem(N, T, max(lengths), H, d, d, torch.bfloat16)
+        ws = torch.empty(B.kda_forward_workspace_bytes(prob), dtype=torch.uint8, device=dev)
+
+        def fwd():
+            B.kda_forward(q, k, v, z, A, beta, initial_state=S0, cu_seqlens=cu, out=out, final_state=fin,
+                          max_seqlen=max(lengths), workspace=ws)
+        for _ in range(2):
+            fwd()
+        torch.cuda.synchronize()
+        barrier()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for e0, e1 in evs:
+            e0.record(stream)
+            fwd()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms_list = sorted(e0.elapsed_time(e1) for e0, e1 in evs)
+        ms = max_over_ranks(sum(ms_list) / len(ms_list))
+        res.append({"workload": w.name, "sequences": N, "tokens": T, "token_heads": T * H, "reps": reps,
+                    "ms_per_step": ms, "median_ms": max_over_ranks(ms_list[len(ms_list) // 2]),
+                    "value": T * world / (ms * 1e-3) / 1e6, "unit": "Mtok/s",
+                    "plan": B.kda_forward_plan(prob, ws.numel()), "l2": "inputs larger than L2"})
+        del q, k, v, z, A, beta, S0, cu, out, fin, ws
+        torch.cuda.empty_cache()
+    return res
 
 
 def bench_decode(args, B, I, dev, stream, max_over_ranks, barrier, pk, pk_src):
