@@ -140,6 +140,7 @@ struct PrefillArgs {
     int32_t seg_chunks;       // chunks per segment
     int32_t max_seg;          // segments of the longest sequence
     int32_t seg_mode;         // 0: outputs; 1: end state from zero (S~); 2: transition (M)
+    int32_t prep_run;         // preparation kernel: 32-token steps per CTA (set by its launcher)
     float* seg_in;            // [N][H][max_seg][d][d] incoming state of every segment (scan output)
     float* seg_st;            // [N][H][max_seg][d][d] S~ of every segment
     float* seg_mt;            // [N][H][max_seg] M of every segment, seg_m_off format (64 KB each)

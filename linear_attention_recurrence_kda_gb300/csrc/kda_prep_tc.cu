@@ -13,8 +13,8 @@
 //   [P ; K~^T] = [[P_a, 0] ; [Z, P_b] ; (K~_a Gamma_Cb)^T, K~_b^T],   Gamma_C = Gamma_Ca Gamma_Cb
 // The sequential state pass (kda_state_tc.cu) then only streams these blocks.
 //
-// One CTA of 256 threads (three per SM) walks a run of up to kRunPairs pairs of one (sequence,
-// head): the q, k, v, z tiles arrive by TMA one chunk ahead; the factors, A, P, T and the cross
+// One CTA of 256 threads (three per SM) walks a run of 2 (small grids) or 8 (grids of many waves)
+// pairs of one (sequence, head): the q, k, v, z tiles arrive by TMA one chunk ahead; the factors, A, P, T and the cross
 // products Y, Z come from the shared preparation functions, W and U~ from warp-level mma.sync, and
 // every part is stored straight into the block in global memory.  Block slot of step s of sequence
 // n: cu[n] / 32 + n + s, so the slots of consecutive sequences never overlap
@@ -32,7 +32,8 @@ using tcc::D;
 using tcc::NGROUP;
 using tcc::PAIR;
 
-constexpr int kRunPairs = 2;                 // 32-token steps per CTA
+constexpr int kRunShort = 2;                 // 32-token steps per CTA: small grids (short tail)
+constexpr int kRunLong = 8;                  // ... grids of many waves (CTA start-up amortised)
 constexpr uint32_t WAIT_LIMIT = 1u << 17;    // tries of up to 20 us each
 
 // shared-memory map (bytes from a 1024-aligned base)
@@ -246,8 +247,9 @@ __global__ void __launch_bounds__(NGROUP, 3) kda_chunk_prep_tc_kernel(PrefillArg
     float* gca = reinterpret_cast<float*>(sm + OFF_GCA);
     float* gcb = reinterpret_cast<float*>(sm + OFF_GCB);
 
+    const int run_pairs = a.prep_run;
     const int64_t pairs_max = ((int64_t)a.chunks_per_seq + 1) / 2;
-    const int runs = (int)((pairs_max + kRunPairs - 1) / kRunPairs);
+    const int runs = (int)((pairs_max + run_pairs - 1) / run_pairs);
     const int n = (int)(blockIdx.x / (unsigned)runs);
     const int run = (int)(blockIdx.x % (unsigned)runs);
     const int h = blockIdx.y;
@@ -259,8 +261,8 @@ __global__ void __launch_bounds__(NGROUP, 3) kda_chunk_prep_tc_kernel(PrefillArg
     if (!seq_range(a, n, q0, q1)) return;
     const int64_t seq_chunks = (q1 - q0 + C - 1) / C;
     const int64_t seq_pairs = (seq_chunks + 1) / 2;
-    const int64_t pb = (int64_t)run * kRunPairs;
-    const int64_t pe = min(pb + kRunPairs, seq_pairs);
+    const int64_t pb = (int64_t)run * run_pairs;
+    const int64_t pe = min(pb + run_pairs, seq_pairs);
     if (pb >= pe) return;
     const int H = a.H;
     const int64_t slot0 = q0 / PAIR + n;  // block slot of the sequence's first step
@@ -365,11 +367,15 @@ cudaError_t launch_chunk_prep_tc(const PrefillArgs& a, cudaStream_t s)
     cudaError_t e = cudaFuncSetAttribute(kda_chunk_prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    // runs of kRunLong steps once the short-run grid would take more than ~8 waves of resident CTAs
     const int64_t pairs = ((int64_t)a.chunks_per_seq + 1) / 2;
-    const int64_t runs = (pairs + kRunPairs - 1) / kRunPairs;
+    const int64_t short_ctas = (pairs + kRunShort - 1) / kRunShort * a.N * a.H;
+    PrefillArgs b = a;
+    b.prep_run = short_ctas > 8LL * 3 * sm_count_of_current_device() ? kRunLong : kRunShort;
+    const int64_t runs = (pairs + b.prep_run - 1) / b.prep_run;
     const int64_t gx = runs * a.N;  // at most N x chunks_per_seq < 2^31 (checked by the caller)
     if (gx == 0) return cudaSuccess;
-    kda_chunk_prep_tc_kernel<<<dim3((unsigned)gx, (unsigned)a.H, 1), NGROUP, SMEM_BYTES, s>>>(a, maps);
+    kda_chunk_prep_tc_kernel<<<dim3((unsigned)gx, (unsigned)a.H, 1), NGROUP, SMEM_BYTES, s>>>(b, maps);
     return cudaGetLastError();
 }
 
