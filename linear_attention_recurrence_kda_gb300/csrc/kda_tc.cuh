@@ -149,11 +149,6 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Store 32-bit registers to this warp's 32 lanes of tensor memory, consecutive columns.
-#define KDA_TMEM_ST4(taddr, v)                                                                     \
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(v[0]), \
-                 "r"(v[1]), "r"(v[2]), "r"(v[3])                                                    \
-                 : "memory")
-
 #define KDA_TMEM_ST8(taddr, v)                                                                       \
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), \
                  "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])  \
@@ -227,25 +222,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                  "l"(src), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
 }
-
-// Hint: bring `bytes` (multiple of 16) of global memory at `src` (16-byte aligned) into L2.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
-// Contiguous shared -> global copy, tracked in this thread's bulk async-group.
-__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
-                 "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// The source shared memory of every committed bulk store may be overwritten.
-__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// Every committed bulk store has completed.
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // ---------------------------------------------------------------- warp-level MMA (16x8x16, bf16 -> fp32)
 
