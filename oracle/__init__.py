@@ -19,6 +19,9 @@ What is computed (see the C file for the step-by-step statement):
                      S_t = (I - b k k^T) Diag(alpha) S_{t-1} + b k v^T, o_t = S_t^T q_t.
 * ``forward``     -- Equation 1 driven by the Equation 5 gate (what ``kda_forward`` computes).
 * ``decode_step`` -- one token per sequence (what ``kda_decode_step`` computes).
+* ``replay``      -- speculative-decode state replay: a window of drafted tokens per sequence read
+                     from a snapshot that is left untouched, with the state kept after the
+                     accepted prefix only (what ``kda_decode_replay`` computes).
 """
 from __future__ import annotations
 
@@ -190,3 +193,38 @@ def decode_step(q, k, v, z, A, beta, S, g_min: float = -5.0, threads: int = 0):
                                         int(threads))
     _check(rc)
     return out, S_new
+
+
+def replay(q, k, v, z, A, beta, S, accepted=None, g_min: float = -5.0, threads: int = 0):
+    """Speculative-decode state replay ("Kimi K3: architecture, derivations and a pinned-source
+    audit", section 10.3 "KDA state replay for speculative decoding", and the replay checks of its
+    "CPU laboratory"): the projected inputs of L drafted tokens per sequence are cached, the
+    verifier reads every drafted token from the snapshot, and once the accepted count is known the
+    state is advanced over the accepted prefix only; the snapshot itself is never modified.
+
+    q, k, z: [N*L, H, d_k] with token t of sequence n at row n*L + t; v: [N*L, H, d_v];
+    beta: [N*L, H]; A: [H]; S: the snapshot [N, H, d_k, d_v]; accepted: N counts in [0, L], or
+    None for all L.
+
+    Returns (out, S_acc): out [N*L, H, d_v] holds o_t for every drafted token, read from the
+    recurrence started at the snapshot and run over the whole window (Equation 1, o_t = S_t^T q_t);
+    S_acc [N, H, d_k, d_v] is the state after the first accepted[n] tokens of sequence n (the
+    snapshot itself where that count is 0).  Both come from :func:`forward`: the window as N
+    sequences of L tokens, and the accepted prefixes gathered as N sequences of accepted[n] tokens.
+    """
+    q, k, v, z, A, beta, S = map(_f64, (q, k, v, z, A, beta, S))
+    N = S.shape[0]
+    T = k.shape[0]
+    if N < 1 or T % N:
+        raise ValueError("oracle.replay: the token count must be a multiple of the sequence count")
+    L = T // N
+    acc = np.full(N, L, dtype=np.int64) if accepted is None else np.asarray(accepted, dtype=np.int64).reshape(N)
+    if (acc < 0).any() or (acc > L).any():
+        raise ValueError("oracle.replay: accepted counts must lie in [0, L]")
+    out, _ = forward(q, k, v, z, A, beta, S0=S, cu_seqlens=np.arange(N + 1, dtype=np.int64) * L, g_min=g_min,
+                     threads=threads)
+    rows = np.concatenate([n * L + np.arange(acc[n], dtype=np.int64) for n in range(N)])
+    cu_acc = np.concatenate([[0], np.cumsum(acc)]).astype(np.int64)
+    _, S_acc = forward(q[rows], k[rows], v[rows], z[rows], A, beta[rows], S0=S, cu_seqlens=cu_acc, g_min=g_min,
+                       threads=threads, want_out=False)
+    return out, S_acc

@@ -354,3 +354,69 @@ def test_decode_step_is_one_token_of_the_recurrence():
     o_dec, s_dec = oracle.decode_step(q[last], k[last], v[last], z[last], A, b[last], s_pre)
     np.testing.assert_allclose(o_dec, o_full[last], rtol=1e-13, atol=1e-13)
     np.testing.assert_allclose(s_dec, s_full, rtol=1e-13, atol=1e-13)
+
+
+# ---------------------------------------------------------------- speculative-decode state replay
+
+def _window(rng, N, L, H, dk, dv):
+    q, k, v, _, b, _ = _rand(rng, N * L, H, dk, dv)
+    z = rng.normal(size=(N * L, H, dk))
+    A = rng.normal(size=H) * 0.5
+    S = rng.normal(size=(N, H, dk, dv))
+    return q, k, v, z, A, b, S
+
+
+def test_replay_accepted_prefix_composes_and_leaves_the_snapshot():
+    """The replay checks of the audit's CPU laboratory: a boundary after 3 tokens, 3 drafts of
+    which 2 are accepted.  Replaying the 2 accepted drafts from the cached boundary state equals
+    running all 5 tokens from the start; replaying all 3 drafts gives another state; the cached
+    snapshot is unchanged by either replay."""
+    rng = np.random.default_rng(41)
+    H, dk, dv = 2, 5, 3
+    q, k, v, z, A, b, S0 = _window(rng, 1, 6, H, dk, dv)
+    _, s_boundary = oracle.forward(q[:3], k[:3], v[:3], z[:3], A, b[:3], S0=S0)
+    snapshot = s_boundary.copy()
+    d = slice(3, 6)
+    _, s_all = oracle.replay(q[d], k[d], v[d], z[d], A, b[d], s_boundary)
+    _, s_two = oracle.replay(q[d], k[d], v[d], z[d], A, b[d], s_boundary, accepted=[2])
+    _, s_five = oracle.forward(q[:5], k[:5], v[:5], z[:5], A, b[:5], S0=S0)
+    np.testing.assert_allclose(s_two, s_five, rtol=1e-12, atol=1e-12)
+    assert not np.allclose(s_all, s_two)
+    np.testing.assert_array_equal(s_boundary, snapshot)
+
+
+def test_replay_matches_chained_decode_steps():
+    """Brute force: each sequence advanced token by token with decode_step from the snapshot.
+    Every drafted token's output matches the chain whatever was accepted, and the state matches
+    the chain after exactly accepted[n] steps (0 and L included)."""
+    rng = np.random.default_rng(42)
+    N, L, H, dk, dv = 5, 4, 2, 6, 5
+    q, k, v, z, A, b, S = _window(rng, N, L, H, dk, dv)
+    accepted = np.array([0, 1, 2, 4, 3])
+    out, s_acc = oracle.replay(q, k, v, z, A, b, S, accepted=accepted)
+    cur = S.copy()
+    states = [cur]
+    for t in range(L):
+        rows = np.arange(N) * L + t
+        o_t, cur = oracle.decode_step(q[rows], k[rows], v[rows], z[rows], A, b[rows], cur)
+        np.testing.assert_allclose(out[rows], o_t, rtol=1e-12, atol=1e-12)
+        states.append(cur)
+    for n in range(N):
+        np.testing.assert_allclose(s_acc[n], states[accepted[n]][n], rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(s_acc[0], S[0])  # nothing accepted: the snapshot itself
+
+
+def test_replay_outputs_do_not_depend_on_acceptance():
+    """The outputs verify the whole window from the snapshot; the accepted counts only choose
+    which state is kept (computing outputs from the kept state would fail this)."""
+    rng = np.random.default_rng(43)
+    N, L, H, dk, dv = 3, 5, 1, 4, 4
+    q, k, v, z, A, b, S = _window(rng, N, L, H, dk, dv)
+    o_all, s_all = oracle.replay(q, k, v, z, A, b, S)
+    o_some, s_some = oracle.replay(q, k, v, z, A, b, S, accepted=[1, 5, 0])
+    np.testing.assert_array_equal(o_all, o_some)
+    np.testing.assert_array_equal(s_all[1], s_some[1])
+    _, s_fwd = oracle.forward(q, k, v, z, A, b, S0=S, cu_seqlens=np.arange(N + 1) * L)
+    np.testing.assert_allclose(s_all, s_fwd, rtol=1e-13, atol=1e-13)
+    with pytest.raises(ValueError):
+        oracle.replay(q, k, v, z, A, b, S, accepted=[1, 6, 0])
