@@ -6,7 +6,8 @@ the decode step (256 sequences x 32 heads, d=128, 512 MiB fp32 state), on one GB
 Prints ONE JSON line.  `value` is prefill throughput in million tokens per second (tokens of all
 16 heads) with inputs resident in HBM, timed with CUDA events on the launching stream; L2 is
 flushed (a 512 MiB write) before every timed step because the workload's 86 MB fit in L2.
-`decode` reports the decode step's state bandwidth.  `e2e` repeats the prefill through the same
+`decode` reports the decode step's state bandwidth, and under `replay` the speculative-decode round
+(verify a 7-token drafted window from the snapshot, then commit the accepted prefix in place).  `e2e` repeats the prefill through the same
 public call with pinned host buffers, host<->device copies inside the timed region.  `roofline`
 is for the kernel with the largest device time, measured live with per-launch CUDA events.
 `cpu_baseline` times the fp64 oracle on the host cores on a bounded sample of the same workload.
@@ -100,7 +101,8 @@ class ClockSampler:
 
 def src_sha(kernel):
     name = {"kda_gate": "kda_gate.cu", "kda_ut_wy": "kda_ut_wy.cu", "kda_chunk_fwd": "kda_chunk_fwd.cu",
-            "kda_decode_step": "kda_decode.cu", "kda_chunk_fwd_tc": "kda_chunk_tc.cu",
+            "kda_decode_step": "kda_decode.cu", "kda_decode_replay": "kda_replay.cu",
+            "kda_chunk_fwd_tc": "kda_chunk_tc.cu",
             "kda_seg_summary_tc": "kda_chunk_tc.cu", "kda_seg_scan": "kda_segment_scan.cu",
             "kda_chunk_prep_tc": "kda_prep_tc.cu", "kda_state_summary_tc": "kda_state_tc.cu",
             "kda_chunk_state_tc": "kda_state_tc.cu"}.get(kernel)
@@ -210,6 +212,7 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-replay", action="store_true", help="skip the speculative-decode replay leg")
     ap.add_argument("--no-shapes", action="store_true", help="skip the varlen and long-context prefill shapes")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -509,13 +512,81 @@ def bench_decode(args, B, I, dev, stream, max_over_ranks, barrier, pk, pk_src):
     kn, kms = prof.get("kda_decode_step", (steps, ms * steps))
     kavg = kms / kn
     gbs = nbytes / (kavg * 1e-3) / 1e9
+    del dq, dk_, dv_, dz, db, outs
+    replay = None if args.no_replay else bench_replay(B, dev, g, toks, A, state, ms, max_over_ranks, barrier, pk,
+                                                      pk_src)
     return {"workload": w.name, "ms_per_step": ms, "tokens_per_s": N / (ms * 1e-3),
             "state_gbs": nbytes / (ms * 1e-3) / 1e9,
             "roofline": {"bound": "hbm", "kernel": "kda_decode_step", "achieved": gbs, "peak": pk["hbm_gbs"],
                          "unit": "GB/s", "frac": gbs / pk["hbm_gbs"], "frac_of_8tbs": gbs / 8000.0,
                          "traffic": ncu_traffic("kda_decode_step"), "peak_source": pk_src,
                          "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": kavg},
-            "gpu_launches": kn}
+            "gpu_launches": kn, "replay": replay}
+
+
+REPLAY_WINDOW = 7  # drafted tokens per sequence and speculation round
+
+
+def replay_bytes(N, H, dk, dv, tokens_read, tokens_out, state_writes, io_bytes=2):
+    """Minimum HBM bytes of one kda_decode_replay launch: the snapshot read once, the drafted
+    tokens' q, k, z, v (io dtype) and beta (fp32) read, outputs and accepted states written."""
+    return (N * H * dk * dv * 4 + tokens_read * H * ((3 * dk + dv) * io_bytes + 4)
+            + tokens_out * H * dv * io_bytes + state_writes * H * dk * dv * 4 + N * 4)
+
+
+def bench_replay(B, dev, g, toks, A, state, decode_ms, max_over_ranks, barrier, pk, pk_src, reps=20):
+    """Speculative-decode rounds on the decode workload's state (256 sequences x 32 heads, d=128):
+    verify a 7-token window per sequence from the snapshot (outputs only), then commit the accepted
+    prefix in place (state only); accepted counts uniform in [0, 7].  The state (512 MiB) exceeds
+    L2, so no flush is needed between launches."""
+    import torch
+    N, H, dd = state.shape[0], state.shape[1], state.shape[2]
+    L = REPLAY_WINDOW
+    rq, rk, rv, rz = toks(reps, N * L, H)
+    rb = torch.sigmoid(torch.randn(reps, N * L, H, generator=g, device=dev)).float()
+    acc = torch.randint(0, L + 1, (reps, N), generator=g, device=dev, dtype=torch.int32)
+    out = torch.empty(N * L, H, dd, dtype=rq.dtype, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def verify(r):
+        B.kda_decode_replay(rq[r], rk[r], rv[r], rz[r], A, rb[r], state, out=out, want_state=False)
+
+    def commit(r):
+        B.kda_decode_replay(rq[r], rk[r], rv[r], rz[r], A, rb[r], state, accepted=acc[r], state_out=state,
+                            want_out=False)
+
+    for r in range(3):
+        verify(r)
+        commit(r)
+    torch.cuda.synchronize()
+    res = {}
+    for name, fn in (("verify", verify), ("commit", commit)):
+        barrier()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+        ev[0].record(stream)
+        for r in range(reps):
+            fn(r)
+            ev[r + 1].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        times = [ev[r].elapsed_time(ev[r + 1]) for r in range(reps)]
+        ms = max_over_ranks(sum(times) / reps)
+        if name == "verify":
+            nbytes = replay_bytes(N, H, dd, dd, N * L, N * L, 0)
+        else:
+            nbytes = replay_bytes(N, H, dd, dd, int(acc.sum().item()) / reps, 0, N)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[name] = {"ms": ms, "median_ms": statistics.median(times), "algorithmic_bytes": nbytes, "gbs": gbs,
+                     "frac": gbs / pk["hbm_gbs"]}
+    round_ms = res["verify"]["ms"] + res["commit"]["ms"]
+    return {"workload": f"{N} sequences x {H} heads, d={dd}, {L}-token drafted window, bf16 inputs, fp32 state",
+            "kernel": "kda_decode_replay", **res, "round_ms": round_ms,
+            "drafted_tokens_per_s": N * L / (round_ms * 1e-3),
+            "accepted_tokens_per_s": float(acc.sum().item()) / reps / (round_ms * 1e-3),
+            "vs_decode_steps": (L * decode_ms) / round_ms,
+            "traffic": ncu_traffic("kda_decode_replay"), "peak": pk["hbm_gbs"], "peak_source": pk_src,
+            "gpu_launches": 2 * reps}
 
 
 def bench_e2e(args, B, inp, dev, stream, max_over_ranks, barrier, world, depth=2):

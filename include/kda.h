@@ -147,6 +147,40 @@ kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const 
                              const kda_problem_t* problem, void* stream);
 
 /*
+ * Speculative-decode state replay: a window of L drafted tokens for each of N sequences, run from a
+ * state snapshot ("Kimi K3: architecture, derivations and a pinned-source audit", section 10.3 "KDA
+ * state replay for speculative decoding": only the projected inputs of drafted tokens are cached,
+ * and the accepted prefix is replayed on chip in one fused kernel instead of rolling the state
+ * back).  Every token is one decode step of the recurrence (as kda_decode_step computes it); one
+ * launch reads each (sequence, head) state once, keeps it on chip across the window and writes at
+ * most one state.  Typical use, per speculation round:
+ *   verify : out given, state_out NULL -- o_t of every drafted token, no state is written, so the
+ *            snapshot stays valid whatever is accepted;
+ *   commit : accepted given, state_out == state_in, out NULL -- the snapshot advances over each
+ *            sequence's accepted prefix; rejected drafts are never applied.
+ * With accepted NULL and both outputs given it is an L-token decode step.
+ *
+ *   q, k, z   : [N*L, H, d_k] io dtype, token t of sequence n at row n*L + t (kda_forward's packed
+ *               layout with N equal lengths L);  v : [N*L, H, d_v] io dtype;  beta : [N*L, H] fp32;
+ *               A : [H] fp32.
+ *   state_in  : [N, H, d_k, d_v] fp32 snapshot; only read (unless state_out is the same pointer).
+ *   accepted  : [N] int32 on the device, the number of window tokens of sequence n to keep, or NULL
+ *               for all L.  Values outside [0, L] are clamped to it.
+ *   state_out : [N, H, d_k, d_v] fp32, the state after the first accepted[n] tokens (the snapshot's
+ *               values where accepted[n] = 0), or NULL (not written).  May be state_in itself
+ *               (in place); any other overlap with an argument is rejected.
+ *   out       : [N*L, H, d_v] io dtype, o_t = S_t^T q_t of every window token from the snapshot,
+ *               whatever is accepted; or NULL (not written).  Must not overlap any argument.
+ *   problem   : num_seqs = N and total_tokens = N*L with L >= 1; max_seqlen and cu_seqlens are
+ *               not used.
+ * At least one of out and state_out must be given.  Argument errors as for kda_decode_step.
+ */
+kda_status_t kda_decode_replay(const void* q, const void* k, const void* v, const void* z,
+                               const float* A, const float* beta, const float* state_in,
+                               const int32_t* accepted, float* state_out, void* out,
+                               const kda_problem_t* problem, void* stream);
+
+/*
  * kda_forward for callers that cannot allocate device memory: a library or plugin that runs
  * inside a host application which owns every device allocation (its own pool or arena) and gives
  * the plugin no allocator, or a latency-critical path that must not enter the driver's allocator.
@@ -188,7 +222,7 @@ const char* kda_status_string(kda_status_t status);
 
 /*
  * Per-kernel device timing, for measurement tools.  While enabled, every kernel launched by
- * kda_forward / kda_decode_step is bracketed by two CUDA events recorded on the call's stream;
+ * kda_forward / kda_decode_step / kda_decode_replay is bracketed by two CUDA events recorded on the call's stream;
  * kda_profile_read synchronises on those events and returns, per kernel name, the number of
  * launches and their summed device time.  Enabling (or disabling) discards earlier records.
  * Events are host-side objects: no device memory is allocated.  Not thread-safe against
@@ -208,7 +242,7 @@ int32_t kda_profile_read(kda_kernel_time_t* out, int32_t max_entries);
 /* ABI version of this header: (major << 16) | minor. */
 uint32_t kda_abi_version(void);
 
-#define KDA_ABI_VERSION ((1u << 16) | 0u)
+#define KDA_ABI_VERSION ((1u << 16) | 1u)
 
 #ifdef __cplusplus
 }

@@ -33,7 +33,7 @@ G_MIN = -5.0
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_forward_workspace_bytes", "kda_forward", "kda_decode_step", "kda_workspace_status",
            "kda_status_string", "kda_profile_enable", "kda_profile_read", "kda_abi_version",
-           "kda_forward_static_scratch", "kda_forward_plan")
+           "kda_forward_static_scratch", "kda_forward_plan", "kda_decode_replay")
 
 # Size of the library's own scratch array used by kda_forward_static_scratch.
 KDA_STATIC_SCRATCH_BYTES = 8 << 20
@@ -84,6 +84,8 @@ def lib():
             L.kda_forward.argtypes = [_vp] * 10 + [P, _vp, ctypes.c_size_t, _vp]
             L.kda_decode_step.restype = ctypes.c_int
             L.kda_decode_step.argtypes = [_vp] * 8 + [P, _vp]
+            L.kda_decode_replay.restype = ctypes.c_int
+            L.kda_decode_replay.argtypes = [_vp] * 10 + [P, _vp]
             L.kda_workspace_status.restype = ctypes.c_int
             L.kda_workspace_status.argtypes = [_vp, ctypes.c_size_t, _vp]
             L.kda_status_string.restype = ctypes.c_char_p
@@ -262,6 +264,44 @@ def kda_decode_step(q, k, v, z, A, beta, state, out=None, g_min: float = G_MIN, 
     if st != KDA_OK:
         raise KdaError(st, "kda_decode_step")
     return out
+
+
+def kda_decode_replay(q, k, v, z, A, beta, state_in, accepted=None, state_out=None, out=None,
+                      want_out: bool = True, want_state: bool = True, g_min: float = G_MIN, stream=None):
+    """A window of L drafted tokens per sequence from the snapshot ``state_in`` (speculative-decode
+    state replay; see include/kda.h): q, k, z [N*L, H, d_k] with token t of sequence n at row
+    n*L + t; v [N*L, H, d_v]; beta [N*L, H] fp32; state_in [N, H, d_k, d_v] fp32; accepted [N]
+    int32 or None (all L).  ``out`` receives o_t of every window token (allocated when
+    ``want_out`` and not given); ``state_out`` the state after each accepted prefix (allocated when
+    ``want_state`` and not given; pass ``state_in`` to advance the snapshot in place).
+    Returns (out or None, state_out or None)."""
+    N, H, dk, dv = state_in.shape
+    T = k.shape[0]
+    dev = k.device
+    dt = k.dtype
+    if N < 1 or T < N or T % N:
+        raise ValueError("the token count must be a positive multiple of the number of sequences")
+    for name, t, shp in (("q", q, (T, H, dk)), ("k", k, (T, H, dk)), ("z", z, (T, H, dk)), ("v", v, (T, H, dv))):
+        _need(t, name, dt, shp, dev)
+    _need(A, "A", torch.float32, (H,), dev)
+    _need(beta, "beta", torch.float32, (T, H), dev)
+    _need(state_in, "state_in", torch.float32, (N, H, dk, dv), dev)
+    if accepted is not None:
+        _need(accepted, "accepted", torch.int32, (N,), dev)
+    if out is None and want_out:
+        out = torch.empty((T, H, dv), dtype=dt, device=dev)
+    if out is not None:
+        _need(out, "out", dt, (T, H, dv), dev)
+    if state_out is None and want_state:
+        state_out = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    if state_out is not None:
+        _need(state_out, "state_out", torch.float32, (N, H, dk, dv), dev)
+    prob = make_problem(N, T, T // N, H, dk, dv, dt, g_min)
+    st = lib().kda_decode_replay(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(beta), _ptr(state_in),
+                                 _ptr(accepted), _ptr(state_out), _ptr(out), ctypes.byref(prob), _stream(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_decode_replay")
+    return out, state_out
 
 
 def kda_workspace_status(workspace, stream=None) -> int:

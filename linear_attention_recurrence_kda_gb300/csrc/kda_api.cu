@@ -37,7 +37,9 @@ bool overlaps(Range a, Range b)
     return a.lo < b.hi && b.lo < a.hi;
 }
 
-kda_status_t check_descriptor(const kda_problem_t* p, bool decode)
+enum class Call { Forward, Decode, Replay };
+
+kda_status_t check_descriptor(const kda_problem_t* p, Call call)
 {
     if (p == nullptr) return KDA_ERR_INVALID_ARG;
     if (p->num_seqs < 1 || p->total_tokens < 0 || p->num_heads < 1 || p->num_heads > 65535) return KDA_ERR_INVALID_ARG;
@@ -49,8 +51,12 @@ kda_status_t check_descriptor(const kda_problem_t* p, bool decode)
     const double elems = (double)p->total_tokens * p->num_heads * (p->d_k > p->d_v ? p->d_k : p->d_v);
     if (elems > 1099511627776.0) return KDA_ERR_UNSUPPORTED;
     if ((double)p->num_seqs * p->num_heads * p->d_k * p->d_v > 1099511627776.0) return KDA_ERR_UNSUPPORTED;
-    if (decode) {
+    if (call == Call::Decode) {
         if (p->total_tokens != p->num_seqs) return KDA_ERR_INVALID_ARG;
+    } else if (call == Call::Replay) {
+        // a window of L >= 1 tokens per sequence, L < 2^31
+        if (p->total_tokens < p->num_seqs || p->total_tokens % p->num_seqs != 0) return KDA_ERR_INVALID_ARG;
+        if (p->total_tokens / p->num_seqs > 2147483647LL) return KDA_ERR_UNSUPPORTED;
     } else {
         if (p->max_seqlen < 0) return KDA_ERR_INVALID_ARG;
     }
@@ -187,14 +193,14 @@ const char* kda_status_string(kda_status_t s)
 
 size_t kda_forward_workspace_bytes(const kda_problem_t* problem)
 {
-    if (check_descriptor(problem, false) != KDA_OK) return 0;
+    if (check_descriptor(problem, Call::Forward) != KDA_OK) return 0;
     return kda::forward_layout(*problem, SIZE_MAX).total;
 }
 
 kda_status_t kda_forward_plan(const kda_problem_t* problem, size_t workspace_bytes, kda_plan_t* plan)
 {
     if (plan == nullptr) return KDA_ERR_INVALID_ARG;
-    const kda_status_t st = check_descriptor(problem, false);
+    const kda_status_t st = check_descriptor(problem, Call::Forward);
     if (st != KDA_OK) return st;
     const ForwardLayout L = kda::forward_layout(*problem, workspace_bytes);
     if (workspace_bytes < L.total) return KDA_ERR_WORKSPACE;
@@ -210,7 +216,7 @@ kda_status_t kda_forward(const void* q, const void* k, const void* v, const void
                          void* out, float* final_state, const kda_problem_t* problem, void* workspace,
                          size_t workspace_bytes, void* stream)
 {
-    kda_status_t st = check_descriptor(problem, false);
+    kda_status_t st = check_descriptor(problem, Call::Forward);
     if (st != KDA_OK) return st;
     const kda_problem_t& p = *problem;
     const bool equal = cu_seqlens == nullptr;
@@ -310,7 +316,7 @@ kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const 
                              const float* beta, float* state, void* out, const kda_problem_t* problem,
                              void* stream)
 {
-    kda_status_t st = check_descriptor(problem, true);
+    kda_status_t st = check_descriptor(problem, Call::Decode);
     if (st != KDA_OK) return st;
     const kda_problem_t& p = *problem;
     if (!q || !k || !v || !z || !A || !beta || !state || !out) return KDA_ERR_INVALID_ARG;
@@ -342,6 +348,54 @@ kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     kda::prof_start("kda_decode_step", s);
     const cudaError_t e = kda::launch_decode(a, p.d_k, p.d_v, p.io_dtype, s);
+    kda::prof_stop(s);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_decode_replay(const void* q, const void* k, const void* v, const void* z, const float* A,
+                               const float* beta, const float* state_in, const int32_t* accepted, float* state_out,
+                               void* out, const kda_problem_t* problem, void* stream)
+{
+    kda_status_t st = check_descriptor(problem, Call::Replay);
+    if (st != KDA_OK) return st;
+    const kda_problem_t& p = *problem;
+    if (!q || !k || !v || !z || !A || !beta || !state_in) return KDA_ERR_INVALID_ARG;
+    if (!out && !state_out) return KDA_ERR_INVALID_ARG;
+    for (const void* ptr : {q, k, v, z, (const void*)state_in, (const void*)state_out, (const void*)out}) {
+        if (!aligned(ptr, 16)) return KDA_ERR_INVALID_ARG;
+    }
+    if (!aligned(A, 4) || !aligned(beta, 4) || !aligned(accepted, 4)) return KDA_ERR_INVALID_ARG;
+    if ((int64_t)p.num_seqs * p.num_heads > 2147483647LL) return KDA_ERR_UNSUPPORTED;
+    const size_t io = io_size(p.io_dtype);
+    const size_t th = (size_t)p.total_tokens * p.num_heads;
+    const size_t nh = (size_t)p.num_seqs * p.num_heads;
+    const Range rq = range_of(q, th * p.d_k * io), rk = range_of(k, th * p.d_k * io);
+    const Range rz = range_of(z, th * p.d_k * io), rv = range_of(v, th * p.d_v * io);
+    const Range ra = range_of(A, p.num_heads * sizeof(float)), rb = range_of(beta, th * sizeof(float));
+    const Range racc = range_of(accepted, (size_t)p.num_seqs * sizeof(int32_t));
+    const Range rsi = range_of(state_in, nh * p.d_k * p.d_v * sizeof(float));
+    const Range rso = range_of(state_out, nh * p.d_k * p.d_v * sizeof(float));
+    const Range ro = range_of(out, th * p.d_v * io);
+    for (Range r : {rq, rk, rz, rv, ra, rb, racc, rsi, rso}) {
+        if (overlaps(ro, r)) return KDA_ERR_INVALID_ARG;
+    }
+    for (Range r : {rq, rk, rz, rv, ra, rb, racc}) {
+        if (overlaps(rso, r)) return KDA_ERR_INVALID_ARG;
+    }
+    // state_out may be state_in itself (each CTA reads its whole state before writing it), nothing else
+    if (state_out != state_in && overlaps(rso, rsi)) return KDA_ERR_INVALID_ARG;
+    for (const void* ptr : {q, k, v, z, (const void*)A, (const void*)beta, (const void*)state_in,
+                            (const void*)accepted, (const void*)state_out, (const void*)out}) {
+        st = check_device_pointer(ptr);
+        if (st != KDA_OK) return st;
+    }
+    kda::ReplayArgs a{};
+    a.q = q; a.k = k; a.v = v; a.z = z; a.A = A; a.beta = beta;
+    a.state_in = state_in; a.accepted = accepted; a.state_out = state_out; a.out = out;
+    a.N = p.num_seqs; a.H = p.num_heads; a.L = (int32_t)(p.total_tokens / p.num_seqs); a.g_min = p.g_min;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    kda::prof_start("kda_decode_replay", s);
+    const cudaError_t e = kda::launch_replay(a, p.d_k, p.d_v, p.io_dtype, s);
     kda::prof_stop(s);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

@@ -178,6 +178,22 @@ struct DecodeArgs {
     float g_min;
 };
 
+// A window of L tokens for each of N sequences from a state snapshot (kda_decode_replay).
+struct ReplayArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* z;
+    const float* A;
+    const float* beta;
+    const float* state_in;    // [N][H][d_k][d_v], read only unless state_out is the same pointer
+    const int32_t* accepted;  // [N] or null (all L)
+    float* state_out;         // [N][H][d_k][d_v] or null
+    void* out;                // [N*L][H][d_v] or null
+    int32_t N, H, L;
+    float g_min;
+};
+
 // Launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_gate(const PrefillArgs& a, kda_dtype_t dt, cudaStream_t s);
 cudaError_t launch_ut_wy(const PrefillArgs& a, kda_dtype_t dt, cudaStream_t s);
@@ -187,6 +203,7 @@ cudaError_t launch_chunk_prep_tc(const PrefillArgs& a, cudaStream_t s);     // o
 cudaError_t launch_prefill_split_tc(const PrefillArgs& a, cudaStream_t s);  // blocks + state pass, all passes
 cudaError_t launch_segment_scan(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
+cudaError_t launch_replay(const ReplayArgs& a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
 
 // SM count of the current device (cached per device; 152 if it cannot be queried).
 int sm_count_of_current_device();

@@ -1,0 +1,439 @@
+// kda_replay.cu -- a window of decode tokens per sequence from a state snapshot (speculative-decode
+// state replay).
+//
+// "Kimi K3: architecture, derivations and a pinned-source audit", section 10.3 "KDA state replay for
+// speculative decoding": the serving stack caches only the projected inputs of the drafted tokens,
+// verifies the window from a snapshot of the state, and then advances the state over the accepted
+// prefix in one fused kernel, so that rejected drafts never have to be rolled back.  The arithmetic
+// of every token is the decode step's (Equation 1 with the gate of Equation 5, o = S'^T q = y + (q.k) u):
+//     alpha = exp(g_min sigmoid(exp(A_h) z)),  r = (Diag(alpha) S)^T k,  y = (Diag(alpha) S)^T q,
+//     u = beta (v - r),  S' = Diag(alpha) S + k u^T.
+//
+// One CTA of 256 threads owns one (sequence, head) for the whole window.  The fp32 state is read
+// from HBM once into registers (warp w holds rows w, w + 8, ...; lane l holds columns
+// l*VEC .. l*VEC + VEC - 1 of each, so a warp reads whole rows with vector loads), advances token
+// by token on chip and is written at most once, right after the last accepted token.  Token inputs
+// are staged in shared memory eight tokens at a time (the gate is evaluated there).  Per token the
+// eight warps' partial sums of r (and of y when outputs are wanted) meet in shared memory behind one
+// barrier; every thread then adds the eight partials of its own columns itself, so u needs no second
+// barrier to reach the threads that apply it.  The partial-sum buffer alternates between consecutive
+// tokens: a buffer is written again two tokens later, after a barrier that every reader of its
+// previous contents has passed.
+#include "kda_internal.cuh"
+
+namespace kda {
+
+namespace {
+
+constexpr int kRepThreads = 256;
+constexpr int kRepWarps = kRepThreads / 32;
+constexpr int kRepGroup = 8;  // tokens staged in shared memory at a time
+
+template <int VEC>
+__device__ __forceinline__ void ld_cols(const float* p, float (&x)[VEC])
+{
+    if constexpr (VEC == 4) {
+        const float4 t = __ldcs(reinterpret_cast<const float4*>(p));
+        x[0] = t.x; x[1] = t.y; x[2] = t.z; x[3] = t.w;
+    } else if constexpr (VEC == 2) {
+        const float2 t = __ldcs(reinterpret_cast<const float2*>(p));
+        x[0] = t.x; x[1] = t.y;
+    } else {
+        x[0] = __ldcs(p);
+    }
+}
+
+template <int VEC>
+__device__ __forceinline__ void st_cols(float* p, const float (&x)[VEC])
+{
+    if constexpr (VEC == 4) {
+        __stcs(reinterpret_cast<float4*>(p), make_float4(x[0], x[1], x[2], x[3]));
+    } else if constexpr (VEC == 2) {
+        __stcs(reinterpret_cast<float2*>(p), make_float2(x[0], x[1]));
+    } else {
+        __stcs(p, x[0]);
+    }
+}
+
+}  // namespace
+
+template <typename TIO, int DK, int DV, bool OUT>
+__global__ void __launch_bounds__(kRepThreads, 2) kda_decode_replay_kernel(ReplayArgs a)
+{
+    constexpr int VEC = DV / 32;
+    constexpr int RPW = DK / kRepWarps;  // rows per warp
+    __shared__ __align__(16) float s_k[kRepGroup][DK];
+    __shared__ __align__(16) float s_q[kRepGroup][DK];
+    __shared__ __align__(16) float s_al[kRepGroup][DK];
+    __shared__ __align__(16) float s_v[kRepGroup][DV];
+    __shared__ float s_beta[kRepGroup];
+    __shared__ float s_qk[kRepGroup];
+    __shared__ __align__(16) float s_red[2][OUT ? 2 : 1][kRepWarps][DV];
+
+    const int nh = blockIdx.x;  // sequence * H + head
+    const int n = nh / a.H;
+    const int h = nh - n * a.H;
+    const int tid = threadIdx.x;
+    const int w = tid >> 5;
+    const int l = tid & 31;
+    const int L = a.L;
+
+    // the whole state in flight first
+    float s[RPW][VEC];
+    {
+        const float* S = a.state_in + (int64_t)nh * DK * DV;
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) ld_cols<VEC>(S + (int64_t)(w + kRepWarps * i) * DV + l * VEC, s[i]);
+    }
+
+    int acc = L;
+    if (a.accepted != nullptr) acc = min(max(a.accepted[n], 0), L);
+    float* Sout = a.state_out != nullptr ? a.state_out + (int64_t)nh * DK * DV : nullptr;
+    auto store_state = [&]() {
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) st_cols<VEC>(Sout + (int64_t)(w + kRepWarps * i) * DV + l * VEC, s[i]);
+    };
+    if (Sout != nullptr && acc == 0) store_state();
+
+    const int steps = OUT ? L : acc;  // without outputs nothing after the accepted prefix matters
+    const TIO* qp = static_cast<const TIO*>(a.q);
+    const TIO* kp = static_cast<const TIO*>(a.k);
+    const TIO* vp = static_cast<const TIO*>(a.v);
+    const TIO* zp = static_cast<const TIO*>(a.z);
+    TIO* op = static_cast<TIO*>(a.out);
+    const float expA = expf(a.A[h]);
+    const int64_t tok0 = (int64_t)n * L;  // first row of this sequence's window
+
+    for (int g0 = 0; g0 < steps; g0 += kRepGroup) {
+        const int ng = min(kRepGroup, steps - g0);
+        __syncthreads();  // the previous group's staged tokens are no longer read
+        for (int e = tid; e < ng * DK; e += kRepThreads) {
+            const int j = e / DK;
+            const int c = e - j * DK;
+            const int64_t idx = ((tok0 + g0 + j) * a.H + h) * DK + c;
+            s_k[j][c] = ld_io(kp, idx);
+            s_q[j][c] = ld_io(qp, idx);
+            s_al[j][c] = expf(log_decay(ld_io(zp, idx), expA, a.g_min));
+        }
+        for (int e = tid; e < ng * DV; e += kRepThreads) {
+            const int j = e / DV;
+            const int c = e - j * DV;
+            s_v[j][c] = ld_io(vp, ((tok0 + g0 + j) * a.H + h) * DV + c);
+        }
+        if (tid < ng) s_beta[tid] = a.beta[(tok0 + g0 + tid) * a.H + h];
+        __syncthreads();
+        if (OUT && w < ng) {  // q.k of token w of the group (read after the first token's barrier)
+            float p = 0.f;
+            for (int c = l; c < DK; c += 32) p += s_q[w][c] * s_k[w][c];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+            if (l == 0) s_qk[w] = p;
+        }
+
+        for (int j = 0; j < ng; ++j) {
+            const int t = g0 + j;
+            const int buf = t & 1;
+            // decay the rows this thread holds and reduce r (and y) over them
+            float r[VEC], y[VEC];
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) r[e] = y[e] = 0.f;
+#pragma unroll
+            for (int i = 0; i < RPW; ++i) {
+                const int c = w + kRepWarps * i;
+                const float al = s_al[j][c], kc = s_k[j][c];
+                const float qc = OUT ? s_q[j][c] : 0.f;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const float d = al * s[i][e];
+                    s[i][e] = d;
+                    r[e] += kc * d;
+                    if (OUT) y[e] += qc * d;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                s_red[buf][0][w][l * VEC + e] = r[e];
+                if (OUT) s_red[buf][OUT ? 1 : 0][w][l * VEC + e] = y[e];
+            }
+            __syncthreads();
+            // every thread: u for its own columns from the eight warps' partial sums
+            float u[VEC];
+            const float b = s_beta[j];
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                float rr = 0.f;
+#pragma unroll
+                for (int ww = 0; ww < kRepWarps; ++ww) rr += s_red[buf][0][ww][l * VEC + e];
+                u[e] = b * (s_v[j][l * VEC + e] - rr);
+            }
+            if (OUT && w == 0) {
+                const float qk = s_qk[j];
+                const int64_t orow = ((tok0 + t) * a.H + h) * DV + l * VEC;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    float yy = 0.f;
+#pragma unroll
+                    for (int ww = 0; ww < kRepWarps; ++ww) yy += s_red[buf][OUT ? 1 : 0][ww][l * VEC + e];
+                    st_io(op, orow + e, yy + qk * u[e]);
+                }
+            }
+            // S' = Diag(alpha) S + k u^T (the decay is already applied)
+#pragma unroll
+            for (int i = 0; i < RPW; ++i) {
+                const float kc = s_k[j][w + kRepWarps * i];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) s[i][e] += kc * u[e];
+            }
+            if (Sout != nullptr && t + 1 == acc) store_state();
+        }
+    }
+}
+
+// ---------------------------------------------------------------- d_k = d_v = 128, bf16, L <= 8
+//
+// The production shape gets a persistent form of the same step: two CTAs per SM walk the
+// (sequence, head) units with the grid as stride, and while one unit's state advances in registers
+// the state (64 KB) and drafted tokens of the CTA's next unit already arrive in shared memory by
+// 16-byte asynchronous copies, so that HBM keeps streaming through the arithmetic of every window.
+// Per unit: wait for the copies, move the state into registers and the tokens into fp32 staging
+// (gate evaluated there; alpha, k and q of a key channel side by side, so a row takes one 16-byte
+// shared load), then start the next unit's copies and run the window.  Column pairs are updated
+// with packed fp32 instructions, in the same order of operations as the kernel above.
+constexpr int kRepD = 128;
+
+struct RepLayout {
+    static constexpr int kRawRow = kRepD * 2;                         // one bf16 token row of q, k, z or v
+    static constexpr int kStage = 0;                                  // fp32 [128][128], next unit's state
+    static constexpr int kRaw = kStage + kRepD * kRepD * 4;           // bf16 [token][q, k, z, v][128]
+    static constexpr int kRawBeta = kRaw + kRepGroup * 4 * kRawRow;   // fp32 [token]
+    static constexpr int kAkq = kRawBeta + kRepGroup * 4;             // float4 [token][row]: alpha, k, q, 0
+    static constexpr int kV = kAkq + kRepGroup * kRepD * 16;          // fp32 [token][128]
+    static constexpr int kRed = kV + kRepGroup * kRepD * 4;           // fp32 [2][r, y][warp][128]
+    static constexpr int kBeta = kRed + 2 * 2 * kRepWarps * kRepD * 4;
+    static constexpr int kQk = kBeta + kRepGroup * 4;
+    static constexpr int kBytes = kQk + kRepGroup * 4;
+};
+static_assert(RepLayout::kAkq % 16 == 0 && RepLayout::kV % 16 == 0 && RepLayout::kRed % 16 == 0, "16-byte alignment");
+static_assert(2 * (RepLayout::kBytes + 1024) <= 228 * 1024, "two CTAs per SM");
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(void* dst, const void* src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+                 : "memory");
+}
+
+template <bool OUT>
+__global__ void __launch_bounds__(kRepThreads, 2) kda_decode_replay_d128_kernel(ReplayArgs a)
+{
+    constexpr int D = kRepD;
+    constexpr int RPW = D / kRepWarps;  // 16 rows per warp
+    using TIO = __nv_bfloat16;
+    extern __shared__ __align__(16) unsigned char smem[];
+    float* stage = reinterpret_cast<float*>(smem + RepLayout::kStage);
+    unsigned char* raw = smem + RepLayout::kRaw;
+    float* raw_beta = reinterpret_cast<float*>(smem + RepLayout::kRawBeta);
+    float4* s_akq = reinterpret_cast<float4*>(smem + RepLayout::kAkq);
+    float* s_v = reinterpret_cast<float*>(smem + RepLayout::kV);
+    float* s_red = reinterpret_cast<float*>(smem + RepLayout::kRed);
+    float* s_beta = reinterpret_cast<float*>(smem + RepLayout::kBeta);
+    float* s_qk = reinterpret_cast<float*>(smem + RepLayout::kQk);
+
+    const int tid = threadIdx.x;
+    const int w = tid >> 5;
+    const int l = tid & 31;
+    const int L = a.L;
+    const int units = a.N * a.H;
+    const TIO* qp = static_cast<const TIO*>(a.q);
+    const TIO* kp = static_cast<const TIO*>(a.k);
+    const TIO* vp = static_cast<const TIO*>(a.v);
+    const TIO* zp = static_cast<const TIO*>(a.z);
+    TIO* op = static_cast<TIO*>(a.out);
+
+    auto acc_of = [&](int unit) {
+        return a.accepted != nullptr ? min(max(a.accepted[unit / a.H], 0), L) : L;
+    };
+    // asynchronous copies of a unit's state and of the `steps` drafted tokens it will use
+    auto prefetch = [&](int unit, int steps) {
+        const int n = unit / a.H;
+        const int h = unit - n * a.H;
+        const float* S = a.state_in + (int64_t)unit * D * D;
+#pragma unroll
+        for (int i = 0; i < D * D / 4 / kRepThreads; ++i) {
+            const int e4 = tid + kRepThreads * i;
+            cp_async16(stage + 4 * e4, S + 4 * e4);
+        }
+        constexpr int CH = RepLayout::kRawRow / 16;  // 16-byte pieces per token row
+        const int64_t tok0 = (int64_t)n * L;
+        for (int e = tid; e < steps * 4 * CH; e += kRepThreads) {
+            const int j = e / (4 * CH);
+            const int rem = e - j * 4 * CH;
+            const int which = rem / CH;
+            const int ch = rem - which * CH;
+            const TIO* base = which == 0 ? qp : which == 1 ? kp : which == 2 ? zp : vp;
+            cp_async16(raw + (size_t)e * 16, base + ((tok0 + j) * a.H + h) * D + ch * 8);
+        }
+        if (tid < steps) cp_async4(raw_beta + tid, a.beta + (tok0 + tid) * a.H + h);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+
+    int unit = blockIdx.x;
+    if (unit >= units) return;
+    int acc = acc_of(unit);
+    prefetch(unit, OUT ? L : acc);
+    for (; unit < units; unit += gridDim.x) {
+        const int next = unit + gridDim.x;
+        const int acc_next = next < units ? acc_of(next) : 0;
+        const int steps = OUT ? L : acc;
+        const int n = unit / a.H;
+        const int h = unit - n * a.H;
+        const float expA = expf(a.A[h]);
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        __syncthreads();  // this unit's state and tokens are in shared memory
+
+        for (int e = tid; e < steps * D; e += kRepThreads) {
+            const int j = e / D;
+            const int c = e - j * D;
+            const TIO* rq = reinterpret_cast<const TIO*>(raw + (j * 4 + 0) * RepLayout::kRawRow);
+            const TIO* rk = reinterpret_cast<const TIO*>(raw + (j * 4 + 1) * RepLayout::kRawRow);
+            const TIO* rz = reinterpret_cast<const TIO*>(raw + (j * 4 + 2) * RepLayout::kRawRow);
+            const TIO* rv = reinterpret_cast<const TIO*>(raw + (j * 4 + 3) * RepLayout::kRawRow);
+            s_akq[e] = make_float4(expf(log_decay(__bfloat162float(rz[c]), expA, a.g_min)), __bfloat162float(rk[c]),
+                                   __bfloat162float(rq[c]), 0.f);
+            s_v[e] = __bfloat162float(rv[c]);
+        }
+        if (tid < steps) s_beta[tid] = raw_beta[tid];
+        if (OUT && w < steps) {  // q.k of token w
+            const TIO* rq = reinterpret_cast<const TIO*>(raw + (w * 4 + 0) * RepLayout::kRawRow);
+            const TIO* rk = reinterpret_cast<const TIO*>(raw + (w * 4 + 1) * RepLayout::kRawRow);
+            float p = 0.f;
+#pragma unroll
+            for (int c = l; c < D; c += 32) p += __bfloat162float(rq[c]) * __bfloat162float(rk[c]);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+            if (l == 0) s_qk[w] = p;
+        }
+        float2 s[RPW][2];  // rows w + 8 i, columns 4 l .. 4 l + 3 as two pairs
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) {
+            const float4 t4 = *reinterpret_cast<const float4*>(stage + (w + kRepWarps * i) * D + 4 * l);
+            s[i][0] = make_float2(t4.x, t4.y);
+            s[i][1] = make_float2(t4.z, t4.w);
+        }
+        __syncthreads();  // staging complete; the copy buffers are free for the next unit
+        if (next < units) prefetch(next, OUT ? L : acc_next);
+
+        float* Sout = a.state_out != nullptr ? a.state_out + (int64_t)unit * D * D : nullptr;
+        auto store_state = [&]() {
+#pragma unroll
+            for (int i = 0; i < RPW; ++i)
+                __stcs(reinterpret_cast<float4*>(Sout + (w + kRepWarps * i) * D + 4 * l),
+                       make_float4(s[i][0].x, s[i][0].y, s[i][1].x, s[i][1].y));
+        };
+        if (Sout != nullptr && acc == 0) store_state();
+
+        for (int t = 0; t < steps; ++t) {
+            float* red = s_red + (t & 1) * (2 * kRepWarps * D);
+            float2 r0 = make_float2(0.f, 0.f), r1 = r0, y0 = r0, y1 = r0;
+#pragma unroll
+            for (int i = 0; i < RPW; ++i) {
+                const float4 f = s_akq[t * D + w + kRepWarps * i];
+                const float2 al = make_float2(f.x, f.x), k2 = make_float2(f.y, f.y);
+                s[i][0] = __fmul2_rn(s[i][0], al);
+                s[i][1] = __fmul2_rn(s[i][1], al);
+                r0 = __ffma2_rn(k2, s[i][0], r0);
+                r1 = __ffma2_rn(k2, s[i][1], r1);
+                if (OUT) {
+                    const float2 q2 = make_float2(f.z, f.z);
+                    y0 = __ffma2_rn(q2, s[i][0], y0);
+                    y1 = __ffma2_rn(q2, s[i][1], y1);
+                }
+            }
+            *reinterpret_cast<float4*>(red + w * D + 4 * l) = make_float4(r0.x, r0.y, r1.x, r1.y);
+            if (OUT) *reinterpret_cast<float4*>(red + (kRepWarps + w) * D + 4 * l) = make_float4(y0.x, y0.y, y1.x, y1.y);
+            __syncthreads();
+            float2 R0 = make_float2(0.f, 0.f), R1 = R0;
+#pragma unroll
+            for (int ww = 0; ww < kRepWarps; ++ww) {
+                const float4 p4 = *reinterpret_cast<const float4*>(red + ww * D + 4 * l);
+                R0 = __fadd2_rn(R0, make_float2(p4.x, p4.y));
+                R1 = __fadd2_rn(R1, make_float2(p4.z, p4.w));
+            }
+            const float4 v4 = *reinterpret_cast<const float4*>(s_v + t * D + 4 * l);
+            const float2 b2 = make_float2(s_beta[t], s_beta[t]);
+            const float2 u0 = __fmul2_rn(b2, __fadd2_rn(make_float2(v4.x, v4.y), make_float2(-R0.x, -R0.y)));
+            const float2 u1 = __fmul2_rn(b2, __fadd2_rn(make_float2(v4.z, v4.w), make_float2(-R1.x, -R1.y)));
+            if (OUT && w == 0) {
+                float2 Y0 = make_float2(0.f, 0.f), Y1 = Y0;
+#pragma unroll
+                for (int ww = 0; ww < kRepWarps; ++ww) {
+                    const float4 p4 = *reinterpret_cast<const float4*>(red + (kRepWarps + ww) * D + 4 * l);
+                    Y0 = __fadd2_rn(Y0, make_float2(p4.x, p4.y));
+                    Y1 = __fadd2_rn(Y1, make_float2(p4.z, p4.w));
+                }
+                const float2 qk2 = make_float2(s_qk[t], s_qk[t]);
+                const float2 o0 = __ffma2_rn(qk2, u0, Y0), o1 = __ffma2_rn(qk2, u1, Y1);
+                __nv_bfloat162 b01 = __floats2bfloat162_rn(o0.x, o0.y), b23 = __floats2bfloat162_rn(o1.x, o1.y);
+                uint2 pk;
+                pk.x = *reinterpret_cast<uint32_t*>(&b01);
+                pk.y = *reinterpret_cast<uint32_t*>(&b23);
+                *reinterpret_cast<uint2*>(op + (((int64_t)n * L + t) * a.H + h) * D + 4 * l) = pk;
+            }
+            // S' = Diag(alpha) S + k u^T (the decay is already applied)
+#pragma unroll
+            for (int i = 0; i < RPW; ++i) {
+                const float kc = s_akq[t * D + w + kRepWarps * i].y;
+                const float2 k2 = make_float2(kc, kc);
+                s[i][0] = __ffma2_rn(k2, u0, s[i][0]);
+                s[i][1] = __ffma2_rn(k2, u1, s[i][1]);
+            }
+            if (Sout != nullptr && t + 1 == acc) store_state();
+        }
+        acc = acc_next;
+    }
+}
+
+template <bool OUT>
+static cudaError_t launch_replay_d128(const ReplayArgs& a, cudaStream_t s)
+{
+    cudaError_t e = cudaFuncSetAttribute(kda_decode_replay_d128_kernel<OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         RepLayout::kBytes);
+    if (e != cudaSuccess) return e;
+    const int64_t units = (int64_t)a.N * a.H;
+    const unsigned grid = (unsigned)(units < 2LL * sm_count_of_current_device() ? units : 2LL * sm_count_of_current_device());
+    kda_decode_replay_d128_kernel<OUT><<<grid, kRepThreads, RepLayout::kBytes, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename TIO, bool OUT>
+static cudaError_t launch_replay_out(const ReplayArgs& a, int dk, int dv, cudaStream_t s)
+{
+    const unsigned grid = (unsigned)((int64_t)a.N * a.H);
+#define KDA_REP_CASE(DKv, DVv)                                                              \
+    if (dk == DKv && dv == DVv) {                                                            \
+        kda_decode_replay_kernel<TIO, DKv, DVv, OUT><<<grid, kRepThreads, 0, s>>>(a);        \
+        return cudaGetLastError();                                                           \
+    }
+    KDA_REP_CASE(32, 32) KDA_REP_CASE(32, 64) KDA_REP_CASE(32, 128)
+    KDA_REP_CASE(64, 32) KDA_REP_CASE(64, 64) KDA_REP_CASE(64, 128)
+    KDA_REP_CASE(128, 32) KDA_REP_CASE(128, 64) KDA_REP_CASE(128, 128)
+#undef KDA_REP_CASE
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_replay(const ReplayArgs& a, int dk, int dv, kda_dtype_t dt, cudaStream_t s)
+{
+    const bool out = a.out != nullptr;
+    if (dt == KDA_BF16 && dk == kRepD && dv == kRepD && a.L <= kRepGroup)
+        return out ? launch_replay_d128<true>(a, s) : launch_replay_d128<false>(a, s);
+    if (dt == KDA_BF16)
+        return out ? launch_replay_out<__nv_bfloat16, true>(a, dk, dv, s) : launch_replay_out<__nv_bfloat16, false>(a, dk, dv, s);
+    return out ? launch_replay_out<float, true>(a, dk, dv, s) : launch_replay_out<float, false>(a, dk, dv, s);
+}
+
+}  // namespace kda

@@ -2,6 +2,7 @@
 
     python -m linear_attention_recurrence_kda_gb300.profile_cases prefill-tc [--tokens T] [--heads H] [--reps R]
     python -m linear_attention_recurrence_kda_gb300.profile_cases decode [--seqs N] [--heads H] [--reps R]
+    python -m linear_attention_recurrence_kda_gb300.profile_cases replay [--seqs N] [--heads H] [--window L] [--reps R]
     python -m linear_attention_recurrence_kda_gb300.profile_cases prefill-simt [...]
 
 Each case generates seeded inputs on the device (same recipe as the benchmark), runs one warm-up
@@ -55,18 +56,38 @@ def decode(seqs: int, heads: int, reps: int, d: int = 128):
     torch.cuda.synchronize()
 
 
+def replay(seqs: int, heads: int, window: int, reps: int, d: int = 128):
+    """Each rep: verify a window of drafted tokens from the snapshot (outputs only), then commit the
+    accepted prefixes in place (state only)."""
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev).manual_seed(5)
+    q, k, v, z = _tokens(g, (seqs * window, heads), d, torch.bfloat16, dev)
+    A = (torch.randn(heads, generator=g, device=dev) * I.A_STD).float()
+    beta = torch.sigmoid(torch.randn(seqs * window, heads, generator=g, device=dev)).float()
+    state = (torch.randn(seqs, heads, d, d, generator=g, device=dev) * 0.1).float()
+    accepted = torch.randint(0, window + 1, (seqs,), generator=g, device=dev, dtype=torch.int32)
+    out = torch.empty(seqs * window, heads, d, dtype=torch.bfloat16, device=dev)
+    for _ in range(reps + 1):
+        B.kda_decode_replay(q, k, v, z, A, beta, state, out=out, want_state=False)
+        B.kda_decode_replay(q, k, v, z, A, beta, state, accepted=accepted, state_out=state, want_out=False)
+    torch.cuda.synchronize()
+
+
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["prefill-tc", "prefill-simt", "decode"])
+    ap.add_argument("case", choices=["prefill-tc", "prefill-simt", "decode", "replay"])
     ap.add_argument("--tokens", type=int, default=4096)
     ap.add_argument("--heads", type=int, default=16)
     ap.add_argument("--seqs", type=int, default=1)
     ap.add_argument("--reps", type=int, default=2)
+    ap.add_argument("--window", type=int, default=7)
     a = ap.parse_args()
     if a.case == "prefill-tc":
         prefill(a.tokens, a.heads, a.reps, torch.bfloat16, seqs=a.seqs)
     elif a.case == "prefill-simt":
         prefill(a.tokens, a.heads, a.reps, torch.float32, seqs=a.seqs)
+    elif a.case == "replay":
+        replay(a.seqs if a.seqs > 1 else 256, a.heads if a.heads != 16 else 32, a.window, a.reps)
     else:
         decode(a.seqs if a.seqs > 1 else 128, a.heads if a.heads != 16 else 32, a.reps)
 

@@ -1,7 +1,7 @@
 """C-ABI checks that need no GPU: the library loads, exports every symbol include/kda.h declares,
 and rejects bad descriptors, pointers, aliasing and workspaces on the host before any launch.
 
-Every kda_forward / kda_decode_step call below is built to fail in a host-only check (the fake
+Every kda_forward / kda_decode_step / kda_decode_replay call below is built to fail in a host-only check (the fake
 addresses are never dereferenced and nothing is launched)."""
 import ctypes
 import os
@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert B.kda_abi_version() == (1 << 16)
+    assert B.kda_abi_version() == (1 << 16) | 1
     for code in range(7):
         s = B.status_string(code)
         assert s.startswith("KDA_")
@@ -153,6 +153,30 @@ def test_decode_rejects_bad_arguments(L):
     assert dec(p, state=_addr(6) + 4) == B.KDA_ERR_INVALID_ARG
     assert dec(p, out=_addr(6)) == B.KDA_ERR_INVALID_ARG       # out on the state
     assert dec(p, state=_addr(2)) == B.KDA_ERR_INVALID_ARG     # state on v
+
+
+def test_replay_rejects_bad_arguments(L):
+    names = ["q", "k", "v", "z", "A", "beta", "state_in", "accepted", "state_out", "out"]
+
+    def rep(prob, **over):
+        ptr = {n: _addr(i) for i, n in enumerate(names)}
+        ptr.update(over)
+        args = [ctypes.c_void_p(ptr[n]) if ptr[n] is not None else None for n in names]
+        return L.kda_decode_replay(*args, ctypes.byref(prob), None)
+
+    p = _prob(num_seqs=4, total_tokens=12, max_seqlen=3)
+    assert rep(_prob(num_seqs=4, total_tokens=10)) == B.KDA_ERR_INVALID_ARG   # not N equal windows
+    assert rep(_prob(num_seqs=4, total_tokens=0)) == B.KDA_ERR_INVALID_ARG    # empty windows
+    assert rep(_prob(num_seqs=4, total_tokens=12, d_v=16)) == B.KDA_ERR_UNSUPPORTED
+    for name in ("q", "k", "v", "z", "A", "beta", "state_in"):
+        assert rep(p, **{name: None}) == B.KDA_ERR_INVALID_ARG, name
+    assert rep(p, out=None, state_out=None) == B.KDA_ERR_INVALID_ARG        # nothing to write
+    assert rep(p, state_out=_addr(8) + 8) == B.KDA_ERR_INVALID_ARG          # misaligned
+    assert rep(p, accepted=_addr(7) + 2) == B.KDA_ERR_INVALID_ARG
+    assert rep(p, out=_addr(6)) == B.KDA_ERR_INVALID_ARG                    # out on the snapshot
+    assert rep(p, state_out=_addr(0)) == B.KDA_ERR_INVALID_ARG              # state_out on q
+    assert rep(p, state_out=_addr(7)) == B.KDA_ERR_INVALID_ARG              # state_out on accepted
+    assert rep(p, state_out=_addr(6) + 16) == B.KDA_ERR_INVALID_ARG         # partly on the snapshot
 
 
 def test_workspace_status_rejects_null(L):

@@ -380,3 +380,114 @@ def test_fused_plan_when_forced(monkeypatch):
     prof = B.kda_profile_read()
     B.kda_profile_enable(False)
     assert set(prof) == {"kda_seg_summary_tc", "kda_seg_scan", "kda_chunk_fwd_tc"}
+
+
+# ---------------------------------------------------------------- speculative-decode state replay
+
+def _replay_case(N, L, H, dk, dv, io, seed):
+    """N windows of L drafted tokens (token t of sequence n at row n*L + t) and a snapshot of the
+    size a prefill leaves behind."""
+    inp = I.make_inputs(1, lengths=[L] * N, num_heads=H, d_k=dk, d_v=dv, io_dtype=io, seed=seed)
+    inp["S0"] = inp["S0"] * 25.0
+    return inp
+
+
+def _oracle_replay(inp, accepted=None):
+    return oracle.replay(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["beta"], inp["S0"],
+                         accepted=None if accepted is None else accepted.cpu().numpy())
+
+
+@pytest.mark.parametrize("io", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("dk,dv", [(32, 32), (64, 128), (128, 32), (128, 128)])
+@pytest.mark.parametrize("L", [1, 3, 8, 19])
+def test_replay_small(io, dk, dv, L):
+    """Outputs of the whole window and the state after each accepted prefix (0 and L included),
+    with the snapshot left bit-identical."""
+    N, H = 6, 3
+    inp = _replay_case(N, L, H, dk, dv, io, seed=L * 131 + dk + dv)
+    accepted = torch.tensor([0, L, 1 % (L + 1), L // 2, max(L - 1, 0), (3 * L) // 4], dtype=torch.int32)
+    ref_o, ref_s = _oracle_replay(inp, accepted)
+    d = to_dev(inp)
+    snap = d["S0"].clone()
+    out, s_acc = B.kda_decode_replay(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], d["S0"],
+                                     accepted=accepted.cuda())
+    torch.cuda.synchronize()
+    check(out, ref_o, io, "replay window outputs")
+    check(s_acc, ref_s, io, "replay accepted state")
+    assert torch.equal(d["S0"], snap)
+    assert torch.equal(s_acc[0], snap[0])  # nothing accepted: the snapshot, bit for bit
+
+
+def test_replay_verify_then_commit_in_place():
+    """The serving round: verify the window (outputs only, no state written), then advance the
+    snapshot in place over the accepted prefixes (no outputs)."""
+    N, L, H, dk, dv = 16, 7, 4, 128, 128
+    inp = _replay_case(N, L, H, dk, dv, torch.bfloat16, seed=77)
+    accepted = torch.randint(0, L + 1, (N,), generator=torch.Generator().manual_seed(7), dtype=torch.int32)
+    ref_o, ref_s = _oracle_replay(inp, accepted)
+    d = to_dev(inp)
+    snap = d["S0"].clone()
+    out, none = B.kda_decode_replay(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], d["S0"], want_state=False)
+    assert none is None
+    torch.cuda.synchronize()
+    assert torch.equal(d["S0"], snap)
+    check(out, ref_o, torch.bfloat16, "verify outputs")
+    none, st = B.kda_decode_replay(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], d["S0"],
+                                   accepted=accepted.cuda(), state_out=d["S0"], want_out=False)
+    torch.cuda.synchronize()
+    assert none is None and st.data_ptr() == d["S0"].data_ptr()
+    check(st, ref_s, torch.bfloat16, "committed state")
+    # the outputs do not depend on what is accepted: same bits with and without the counts
+    out2, _ = B.kda_decode_replay(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], snap,
+                                  accepted=accepted.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2)
+
+
+def test_replay_matches_chained_decode_steps():
+    """All accepted: the window equals L chained kda_decode_step calls (different kernels, the same
+    recurrence), outputs and final state within the bf16 tolerance of each other."""
+    N, L, H, dk, dv = 8, 5, 2, 128, 128
+    inp = _replay_case(N, L, H, dk, dv, torch.bfloat16, seed=78)
+    d = to_dev(inp)
+    out, s_all = B.kda_decode_replay(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], d["S0"])
+    st = d["S0"].clone()
+    view = lambda x: x.view(N, L, *x.shape[1:])
+    steps = []
+    for t in range(L):
+        steps.append(B.kda_decode_step(*(view(d[x])[:, t].contiguous() for x in ("q", "k", "v", "z")), d["A"],
+                                       view(d["beta"])[:, t].contiguous(), st))
+    torch.cuda.synchronize()
+    chained = torch.stack(steps, 1).reshape(N * L, H, dv)
+    check(out, _f64(chained), torch.bfloat16, "replay vs chained decode outputs")
+    check(s_all, _f64(st), torch.bfloat16, "replay vs chained decode state")
+
+
+def test_replay_clamps_accepted_counts():
+    N, L, H, dk, dv = 4, 6, 2, 64, 64
+    inp = _replay_case(N, L, H, dk, dv, torch.float32, seed=79)
+    acc = torch.tensor([-3, 0, 6, 100], dtype=torch.int32)
+    _, ref_s = _oracle_replay(inp, acc.clamp(0, L))
+    d = to_dev(inp)
+    _, s_acc = B.kda_decode_replay(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], d["S0"],
+                                   accepted=acc.cuda(), want_out=False)
+    torch.cuda.synchronize()
+    check(s_acc, ref_s, torch.float32, "clamped accepted state")
+
+
+def test_replay_full_size_sampled():
+    """256 sequences x 32 heads, a 7-token window (the draft length the audit's speculative-decoding
+    section trains for), random accepted counts; the oracle checks a sample of 32 sequences."""
+    N, L, H, d_ = 256, 7, 32, 128
+    inp = _replay_case(N, L, H, d_, d_, torch.bfloat16, seed=80)
+    accepted = torch.randint(0, L + 1, (N,), generator=torch.Generator().manual_seed(80), dtype=torch.int32)
+    d = to_dev(inp)
+    out, s_acc = B.kda_decode_replay(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], d["S0"],
+                                     accepted=accepted.cuda())
+    torch.cuda.synchronize()
+    sample = list(range(3, N, 8))
+    rows = torch.cat([torch.arange(n * L, (n + 1) * L) for n in sample])
+    ref_o, ref_s = oracle.replay(inp["q"][rows], inp["k"][rows], inp["v"][rows], inp["z"][rows], inp["A"],
+                                 inp["beta"][rows], inp["S0"][sample], accepted=accepted[sample].numpy())
+    check(out[rows.cuda()], ref_o, torch.bfloat16, "full-size window outputs (sample)")
+    check(s_acc[sample], ref_s, torch.bfloat16, "full-size accepted states (sample)")
