@@ -101,7 +101,8 @@ class ClockSampler:
 
 def src_sha(kernel):
     name = {"kda_gate": "kda_gate.cu", "kda_ut_wy": "kda_ut_wy.cu", "kda_chunk_fwd": "kda_chunk_fwd.cu",
-            "kda_decode_step": "kda_decode.cu", "kda_decode_replay": "kda_replay.cu",
+            "kda_decode_step": "kda_decode.cu", "kda_decode_replay_verify": "kda_replay.cu",
+            "kda_decode_replay_commit": "kda_replay.cu",
             "kda_chunk_fwd_tc": "kda_chunk_tc.cu",
             "kda_seg_summary_tc": "kda_chunk_tc.cu", "kda_seg_scan": "kda_segment_scan.cu",
             "kda_chunk_prep_tc": "kda_prep_tc.cu", "kda_state_summary_tc": "kda_state_tc.cu",
@@ -578,14 +579,14 @@ def bench_replay(B, dev, g, toks, A, state, decode_ms, max_over_ranks, barrier, 
             nbytes = replay_bytes(N, H, dd, dd, int(acc.sum().item()) / reps, 0, N)
         gbs = nbytes / (ms * 1e-3) / 1e9
         res[name] = {"ms": ms, "median_ms": statistics.median(times), "algorithmic_bytes": nbytes, "gbs": gbs,
-                     "frac": gbs / pk["hbm_gbs"]}
+                     "frac": gbs / pk["hbm_gbs"], "traffic": ncu_traffic(f"kda_decode_replay_{name}")}
     round_ms = res["verify"]["ms"] + res["commit"]["ms"]
     return {"workload": f"{N} sequences x {H} heads, d={dd}, {L}-token drafted window, bf16 inputs, fp32 state",
             "kernel": "kda_decode_replay", **res, "round_ms": round_ms,
             "drafted_tokens_per_s": N * L / (round_ms * 1e-3),
             "accepted_tokens_per_s": float(acc.sum().item()) / reps / (round_ms * 1e-3),
             "vs_decode_steps": (L * decode_ms) / round_ms,
-            "traffic": ncu_traffic("kda_decode_replay"), "peak": pk["hbm_gbs"], "peak_source": pk_src,
+            "peak": pk["hbm_gbs"], "peak_source": pk_src,
             "gpu_launches": 2 * reps}
 
 
