@@ -398,6 +398,326 @@ __global__ void __launch_bounds__(kRepThreads, 2) kda_decode_replay_d128_kernel(
     }
 }
 
+// ---------------------------------------------------------------- verify only: the in-window chunk form
+//
+// A verify launch (outputs, no state written) needs only o_1 .. o_L from the snapshot S, so the window
+// is treated as one chunk, with Gamma_t = alpha_1 ... alpha_t (inclusive, per key channel; at most 8
+// tokens, so the accumulated log-decay stays >= 8 g_min and Gamma, 1/Gamma are normal fp32 numbers):
+//     KG = K * Gamma, QG = Q * Gamma, KI = K / Gamma                 (rows = window tokens)
+//     A[t][i] = beta_t KG_t . KI_i (i < t),  P[t][i] = QG_t . KI_i (i <= t)
+//     [W0; Y0] = [KG; QG] S                                            (the only d_k x d_v work)
+//     U = (I + A)^-1 diag(beta) (V - W0),   O = Y0 + P U
+// which is the recurrence substituted token by token (u_t needs the state decayed to t and read
+// along k_t; every earlier write k_i u_i^T reaches it scaled by Gamma_t / Gamma_i).  Per element of S
+// that is two multiply-adds per token instead of four, and no barrier per token.  [KG; QG] S is a
+// 16 x 128 x 128 product per (sequence, head): warp w computes value columns 16w .. 16w + 15 with
+// mma.sync m16n8k8 tf32, every operand split into a tf32 pair (x = hi + lo, products hi.hi + hi.lo +
+// lo.hi with fp32 accumulation: about fp32 accuracy).  The snapshot goes from shared memory straight
+// into B-fragment registers (rows of the staged copy XOR-swizzled in 16-byte pieces so those loads
+// are free of bank conflicts), which frees the copy buffer for the next unit early.
+struct RepVLayout {
+    static constexpr int kRow = kRepD + 4;                              // padded fp32 row of the token-row tiles
+    static constexpr int kStage = 0;                                    // fp32 [128][128], swizzled
+    static constexpr int kRaw = kStage + kRepD * kRepD * 4;             // bf16 [token][q, k, z, v][128]
+    static constexpr int kRawBeta = kRaw + kRepGroup * 4 * kRepD * 2;   // fp32 [token]
+    static constexpr int kKQhi = kRawBeta + kRepGroup * 4;              // tf32 [16][kRow]: KG rows 0..7, QG rows 8..15
+    static constexpr int kKQlo = kKQhi + 16 * kRow * 4;
+    static constexpr int kKI = kKQlo + 16 * kRow * 4;                   // fp32 [token][kRow]
+    static constexpr int kV = kKI + kRepGroup * kRow * 4;               // fp32 [token][128]
+    static constexpr int kWY = kV + kRepGroup * kRepD * 4;              // fp32 [16][kRow]: W0 rows 0..7, Y0 rows 8..15;
+                                                                        // before that, the base-2 log-decays [token][128]
+    static constexpr int kGram = kWY + 16 * kRow * 4;                   // fp32 [warp][16][8]: partial [KG; QG] KI^T
+    static constexpr int kGsum = kGram + kRepWarps * 16 * 8 * 4;        // fp32 [16][8]: its sum
+    static constexpr int kT = kGsum + 16 * 8 * 4;                       // fp32 [8][8]: (I + A)^-1 diag(beta)
+    static constexpr int kBeta = kT + 64 * 4;
+    static constexpr int kBytes = kBeta + kRepGroup * 4;
+};
+static_assert(RepVLayout::kKQhi % 16 == 0 && RepVLayout::kWY % 16 == 0 && RepVLayout::kGram % 16 == 0, "alignment");
+static_assert(2 * (RepVLayout::kBytes + 1024) <= 228 * 1024, "two CTAs per SM");
+
+// word offset of element (c, j) of the staged snapshot: 16-byte piece j/4 of row c moves to
+// (j/4) xor 2 (c mod 4), so that the B fragments (four rows x eight columns per warp load) hit 32
+// different banks
+__device__ __forceinline__ int vstage_word(int c, int j) { return c * kRepD + ((((j >> 2) ^ ((c & 3) << 1)) << 2) | (j & 3)); }
+
+__device__ __forceinline__ uint32_t to_tf32(float x)
+{
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// acc += (hi + lo of A) (b0, b1 split into a tf32 pair), dropping lo.lo
+__device__ __forceinline__ void mma_tf32x3(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4], float b0, float b1)
+{
+    const uint32_t bh0 = to_tf32(b0), bh1 = to_tf32(b1);
+    const uint32_t bl0 = to_tf32(b0 - __uint_as_float(bh0)), bl1 = to_tf32(b1 - __uint_as_float(bh1));
+    mma_tf32(d, al, bh0, bh1);
+    mma_tf32(d, ah, bl0, bl1);
+    mma_tf32(d, ah, bh0, bh1);
+}
+
+__global__ void __launch_bounds__(kRepThreads, 2) kda_decode_replay_verify_d128_kernel(ReplayArgs a)
+{
+    constexpr int D = kRepD;
+    constexpr int R = RepVLayout::kRow;
+    using TIO = __nv_bfloat16;
+    extern __shared__ __align__(16) unsigned char smem[];
+    float* stage = reinterpret_cast<float*>(smem + RepVLayout::kStage);
+    unsigned char* raw = smem + RepVLayout::kRaw;
+    float* raw_beta = reinterpret_cast<float*>(smem + RepVLayout::kRawBeta);
+    float* s_kqhi = reinterpret_cast<float*>(smem + RepVLayout::kKQhi);
+    float* s_kqlo = reinterpret_cast<float*>(smem + RepVLayout::kKQlo);
+    float* s_ki = reinterpret_cast<float*>(smem + RepVLayout::kKI);
+    float* s_v = reinterpret_cast<float*>(smem + RepVLayout::kV);
+    float* s_wy = reinterpret_cast<float*>(smem + RepVLayout::kWY);
+    float* s_g2 = s_wy;  // the log-decays live there until the products overwrite them
+    float* s_gram = reinterpret_cast<float*>(smem + RepVLayout::kGram);
+    float* s_gsum = reinterpret_cast<float*>(smem + RepVLayout::kGsum);
+    float* s_T = reinterpret_cast<float*>(smem + RepVLayout::kT);
+    float* s_beta = reinterpret_cast<float*>(smem + RepVLayout::kBeta);
+
+    const int tid = threadIdx.x;
+    const int w = tid >> 5;
+    const int l = tid & 31;
+    const int g8 = l >> 2;  // mma fragment row / column group
+    const int t4 = l & 3;   // mma fragment thread in group
+    const int L = a.L;
+    const int units = a.N * a.H;
+    const TIO* qp = static_cast<const TIO*>(a.q);
+    const TIO* kp = static_cast<const TIO*>(a.k);
+    const TIO* vp = static_cast<const TIO*>(a.v);
+    const TIO* zp = static_cast<const TIO*>(a.z);
+    TIO* op = static_cast<TIO*>(a.out);
+    constexpr float kLog2e = 1.4426950408889634f;
+    const float gm2 = kLog2e * a.g_min;
+
+    auto prefetch = [&](int unit) {
+        const int n = unit / a.H;
+        const int h = unit - n * a.H;
+        const float* S = a.state_in + (int64_t)unit * D * D;
+#pragma unroll
+        for (int i = 0; i < D * D / 4 / kRepThreads; ++i) {
+            const int e4 = tid + kRepThreads * i;  // 16-byte piece e4 % 32 of row e4 / 32
+            const int c = e4 >> 5;
+            cp_async16(stage + c * D + (((e4 & 31) ^ ((c & 3) << 1)) << 2), S + 4 * e4);
+        }
+        constexpr int CH = D * 2 / 16;
+        const int64_t tok0 = (int64_t)n * L;
+        for (int e = tid; e < L * 4 * CH; e += kRepThreads) {
+            const int j = e / (4 * CH);
+            const int rem = e - j * 4 * CH;
+            const int which = rem / CH;
+            const int ch = rem - which * CH;
+            const TIO* base = which == 0 ? qp : which == 1 ? kp : which == 2 ? zp : vp;
+            cp_async16(raw + (size_t)e * 16, base + ((tok0 + j) * a.H + h) * D + ch * 8);
+        }
+        if (tid < L) cp_async4(raw_beta + tid, a.beta + (tok0 + tid) * a.H + h);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    auto raw_at = [&](int t, int which, int c) {
+        return __bfloat162float(reinterpret_cast<const TIO*>(raw + (t * 4 + which) * D * 2)[c]);
+    };
+
+    int unit = blockIdx.x;
+    if (unit >= units) return;
+    prefetch(unit);
+    for (; unit < units; unit += gridDim.x) {
+        const int next = unit + gridDim.x;
+        const int n = unit / a.H;
+        const int h = unit - n * a.H;
+        const float xs = -kLog2e * expf(a.A[h]);  // exp2(xs |z|) = exp(-exp(A_h) |z|)
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        __syncthreads();  // (1) this unit's snapshot and tokens are in shared memory
+
+        // the snapshot columns 16w .. 16w + 15 as B fragments: [k step][n tile][b0, b1]
+        float bf[D / 8][2][2];
+#pragma unroll
+        for (int ks = 0; ks < D / 8; ++ks)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int j = 16 * w + 8 * nt + g8;
+                bf[ks][nt][0] = stage[vstage_word(8 * ks + t4, j)];
+                bf[ks][nt][1] = stage[vstage_word(8 * ks + t4 + 4, j)];
+            }
+        // gate of every (token, key channel) in base 2, and v, over all threads
+#pragma unroll
+        for (int m = 0; m < kRepGroup * D / kRepThreads; ++m) {
+            const int e = tid + kRepThreads * m;
+            const int t = e / D;
+            const int c = e - t * D;
+            if (t < L) {
+                const float z = raw_at(t, 2, c);
+                const float ez = ex2_approx(xs * fabsf(z));  // exp(-exp(A_h) |z|)
+                const float r = rcp_approx(1.f + ez);
+                s_g2[e] = gm2 * ((z >= 0.f) ? r : ez * r);   // log2 of alpha: g_min sigmoid(exp(A_h) z) / ln 2
+                s_v[e] = raw_at(t, 3, c);
+            }
+        }
+        if (tid < L) s_beta[tid] = raw_beta[tid];
+        __syncthreads();
+        {
+            // key channel c, tokens 4 half .. 4 half + 3: cumulative decay and the scaled rows
+            const int c = tid & (D - 1);
+            const int t0 = (tid >> 7) * 4;
+            float G2 = 0.f;
+            for (int t = 0; t < t0 && t < L; ++t) G2 += s_g2[t * D + c];
+#pragma unroll
+            for (int t = t0; t < t0 + 4; ++t) {
+                float kg = 0.f, qg = 0.f, ki = 0.f;
+                if (t < L) {
+                    G2 += s_g2[t * D + c];
+                    const float gam = ex2_approx(G2), igam = ex2_approx(-G2);
+                    const float kc = raw_at(t, 1, c);
+                    kg = kc * gam;
+                    qg = raw_at(t, 0, c) * gam;
+                    ki = kc * igam;
+                }
+                const uint32_t kh = to_tf32(kg), qh = to_tf32(qg);
+                s_kqhi[t * R + c] = __uint_as_float(kh);
+                s_kqlo[t * R + c] = __uint_as_float(to_tf32(kg - __uint_as_float(kh)));
+                s_kqhi[(8 + t) * R + c] = __uint_as_float(qh);
+                s_kqlo[(8 + t) * R + c] = __uint_as_float(to_tf32(qg - __uint_as_float(qh)));
+                s_ki[t * R + c] = ki;
+            }
+        }
+        __syncthreads();  // (2) staged; the copy buffers are free for the next unit
+        if (next < units) prefetch(next);
+
+        // [W0; Y0] = [KG; QG] S for value columns 16w .. 16w + 15, and this warp's two k steps of
+        // [KG; QG] KI^T (the in-window Gram block: A and P)
+        float acc[2][4], gacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < D / 8; ++ks) {
+            const int k0 = 8 * ks + t4;
+            const uint32_t ah[4] = {__float_as_uint(s_kqhi[g8 * R + k0]), __float_as_uint(s_kqhi[(g8 + 8) * R + k0]),
+                                    __float_as_uint(s_kqhi[g8 * R + k0 + 4]), __float_as_uint(s_kqhi[(g8 + 8) * R + k0 + 4])};
+            const uint32_t al[4] = {__float_as_uint(s_kqlo[g8 * R + k0]), __float_as_uint(s_kqlo[(g8 + 8) * R + k0]),
+                                    __float_as_uint(s_kqlo[g8 * R + k0 + 4]), __float_as_uint(s_kqlo[(g8 + 8) * R + k0 + 4])};
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) mma_tf32x3(acc[nt], ah, al, bf[ks][nt][0], bf[ks][nt][1]);
+            if ((ks >> 1) == w) mma_tf32x3(gacc, ah, al, s_ki[g8 * R + k0], s_ki[g8 * R + k0 + 4]);
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int j = 16 * w + 8 * nt + 2 * t4;
+            *reinterpret_cast<float2*>(s_wy + g8 * R + j) = make_float2(acc[nt][0], acc[nt][1]);
+            *reinterpret_cast<float2*>(s_wy + (g8 + 8) * R + j) = make_float2(acc[nt][2], acc[nt][3]);
+        }
+        *reinterpret_cast<float2*>(s_gram + (w * 16 + g8) * 8 + 2 * t4) = make_float2(gacc[0], gacc[1]);
+        *reinterpret_cast<float2*>(s_gram + (w * 16 + g8 + 8) * 8 + 2 * t4) = make_float2(gacc[2], gacc[3]);
+        __syncthreads();  // (3) W0, Y0 and the partial Gram blocks complete
+
+        if (w == 0) {
+            // Gram block [KG; QG] KI^T = sum of the eight warps' k slices
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int e = l + 32 * m;
+                float x = 0.f;
+#pragma unroll
+                for (int ww = 0; ww < kRepWarps; ++ww) x += s_gram[ww * 128 + e];
+                s_gsum[e] = x;
+            }
+            __syncwarp();
+            if (l < L) {
+                // column l of T = (I + A)^-1 with A[t][m] = beta_t KG_t . KI_m (m < t), then scaled by beta_l
+                float col[kRepGroup];
+#pragma unroll
+                for (int t = 0; t < kRepGroup; ++t) {
+                    float x = (t == l) ? 1.f : 0.f;
+                    if (t > l && t < L) {
+                        float sum = 0.f;
+#pragma unroll
+                        for (int m = 0; m < t; ++m)
+                            if (m >= l) sum += s_gsum[t * 8 + m] * col[m];
+                        x = -s_beta[t] * sum;
+                    }
+                    col[t] = x;
+                }
+                const float bl = s_beta[l];
+#pragma unroll
+                for (int t = 0; t < kRepGroup; ++t)
+                    if (t < L) s_T[t * 8 + l] = col[t] * bl;
+            }
+        }
+        __syncthreads();  // (4) T' complete
+
+        {
+            // U = T' (V - W0) and O = Y0 + P U (P[t][i] = QG_t . KI_i, i <= t) for this warp's value
+            // columns, as two more split-tf32 products with M = tokens (rows 8..15 zero), K = 8 tokens.
+            // Entries outside t < L, i <= t are zeroed so that stale rows never enter.
+            const bool row_ok = g8 < L;
+            const float tA0 = (row_ok && t4 <= g8) ? s_T[g8 * 8 + t4] : 0.f;
+            const float tA2 = (row_ok && t4 + 4 <= g8) ? s_T[g8 * 8 + t4 + 4] : 0.f;
+            const float pA0 = (row_ok && t4 <= g8) ? s_gsum[(8 + g8) * 8 + t4] : 0.f;
+            const float pA2 = (row_ok && t4 + 4 <= g8) ? s_gsum[(8 + g8) * 8 + t4 + 4] : 0.f;
+            uint32_t th[4] = {to_tf32(tA0), 0u, to_tf32(tA2), 0u};
+            uint32_t tl[4] = {to_tf32(tA0 - __uint_as_float(th[0])), 0u, to_tf32(tA2 - __uint_as_float(th[2])), 0u};
+            uint32_t ph[4] = {to_tf32(pA0), 0u, to_tf32(pA2), 0u};
+            uint32_t pl[4] = {to_tf32(pA0 - __uint_as_float(ph[0])), 0u, to_tf32(pA2 - __uint_as_float(ph[2])), 0u};
+            float* s_u = s_kqhi;  // [token][kRow]; the operand tiles are no longer read
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int jb = 16 * w + 8 * nt + g8;  // B-fragment column
+                const float x0 = (t4 < L) ? s_v[t4 * D + jb] - s_wy[t4 * R + jb] : 0.f;
+                const float x1 = (t4 + 4 < L) ? s_v[(t4 + 4) * D + jb] - s_wy[(t4 + 4) * R + jb] : 0.f;
+                float u4[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_tf32x3(u4, th, tl, x0, x1);
+                const int jd = 16 * w + 8 * nt + 2 * t4;  // D-fragment columns jd, jd + 1
+                *reinterpret_cast<float2*>(s_u + g8 * R + jd) = make_float2(u4[0], u4[1]);
+            }
+            __syncwarp();
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int jb = 16 * w + 8 * nt + g8;
+                const int jd = 16 * w + 8 * nt + 2 * t4;
+                const float2 y = *reinterpret_cast<const float2*>(s_wy + (8 + g8) * R + jd);
+                float o4[4] = {y.x, y.y, 0.f, 0.f};
+                mma_tf32x3(o4, ph, pl, s_u[t4 * R + jb], s_u[(t4 + 4) * R + jb]);
+                if (row_ok)
+                    *reinterpret_cast<__nv_bfloat162*>(op + (((int64_t)n * L + g8) * a.H + h) * D + jd) =
+                        __floats2bfloat162_rn(o4[0], o4[1]);
+            }
+        }
+    }
+}
+
+static cudaError_t launch_replay_verify_d128(const ReplayArgs& a, cudaStream_t s)
+{
+    cudaError_t e = cudaFuncSetAttribute(kda_decode_replay_verify_d128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         RepVLayout::kBytes);
+    if (e != cudaSuccess) return e;
+    const int64_t units = (int64_t)a.N * a.H;
+    const unsigned grid = (unsigned)(units < 2LL * sm_count_of_current_device() ? units : 2LL * sm_count_of_current_device());
+    kda_decode_replay_verify_d128_kernel<<<grid, kRepThreads, RepVLayout::kBytes, s>>>(a);
+    return cudaGetLastError();
+}
+
 template <bool OUT>
 static cudaError_t launch_replay_d128(const ReplayArgs& a, cudaStream_t s)
 {
@@ -429,8 +749,10 @@ static cudaError_t launch_replay_out(const ReplayArgs& a, int dk, int dv, cudaSt
 cudaError_t launch_replay(const ReplayArgs& a, int dk, int dv, kda_dtype_t dt, cudaStream_t s)
 {
     const bool out = a.out != nullptr;
-    if (dt == KDA_BF16 && dk == kRepD && dv == kRepD && a.L <= kRepGroup)
+    if (dt == KDA_BF16 && dk == kRepD && dv == kRepD && a.L <= kRepGroup) {
+        if (out && a.state_out == nullptr) return launch_replay_verify_d128(a, s);
         return out ? launch_replay_d128<true>(a, s) : launch_replay_d128<false>(a, s);
+    }
     if (dt == KDA_BF16)
         return out ? launch_replay_out<__nv_bfloat16, true>(a, dk, dv, s) : launch_replay_out<__nv_bfloat16, false>(a, dk, dv, s);
     return out ? launch_replay_out<float, true>(a, dk, dv, s) : launch_replay_out<float, false>(a, dk, dv, s);

@@ -437,11 +437,14 @@ def test_replay_verify_then_commit_in_place():
     torch.cuda.synchronize()
     assert none is None and st.data_ptr() == d["S0"].data_ptr()
     check(st, ref_s, torch.bfloat16, "committed state")
-    # the outputs do not depend on what is accepted: same bits with and without the counts
+    # the outputs do not depend on what is accepted: same bits with and without the counts (one
+    # kernel: both calls also write a state), and the verify-only kernel within the tolerance
     out2, _ = B.kda_decode_replay(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], snap,
                                   accepted=accepted.cuda())
+    out3, _ = B.kda_decode_replay(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], snap)
     torch.cuda.synchronize()
-    assert torch.equal(out, out2)
+    assert torch.equal(out2, out3)
+    check(out, _f64(out2), torch.bfloat16, "verify-only vs outputs written with a state")
 
 
 def test_replay_matches_chained_decode_steps():
@@ -461,6 +464,26 @@ def test_replay_matches_chained_decode_steps():
     chained = torch.stack(steps, 1).reshape(N * L, H, dv)
     check(out, _f64(chained), torch.bfloat16, "replay vs chained decode outputs")
     check(s_all, _f64(st), torch.bfloat16, "replay vs chained decode state")
+
+
+@pytest.mark.parametrize("L", [1, 2, 5, 8])
+def test_replay_verify_only(L):
+    """Outputs only (no state written): bf16 with d = 128 takes the in-window chunk form; 320
+    (sequence, head) units, more than the persistent grid, so CTAs walk several units."""
+    N, H, dk, dv = 40, 8, 128, 128
+    inp = _replay_case(N, L, H, dk, dv, torch.bfloat16, seed=90 + L)
+    ref_o, _ = _oracle_replay(inp)
+    d = to_dev(inp)
+    snap = d["S0"].clone()
+    out, none = B.kda_decode_replay(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], d["S0"], want_state=False)
+    torch.cuda.synchronize()
+    assert none is None
+    assert torch.equal(d["S0"], snap)
+    check(out, ref_o, torch.bfloat16, f"verify outputs, L={L}")
+    # the same outputs as the recurrence kernel (which runs when a state is also written)
+    out_rec, _ = B.kda_decode_replay(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], d["S0"])
+    torch.cuda.synchronize()
+    check(out, _f64(out_rec), torch.bfloat16, "chunk-form verify vs recurrence")
 
 
 def test_replay_clamps_accepted_counts():
@@ -491,3 +514,7 @@ def test_replay_full_size_sampled():
                                  inp["beta"][rows], inp["S0"][sample], accepted=accepted[sample].numpy())
     check(out[rows.cuda()], ref_o, torch.bfloat16, "full-size window outputs (sample)")
     check(s_acc[sample], ref_s, torch.bfloat16, "full-size accepted states (sample)")
+    # the verify launch alone (outputs, no state), as a speculation round issues it
+    out_v, _ = B.kda_decode_replay(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], d["S0"], want_state=False)
+    torch.cuda.synchronize()
+    check(out_v[rows.cuda()], ref_o, torch.bfloat16, "full-size verify outputs (sample)")
