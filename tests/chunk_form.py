@@ -67,3 +67,22 @@ def chunk_forward(q, k, v, g, beta, S0=None, cu_seqlens=None, C=16, keep=False):
     if keep:
         return out, Sf, inter
     return out, Sf
+
+
+def window_verify(q, k, v, g, beta, S0, dtype=np.float64):
+    """Outputs of a window of L tokens read from the state S0 as ONE chunk, in the form the verify
+    half of the speculative-decode replay uses: Gamma and 1/Gamma formed separately (reciprocal
+    rescaling), [W0; Y0] = [K*Gamma; Q*Gamma] S0, A = beta (K*Gamma)(K/Gamma)^T strictly lower,
+    P = (Q*Gamma)(K/Gamma)^T lower inclusive, U = (I + A)^-1 diag(beta) (V - W0), O = Y0 + P U.
+
+    One sequence and head: q, k, g [L, dk]; v [L, dv]; beta [L]; S0 [dk, dv].  ``dtype`` sets the
+    arithmetic (float32 mirrors the kernel's range: with L <= 8 and g >= -5, Gamma >= e^-40)."""
+    q, k, v, g, beta, S0 = (np.asarray(x, dtype=dtype) for x in (q, k, v, g, beta, S0))
+    L = k.shape[0]
+    G = np.cumsum(g, axis=0, dtype=dtype)
+    KG, QG, KI = k * np.exp(G), q * np.exp(G), k * np.exp(-G)
+    A = np.tril(beta[:, None] * (KG @ KI.T), -1)
+    P = np.tril(QG @ KI.T)
+    Tp = np.linalg.inv(np.eye(L, dtype=dtype) + A) * beta[None, :]
+    U = Tp @ (v - KG @ S0)
+    return QG @ S0 + P @ U

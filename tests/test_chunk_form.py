@@ -42,3 +42,30 @@ def test_chunk_form_extreme_decay_stays_finite():
     assert np.isfinite(o).all()
     np.testing.assert_allclose(o, o_ref, atol=1e-12)
     np.testing.assert_allclose(s, s_ref, atol=1e-12)
+
+
+@pytest.mark.parametrize("L,floor", [(1, False), (5, False), (8, False), (8, True)])
+def test_window_verify_form_matches_token_oracle(L, floor):
+    """The one-chunk window form of the replay's verify (reciprocal rescaling) equals the token
+    oracle in fp64, and stays within fp32 rounding of it in fp32 even with every decay at the
+    floor (the window then spans e^-40)."""
+    from chunk_form import window_verify
+    rng = np.random.default_rng(100 + L + floor)
+    H, dk, dv = 1, 16, 8
+    q = rng.normal(size=(L, H, dk))
+    k = rng.normal(size=(L, H, dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    v = rng.normal(size=(L, H, dv))
+    z = np.full((L, H, dk), 60.0) if floor else rng.normal(size=(L, H, dk))
+    A = np.zeros(H) if floor else rng.normal(size=H) * 0.5
+    b = 1 / (1 + np.exp(-rng.normal(size=(L, H))))
+    S0 = rng.normal(size=(1, H, dk, dv))
+    g, _ = oracle.gate(z, A)
+    o_ref, _ = oracle.forward(q, k, v, z, A, b, S0=S0)
+    scale = max(1.0, np.abs(o_ref).max())
+    o64 = window_verify(q[:, 0], k[:, 0], v[:, 0], g[:, 0], b[:, 0], S0[0, 0])
+    np.testing.assert_allclose(o64, o_ref[:, 0], rtol=0, atol=1e-12 * scale)
+    o32 = window_verify(q[:, 0], k[:, 0], v[:, 0], g[:, 0], b[:, 0], S0[0, 0], dtype=np.float32)
+    assert np.isfinite(o32).all()
+    np.testing.assert_allclose(o32, o_ref[:, 0], rtol=0, atol=2e-5 * scale)
