@@ -22,6 +22,9 @@ What is computed (see the C file for the step-by-step statement):
 * ``replay``      -- speculative-decode state replay: a window of drafted tokens per sequence read
                      from a snapshot that is left untouched, with the state kept after the
                      accepted prefix only (what ``kda_decode_replay`` computes).
+* ``prologue``    -- short convolution, Swish and (q, k) regularised L2 normalisation of the
+                     projections (what ``kda_prologue`` computes), numpy in float64.
+* ``epilogue``    -- head-wise RMSNorm and sigmoid output gate (what ``kda_epilogue`` computes).
 """
 from __future__ import annotations
 
@@ -228,3 +231,62 @@ def replay(q, k, v, z, A, beta, S, accepted=None, g_min: float = -5.0, threads: 
     _, S_acc = forward(q[rows], k[rows], v[rows], z[rows], A, beta[rows], S0=S, cu_seqlens=cu_acc, g_min=g_min,
                        threads=threads, want_out=False)
     return out, S_acc
+
+
+def _sigmoid(x):
+    """Logistic function in the overflow-free form for both signs."""
+    e = np.exp(-np.abs(x))
+    return np.where(x >= 0, 1.0 / (1.0 + e), e / (1.0 + e))
+
+
+def _seq_index(T: int, cu) -> np.ndarray:
+    """Sequence start of every token (tokens of empty sequences do not exist)."""
+    cu = _cu(cu, T)
+    start = np.zeros(T, dtype=np.int64)
+    for n in range(len(cu) - 1):
+        start[cu[n]:cu[n + 1]] = cu[n]
+    return start
+
+
+def prologue(x, w, cu_seqlens=None, normalise: bool = True, eps: float = 1e-6):
+    """The per-head preparation of q, k (``normalise``) or v from their projections ("Kimi K3: the
+    paper and proofs side by side", section 2.1.1, "Preparing the queries, keys, values, and decay";
+    "Kimi K3: architecture, derivations and a pinned-source audit", section 4.3):
+
+        y_t = sum_{i < K} w[h, c, i] x_{t-i}     causal depthwise short convolution, x = 0 before
+                                                 the sequence start
+        y_t = y_t * sigmoid(y_t)                 Swish
+        y_t = y_t / sqrt(sum_c y_t^2 + eps)      regularised L2 normalisation (q and k only)
+
+    x: [T, H, d]; w: [H, d, K] (w[..., 0] weighs the current token); cu_seqlens: [N+1] or None.
+    Returns float64 [T, H, d]."""
+    x = _f64(x)
+    w = _f64(w)
+    T, H, d = x.shape
+    K = w.shape[2]
+    start = _seq_index(T, cu_seqlens)
+    y = np.zeros_like(x)
+    for i in range(K):
+        src = np.arange(T) - i
+        ok = src >= start
+        xs = np.where(ok[:, None, None], x[np.maximum(src, 0)], 0.0)
+        y += xs * w[None, :, :, i]
+    y = y * _sigmoid(y)
+    if normalise:
+        y = y / np.sqrt((y * y).sum(-1, keepdims=True) + eps)
+    return y
+
+
+def epilogue(o, gate, weight, eps: float):
+    """Head-wise RMSNorm of the recurrence output followed by the sigmoid output gate ("Kimi K3:
+    architecture, derivations and a pinned-source audit", section 4.3; the gate of Equation 6 in
+    "Kimi K3: the paper and proofs side by side", section 2.1.1):
+
+        y = o / sqrt(mean_c o^2 + eps) * weight * sigmoid(gate)
+
+    o, gate: [T, H, d_v]; weight: [d_v] (shared by the heads).  Returns float64 [T, H, d_v]."""
+    o = _f64(o)
+    gate = _f64(gate)
+    weight = _f64(weight)
+    rms = np.sqrt((o * o).mean(-1, keepdims=True) + eps)
+    return o / rms * weight * _sigmoid(gate)

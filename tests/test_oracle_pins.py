@@ -420,3 +420,62 @@ def test_replay_outputs_do_not_depend_on_acceptance():
     np.testing.assert_allclose(s_all, s_fwd, rtol=1e-13, atol=1e-13)
     with pytest.raises(ValueError):
         oracle.replay(q, k, v, z, A, b, S, accepted=[1, 6, 0])
+
+
+# ---------------------------------------------------------------- layer prologue / epilogue
+
+def test_prologue_regularised_l2_norm_facts():
+    """The pages' statements about the regularised L2 normalisation: the result has norm strictly
+    below one, and a zero vector stays zero."""
+    rng = np.random.default_rng(50)
+    x = rng.normal(size=(20, 2, 8)) * np.logspace(-3, 2, 20)[:, None, None]
+    w = np.zeros((2, 8, 1))
+    w[..., 0] = 1.0
+    y = oracle.prologue(x, w)
+    n = np.linalg.norm(y, axis=-1)
+    assert np.all(n < 1.0) and n.max() > 0.999  # large vectors approach one from below
+    z = oracle.prologue(np.zeros((3, 1, 4)), w[:1, :4])
+    np.testing.assert_array_equal(z, 0.0)
+
+
+def test_prologue_swish_values_and_causal_shift():
+    """Swish at printed points (0, +-1) through an identity tap; a one-token shift tap reads the
+    previous token of the same sequence and zero at every sequence start."""
+    x = np.array([0.0, 1.0, -1.0, 2.0, 3.0, -4.0]).reshape(6, 1, 1)
+    ident = np.array([1.0, 0.0]).reshape(1, 1, 2)
+    y = oracle.prologue(x, ident, normalise=False)[:, 0, 0]
+    np.testing.assert_allclose(y[:3], [0.0, 0.7310585786300049, -0.2689414213699951], rtol=1e-14, atol=1e-15)
+    shift = np.array([0.0, 1.0]).reshape(1, 1, 2)
+    cu = np.array([0, 2, 2, 6])  # sequences of 2, 0 and 4 tokens
+    ys = oracle.prologue(x, shift, cu_seqlens=cu, normalise=False)[:, 0, 0]
+    swish = lambda a: a / (1 + np.exp(-a))
+    np.testing.assert_allclose(ys, [0.0, swish(0.0), 0.0, swish(-1.0), swish(2.0), swish(3.0)], rtol=1e-14, atol=1e-15)
+
+
+def test_prologue_taps_add_linearly_before_the_activation():
+    """Two taps equal the sum of the one-tap convolutions before Swish (checked through the
+    activation's inverse-free form: with normalise off, y = s * sigmoid(s) where s is the sum)."""
+    rng = np.random.default_rng(51)
+    x = rng.normal(size=(9, 1, 3))
+    w = rng.normal(size=(1, 3, 3))
+    y = oracle.prologue(x, w, normalise=False)
+    s = w[None, :, :, 0] * x
+    s[1:] += w[None, :, :, 1] * x[:-1]
+    s[2:] += w[None, :, :, 2] * x[:-2]
+    np.testing.assert_allclose(y, s / (1 + np.exp(-s)), rtol=1e-13, atol=1e-15)
+
+
+def test_epilogue_closed_forms():
+    """RMSNorm of a constant row is its sign (up to eps); a zero gate halves; the output does not
+    depend on the scale of o (eps aside); the normalised row has unit RMS."""
+    eps = 1e-6
+    o = np.full((1, 1, 8), -3.0)
+    y = oracle.epilogue(o, np.zeros((1, 1, 8)), np.ones(8), eps)
+    np.testing.assert_allclose(y, -0.5 / np.sqrt(1 + eps / 9.0), rtol=1e-14)
+    rng = np.random.default_rng(52)
+    o = rng.normal(size=(5, 2, 16))
+    g = rng.normal(size=(5, 2, 16))
+    wt = rng.normal(size=16)
+    np.testing.assert_allclose(oracle.epilogue(7.5 * o, g, wt, 0.0), oracle.epilogue(o, g, wt, 0.0), rtol=1e-13)
+    y = oracle.epilogue(o, np.full_like(g, 40.0), np.ones(16), 0.0)
+    np.testing.assert_allclose(np.sqrt((y * y).mean(-1)), 1.0, rtol=1e-12)
