@@ -7,7 +7,8 @@ Prints ONE JSON line.  `value` is prefill throughput in million tokens per secon
 16 heads) with inputs resident in HBM, timed with CUDA events on the launching stream; L2 is
 flushed (a 512 MiB write) before every timed step because the workload's 86 MB fit in L2.
 `decode` reports the decode step's state bandwidth, and under `replay` the speculative-decode round
-(verify a 7-token drafted window from the snapshot, then commit the accepted prefix in place).  `e2e` repeats the prefill through the same
+(verify a 7-token drafted window from the snapshot, then commit the accepted prefix in place);
+`layer` times the layer prologue and epilogue kernels at the prefill shape.  `e2e` repeats the prefill through the same
 public call with pinned host buffers, host<->device copies inside the timed region.  `roofline`
 is for the kernel with the largest device time, measured live with per-launch CUDA events.
 `cpu_baseline` times the fp64 oracle on the host cores on a bounded sample of the same workload.
@@ -102,7 +103,8 @@ class ClockSampler:
 def src_sha(kernel):
     name = {"kda_gate": "kda_gate.cu", "kda_ut_wy": "kda_ut_wy.cu", "kda_chunk_fwd": "kda_chunk_fwd.cu",
             "kda_decode_step": "kda_decode.cu", "kda_decode_replay_verify": "kda_replay.cu",
-            "kda_decode_replay_commit": "kda_replay.cu",
+            "kda_decode_replay_commit": "kda_replay.cu", "kda_prologue": "kda_layer.cu",
+            "kda_epilogue": "kda_layer.cu",
             "kda_chunk_fwd_tc": "kda_chunk_tc.cu",
             "kda_seg_summary_tc": "kda_chunk_tc.cu", "kda_seg_scan": "kda_segment_scan.cu",
             "kda_chunk_prep_tc": "kda_prep_tc.cu", "kda_state_summary_tc": "kda_state_tc.cu",
@@ -214,6 +216,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-replay", action="store_true", help="skip the speculative-decode replay leg")
+    ap.add_argument("--no-layer", action="store_true", help="skip the layer prologue / epilogue leg")
     ap.add_argument("--no-shapes", action="store_true", help="skip the varlen and long-context prefill shapes")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -383,6 +386,10 @@ def main():
     if not args.no_decode:
         decode = bench_decode(args, B, I, dev, stream, max_over_ranks, barrier, pk, pk_src)
 
+    # ---- layer prologue / epilogue around the recurrence (same shape, L2 flushed before each launch)
+    layer = None if args.no_layer else bench_layer(B, dev, stream, flush, T, H, dk, dv, max_over_ranks, barrier, pk,
+                                                   pk_src)
+
     # ---- e2e through the public call with pinned host buffers
     e2e = bench_e2e(args, B, inp, dev, stream, max_over_ranks, barrier, world)
 
@@ -399,7 +406,7 @@ def main():
                    "arithmetic": "bf16 tensor-core products (split hi/lo where precision needs it) with fp32 "
                                  "accumulation; fp32 state",
                    "l2": "flushed by a 512 MiB write before every timed step"},
-        "step_stats": step_stats, "roofline": roofline, "tensor": tensor, "decode": decode,
+        "step_stats": step_stats, "roofline": roofline, "tensor": tensor, "decode": decode, "layer": layer,
         "cpu_baseline": cpu, "e2e": e2e, "shapes": shapes, "gpu_launches": launches, "clocks": clk,
     }
     if rank == 0:
@@ -523,6 +530,52 @@ def bench_decode(args, B, I, dev, stream, max_over_ranks, barrier, pk, pk_src):
                          "traffic": ncu_traffic("kda_decode_step"), "peak_source": pk_src,
                          "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": kavg},
             "gpu_launches": kn, "replay": replay}
+
+
+def bench_layer(B, dev, stream, flush, T, H, dk, dv, max_over_ranks, barrier, pk, pk_src, reps=20, conv_width=4):
+    """The KDA layer's prologue (short convolution, Swish, q/k L2 norm of the three projections) and
+    epilogue (head-wise RMSNorm and sigmoid output gate) at the prefill workload's shape, bf16, each
+    launch timed with CUDA events after an L2 flush."""
+    import torch
+    g = torch.Generator(device=dev).manual_seed(6)
+    x = [torch.randn(T, H, d, generator=g, device=dev).to(torch.bfloat16) for d in (dk, dk, dv)]
+    w = [(torch.randn(H, d, conv_width, generator=g, device=dev) * 0.5).float() for d in (dk, dk, dv)]
+    outs = [torch.empty_like(t) for t in x]
+    o = torch.randn(T, H, dv, generator=g, device=dev).to(torch.bfloat16)
+    gate = torch.randn(T, H, dv, generator=g, device=dev).to(torch.bfloat16)
+    wt = torch.randn(dv, generator=g, device=dev).float()
+    y = torch.empty_like(o)
+
+    def pro():
+        B.kda_prologue(*x, *w, q=outs[0], k=outs[1], v=outs[2])
+
+    def epi():
+        B.kda_epilogue(o, gate, wt, eps=1e-5, y=y)
+
+    res = {}
+    for name, fn, nbytes in (("prologue", pro, 2 * T * H * (2 * dk + dv) * 2 + H * (2 * dk + dv) * conv_width * 4),
+                             ("epilogue", epi, 3 * T * H * dv * 2 + dv * 4)):
+        for _ in range(3):
+            fn()
+        barrier()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        barrier()
+        ms = max_over_ranks(sum(times) / reps)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[name] = {"ms": ms, "median_ms": statistics.median(times), "algorithmic_bytes": nbytes, "gbs": gbs,
+                     "frac": gbs / pk["hbm_gbs"], "traffic": ncu_traffic(f"kda_{name}")}
+    return {"workload": f"T={T} H={H} d_k={dk} d_v={dv} bf16, short convolution width {conv_width}",
+            **res, "peak": pk["hbm_gbs"], "peak_source": pk_src, "gpu_launches": 2 * (reps + 3),
+            "l2": "flushed by a 512 MiB write before every timed launch"}
 
 
 REPLAY_WINDOW = 7  # drafted tokens per sequence and speculation round

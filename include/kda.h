@@ -181,6 +181,44 @@ kda_status_t kda_decode_replay(const void* q, const void* k, const void* v, cons
                                const kda_problem_t* problem, void* stream);
 
 /*
+ * Layer prologue: the recurrence's q, k, v from their projections, per head ("Kimi K3: the paper
+ * and proofs side by side", section 2.1.1, "Preparing the queries, keys, values, and decay";
+ * "Kimi K3: architecture, derivations and a pinned-source audit", section 4.3):
+ *     y_t = sum_{i < conv_width} w[h][c][i] x_{t-i}   causal depthwise short convolution; tokens
+ *                                                      before the sequence start count as zero
+ *     y_t = y_t * sigmoid(y_t)                         Swish
+ *     y_t = y_t / sqrt(sum_c y_t[c]^2 + 1e-6)          regularised L2 normalisation, q and k only
+ *
+ *   xq, xk : [T_tot, H, d_k] io dtype;  xv : [T_tot, H, d_v] io dtype  (the projections).
+ *   wq, wk : [H, d_k, conv_width] fp32;  wv : [H, d_v, conv_width] fp32  (w[..., 0] weighs the
+ *            current token, w[..., i] the token i places earlier).
+ *   conv_width : 1 .. 4.
+ *   cu_seqlens : as for kda_forward (device [N+1], or NULL for N equal lengths).  Offsets are not
+ *            validated on the device here: invalid offsets give unspecified outputs (never an
+ *            access outside the tensors).
+ *   q, k, v : outputs, shaped like xq, xk, xv; must not overlap any input or each other.
+ *   problem : num_seqs, total_tokens, num_heads, d_k, d_v, io_dtype as for kda_forward.
+ */
+kda_status_t kda_prologue(const void* xq, const void* xk, const void* xv, const float* wq,
+                          const float* wk, const float* wv, int32_t conv_width,
+                          const int32_t* cu_seqlens, void* q, void* k, void* v,
+                          const kda_problem_t* problem, void* stream);
+
+/*
+ * Layer epilogue: head-wise RMSNorm of the recurrence output and the sigmoid output gate
+ * ("Kimi K3: architecture, derivations and a pinned-source audit", section 4.3; the output gate of
+ * Equation 6 in "Kimi K3: the paper and proofs side by side", section 2.1.1):
+ *     y = o / sqrt(mean_c o[c]^2 + eps) * weight * sigmoid(gate)
+ *
+ *   o, gate : [T_tot, H, d_v] io dtype (gate: the output-gate projection, before the sigmoid).
+ *   weight  : [d_v] fp32, the RMSNorm weight shared by the heads.
+ *   eps     : >= 0, finite (the pages name no value for the RMSNorm stabiliser).
+ *   y       : [T_tot, H, d_v] io dtype; may be o itself (in place); any other overlap is rejected.
+ */
+kda_status_t kda_epilogue(const void* o, const void* gate, const float* weight, float eps, void* y,
+                          const kda_problem_t* problem, void* stream);
+
+/*
  * kda_forward for callers that cannot allocate device memory: a library or plugin that runs
  * inside a host application which owns every device allocation (its own pool or arena) and gives
  * the plugin no allocator, or a latency-critical path that must not enter the driver's allocator.
@@ -222,7 +260,7 @@ const char* kda_status_string(kda_status_t status);
 
 /*
  * Per-kernel device timing, for measurement tools.  While enabled, every kernel launched by
- * kda_forward / kda_decode_step / kda_decode_replay is bracketed by two CUDA events recorded on the call's stream;
+ * kda_forward / kda_decode_step / kda_decode_replay / kda_prologue / kda_epilogue is bracketed by two CUDA events recorded on the call's stream;
  * kda_profile_read synchronises on those events and returns, per kernel name, the number of
  * launches and their summed device time.  Enabling (or disabling) discards earlier records.
  * Events are host-side objects: no device memory is allocated.  Not thread-safe against
@@ -242,7 +280,7 @@ int32_t kda_profile_read(kda_kernel_time_t* out, int32_t max_entries);
 /* ABI version of this header: (major << 16) | minor. */
 uint32_t kda_abi_version(void);
 
-#define KDA_ABI_VERSION ((1u << 16) | 1u)
+#define KDA_ABI_VERSION ((1u << 16) | 2u)
 
 #ifdef __cplusplus
 }

@@ -33,7 +33,8 @@ G_MIN = -5.0
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_forward_workspace_bytes", "kda_forward", "kda_decode_step", "kda_workspace_status",
            "kda_status_string", "kda_profile_enable", "kda_profile_read", "kda_abi_version",
-           "kda_forward_static_scratch", "kda_forward_plan", "kda_decode_replay")
+           "kda_forward_static_scratch", "kda_forward_plan", "kda_decode_replay", "kda_prologue",
+           "kda_epilogue")
 
 # Size of the library's own scratch array used by kda_forward_static_scratch.
 KDA_STATIC_SCRATCH_BYTES = 8 << 20
@@ -86,6 +87,10 @@ def lib():
             L.kda_decode_step.argtypes = [_vp] * 8 + [P, _vp]
             L.kda_decode_replay.restype = ctypes.c_int
             L.kda_decode_replay.argtypes = [_vp] * 10 + [P, _vp]
+            L.kda_prologue.restype = ctypes.c_int
+            L.kda_prologue.argtypes = [_vp] * 6 + [ctypes.c_int32] + [_vp] * 4 + [P, _vp]
+            L.kda_epilogue.restype = ctypes.c_int
+            L.kda_epilogue.argtypes = [_vp, _vp, _vp, ctypes.c_float, _vp, P, _vp]
             L.kda_workspace_status.restype = ctypes.c_int
             L.kda_workspace_status.argtypes = [_vp, ctypes.c_size_t, _vp]
             L.kda_status_string.restype = ctypes.c_char_p
@@ -302,6 +307,57 @@ def kda_decode_replay(q, k, v, z, A, beta, state_in, accepted=None, state_out=No
     if st != KDA_OK:
         raise KdaError(st, "kda_decode_replay")
     return out, state_out
+
+
+def kda_prologue(xq, xk, xv, wq, wk, wv, cu_seqlens=None, num_seqs: Optional[int] = None, q=None, k=None, v=None,
+                 stream=None):
+    """Layer prologue (see include/kda.h): short causal convolution, Swish and (q, k) regularised
+    L2 normalisation of the projections xq, xk [T, H, d_k] and xv [T, H, d_v]; conv weights
+    w* [H, d, K] fp32 with K = 1..4; cu_seqlens [N+1] int32 or None (``num_seqs`` equal lengths,
+    default 1).  Returns (q, k, v)."""
+    T, H, dk = xk.shape
+    dv = xv.shape[2]
+    dev = xk.device
+    dt = xk.dtype
+    K = wq.shape[2]
+    for name, t, shp in (("xq", xq, (T, H, dk)), ("xk", xk, (T, H, dk)), ("xv", xv, (T, H, dv))):
+        _need(t, name, dt, shp, dev)
+    for name, t, shp in (("wq", wq, (H, dk, K)), ("wk", wk, (H, dk, K)), ("wv", wv, (H, dv, K))):
+        _need(t, name, torch.float32, shp, dev)
+    if cu_seqlens is not None:
+        N = cu_seqlens.shape[0] - 1
+        _need(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,), dev)
+    else:
+        N = 1 if num_seqs is None else int(num_seqs)
+    q = torch.empty_like(xq) if q is None else q
+    k = torch.empty_like(xk) if k is None else k
+    v = torch.empty_like(xv) if v is None else v
+    for name, t, shp in (("q", q, (T, H, dk)), ("k", k, (T, H, dk)), ("v", v, (T, H, dv))):
+        _need(t, name, dt, shp, dev)
+    prob = make_problem(N, T, 0, H, dk, dv, dt)
+    st = lib().kda_prologue(_ptr(xq), _ptr(xk), _ptr(xv), _ptr(wq), _ptr(wk), _ptr(wv), ctypes.c_int32(K),
+                            _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(v), ctypes.byref(prob), _stream(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_prologue")
+    return q, k, v
+
+
+def kda_epilogue(o, gate, weight, eps: float = 1e-5, y=None, stream=None):
+    """Layer epilogue (see include/kda.h): head-wise RMSNorm of o [T, H, d_v] with weight [d_v]
+    fp32, times sigmoid(gate) [T, H, d_v].  ``y`` may be ``o`` (in place).  Returns y."""
+    T, H, dv = o.shape
+    dev = o.device
+    dt = o.dtype
+    _need(gate, "gate", dt, (T, H, dv), dev)
+    _need(weight, "weight", torch.float32, (dv,), dev)
+    y = torch.empty_like(o) if y is None else y
+    _need(y, "y", dt, (T, H, dv), dev)
+    prob = make_problem(1, T, 0, H, dv, dv, dt)
+    st = lib().kda_epilogue(_ptr(o), _ptr(gate), _ptr(weight), ctypes.c_float(eps), _ptr(y), ctypes.byref(prob),
+                            _stream(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_epilogue")
+    return y
 
 
 def kda_workspace_status(workspace, stream=None) -> int:

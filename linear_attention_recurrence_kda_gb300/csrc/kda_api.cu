@@ -400,6 +400,88 @@ kda_status_t kda_decode_replay(const void* q, const void* k, const void* v, cons
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+kda_status_t kda_prologue(const void* xq, const void* xk, const void* xv, const float* wq, const float* wk,
+                          const float* wv, int32_t conv_width, const int32_t* cu_seqlens, void* q, void* k, void* v,
+                          const kda_problem_t* problem, void* stream)
+{
+    kda_status_t st = check_descriptor(problem, Call::Forward);
+    if (st != KDA_OK) return st;
+    const kda_problem_t& p = *problem;
+    if (conv_width < 1 || conv_width > kda::kMaxConv) return KDA_ERR_UNSUPPORTED;
+    if (!xq || !xk || !xv || !wq || !wk || !wv || !q || !k || !v) return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens == nullptr && p.total_tokens % p.num_seqs != 0) return KDA_ERR_INVALID_ARG;
+    for (const void* ptr : {xq, xk, xv, (const void*)q, (const void*)k, (const void*)v}) {
+        if (!aligned(ptr, 16)) return KDA_ERR_INVALID_ARG;
+    }
+    for (const void* ptr : {(const void*)wq, (const void*)wk, (const void*)wv, (const void*)cu_seqlens}) {
+        if (!aligned(ptr, 4)) return KDA_ERR_INVALID_ARG;
+    }
+    const size_t io = io_size(p.io_dtype);
+    const size_t th = (size_t)p.total_tokens * p.num_heads;
+    const Range in[7] = {range_of(xq, th * p.d_k * io), range_of(xk, th * p.d_k * io), range_of(xv, th * p.d_v * io),
+                         range_of(wq, (size_t)p.num_heads * p.d_k * conv_width * 4),
+                         range_of(wk, (size_t)p.num_heads * p.d_k * conv_width * 4),
+                         range_of(wv, (size_t)p.num_heads * p.d_v * conv_width * 4),
+                         range_of(cu_seqlens, ((size_t)p.num_seqs + 1) * 4)};
+    const Range out[3] = {range_of(q, th * p.d_k * io), range_of(k, th * p.d_k * io), range_of(v, th * p.d_v * io)};
+    for (int i = 0; i < 3; ++i) {
+        for (const Range& r : in) {
+            if (overlaps(out[i], r)) return KDA_ERR_INVALID_ARG;
+        }
+        for (int j = 0; j < i; ++j) {
+            if (overlaps(out[i], out[j])) return KDA_ERR_INVALID_ARG;
+        }
+    }
+    for (const void* ptr : {xq, xk, xv, (const void*)wq, (const void*)wk, (const void*)wv, (const void*)cu_seqlens,
+                            (const void*)q, (const void*)k, (const void*)v}) {
+        st = check_device_pointer(ptr);
+        if (st != KDA_OK) return st;
+    }
+    kda::PrologueArgs a{};
+    a.x[0] = xq; a.x[1] = xk; a.x[2] = xv;
+    a.w[0] = wq; a.w[1] = wk; a.w[2] = wv;
+    a.y[0] = q; a.y[1] = k; a.y[2] = v;
+    a.cu = cu_seqlens;
+    a.T = p.total_tokens; a.N = p.num_seqs; a.H = p.num_heads; a.dk = p.d_k; a.dv = p.d_v; a.K = conv_width;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    kda::prof_start("kda_prologue", s);
+    const cudaError_t e = kda::launch_prologue(a, p.io_dtype, s);
+    kda::prof_stop(s);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_epilogue(const void* o, const void* gate, const float* weight, float eps, void* y,
+                          const kda_problem_t* problem, void* stream)
+{
+    kda_status_t st = check_descriptor(problem, Call::Forward);
+    if (st != KDA_OK) return st;
+    const kda_problem_t& p = *problem;
+    if (!o || !gate || !weight || !y) return KDA_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return KDA_ERR_INVALID_ARG;
+    for (const void* ptr : {o, gate, (const void*)y}) {
+        if (!aligned(ptr, 16)) return KDA_ERR_INVALID_ARG;
+    }
+    if (!aligned(weight, 4)) return KDA_ERR_INVALID_ARG;
+    const size_t io = io_size(p.io_dtype);
+    const size_t bytes = (size_t)p.total_tokens * p.num_heads * p.d_v * io;
+    const Range ro = range_of(o, bytes), rg = range_of(gate, bytes), rw = range_of(weight, (size_t)p.d_v * 4);
+    const Range ry = range_of(y, bytes);
+    if (overlaps(ry, rg) || overlaps(ry, rw)) return KDA_ERR_INVALID_ARG;
+    if (y != o && overlaps(ry, ro)) return KDA_ERR_INVALID_ARG;  // in place, or apart
+    for (const void* ptr : {o, gate, (const void*)weight, (const void*)y}) {
+        st = check_device_pointer(ptr);
+        if (st != KDA_OK) return st;
+    }
+    kda::EpilogueArgs a{};
+    a.o = o; a.gate = gate; a.weight = weight; a.y = y;
+    a.rows = p.total_tokens * p.num_heads; a.eps = eps;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    kda::prof_start("kda_epilogue", s);
+    const cudaError_t e = kda::launch_epilogue(a, p.d_v, p.io_dtype, s);
+    kda::prof_stop(s);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 kda_status_t kda_workspace_status(const void* workspace, size_t workspace_bytes, void* stream)
 {
     if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < 256) return KDA_ERR_WORKSPACE;

@@ -194,6 +194,25 @@ struct ReplayArgs {
     float g_min;
 };
 
+// Layer prologue / epilogue (kda_prologue, kda_epilogue).
+constexpr int kMaxConv = 4;  // widest short convolution supported
+struct PrologueArgs {
+    const void* x[3];      // q, k, v projections [T][H][d_k | d_k | d_v]
+    const float* w[3];     // depthwise convolution weights [H][d][K]
+    void* y[3];            // prepared q, k, v
+    const int32_t* cu;     // [N + 1] or null (N equal lengths)
+    int64_t T;
+    int32_t N, H, dk, dv, K;
+};
+struct EpilogueArgs {
+    const void* o;         // [rows][d_v]
+    const void* gate;      // [rows][d_v]
+    const float* weight;   // [d_v]
+    void* y;               // [rows][d_v], may be o
+    int64_t rows;          // T * H
+    float eps;
+};
+
 // Launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_gate(const PrefillArgs& a, kda_dtype_t dt, cudaStream_t s);
 cudaError_t launch_ut_wy(const PrefillArgs& a, kda_dtype_t dt, cudaStream_t s);
@@ -204,6 +223,8 @@ cudaError_t launch_prefill_split_tc(const PrefillArgs& a, cudaStream_t s);  // b
 cudaError_t launch_segment_scan(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
 cudaError_t launch_replay(const ReplayArgs& a, int dk, int dv, kda_dtype_t dt, cudaStream_t s);
+cudaError_t launch_prologue(const PrologueArgs& a, kda_dtype_t dt, cudaStream_t s);
+cudaError_t launch_epilogue(const EpilogueArgs& a, int dv, kda_dtype_t dt, cudaStream_t s);
 
 // SM count of the current device (cached per device; 152 if it cannot be queried).
 int sm_count_of_current_device();

@@ -1,0 +1,250 @@
+// kda_layer.cu -- the per-head work around the recurrence in a KDA layer: the prologue that turns
+// the q, k, v projections into the recurrence's inputs, and the epilogue applied to its output.
+//
+// "Kimi K3: the paper and proofs side by side", section 2.1.1 ("Preparing the queries, keys,
+// values, and decay", Equations 2-6) and "Kimi K3: architecture, derivations and a pinned-source
+// audit", section 4.3:
+//   prologue  y_t = sum_{i<K} w[h,c,i] x_{t-i}     causal depthwise short convolution (zero before
+//                                                  each sequence start)
+//             y_t = y_t sigmoid(y_t)               Swish
+//             y_t = y_t / sqrt(|y_t|^2 + 1e-6)     regularised L2 normalisation (q and k only)
+//   epilogue  y = o / sqrt(mean_c o^2 + eps) * weight * sigmoid(gate)
+//                                                  head-wise RMSNorm and sigmoid output gate
+// The projections themselves (x W) are plain GEMMs outside this library.
+//
+// Both are streaming kernels bound by HBM: every element is read and written once.  A prologue warp
+// walks 16 consecutive tokens of one head and one tensor (lane l owns channels l*VEC ..
+// l*VEC + VEC - 1), keeping the convolution window of its channels in registers, so each input row
+// is read once (plus a K-1 row halo per 16 tokens); the L2 norm is a warp reduction.  An epilogue
+// warp normalises whole token-head rows with one warp reduction each.
+#include "kda_internal.cuh"
+
+namespace kda {
+
+namespace {
+
+constexpr int kLayerThreads = 256;
+constexpr int kLayerWarps = kLayerThreads / 32;
+constexpr int kProTokens = 16;  // tokens per prologue warp
+
+template <typename TIO, int VEC>
+__device__ __forceinline__ void ld_vec(const TIO* p, float (&x)[VEC])
+{
+    if constexpr (sizeof(TIO) == 2 && VEC == 4) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
+        x[0] = __low2float(a); x[1] = __high2float(a); x[2] = __low2float(b); x[3] = __high2float(b);
+    } else if constexpr (sizeof(TIO) == 4 && VEC == 4) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(p));
+        x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+    } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) x[e] = ld_io(p, e);
+    }
+}
+
+template <typename TIO, int VEC>
+__device__ __forceinline__ void st_vec(TIO* p, const float (&x)[VEC])
+{
+    if constexpr (sizeof(TIO) == 2 && VEC == 4) {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(x[2], x[3]);
+        uint2 u;
+        u.x = *reinterpret_cast<const uint32_t*>(&a);
+        u.y = *reinterpret_cast<const uint32_t*>(&b);
+        *reinterpret_cast<uint2*>(p) = u;
+    } else if constexpr (sizeof(TIO) == 4 && VEC == 4) {
+        *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) st_io(p, e, x[e]);
+    }
+}
+
+__device__ __forceinline__ float sigmoid_f(float x)
+{
+    const float e = expf(-fabsf(x));
+    return (x >= 0.f) ? 1.f / (1.f + e) : e / (1.f + e);
+}
+
+__device__ __forceinline__ float warp_sum(float x)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+// sequence containing token t: the largest n with cu[n] <= t (so an empty sequence is skipped),
+// clamped so that garbage offsets never index outside [0, N]
+__device__ __forceinline__ int find_seq(const int32_t* cu, int N, int64_t t)
+{
+    int lo = 0, hi = N - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)cu[mid] <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+}  // namespace
+
+template <typename TIO, int VEC>
+__global__ void __launch_bounds__(kLayerThreads) kda_prologue_kernel(PrologueArgs a, int first)
+{
+    constexpr int D = 32 * VEC;
+    const int which = first + blockIdx.z;  // 0: q, 1: k, 2: v
+    const int h = blockIdx.y;
+    const int w = threadIdx.x >> 5;
+    const int l = threadIdx.x & 31;
+    const int64_t t0 = ((int64_t)blockIdx.x * kLayerWarps + w) * kProTokens;
+    if (t0 >= a.T) return;
+    const int64_t t1 = min(t0 + (int64_t)kProTokens, a.T);
+    // selected without indexing the parameter arrays (which would copy them to local memory)
+    const TIO* x = static_cast<const TIO*>(which == 0 ? a.x[0] : which == 1 ? a.x[1] : a.x[2]);
+    TIO* y = static_cast<TIO*>(which == 0 ? a.y[0] : which == 1 ? a.y[1] : a.y[2]);
+    const float* wt = which == 0 ? a.w[0] : which == 1 ? a.w[1] : a.w[2];
+    const int K = a.K;
+
+    // the sequence of t0: [start, end)
+    int64_t start, end;
+    int n = 0;
+    if (a.cu != nullptr) {
+        n = find_seq(a.cu, a.N, t0);
+        start = min((int64_t)max(a.cu[n], 0), t0);
+        end = max((int64_t)a.cu[n + 1], t0 + 1);
+    } else {
+        const int64_t len = a.T / a.N;
+        start = (t0 / len) * len;
+        end = start + len;
+    }
+
+    float wk[VEC][kMaxConv];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e)
+#pragma unroll
+        for (int i = 0; i < kMaxConv; ++i) wk[e][i] = (i < K) ? wt[((int64_t)h * D + l * VEC + e) * K + i] : 0.f;
+
+    // win[i] holds x_{t-1-i} of this lane's channels (zero before the sequence start)
+    float win[kMaxConv - 1][VEC];
+#pragma unroll
+    for (int i = 0; i < kMaxConv - 1; ++i) {
+        const int64_t ts = t0 - 1 - i;
+        if (i + 1 < K && ts >= start) {
+            ld_vec<TIO, VEC>(x + (ts * a.H + h) * D + l * VEC, win[i]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) win[i][e] = 0.f;
+        }
+    }
+
+    for (int64_t t = t0; t < t1; ++t) {
+        if (t >= end) {  // a new sequence starts here: the window restarts from zeros
+            if (a.cu != nullptr) {
+                while (n + 1 < a.N && (int64_t)a.cu[n + 1] <= t) ++n;
+                end = max((int64_t)a.cu[n + 1], t + 1);
+            } else {
+                end = t + a.T / a.N;
+            }
+#pragma unroll
+            for (int i = 0; i < kMaxConv - 1; ++i)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) win[i][e] = 0.f;
+        }
+        float xt[VEC], yv[VEC];
+        ld_vec<TIO, VEC>(x + (t * a.H + h) * D + l * VEC, xt);
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            float s = wk[e][0] * xt[e];
+#pragma unroll
+            for (int i = 1; i < kMaxConv; ++i) s += wk[e][i] * win[i - 1][e];
+            const float sw = s * sigmoid_f(s);
+            yv[e] = sw;
+            ss += sw * sw;
+        }
+#pragma unroll
+        for (int i = kMaxConv - 2; i > 0; --i)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) win[i][e] = win[i - 1][e];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) win[0][e] = xt[e];
+        if (which < 2) {
+            const float inv = 1.f / sqrtf(warp_sum(ss) + 1e-6f);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) yv[e] *= inv;
+        }
+        st_vec<TIO, VEC>(y + (t * a.H + h) * D + l * VEC, yv);
+    }
+}
+
+template <typename TIO, int VEC>
+__global__ void __launch_bounds__(kLayerThreads) kda_epilogue_kernel(EpilogueArgs a)
+{
+    constexpr int D = 32 * VEC;
+    const int l = threadIdx.x & 31;
+    const TIO* o = static_cast<const TIO*>(a.o);
+    const TIO* g = static_cast<const TIO*>(a.gate);
+    TIO* y = static_cast<TIO*>(a.y);
+    float wt[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) wt[e] = a.weight[l * VEC + e];
+    const int64_t stride = (int64_t)gridDim.x * kLayerWarps;
+    for (int64_t row = (int64_t)blockIdx.x * kLayerWarps + (threadIdx.x >> 5); row < a.rows; row += stride) {
+        float ov[VEC], gv[VEC];
+        ld_vec<TIO, VEC>(o + row * D + l * VEC, ov);
+        ld_vec<TIO, VEC>(g + row * D + l * VEC, gv);
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) ss += ov[e] * ov[e];
+        const float inv = 1.f / sqrtf(warp_sum(ss) * (1.f / D) + a.eps);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) ov[e] = ov[e] * inv * wt[e] * sigmoid_f(gv[e]);
+        st_vec<TIO, VEC>(y + row * D + l * VEC, ov);
+    }
+}
+
+template <typename TIO>
+static cudaError_t launch_prologue_io(const PrologueArgs& a, cudaStream_t s)
+{
+    const unsigned gx = (unsigned)((a.T + (int64_t)kLayerWarps * kProTokens - 1) / ((int64_t)kLayerWarps * kProTokens));
+    if (gx == 0) return cudaSuccess;
+    auto go = [&](int d, int first, int count) -> cudaError_t {
+        const dim3 grid(gx, (unsigned)a.H, (unsigned)count);
+        if (d == 32) kda_prologue_kernel<TIO, 1><<<grid, kLayerThreads, 0, s>>>(a, first);
+        else if (d == 64) kda_prologue_kernel<TIO, 2><<<grid, kLayerThreads, 0, s>>>(a, first);
+        else if (d == 128) kda_prologue_kernel<TIO, 4><<<grid, kLayerThreads, 0, s>>>(a, first);
+        else return cudaErrorInvalidValue;
+        return cudaGetLastError();
+    };
+    if (a.dk == a.dv) return go(a.dk, 0, 3);
+    const cudaError_t e = go(a.dk, 0, 2);
+    return e != cudaSuccess ? e : go(a.dv, 2, 1);
+}
+
+cudaError_t launch_prologue(const PrologueArgs& a, kda_dtype_t dt, cudaStream_t s)
+{
+    return dt == KDA_BF16 ? launch_prologue_io<__nv_bfloat16>(a, s) : launch_prologue_io<float>(a, s);
+}
+
+template <typename TIO>
+static cudaError_t launch_epilogue_io(const EpilogueArgs& a, int dv, cudaStream_t s)
+{
+    if (a.rows == 0) return cudaSuccess;
+    const int64_t ctas = (a.rows + kLayerWarps - 1) / kLayerWarps;
+    const int64_t cap = (int64_t)sm_count_of_current_device() * 8 * 4;  // a few waves of 8 CTAs per SM
+    const unsigned grid = (unsigned)(ctas < cap ? ctas : cap);
+    if (dv == 32) kda_epilogue_kernel<TIO, 1><<<grid, kLayerThreads, 0, s>>>(a);
+    else if (dv == 64) kda_epilogue_kernel<TIO, 2><<<grid, kLayerThreads, 0, s>>>(a);
+    else if (dv == 128) kda_epilogue_kernel<TIO, 4><<<grid, kLayerThreads, 0, s>>>(a);
+    else return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_epilogue(const EpilogueArgs& a, int dv, kda_dtype_t dt, cudaStream_t s)
+{
+    return dt == KDA_BF16 ? launch_epilogue_io<__nv_bfloat16>(a, dv, s) : launch_epilogue_io<float>(a, dv, s);
+}
+
+}  // namespace kda

@@ -3,6 +3,7 @@
     python -m linear_attention_recurrence_kda_gb300.profile_cases prefill-tc [--tokens T] [--heads H] [--reps R]
     python -m linear_attention_recurrence_kda_gb300.profile_cases decode [--seqs N] [--heads H] [--reps R]
     python -m linear_attention_recurrence_kda_gb300.profile_cases replay [--seqs N] [--heads H] [--window L] [--reps R]
+    python -m linear_attention_recurrence_kda_gb300.profile_cases layer [--tokens T] [--heads H] [--reps R]
     python -m linear_attention_recurrence_kda_gb300.profile_cases prefill-simt [...]
 
 Each case generates seeded inputs on the device (same recipe as the benchmark), runs one warm-up
@@ -73,9 +74,24 @@ def replay(seqs: int, heads: int, window: int, reps: int, d: int = 128):
     torch.cuda.synchronize()
 
 
+def layer(tokens: int, heads: int, reps: int, d: int = 128, conv_width: int = 4):
+    """Each rep: the prologue over the three projections, then the epilogue."""
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev).manual_seed(6)
+    x = [torch.randn(tokens, heads, d, generator=g, device=dev).to(torch.bfloat16) for _ in range(3)]
+    w = [(torch.randn(heads, d, conv_width, generator=g, device=dev) * 0.5).float() for _ in range(3)]
+    o = torch.randn(tokens, heads, d, generator=g, device=dev).to(torch.bfloat16)
+    gate = torch.randn(tokens, heads, d, generator=g, device=dev).to(torch.bfloat16)
+    wt = torch.randn(d, generator=g, device=dev).float()
+    for _ in range(reps + 1):
+        B.kda_prologue(*x, *w)
+        B.kda_epilogue(o, gate, wt)
+    torch.cuda.synchronize()
+
+
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["prefill-tc", "prefill-simt", "decode", "replay"])
+    ap.add_argument("case", choices=["prefill-tc", "prefill-simt", "decode", "replay", "layer"])
     ap.add_argument("--tokens", type=int, default=4096)
     ap.add_argument("--heads", type=int, default=16)
     ap.add_argument("--seqs", type=int, default=1)
@@ -86,6 +102,8 @@ def main():
         prefill(a.tokens, a.heads, a.reps, torch.bfloat16, seqs=a.seqs)
     elif a.case == "prefill-simt":
         prefill(a.tokens, a.heads, a.reps, torch.float32, seqs=a.seqs)
+    elif a.case == "layer":
+        layer(a.tokens, a.heads, a.reps)
     elif a.case == "replay":
         replay(a.seqs if a.seqs > 1 else 256, a.heads if a.heads != 16 else 32, a.window, a.reps)
     else:

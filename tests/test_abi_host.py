@@ -1,7 +1,7 @@
 """C-ABI checks that need no GPU: the library loads, exports every symbol include/kda.h declares,
 and rejects bad descriptors, pointers, aliasing and workspaces on the host before any launch.
 
-Every kda_forward / kda_decode_step / kda_decode_replay call below is built to fail in a host-only check (the fake
+Every kda_forward / kda_decode_step / kda_decode_replay / kda_prologue / kda_epilogue call below is built to fail in a host-only check (the fake
 addresses are never dereferenced and nothing is launched)."""
 import ctypes
 import os
@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert B.kda_abi_version() == (1 << 16) | 1
+    assert B.kda_abi_version() == (1 << 16) | 2
     for code in range(7):
         s = B.status_string(code)
         assert s.startswith("KDA_")
@@ -177,6 +177,45 @@ def test_replay_rejects_bad_arguments(L):
     assert rep(p, state_out=_addr(0)) == B.KDA_ERR_INVALID_ARG              # state_out on q
     assert rep(p, state_out=_addr(7)) == B.KDA_ERR_INVALID_ARG              # state_out on accepted
     assert rep(p, state_out=_addr(6) + 16) == B.KDA_ERR_INVALID_ARG         # partly on the snapshot
+
+
+def test_prologue_and_epilogue_reject_bad_arguments(L):
+    pro_names = ["xq", "xk", "xv", "wq", "wk", "wv", "cu", "q", "k", "v"]
+
+    def pro(prob, K=4, **over):
+        ptr = {n: _addr(i) for i, n in enumerate(pro_names)}
+        ptr["cu"] = None
+        ptr.update(over)
+        a = [ctypes.c_void_p(ptr[n]) if ptr[n] is not None else None for n in pro_names]
+        return L.kda_prologue(*a[:6], ctypes.c_int32(K), *a[6:], ctypes.byref(prob), None)
+
+    p = _prob(num_seqs=2, total_tokens=64)
+    assert pro(p, K=0) == B.KDA_ERR_UNSUPPORTED
+    assert pro(p, K=5) == B.KDA_ERR_UNSUPPORTED
+    assert pro(_prob(num_seqs=3, total_tokens=64)) == B.KDA_ERR_INVALID_ARG   # unequal lengths without offsets
+    for name in ("xq", "xk", "xv", "wq", "wk", "wv", "q", "k", "v"):
+        assert pro(p, **{name: None}) == B.KDA_ERR_INVALID_ARG, name
+    assert pro(p, q=_addr(7) + 8) == B.KDA_ERR_INVALID_ARG                   # misaligned
+    assert pro(p, wk=_addr(4) + 2) == B.KDA_ERR_INVALID_ARG
+    assert pro(p, q=_addr(0)) == B.KDA_ERR_INVALID_ARG                       # in place is not allowed
+    assert pro(p, v=_addr(7)) == B.KDA_ERR_INVALID_ARG                       # outputs overlap
+    assert pro(p, k=_addr(5)) == B.KDA_ERR_INVALID_ARG                       # output on the weights
+
+    epi_names = ["o", "gate", "weight", "y"]
+
+    def epi(prob, eps=1e-5, **over):
+        ptr = {n: _addr(i) for i, n in enumerate(epi_names)}
+        ptr.update(over)
+        a = [ctypes.c_void_p(ptr[n]) if ptr[n] is not None else None for n in epi_names]
+        return L.kda_epilogue(a[0], a[1], a[2], ctypes.c_float(eps), a[3], ctypes.byref(prob), None)
+
+    for name in epi_names:
+        assert epi(p, **{name: None}) == B.KDA_ERR_INVALID_ARG, name
+    assert epi(p, eps=-1.0) == B.KDA_ERR_INVALID_ARG
+    assert epi(p, eps=float("inf")) == B.KDA_ERR_INVALID_ARG
+    assert epi(p, y=_addr(1)) == B.KDA_ERR_INVALID_ARG                       # y on the gate
+    assert epi(p, y=_addr(0) + 16) == B.KDA_ERR_INVALID_ARG                  # partly on o
+    assert epi(_prob(d_v=16)) == B.KDA_ERR_UNSUPPORTED
 
 
 def test_workspace_status_rejects_null(L):

@@ -518,3 +518,79 @@ def test_replay_full_size_sampled():
     out_v, _ = B.kda_decode_replay(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], d["S0"], want_state=False)
     torch.cuda.synchronize()
     check(out_v[rows.cuda()], ref_o, torch.bfloat16, "full-size verify outputs (sample)")
+
+
+# ---------------------------------------------------------------- layer prologue / epilogue
+
+def _layer_inputs(lengths, H, dk, dv, K, io, seed):
+    g = torch.Generator().manual_seed(seed)
+    T = sum(lengths)
+    x = [torch.randn(T, H, d, generator=g).to(io) for d in (dk, dk, dv)]
+    w = [(torch.randn(H, d, K, generator=g) * 0.7).float() for d in (dk, dk, dv)]
+    cu = torch.tensor([0] + list(np.cumsum(lengths)), dtype=torch.int32)
+    return x, w, cu
+
+
+@pytest.mark.parametrize("io", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("dk,dv", [(32, 32), (64, 128), (128, 128)])
+@pytest.mark.parametrize("K", [1, 2, 4])
+def test_prologue_matches_oracle(io, dk, dv, K):
+    lengths = [5, 0, 40, 16, 1, 130, 17]
+    H = 3
+    x, w, cu = _layer_inputs(lengths, H, dk, dv, K, io, seed=dk + dv + K)
+    q, k, v = B.kda_prologue(*(t.cuda() for t in x), *(t.cuda() for t in w), cu_seqlens=cu.cuda())
+    torch.cuda.synchronize()
+    for name, got, xi, wi, norm in (("q", q, x[0], w[0], True), ("k", k, x[1], w[1], True), ("v", v, x[2], w[2], False)):
+        ref = oracle.prologue(xi, wi, cu_seqlens=cu.numpy(), normalise=norm)
+        check(got, ref, io, f"prologue {name}")
+
+
+def test_prologue_equal_lengths_without_offsets():
+    H, d, K, N, Ls = 2, 128, 4, 3, 50
+    x, w, _ = _layer_inputs([Ls] * N, H, d, d, K, torch.bfloat16, seed=11)
+    q, k, v = B.kda_prologue(*(t.cuda() for t in x), *(t.cuda() for t in w), num_seqs=N)
+    torch.cuda.synchronize()
+    cu = np.arange(N + 1) * Ls
+    check(q, oracle.prologue(x[0], w[0], cu_seqlens=cu), torch.bfloat16, "q")
+    check(v, oracle.prologue(x[2], w[2], cu_seqlens=cu, normalise=False), torch.bfloat16, "v")
+
+
+@pytest.mark.parametrize("io", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("dv", [32, 64, 128])
+def test_epilogue_matches_oracle(io, dv):
+    g = torch.Generator().manual_seed(dv)
+    T, H = 301, 5
+    o = (torch.randn(T, H, dv, generator=g) * 3).to(io)
+    gate = torch.randn(T, H, dv, generator=g).to(io)
+    wt = torch.randn(dv, generator=g).float()
+    ref = oracle.epilogue(o, gate, wt, 1e-5)
+    y = B.kda_epilogue(o.cuda(), gate.cuda(), wt.cuda(), eps=1e-5)
+    od = o.cuda()
+    y2 = B.kda_epilogue(od, gate.cuda(), wt.cuda(), eps=1e-5, y=od)  # in place
+    torch.cuda.synchronize()
+    check(y, ref, io, "epilogue")
+    assert torch.equal(y, y2)
+
+
+def test_layer_chain_prologue_forward_epilogue():
+    """prologue -> kda_forward -> epilogue through the C ABI on a varlen bf16 batch.  Each stage is
+    checked against the oracle run on the previous GPU stage's output: the recurrence on the GPU
+    prologue's q, k, v, the epilogue on the GPU recurrence output.  (The RMSNorm rescales every row
+    to unit RMS, so a row of small outputs would magnify the recurrence's own tolerance.)"""
+    lengths, H, d, K = [70, 0, 33, 200], 4, 128, 4
+    x, w, cu = _layer_inputs(lengths, H, d, d, K, torch.bfloat16, seed=21)
+    T = sum(lengths)
+    g = torch.Generator().manual_seed(22)
+    z = torch.randn(T, H, d, generator=g).to(torch.bfloat16)
+    A = (torch.randn(H, generator=g) * 0.5).float()
+    beta = torch.sigmoid(torch.randn(T, H, generator=g)).float()
+    gate = torch.randn(T, H, d, generator=g).to(torch.bfloat16)
+    wt = torch.randn(d, generator=g).float()
+    cud = cu.cuda()
+    q, k, v = B.kda_prologue(*(t.cuda() for t in x), *(t.cuda() for t in w), cu_seqlens=cud)
+    o, _ = B.kda_forward(q, k, v, z.cuda(), A.cuda(), beta.cuda(), cu_seqlens=cud)
+    y = B.kda_epilogue(o, gate.cuda(), wt.cuda(), eps=1e-5)
+    torch.cuda.synchronize()
+    ref_o, _ = oracle.forward(q.cpu(), k.cpu(), v.cpu(), z, A, beta, cu_seqlens=cu.numpy())
+    check(o, ref_o, torch.bfloat16, "layer recurrence output")
+    check(y, oracle.epilogue(o.cpu(), gate, wt, 1e-5), torch.bfloat16, "layer output")
