@@ -149,9 +149,9 @@ kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const 
 /*
  * Speculative-decode state replay: a window of L drafted tokens for each of N sequences, run from a
  * state snapshot ("Kimi K3: architecture, derivations and a pinned-source audit", section 10.3 "KDA
- * state replay for speculative decoding": only the projected inputs of drafted tokens are cached,
- * and the accepted prefix is replayed on chip in one fused kernel instead of rolling the state
- * back).  Every token is one decode step of the recurrence (as kda_decode_step computes it); one
+ * state replay for speculative decoding": a speculating server keeps only its drafts' per-token
+ * inputs and, once it knows which drafts survived, moves the saved state forward over them on chip
+ * in one launch, so no rejected draft ever has to be undone).  Every token is one decode step of the recurrence (as kda_decode_step computes it); one
  * launch reads each (sequence, head) state once, keeps it on chip across the window and writes at
  * most one state.  Typical use, per speculation round:
  *   verify : out given, state_out NULL -- o_t of every drafted token, no state is written, so the

@@ -2,9 +2,10 @@
 // state replay).
 //
 // "Kimi K3: architecture, derivations and a pinned-source audit", section 10.3 "KDA state replay for
-// speculative decoding": the serving stack caches only the projected inputs of the drafted tokens,
-// verifies the window from a snapshot of the state, and then advances the state over the accepted
-// prefix in one fused kernel, so that rejected drafts never have to be rolled back.  The arithmetic
+// speculative decoding": a speculating server keeps just the per-token inputs of its drafts (far
+// less memory than a copy of the state), checks the drafted window against a saved state, and then
+// moves that state forward over the drafts that survived, on chip and in one launch; a draft that
+// was rejected is therefore never applied and never has to be undone.  The arithmetic
 // of every token is the decode step's (Equation 1 with the gate of Equation 5, o = S'^T q = y + (q.k) u):
 //     alpha = exp(g_min sigmoid(exp(A_h) z)),  r = (Diag(alpha) S)^T k,  y = (Diag(alpha) S)^T q,
 //     u = beta (v - r),  S' = Diag(alpha) S + k u^T.

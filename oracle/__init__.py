@@ -201,9 +201,10 @@ def decode_step(q, k, v, z, A, beta, S, g_min: float = -5.0, threads: int = 0):
 def replay(q, k, v, z, A, beta, S, accepted=None, g_min: float = -5.0, threads: int = 0):
     """Speculative-decode state replay ("Kimi K3: architecture, derivations and a pinned-source
     audit", section 10.3 "KDA state replay for speculative decoding", and the replay checks of its
-    "CPU laboratory"): the projected inputs of L drafted tokens per sequence are cached, the
-    verifier reads every drafted token from the snapshot, and once the accepted count is known the
-    state is advanced over the accepted prefix only; the snapshot itself is never modified.
+    "CPU laboratory"): a speculating server keeps, for each of L drafted tokens per sequence, only
+    that token's inputs (far less memory than a copy of the state); the verifier reads every
+    drafted token from the saved state, and once it is known how many drafts survive, the state
+    is moved forward over those alone.  The saved state is never modified.
 
     q, k, z: [N*L, H, d_k] with token t of sequence n at row n*L + t; v: [N*L, H, d_v];
     beta: [N*L, H]; A: [H]; S: the snapshot [N, H, d_k, d_v]; accepted: N counts in [0, L], or
