@@ -425,8 +425,8 @@ def test_replay_outputs_do_not_depend_on_acceptance():
 # ---------------------------------------------------------------- layer prologue / epilogue
 
 def test_prologue_regularised_l2_norm_facts():
-    """The pages' statements about the regularised L2 normalisation: the result has norm strictly
-    below one, and a zero vector stays zero."""
+    """What the pages state about the regularised L2 normalisation: a normalised vector is always
+    shorter than one (approaching it for long inputs), and the zero vector maps to itself."""
     rng = np.random.default_rng(50)
     x = rng.normal(size=(20, 2, 8)) * np.logspace(-3, 2, 20)[:, None, None]
     w = np.zeros((2, 8, 1))
