@@ -25,6 +25,7 @@ What is computed (see the C file for the step-by-step statement):
 * ``prologue``    -- short convolution, Swish and (q, k) regularised L2 normalisation of the
                      projections (what ``kda_prologue`` computes), numpy in float64.
 * ``epilogue``    -- head-wise RMSNorm and sigmoid output gate (what ``kda_epilogue`` computes).
+* ``backward``    -- reverse-mode gradients of ``forward`` (numpy, float64; no GPU counterpart yet).
 """
 from __future__ import annotations
 
@@ -291,3 +292,67 @@ def epilogue(o, gate, weight, eps: float):
     weight = _f64(weight)
     rms = np.sqrt((o * o).mean(-1, keepdims=True) + eps)
     return o / rms * weight * _sigmoid(gate)
+
+
+def backward(q, k, v, z, A, beta, dO, dS_final, S0=None, cu_seqlens=None, g_min: float = -5.0):
+    """Reverse-mode gradients of ``forward``: for the scalar
+    L = sum(dO * out) + sum(dS_final * S_final), returns (dq, dk, dv, dz, dA, dbeta, dS0) with the
+    shapes of q, k, v, z, A, beta and S0 (zeros when S0 is None).
+
+    The chain rule is taken through each token's steps in reverse order ("Kimi K3: the paper and
+    proofs side by side", section 2.1.1, Equation 1 with the gate of Equation 5), per sequence and
+    head, with the states of the forward pass kept:
+        x = e^{A_h} z,  g = g_min sigmoid(x),  alpha = e^g
+        Sbar = Diag(alpha) S_{t-1},  r = Sbar^T k,  u = beta (v - r),  S_t = Sbar + k u^T,
+        o_t = S_t^T q.
+    Going back from dS (the gradient reaching S_t):
+        dq = S_t dO_t;  dS += q dO_t^T;  dk = dS u;  du = dS^T k;  dv = beta du;
+        dbeta = du . (v - r);  dr = -beta du;  dSbar = dS + k dr^T;  dk += Sbar dr;
+        dalpha_c = sum_j dSbar[c, j] S_{t-1}[c, j];  dS_{t-1} = Diag(alpha) dSbar;
+        dx = dalpha alpha g_min sigmoid(x) (1 - sigmoid(x));  dz = dx e^{A_h};  dA_h += sum dx x.
+    Plain numpy in float64, for test sizes."""
+    q, k, v, z, A, beta, dO, dS_final, S0 = map(_f64, (q, k, v, z, A, beta, dO, dS_final, S0))
+    T, H, dk_ = k.shape
+    dv_ = v.shape[2]
+    cu = _cu(cu_seqlens, T)
+    N = cu.shape[0] - 1
+    grads = [np.zeros_like(a) for a in (q, k, v, z)]
+    dq, dkk, dvv, dz = grads
+    dA = np.zeros(H)
+    dbeta = np.zeros_like(beta)
+    dS0 = np.zeros((N, H, dk_, dv_))
+    for n in range(N):
+        t0, t1 = int(cu[n]), int(cu[n + 1])
+        for h in range(H):
+            eA = np.exp(A[h])
+            S = np.zeros((dk_, dv_)) if S0 is None else S0[n, h].copy()
+            saved = []
+            for t in range(t0, t1):
+                x = eA * z[t, h]
+                sig = _sigmoid(x)
+                al = np.exp(g_min * sig)
+                Sbar = al[:, None] * S
+                r = Sbar.T @ k[t, h]
+                u = beta[t, h] * (v[t, h] - r)
+                saved.append((S, Sbar, x, sig, al, r, u))
+                S = Sbar + np.outer(k[t, h], u)
+            dS = dS_final[n, h].copy()
+            for t in range(t1 - 1, t0 - 1, -1):
+                S_prev, Sbar, x, sig, al, r, u = saved[t - t0]
+                S_t = Sbar + np.outer(k[t, h], u)
+                dq[t, h] = S_t @ dO[t, h]
+                dS = dS + np.outer(q[t, h], dO[t, h])
+                dk_t = dS @ u
+                du = dS.T @ k[t, h]
+                dvv[t, h] = beta[t, h] * du
+                dbeta[t, h] = du @ (v[t, h] - r)
+                dr = -beta[t, h] * du
+                dSbar = dS + np.outer(k[t, h], dr)
+                dkk[t, h] = dk_t + Sbar @ dr
+                dal = (dSbar * S_prev).sum(axis=1)
+                dS = al[:, None] * dSbar
+                dx = dal * al * g_min * sig * (1.0 - sig)
+                dz[t, h] = dx * eA
+                dA[h] += (dx * x).sum()
+            dS0[n, h] = dS
+    return dq, dkk, dvv, dz, dA, dbeta, dS0

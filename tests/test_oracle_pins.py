@@ -479,3 +479,69 @@ def test_epilogue_closed_forms():
     np.testing.assert_allclose(oracle.epilogue(7.5 * o, g, wt, 0.0), oracle.epilogue(o, g, wt, 0.0), rtol=1e-13)
     y = oracle.epilogue(o, np.full_like(g, 40.0), np.ones(16), 0.0)
     np.testing.assert_allclose(np.sqrt((y * y).mean(-1)), 1.0, rtol=1e-12)
+
+
+# ---------------------------------------------------------------- gradients (backward)
+
+def _bw_case(rng, lens, H, dk, dv):
+    T = sum(lens)
+    q = rng.normal(size=(T, H, dk))
+    k = rng.normal(size=(T, H, dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.normal(size=(T, H, dv))
+    z = rng.normal(size=(T, H, dk))
+    A = rng.normal(size=H) * 0.5
+    b = rng.uniform(0.1, 0.9, size=(T, H))
+    S0 = rng.normal(size=(len(lens), H, dk, dv))
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    dO = rng.normal(size=(T, H, dv))
+    dSf = rng.normal(size=(len(lens), H, dk, dv))
+    return q, k, v, z, A, b, S0, cu, dO, dSf
+
+
+def test_backward_matches_central_differences():
+    """Every gradient entry against a central difference of L = sum(dO * out) + sum(dS_f * S_f)
+    through the forward oracle (two sequences of 3 and 2 tokens, two heads, d_k = 3, d_v = 2)."""
+    rng = np.random.default_rng(60)
+    q, k, v, z, A, b, S0, cu, dO, dSf = _bw_case(rng, [3, 2], 2, 3, 2)
+
+    def loss(*args):
+        o, sf = oracle.forward(*args[:6], S0=args[6], cu_seqlens=cu)
+        return float((dO * o).sum() + (dSf * sf).sum())
+
+    args = [q, k, v, z, A, b, S0]
+    grads = oracle.backward(q, k, v, z, A, b, dO, dSf, S0=S0, cu_seqlens=cu)
+    order = [0, 1, 2, 3, 4, 5, 6]  # q k v z A beta S0 <- dq dk dv dz dA dbeta dS0
+    eps = 1e-6
+    for ai, gi in zip(order, range(7)):
+        base = args[ai]
+        num = np.zeros_like(base)
+        for idx in np.ndindex(base.shape):
+            plus = [a.copy() for a in args]
+            minus = [a.copy() for a in args]
+            plus[ai][idx] += eps
+            minus[ai][idx] -= eps
+            num[idx] = (loss(*plus) - loss(*minus)) / (2 * eps)
+        np.testing.assert_allclose(grads[gi], num, rtol=1e-6, atol=1e-7)
+
+
+def test_backward_one_step_sum_of_squares():
+    """The gradient of sum(S_1^2) with respect to the old state after one token, in closed form:
+    S_1 = (I - b k k^T) Diag(alpha) S_0 + b k v^T gives 2 Diag(alpha) (I - b k k^T) S_1."""
+    rng = np.random.default_rng(61)
+    q, k, v, z, A, b, S0, cu, _, _ = _bw_case(rng, [1], 1, 4, 3)
+    _, S1 = oracle.forward(q, k, v, z, A, b, S0=S0)
+    _, al = oracle.gate(z, A)
+    kk = k[0, 0]
+    P = np.eye(4) - b[0, 0] * np.outer(kk, kk)
+    expect = 2 * np.diag(al[0, 0]) @ P @ S1[0, 0]
+    grads = oracle.backward(q, k, v, z, A, b, np.zeros((1, 1, 3)), 2 * S1, S0=S0)
+    np.testing.assert_allclose(grads[6][0, 0], expect, rtol=1e-12, atol=1e-13)
+
+
+def test_backward_zero_upstream_gives_zero():
+    rng = np.random.default_rng(62)
+    q, k, v, z, A, b, S0, cu, dO, dSf = _bw_case(rng, [4, 0, 2], 2, 3, 3)
+    grads = oracle.backward(q, k, v, z, A, b, np.zeros_like(dO), np.zeros_like(dSf), S0=S0, cu_seqlens=cu)
+    for gr in grads:
+        np.testing.assert_array_equal(gr, 0.0)
