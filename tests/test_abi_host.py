@@ -260,3 +260,31 @@ def test_forward_plan(L, monkeypatch):
         B.kda_forward_plan(_prob(d_k=96))
     assert e.value.status == B.KDA_ERR_UNSUPPORTED
     assert L.kda_forward_plan(ctypes.byref(p), ctypes.c_size_t(1 << 40), None) == B.KDA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("T,N,H", [(4096, 1, 16), (58337, 8, 32), (1 << 20, 1, 8), (300, 3, 4), (16, 1, 1)])
+def test_forward_plan_properties(L, monkeypatch, T, N, H):
+    """Over workspace sizes from the fastest plan's need down to the 256-byte minimum, every plan
+    fits, its segments cover the longest sequence without an empty last segment, the split plan's
+    segments hold whole pairs of chunks, and any workspace at least the reported need gets the
+    fastest plan."""
+    monkeypatch.delenv("KDA_TC_PLAN", raising=False)
+    monkeypatch.delenv("KDA_SEGMENT_CHUNKS", raising=False)
+    max_len = -(-T // N) if N > 1 else T
+    p = _prob(num_seqs=N, total_tokens=T, max_seqlen=max_len, num_heads=H, d_k=128, d_v=128, io_dtype=B.KDA_BF16)
+    full = B.kda_forward_workspace_bytes(p)
+    assert full >= 256 and full % 256 == 0
+    fastest = B.kda_forward_plan(p, full)
+    assert B.kda_forward_plan(p, 2 * full) == fastest
+    chunks = -(-max_len // 16)
+    for frac in (1.0, 0.7, 0.5, 0.3, 0.1, 0.02, 0.005, 0.0):
+        ws = max(256, int(full * frac))
+        pl = B.kda_forward_plan(p, ws)
+        if pl["num_segments"] > 1:
+            sc, ns = pl["seg_chunks"], pl["num_segments"]
+            assert sc * ns >= chunks and (ns - 1) * sc < chunks, (ws, pl)
+            if pl["split"]:
+                assert sc % 2 == 0, (ws, pl)
+        else:
+            assert pl["seg_chunks"] == 0
+    assert B.kda_forward_plan(p, 256) == {"split": False, "seg_chunks": 0, "num_segments": 1}
