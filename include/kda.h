@@ -212,7 +212,8 @@ kda_status_t kda_prologue(const void* xq, const void* xk, const void* xv, const 
  *
  *   o, gate : [T_tot, H, d_v] io dtype (gate: the output-gate projection, before the sigmoid).
  *   weight  : [d_v] fp32, the RMSNorm weight shared by the heads.
- *   eps     : >= 0, finite (the pages name no value for the RMSNorm stabiliser).
+ *   eps     : >= 0, finite (the pages name no value for the RMSNorm stabiliser).  With eps = 0 an
+ *             all-zero row has no defined output (0 / 0), as in the formula.
  *   y       : [T_tot, H, d_v] io dtype; may be o itself (in place); any other overlap is rejected.
  */
 kda_status_t kda_epilogue(const void* o, const void* gate, const float* weight, float eps, void* y,
