@@ -86,3 +86,76 @@ def window_verify(q, k, v, g, beta, S0, dtype=np.float64):
     Tp = np.linalg.inv(np.eye(L, dtype=dtype) + A) * beta[None, :]
     U = Tp @ (v - KG @ S0)
     return QG @ S0 + P @ U
+
+
+def chunk_backward(q, k, v, g, beta, dO, dS_final, S0=None, cu_seqlens=None, C=16):
+    """Reverse-mode gradients of ``chunk_forward`` taken chunk by chunk (fp64): the chunk-wise
+    backward a tensor-core kernel would implement, restated plainly.  Returns
+    (dq, dk, dv, dg, dbeta, dS0) for L = sum(dO * out) + sum(dS_final * S_final); ``g`` is the
+    log-decay (the gate's own chain rule is left to the caller).
+
+    Per chunk entering with state S (forward as in ``chunk_forward``, G inclusive cumsum of g,
+    KG = K e^G, QG = Q e^G, KI = K e^-G, Kt = K e^(G_C - G), A = tril_strict(diag(b) KG KI^T),
+    T = (I + A)^-1, W = T diag(b) KG, Ut = T diag(b) V, U = Ut - W S, P = tril(QG KI^T),
+    O = QG S + P U, S' = e^G_C S + Kt^T U), going back from dO and dS':
+        dS = e^G_C dS' + QG^T dO - W^T dU;   dU = Kt dS' + P^T dO
+        dKt = U dS'^T;  dQG = dO S^T + tril(dP) KI;  dP = tril(dO U^T);  dW = -dU S^T
+        dT = dU (diag(b) V)^T + dW (diag(b) KG)^T;  dA = -tril_strict(T^T dT T^T)
+        dV = diag(b) T^T dU;  dKG = diag(b) T^T dW + diag(b) dA KI
+        dKI = dA^T diag(b) KG + tril(dP)^T QG
+        dbeta = rowsum(T^T dU * V) + rowsum(T^T dW * KG) + rowsum(dA * KG KI^T)
+    and the gradients reach G through the scaled rows themselves (never through 1/Gamma^2):
+        dG = dKG * KG + dQG * QG - dKI * KI - dKt * Kt,  dG_C += sum_t dKt * Kt + e^G_C rowsum(dS' * S)
+    then dg = reversed cumulative sum of dG over the chunk."""
+    q, k, v, g, beta, dO, dS_final = (np.asarray(x, dtype=np.float64) for x in (q, k, v, g, beta, dO, dS_final))
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    cu = np.array([0, T]) if cu_seqlens is None else np.asarray(cu_seqlens, dtype=np.int64)
+    N = len(cu) - 1
+    dq, dkk, dvv, dg = (np.zeros_like(x) for x in (q, k, v, g))
+    dbeta = np.zeros_like(beta)
+    dS0 = np.zeros((N, H, dk, dv))
+    for n in range(N):
+        for h in range(H):
+            S = np.zeros((dk, dv)) if S0 is None else np.array(S0[n, h], dtype=np.float64)
+            chunks = []
+            for t0 in range(cu[n], cu[n + 1], C):  # forward, keeping each chunk's entering state
+                t1 = min(t0 + C, cu[n + 1])
+                Kc, Qc, Vc, b = k[t0:t1, h], q[t0:t1, h], v[t0:t1, h], beta[t0:t1, h]
+                G = np.cumsum(g[t0:t1, h], axis=0)
+                KG, QG, KI = Kc * np.exp(G), Qc * np.exp(G), Kc * np.exp(-G)
+                Kt = Kc * np.exp(G[-1][None, :] - G)
+                c = t1 - t0
+                M = KG @ KI.T
+                A = np.tril(b[:, None] * M, -1)
+                Tn = np.linalg.inv(np.eye(c) + A)
+                W = Tn @ (b[:, None] * KG)
+                U = Tn @ (b[:, None] * Vc) - W @ S
+                P = np.tril(QG @ KI.T)
+                chunks.append((t0, t1, S, G, KG, QG, KI, Kt, M, Tn, W, U, P))
+                S = np.exp(G[-1])[:, None] * S + Kt.T @ U
+            dS = dS_final[n, h].copy()
+            for (t0, t1, S, G, KG, QG, KI, Kt, M, Tn, W, U, P) in reversed(chunks):
+                Vc, b, dOc = v[t0:t1, h], beta[t0:t1, h], dO[t0:t1, h]
+                eGC = np.exp(G[-1])
+                dSn = dS
+                dKt = U @ dSn.T
+                dU = Kt @ dSn + P.T @ dOc
+                dP = np.tril(dOc @ U.T)
+                dQG = dOc @ S.T + dP @ KI
+                dW = -dU @ S.T
+                dS = eGC[:, None] * dSn + QG.T @ dOc - W.T @ dU
+                dTn = dU @ (b[:, None] * Vc).T + dW @ (b[:, None] * KG).T
+                dA = -np.tril(Tn.T @ dTn @ Tn.T, -1)
+                TdU, TdW = Tn.T @ dU, Tn.T @ dW
+                dvv[t0:t1, h] = b[:, None] * TdU
+                dKG = b[:, None] * TdW + b[:, None] * (dA @ KI)
+                dKI = (b[:, None] * dA).T @ KG + dP.T @ QG
+                dbeta[t0:t1, h] = (TdU * Vc).sum(1) + (TdW * KG).sum(1) + (dA * M).sum(1)
+                dkk[t0:t1, h] = dKG * np.exp(G) + dKI * np.exp(-G) + dKt * np.exp(G[-1][None, :] - G)
+                dq[t0:t1, h] = dQG * np.exp(G)
+                dG = dKG * KG + dQG * QG - dKI * KI - dKt * Kt
+                dG[-1] += (dKt * Kt).sum(0) + eGC * (dSn * S).sum(1)
+                dg[t0:t1, h] = np.cumsum(dG[::-1], axis=0)[::-1]
+            dS0[n, h] = dS
+    return dq, dkk, dvv, dg, dbeta, dS0

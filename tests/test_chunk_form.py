@@ -69,3 +69,38 @@ def test_window_verify_form_matches_token_oracle(L, floor):
     o32 = window_verify(q[:, 0], k[:, 0], v[:, 0], g[:, 0], b[:, 0], S0[0, 0], dtype=np.float32)
     assert np.isfinite(o32).all()
     np.testing.assert_allclose(o32, o_ref[:, 0], rtol=0, atol=2e-5 * scale)
+
+
+@pytest.mark.parametrize("lens,C", [([40], 16), ([5, 0, 33, 17], 16), ([29], 8)])
+def test_chunk_backward_matches_token_oracle(lens, C):
+    """The chunk-wise backward (gradients reaching the log-decay through the scaled rows) equals
+    the token-level reverse-mode oracle; the gate's chain rule links dg to dz and dA."""
+    from chunk_form import chunk_backward
+    rng = np.random.default_rng(300 + sum(lens) + C)
+    T, H, dk, dv = sum(lens), 2, 6, 5
+    q = rng.normal(size=(T, H, dk))
+    k = rng.normal(size=(T, H, dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.normal(size=(T, H, dv))
+    z = rng.normal(size=(T, H, dk))
+    A = rng.normal(size=H) * 0.5
+    b = rng.uniform(0.1, 0.9, size=(T, H))
+    S0 = rng.normal(size=(len(lens), H, dk, dv)) * 0.3
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    dO = rng.normal(size=(T, H, dv))
+    dSf = rng.normal(size=(len(lens), H, dk, dv))
+    g, _ = oracle.gate(z, A)
+    ref = oracle.backward(q, k, v, z, A, b, dO, dSf, S0=S0, cu_seqlens=cu)
+    dq, dk_, dv_, dg, db, dS0 = chunk_backward(q, k, v, g, b, dO, dSf, S0=S0, cu_seqlens=cu, C=C)
+    tol = dict(rtol=1e-9, atol=1e-10)
+    np.testing.assert_allclose(dq, ref[0], **tol)
+    np.testing.assert_allclose(dk_, ref[1], **tol)
+    np.testing.assert_allclose(dv_, ref[2], **tol)
+    np.testing.assert_allclose(db, ref[5], **tol)
+    np.testing.assert_allclose(dS0, ref[6], **tol)
+    # dz = dg * g_min sigmoid'(x) e^A with x = e^A z; dA = sum dg * g_min sigmoid'(x) x
+    x = np.exp(A)[None, :, None] * z
+    s = 1 / (1 + np.exp(-x))
+    dx = dg * -5.0 * s * (1 - s)
+    np.testing.assert_allclose(dx * np.exp(A)[None, :, None], ref[3], **tol)
+    np.testing.assert_allclose((dx * x).sum(axis=(0, 2)), ref[4], **tol)
