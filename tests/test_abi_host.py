@@ -288,3 +288,13 @@ def test_forward_plan_properties(L, monkeypatch, T, N, H):
         else:
             assert pl["seg_chunks"] == 0
     assert B.kda_forward_plan(p, 256) == {"split": False, "seg_chunks": 0, "num_segments": 1}
+
+
+def test_compute_entry_points_cite_their_passage():
+    """Every computing entry point's declaration in include/kda.h is preceded by a comment that
+    names the page and section defining the operation."""
+    src = open(HEADER).read()
+    for name in ("kda_forward", "kda_decode_step", "kda_decode_replay", "kda_prologue", "kda_epilogue"):
+        decl = src.index(f"kda_status_t {name}(")
+        comment = src[src.rindex("/*", 0, decl):decl]
+        assert "Kimi K3" in comment and "section" in comment, name
