@@ -298,3 +298,23 @@ def test_compute_entry_points_cite_their_passage():
         decl = src.index(f"kda_status_t {name}(")
         comment = src[src.rindex("/*", 0, decl):decl]
         assert "Kimi K3" in comment and "section" in comment, name
+
+
+def test_fp32_stage_layout_matches_the_library():
+    """The layout the stage-parity test reads (check word, G, W, U~) has exactly the size the
+    library reports for the fp32 path, and packing then reading it round-trips."""
+    import numpy as np
+    import torch
+    from stages import fp32_stage_layout, fp32_stage_views
+    for (T, H, dk, dv) in ((120, 3, 32, 64), (1, 1, 128, 32), (1000, 2, 64, 128)):
+        p = _prob(num_seqs=1, total_tokens=T, max_seqlen=T, num_heads=H, d_k=dk, d_v=dv)
+        assert fp32_stage_layout(T, H, dk, dv)[3] == B.kda_forward_workspace_bytes(p)
+    T, H, dk, dv = 37, 2, 32, 64
+    g_off, w_off, ut_off, total = fp32_stage_layout(T, H, dk, dv)
+    rng = np.random.default_rng(0)
+    ref = [rng.normal(size=(T, H, d)).astype(np.float32) for d in (dk, dk, dv)]
+    ws = torch.zeros(total, dtype=torch.uint8)
+    for off, a in zip((g_off, w_off, ut_off), ref):
+        ws[off:off + a.nbytes] = torch.from_numpy(a.reshape(-1).view(np.uint8).copy())
+    for got, want in zip(fp32_stage_views(ws, T, H, dk, dv), ref):
+        np.testing.assert_array_equal(got, want)

@@ -594,3 +594,30 @@ def test_layer_chain_prologue_forward_epilogue():
     ref_o, _ = oracle.forward(q.cpu(), k.cpu(), v.cpu(), z, A, beta, cu_seqlens=cu.numpy())
     check(o, ref_o, torch.bfloat16, "layer recurrence output")
     check(y, oracle.epilogue(o.cpu(), gate, wt, 1e-5), torch.bfloat16, "layer output")
+
+
+# ---------------------------------------------------------------- stage parity (fp32 path)
+
+@pytest.mark.parametrize("dk,dv", [(32, 64), (128, 32)])
+def test_stage_parity_fp32_path(dk, dv):
+    """The fp32 path's per-chunk intermediates as they sit in the workspace after kda_forward --
+    the in-chunk cumulative log-decay G, W = T diag(beta)(K*Gamma) and U~ = T diag(beta) V -- against
+    the fp64 chunk-form restatement (itself matched to the token oracle), on a varlen batch with an
+    empty sequence and a ragged last chunk."""
+    from stages import chunk_reference_stages, fp32_stage_views
+    lengths, H = [37, 0, 16, 50], 3
+    inp = I.make_inputs(1, lengths=lengths, num_heads=H, d_k=dk, d_v=dv, io_dtype=torch.float32, seed=13 + dk)
+    T, N = sum(lengths), len(lengths)
+    d = to_dev(inp)
+    prob = B.make_problem(N, T, max(lengths), H, dk, dv, torch.float32)
+    ws = torch.zeros(B.kda_forward_workspace_bytes(prob), dtype=torch.uint8, device="cuda")
+    B.kda_forward(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], initial_state=d["S0"],
+                  cu_seqlens=d["cu_seqlens"], max_seqlen=max(lengths), workspace=ws)
+    torch.cuda.synchronize()
+    G, W, Ut = fp32_stage_views(ws, T, H, dk, dv)
+    g, _ = oracle.gate(inp["z"], inp["A"])
+    rG, rW, rUt = chunk_reference_stages(inp["q"], inp["k"], inp["v"], g, inp["beta"], inp["S0"],
+                                         inp["cu_seqlens"].numpy())
+    check(G, rG, torch.float32, "stage G")
+    check(W, rW, torch.float32, "stage W")
+    check(Ut, rUt, torch.float32, "stage U~")
