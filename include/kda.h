@@ -122,7 +122,12 @@ kda_status_t kda_forward_plan(const kda_problem_t* problem, size_t workspace_byt
  *                   (KDA_ERR_WORKSPACE).  Results do not depend on the plan beyond rounding.
  *                   Environment overrides, read on every call: KDA_TC_PLAN=fused keeps the fused
  *                   kernel; KDA_SEGMENT_CHUNKS=<n> forces n chunks per segment (0: unsegmented;
- *                   the pair-step plan rounds n up to an even count).
+ *                   the pair-step plan rounds n up to an even count).  KDA_DEBUG_HANDOFF_TRIES=<n>
+ *                   (a debugging aid, off unless set) gives the split plan's state-pass hand-off
+ *                   waits n tries of up to 20 us instead of ~2.6 s; with n = 0 every such wait gives
+ *                   up at once, the kernels stop early without touching memory they do not own, and
+ *                   the status readers report KDA_ERR_TIMEOUT (outputs and final states are then
+ *                   unspecified).
  *
  * Returns KDA_OK once all kernels are enqueued on `stream`.
  */
@@ -235,18 +240,29 @@ kda_status_t kda_epilogue(const void* o, const void* gate, const float* weight, 
  *     with KDA_ERR_WORKSPACE before anything is launched.  (bf16 problems with d_k = d_v = 128
  *     need only a few hundred bytes, and use as many parallel sequence segments as the array
  *     holds; the fp32 path needs 4 (2 d_k + d_v) bytes per token and head.)
- *   - The first call on each device looks up that device's copy of the array, with the device
- *     current; make that first call before any stream capture.
+ *   - Every call looks up the array's address in the caller's current context (a lookup, no
+ *     allocation); the first call in a context also loads the library's device code there, so make
+ *     that first call before any stream capture.  The address is never cached across calls, so it
+ *     stays right after cudaDeviceReset or when the caller switches contexts.
  *   - All calls on a device share the one array, and it keeps the last call's contents (the
  *     check word is cleared at the start of every call).  Calls whose GPU work overlaps -- on
  *     different streams, or from different host threads -- race on it; serialise them.
- *   - kda_workspace_status() cannot be used with this entry point (there is no caller workspace).
+ *   - The device-side check word of the last call (bad cu_seqlens, a bounded wait that gave up) is
+ *     read with kda_static_scratch_status(), not kda_workspace_status().
  */
 #define KDA_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
 kda_status_t kda_forward_static_scratch(const void* q, const void* k, const void* v, const void* z,
                                         const float* A, const float* beta, const float* initial_state,
                                         const int32_t* cu_seqlens, void* out, float* final_state,
                                         const kda_problem_t* problem, void* stream);
+
+/*
+ * Synchronises `stream` and reads the check word of the last kda_forward_static_scratch call in the
+ * current context (the word at the start of the library's scratch array): KDA_OK,
+ * KDA_ERR_DEVICE_CHECK or KDA_ERR_TIMEOUT as for kda_workspace_status.  Allocates nothing.
+ * The paper has no counterpart to this call.
+ */
+kda_status_t kda_static_scratch_status(void* stream);
 
 /*
  * Synchronises `stream` and reads the device-side check word that kda_forward keeps in its
@@ -281,7 +297,7 @@ int32_t kda_profile_read(kda_kernel_time_t* out, int32_t max_entries);
 /* ABI version of this header: (major << 16) | minor. */
 uint32_t kda_abi_version(void);
 
-#define KDA_ABI_VERSION ((1u << 16) | 2u)
+#define KDA_ABI_VERSION ((1u << 16) | 3u)
 
 #ifdef __cplusplus
 }

@@ -34,7 +34,7 @@ G_MIN = -5.0
 EXPORTS = ("kda_forward_workspace_bytes", "kda_forward", "kda_decode_step", "kda_workspace_status",
            "kda_status_string", "kda_profile_enable", "kda_profile_read", "kda_abi_version",
            "kda_forward_static_scratch", "kda_forward_plan", "kda_decode_replay", "kda_prologue",
-           "kda_epilogue")
+           "kda_epilogue", "kda_static_scratch_status")
 
 # Size of the library's own scratch array used by kda_forward_static_scratch.
 KDA_STATIC_SCRATCH_BYTES = 8 << 20
@@ -101,6 +101,8 @@ def lib():
             L.kda_profile_read.argtypes = [ctypes.POINTER(KdaKernelTime), ctypes.c_int32]
             L.kda_forward_static_scratch.restype = ctypes.c_int
             L.kda_forward_static_scratch.argtypes = [_vp] * 10 + [P, _vp]
+            L.kda_static_scratch_status.restype = ctypes.c_int
+            L.kda_static_scratch_status.argtypes = [_vp]
             L.kda_forward_plan.restype = ctypes.c_int
             L.kda_forward_plan.argtypes = [P, ctypes.c_size_t, ctypes.POINTER(KdaPlan)]
             L.kda_abi_version.restype = ctypes.c_uint32
@@ -363,6 +365,12 @@ def kda_epilogue(o, gate, weight, eps: float = 1e-5, y=None, stream=None):
 def kda_workspace_status(workspace, stream=None) -> int:
     """Synchronise and return the device-side check status of a forward workspace."""
     return int(lib().kda_workspace_status(_ptr(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream)))
+
+
+def kda_static_scratch_status(stream=None) -> int:
+    """Synchronise and return the device-side check status of the last kda_forward_static_scratch
+    call in the current context."""
+    return int(lib().kda_static_scratch_status(_stream(stream)))
 
 
 def kda_abi_version() -> int:

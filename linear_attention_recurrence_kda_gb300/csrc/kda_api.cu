@@ -284,6 +284,14 @@ kda_status_t kda_forward(const void* q, const void* k, const void* v, const void
     a.seg_chunks = L.seg_chunks;
     a.max_seg = L.max_seg;
     a.seg_mode = 0;
+    a.handoff_tries = kda::kHandoffTries;
+    if (const char* env = std::getenv("KDA_DEBUG_HANDOFF_TRIES")) {
+        // debugging aid, off unless set: fewer tries make the state pass's hand-off waits give up,
+        // which exercises the timeout path (reported as KDA_ERR_TIMEOUT by the status readers)
+        char* end = nullptr;
+        const unsigned long v = std::strtoul(env, &end, 10);
+        if (end != env && *end == '\0' && v < kda::kHandoffTries) a.handoff_tries = (uint32_t)v;
+    }
     a.seg_in = reinterpret_cast<float*>(ws + L.seg_in_off);
     a.seg_st = reinterpret_cast<float*>(ws + L.seg_st_off);
     a.seg_mt = reinterpret_cast<float*>(ws + L.seg_mt_off);

@@ -32,6 +32,11 @@ constexpr int kChunk = 16;  // tokens per chunk: a chunk's log-decay stays in [1
 constexpr uint32_t kCheckBadSeqlens = 1u;
 constexpr uint32_t kCheckTimeout = 2u;
 
+// Tries (of up to 20 us each) of a bounded wait in the tensor-core kernels: ~2.6 s at most.
+constexpr uint32_t kWaitTries = 1u << 17;
+// Default tries of the split plan's state-pass hand-off waits (one warp role waiting for another).
+constexpr uint32_t kHandoffTries = kWaitTries;
+
 struct ForwardLayout {
     size_t status_off, g_off, w_off, ut_off, blocks_off, seg_in_off, seg_st_off, seg_mt_off, total;
     int32_t seg_chunks, max_seg;
@@ -141,6 +146,8 @@ struct PrefillArgs {
     int32_t max_seg;          // segments of the longest sequence
     int32_t seg_mode;         // 0: outputs; 1: end state from zero (S~); 2: transition (M)
     int32_t prep_run;         // preparation kernel: 32-token steps per CTA (set by its launcher)
+    uint32_t handoff_tries;   // state pass: tries of a hand-off wait before it gives up (kHandoffTries;
+                              // KDA_DEBUG_HANDOFF_TRIES lowers it to exercise the timeout path)
     float* seg_in;            // [N][H][max_seg][d][d] incoming state of every segment (scan output)
     float* seg_st;            // [N][H][max_seg][d][d] S~ of every segment
     float* seg_mt;            // [N][H][max_seg] M of every segment, seg_m_off format (64 KB each)

@@ -54,7 +54,7 @@ using tcc::u2f;
 constexpr int NEPI = 256;                  // epilogue threads (warps 0..7)
 constexpr int NTHREADS = NEPI + 32;        // + the control warp
 constexpr int CTRL = NEPI;                 // the control thread (warp 8, lane 0)
-constexpr uint32_t WAIT_LIMIT = 1u << 17;  // tries of up to 20 us each: ~2.6 s at most
+constexpr uint32_t WAIT_LIMIT = kWaitTries;  // drain waits: tries of up to 20 us each, ~2.6 s at most
 constexpr int CT = tcc::PAIR;              // tokens per step (32)
 constexpr int NSLOT = 2;                   // ring depth (steps in flight)
 constexpr uint32_t SLOT = 54272;           // ring slot stride (a multiple of 1024 >= BLK_BYTES)
@@ -83,12 +83,16 @@ constexpr uint32_t TM_S = 64;     // S^T fp32 (lanes = j, columns = c), 128 colu
 constexpr uint32_t TM_SA = 192;   // bf16 S^T as the A operand of D1: c pairs, 64 columns
 constexpr uint32_t TM_COLS = 256;
 
-// Bounded wait that gives up at once when the CTA has been told to stop; on a timeout it raises
-// the stop flag itself.  Returns true when the phase completed.
-__device__ __forceinline__ bool wait_or_stop(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag)
+// Bounded hand-off wait (`tries` tries) that gives up at once when the CTA has been told to stop;
+// on a timeout it raises the stop flag itself.  Returns true when the phase completed.  Giving up
+// here is always safe: whoever stops touches no ring slot or tensor memory afterwards, and the
+// control thread drains its copies and tensor-core work (with the full WAIT_LIMIT) before the CTA
+// releases its shared and tensor memory.
+__device__ __forceinline__ bool wait_or_stop(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                             uint32_t tries)
 {
     if (*abort_flag != 0u) return false;
-    if (tc::mbar_wait(bar, parity, WAIT_LIMIT)) return true;
+    if (tc::mbar_wait(bar, parity, tries)) return true;
     *abort_flag = 1u;
     return false;
 }
@@ -174,9 +178,9 @@ __device__ __forceinline__ void state_pass(const PrefillArgs& a)
         const uint32_t boff = mode == 0 ? tcc::BLK_PK : tcc::BLK_KT;
         for (int s = 0; s < nsteps; ++s) {
             unsigned char* blk = slot_ptr(s);
-            if (!wait_or_stop(&bar_f[s % NSLOT], fill_parity(s), abort_flag)) break;
+            if (!wait_or_stop(&bar_f[s % NSLOT], fill_parity(s), abort_flag, a.handoff_tries)) break;
             seen = (uint32_t)s + 1;
-            if (!wait_or_stop(bar_sa, (uint32_t)(s & 1), abort_flag)) break;
+            if (!wait_or_stop(bar_sa, (uint32_t)(s & 1), abort_flag, a.handoff_tries)) break;
             tc::fence_after_sync();
             const uint64_t d0 = tc::desc_sw128(tc::smem_u32(blk + tcc::BLK_WQ));
 #pragma unroll
@@ -187,7 +191,7 @@ __device__ __forceinline__ void state_pass(const PrefillArgs& a)
             }
             tc::umma_commit(bar_d1);
             committed = true;
-            if (!wait_or_stop(bar_u, (uint32_t)(s & 1), abort_flag)) break;
+            if (!wait_or_stop(bar_u, (uint32_t)(s & 1), abort_flag, a.handoff_tries)) break;
             tc::fence_after_sync();
             // [O^T | S^T] += U^T [P ; K~^T]^T as hi*hi + hi*lo + lo*hi, one K = 16 half of the step's
             // tokens at a time (without outputs: S^T += U^T K~ alone)
@@ -204,7 +208,7 @@ __device__ __forceinline__ void state_pass(const PrefillArgs& a)
             tc::umma_commit(bar_fu);
             // the update is the last reader of this slot: refill it once the update is done
             if (s + NSLOT < nsteps) {
-                if (!wait_or_stop(bar_fu, (uint32_t)(s & 1), abort_flag)) break;
+                if (!wait_or_stop(bar_fu, (uint32_t)(s & 1), abort_flag, a.handoff_tries)) break;
                 committed = false;
                 issue_load(s + NSLOT);
             }
@@ -224,7 +228,7 @@ __device__ __forceinline__ void state_pass(const PrefillArgs& a)
         // every wait is decided for the whole warp, so that the warp-collective tensor-memory
         // instructions below always run on all 32 lanes
         auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
-            return __all_sync(0xffffffffu, wait_or_stop(bar, parity, abort_flag));
+            return __all_sync(0xffffffffu, wait_or_stop(bar, parity, abort_flag, a.handoff_tries));
         };
         const int q4 = w & 3;    // TMEM lane quarter
         const int h2 = w >> 2;   // which half of the key channels (and of the step's tokens) this warp covers

@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert B.kda_abi_version() == (1 << 16) | 2
+    assert B.kda_abi_version() == (1 << 16) | 3
     for code in range(7):
         s = B.status_string(code)
         assert s.startswith("KDA_")
@@ -318,3 +318,17 @@ def test_fp32_stage_layout_matches_the_library():
         ws[off:off + a.nbytes] = torch.from_numpy(a.reshape(-1).view(np.uint8).copy())
     for got, want in zip(fp32_stage_views(ws, T, H, dk, dv), ref):
         np.testing.assert_array_equal(got, want)
+
+
+def test_split_stage_layout_matches_the_library(monkeypatch):
+    """The split-plan layout the stage-parity tests read (check word, operand blocks, then S_in, S~
+    and M per segment) has exactly the size the library reports, unsegmented and segmented."""
+    from stages import split_layout
+    for seg in ("0", "4", "2"):
+        monkeypatch.setenv("KDA_SEGMENT_CHUNKS", seg)
+        for (N, T, ml, H) in ((5, 464, 250, 2), (1, 4096, 4096, 16), (3, 97, 64, 1)):
+            p = _prob(num_seqs=N, total_tokens=T, max_seqlen=ml, num_heads=H, d_k=128, d_v=128, io_dtype=B.KDA_BF16)
+            wsb = B.kda_forward_workspace_bytes(p)
+            pl = B.kda_forward_plan(p, wsb)
+            assert pl["split"]
+            assert split_layout(T, N, H, pl["num_segments"])[4] == wsb, (seg, N, T, H, pl)

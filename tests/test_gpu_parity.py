@@ -210,6 +210,59 @@ def test_gate_floor_extreme_decay_fp32():
     check(sf, ref_s, torch.float32, "state")
 
 
+@pytest.mark.parametrize("d", [32, 64, 128])
+def test_gate_floor_extreme_decay_fp32_all_widths(d):
+    """The fp32 path at the decay floor for every supported width, with a ragged varlen batch."""
+    inp = I.make_inputs(1, lengths=[48, 17, 0, 33], num_heads=2, d=d, io_dtype=torch.float32, seed=12 + d)
+    inp["z"] = torch.full_like(inp["z"], 60.0)
+    out, sf = gpu_forward(inp)
+    ref_o, ref_s = oracle_forward(inp)
+    check(out, ref_o, torch.float32, "out")
+    check(sf, ref_s, torch.float32, "state")
+
+
+def _decay_floor(inp):
+    inp["z"] = torch.full_like(inp["z"], 60.0)  # sigmoid saturates: every log-decay at g_min
+
+
+def _half_floor(inp):
+    z = inp["z"].float()
+    z[..., :64] = -1e4  # no decay at all on half the key channels ...
+    z[..., 64:] = 60.0  # ... and the floor on the other half
+    inp["z"] = z.to(inp["z"].dtype)
+
+
+def _large_a(inp):
+    inp["A"] = torch.full_like(inp["A"], 4.0)  # e^A = 55: the gate is a near step function of z
+
+
+def _small_a(inp):
+    inp["A"] = torch.full_like(inp["A"], -4.0)  # e^A = 0.018: every log-decay near g_min / 2
+
+
+DECAY_EXTREMES = {"floor": _decay_floor, "half-floor": _half_floor, "large-A": _large_a, "small-A": _small_a}
+
+
+@pytest.mark.parametrize("case", list(DECAY_EXTREMES))
+@pytest.mark.parametrize("plan,seg", [("split", "0"), ("split", "2"), ("split", "6"), ("fused", "0"), ("fused", "3")],
+                         ids=["split-1seg", "split-seg2", "split-seg6", "fused-1seg", "fused-seg3"])
+def test_tensor_core_decay_extremes(monkeypatch, case, plan, seg):
+    """The bf16 d = 128 tensor-core path at the edges of the gate's range, on both plans, unsegmented
+    and with several segments: every log-decay at the floor (a 16-token chunk spans e^-80 and a
+    32-token step e^-160, so K / Gamma reaches e^80 and Q Gamma e^-80 inside the hi/lo operands), no
+    decay on half the key channels next to the floor on the other half, and a near-step gate
+    (large A^h) or a flat one (small A^h).  Lengths 17, 33 and 250 give ragged last chunks and steps."""
+    monkeypatch.setenv("KDA_TC_PLAN", plan)
+    monkeypatch.setenv("KDA_SEGMENT_CHUNKS", seg)
+    inp = I.make_inputs(1, lengths=[17, 33, 250, 0, 64], num_heads=3, d=128, seed=41)
+    DECAY_EXTREMES[case](inp)
+    out, sf = gpu_forward(inp)
+    ref_o, ref_s = oracle_forward(inp)
+    e1 = check(out, ref_o, torch.bfloat16, "out")
+    e2 = check(sf, ref_s, torch.bfloat16, "final_state")
+    print(f"{case} {plan} seg={seg}: out {e1:.2e}, state {e2:.2e}")
+
+
 def test_in_place_carry_and_no_final_state():
     inp = I.make_inputs(1, lengths=[40, 24], num_heads=2, d=64, io_dtype=torch.float32, seed=13)
     d = to_dev(inp)
@@ -358,7 +411,7 @@ def test_workspace_smaller_than_the_fastest_plan():
 def test_reported_workspace_runs_the_segmented_plan():
     """With exactly kda_forward_workspace_bytes of workspace, a 4096-token, 16-head prefill runs
     the split, segmented plan (operand blocks, segment summaries, scan, outputs), one launch each."""
-    from linear_attention_recurrence_kda_gb300 import profile_cases as P
+    import cases as P
     B.kda_profile_enable(True)
     P.prefill(4096, 16, 0, torch.bfloat16)
     prof = B.kda_profile_read()
@@ -370,7 +423,7 @@ def test_reported_workspace_runs_the_segmented_plan():
 def test_fused_plan_when_forced(monkeypatch):
     """KDA_TC_PLAN=fused selects the fused kernel (its three segmented passes) for the same
     prefill, with a correspondingly smaller reported workspace."""
-    from linear_attention_recurrence_kda_gb300 import profile_cases as P
+    import cases as P
     prob = B.make_problem(1, 4096, 4096, 16, 128, 128, torch.bfloat16)
     split_ws = B.kda_forward_workspace_bytes(prob)
     monkeypatch.setenv("KDA_TC_PLAN", "fused")

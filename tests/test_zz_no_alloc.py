@@ -52,3 +52,23 @@ def test_rejects_problems_larger_than_the_static_scratch():
     assert e.value.status == B.KDA_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert torch.all(out == 3.0)
+
+
+def test_static_scratch_status_reports_bad_offsets():
+    """The check word of a call without a workspace is read back through kda_static_scratch_status:
+    offsets that violate the descriptor are reported (the bad sequences skipped, the good one
+    computed), and the next valid call clears the word."""
+    inp = I.make_inputs(1, lengths=[32, 32, 32], num_heads=2, d=32, io_dtype=torch.float32, seed=16)
+    d = to_dev(inp)
+    bad = torch.tensor([0, 32, 20, 96], dtype=torch.int32, device="cuda")  # lengths 32, -12, 76 > 64
+    out = torch.full((96, 2, 32), 7.0, device="cuda")
+    B.kda_forward_static_scratch(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], initial_state=d["S0"],
+                                 cu_seqlens=bad, max_seqlen=64, out=out)
+    assert B.kda_static_scratch_status() == B.KDA_ERR_DEVICE_CHECK
+    assert torch.all(out[32:] == 7.0)
+    ref_o, _ = B.kda_forward(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], initial_state=d["S0"],
+                             cu_seqlens=d["cu_seqlens"], max_seqlen=32)
+    check(out[:32], ref_o[:32].double().cpu().numpy(), torch.float32, "sequence 0")
+    B.kda_forward_static_scratch(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], cu_seqlens=d["cu_seqlens"],
+                                 max_seqlen=32)
+    assert B.kda_static_scratch_status() == B.KDA_OK
