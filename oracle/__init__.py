@@ -25,7 +25,8 @@ What is computed (see the C file for the step-by-step statement):
 * ``prologue``    -- short convolution, Swish and (q, k) regularised L2 normalisation of the
                      projections (what ``kda_prologue`` computes), numpy in float64.
 * ``epilogue``    -- head-wise RMSNorm and sigmoid output gate (what ``kda_epilogue`` computes).
-* ``backward``    -- reverse-mode gradients of ``forward`` (numpy, float64; no GPU counterpart yet).
+* ``backward``    -- reverse-mode gradients of ``forward`` (numpy, float64; what ``kda_backward``
+                     computes).
 """
 from __future__ import annotations
 
@@ -241,6 +242,14 @@ def _sigmoid(x):
     return np.where(x >= 0, 1.0 / (1.0 + e), e / (1.0 + e))
 
 
+def _sigmoid_slope(x):
+    """Slope of the logistic function, sigmoid(x) (1 - sigmoid(x)), as e^{-|x|} / (1 + e^{-|x|})^2: the
+    same function, written so that no 1 - sigmoid(x) is formed (that difference cancels to zero in
+    float64 once |x| passes about 37, where the gate saturates)."""
+    e = np.exp(-np.abs(x))
+    return e / ((1.0 + e) * (1.0 + e))
+
+
 def _seq_index(T: int, cu) -> np.ndarray:
     """Sequence start of every token (tokens of empty sequences do not exist)."""
     cu = _cu(cu, T)
@@ -309,7 +318,8 @@ def backward(q, k, v, z, A, beta, dO, dS_final, S0=None, cu_seqlens=None, g_min:
         dq = S_t dO_t;  dS += q dO_t^T;  dk = dS u;  du = dS^T k;  dv = beta du;
         dbeta = du . (v - r);  dr = -beta du;  dSbar = dS + k dr^T;  dk += Sbar dr;
         dalpha_c = sum_j dSbar[c, j] S_{t-1}[c, j];  dS_{t-1} = Diag(alpha) dSbar;
-        dx = dalpha alpha g_min sigmoid(x) (1 - sigmoid(x));  dz = dx e^{A_h};  dA_h += sum dx x.
+        dx = dalpha alpha g_min sigmoid'(x);  dz = dx e^{A_h};  dA_h += sum dx x
+    (sigmoid'(x) = sigmoid(x) (1 - sigmoid(x)), evaluated without cancellation).
     Plain numpy in float64, for test sizes."""
     q, k, v, z, A, beta, dO, dS_final, S0 = map(_f64, (q, k, v, z, A, beta, dO, dS_final, S0))
     T, H, dk_ = k.shape
@@ -351,7 +361,7 @@ def backward(q, k, v, z, A, beta, dO, dS_final, S0=None, cu_seqlens=None, g_min:
                 dkk[t, h] = dk_t + Sbar @ dr
                 dal = (dSbar * S_prev).sum(axis=1)
                 dS = al[:, None] * dSbar
-                dx = dal * al * g_min * sig * (1.0 - sig)
+                dx = dal * al * g_min * _sigmoid_slope(x)
                 dz[t, h] = dx * eA
                 dA[h] += (dx * x).sum()
             dS0[n, h] = dS

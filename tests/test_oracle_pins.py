@@ -545,3 +545,31 @@ def test_backward_zero_upstream_gives_zero():
     grads = oracle.backward(q, k, v, z, A, b, np.zeros_like(dO), np.zeros_like(dSf), S0=S0, cu_seqlens=cu)
     for gr in grads:
         np.testing.assert_array_equal(gr, 0.0)
+
+
+def test_sigmoid_slope_closed_form():
+    """The gate's slope sigmoid(x) (1 - sigmoid(x)) equals 1 / (4 cosh^2(x / 2)) everywhere, including
+    where the sigmoid saturates and 1 - sigmoid(x) cannot be formed in float64."""
+    x = np.concatenate([np.linspace(-700.0, 700.0, 2801), [0.0, 1e-9, -36.9, 37.5, 45.0, -60.0]])
+    np.testing.assert_allclose(oracle._sigmoid_slope(x), 0.25 / np.cosh(x / 2.0) ** 2, rtol=1e-13, atol=0)
+    assert oracle._sigmoid_slope(np.array([45.0]))[0] > 0.0
+
+
+def test_backward_dz_at_a_saturated_gate():
+    """One token from a random state, L = sum(dS_f * S_1): with S_1 = (I - b k k^T) Diag(alpha) S_0 +
+    b k v^T, dL/dalpha_c = sum_j [(I - b k k^T)^T dS_f]_{cj} S_0[c, j], and through Equation 5
+    dz_c = dL/dalpha_c * alpha_c * g_min * e^{-x_c} / (1 + e^{-x_c})^2 * e^A with x = e^A z.  Here
+    x reaches 45 (a gate at its floor), where a central difference cannot resolve the slope."""
+    rng = np.random.default_rng(63)
+    q, k, v, z, A, b, S0, cu, _, dSf = _bw_case(rng, [1], 1, 4, 3)
+    z = np.array([[[30.0, 12.0, -25.0, 2.0]]])
+    A = np.array([np.log(1.5)])
+    _, al = oracle.gate(z, A)
+    kk = k[0, 0]
+    P = np.eye(4) - b[0, 0] * np.outer(kk, kk)
+    dal = ((P.T @ dSf[0, 0]) * S0[0, 0]).sum(axis=1)
+    x = 1.5 * z[0, 0]
+    expect = dal * al[0, 0] * (-5.0) * np.exp(-np.abs(x)) / (1.0 + np.exp(-np.abs(x))) ** 2 * 1.5
+    grads = oracle.backward(q, k, v, z, A, b, np.zeros((1, 1, 3)), dSf, S0=S0)
+    np.testing.assert_allclose(grads[3][0, 0], expect, rtol=1e-10, atol=0)
+    assert abs(grads[3][0, 0, 0]) > 0.0
