@@ -112,7 +112,9 @@ kda_status_t kda_forward_plan(const kda_problem_t* problem, size_t workspace_byt
  *                   initial_state (in-place carry); any other overlap is rejected.
  *   workspace     : device scratch, 256-byte aligned, not shared with a concurrently running
  *                   call.  kda_forward_workspace_bytes(problem) bytes allow the fastest plan.  For
- *                   bf16 inputs with d_k = d_v = 128 that plan first prepares the
+ *                   bf16 inputs with d_k = d_v = 128 and g_min >= -5 (steeper floors run on the
+ *                   fp32 path, whose workspace holds 4 (2 d_k + d_v) bytes per token and head)
+ *                   that plan first prepares the
  *                   state-independent operands of every pair of chunks in parallel (52.5 KB per
  *                   32 tokens and head, held in the workspace) and then runs the sequential state
  *                   pass in 32-token steps; a workspace too
@@ -150,6 +152,45 @@ kda_status_t kda_forward(const void* q, const void* k, const void* v, const void
 kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const void* z,
                              const float* A, const float* beta, float* state, void* out,
                              const kda_problem_t* problem, void* stream);
+
+/*
+ * Bytes of device workspace kda_backward needs for this problem (0 if the descriptor is invalid):
+ * per token and head 4 (2 d_k + 3 d_v + 16) bytes, plus two fp32 d_k x d_v states (the state
+ * entering each 16-token chunk and the gradient reaching its end) per chunk slot and head, with
+ * T_tot / 16 + N + 1 slots -- about 10.6 KiB per token and head at d_k = d_v = 128.
+ */
+size_t kda_backward_workspace_bytes(const kda_problem_t* problem);
+
+/*
+ * Gradients of kda_forward for training: given dL/d(out) and dL/d(final_state), the gradients of
+ * L with respect to q, k, v, z, A, beta and the initial state.  The derivative is the analytic one
+ * of the recurrence (Equation 1 with the gate of Equation 5, "Kimi K3: the paper and proofs side
+ * by side", section 2.1.1) taken chunk by chunk in reverse; the pages check the same analytic
+ * derivative against finite differences ("Kimi K3: architecture, derivations and a pinned-source
+ * audit", section "CPU laboratory") and name comparing "sequence outputs and gradients" as the
+ * test of a kernel (same page, section "Pinned evidence and execution boundary").
+ *
+ *   q, k, v, z, A, beta, initial_state, cu_seqlens : the forward call's inputs, as for kda_forward
+ *                   (initial_state NULL: zeros).
+ *   d_out         : [T_tot,H,d_v] io dtype, dL/d(out).
+ *   d_final_state : [N,H,d_k,d_v] fp32, dL/d(final_state), or NULL (zero).
+ *   dq, dk, dz    : [T_tot,H,d_k] io dtype outputs;  dv : [T_tot,H,d_v] io dtype output.
+ *   dA            : [H] fp32 output (summed over all tokens, key channels and sequences).
+ *   dbeta         : [T_tot,H] fp32 output.
+ *   d_initial_state : [N,H,d_k,d_v] fp32 output, or NULL (not written).
+ *   workspace     : kda_backward_workspace_bytes(problem) bytes of device scratch, 256-byte
+ *                   aligned, not shared with a concurrently running call.
+ * Outputs must not overlap any input, each other or the workspace.  Supported: every d_k, d_v and io
+ * dtype of kda_forward with g_min >= -5.4 (a 16-token chunk's 1/Gamma stays a finite fp32 number;
+ * steeper floors return KDA_ERR_UNSUPPORTED).  The forward pass is recomputed inside the call (only
+ * the inputs are needed).  Arithmetic is fp32 throughout; gradients are rounded to the io dtype once.
+ * Invalid cu_seqlens are reported through kda_workspace_status() as for kda_forward.
+ */
+kda_status_t kda_backward(const void* q, const void* k, const void* v, const void* z, const float* A,
+                          const float* beta, const float* initial_state, const int32_t* cu_seqlens,
+                          const void* d_out, const float* d_final_state, void* dq, void* dk, void* dv, void* dz,
+                          float* dA, float* dbeta, float* d_initial_state, const kda_problem_t* problem,
+                          void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Speculative-decode state replay: a window of L drafted tokens for each of N sequences, run from a
@@ -277,7 +318,7 @@ const char* kda_status_string(kda_status_t status);
 
 /*
  * Per-kernel device timing, for measurement tools.  While enabled, every kernel launched by
- * kda_forward / kda_decode_step / kda_decode_replay / kda_prologue / kda_epilogue is bracketed by two CUDA events recorded on the call's stream;
+ * kda_forward / kda_backward / kda_decode_step / kda_decode_replay / kda_prologue / kda_epilogue is bracketed by two CUDA events recorded on the call's stream;
  * kda_profile_read synchronises on those events and returns, per kernel name, the number of
  * launches and their summed device time.  Enabling (or disabling) discards earlier records.
  * Events are host-side objects: no device memory is allocated.  Not thread-safe against
@@ -297,7 +338,7 @@ int32_t kda_profile_read(kda_kernel_time_t* out, int32_t max_entries);
 /* ABI version of this header: (major << 16) | minor. */
 uint32_t kda_abi_version(void);
 
-#define KDA_ABI_VERSION ((1u << 16) | 3u)
+#define KDA_ABI_VERSION ((1u << 16) | 4u)
 
 #ifdef __cplusplus
 }

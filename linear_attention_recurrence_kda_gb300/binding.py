@@ -34,7 +34,7 @@ G_MIN = -5.0
 EXPORTS = ("kda_forward_workspace_bytes", "kda_forward", "kda_decode_step", "kda_workspace_status",
            "kda_status_string", "kda_profile_enable", "kda_profile_read", "kda_abi_version",
            "kda_forward_static_scratch", "kda_forward_plan", "kda_decode_replay", "kda_prologue",
-           "kda_epilogue", "kda_static_scratch_status")
+           "kda_epilogue", "kda_static_scratch_status", "kda_backward_workspace_bytes", "kda_backward")
 
 # Size of the library's own scratch array used by kda_forward_static_scratch.
 KDA_STATIC_SCRATCH_BYTES = 8 << 20
@@ -101,6 +101,10 @@ def lib():
             L.kda_profile_read.argtypes = [ctypes.POINTER(KdaKernelTime), ctypes.c_int32]
             L.kda_forward_static_scratch.restype = ctypes.c_int
             L.kda_forward_static_scratch.argtypes = [_vp] * 10 + [P, _vp]
+            L.kda_backward_workspace_bytes.restype = ctypes.c_size_t
+            L.kda_backward_workspace_bytes.argtypes = [P]
+            L.kda_backward.restype = ctypes.c_int
+            L.kda_backward.argtypes = [_vp] * 17 + [P, _vp, ctypes.c_size_t, _vp]
             L.kda_static_scratch_status.restype = ctypes.c_int
             L.kda_static_scratch_status.argtypes = [_vp]
             L.kda_forward_plan.restype = ctypes.c_int
@@ -248,6 +252,58 @@ def kda_forward_static_scratch(q, k, v, z, A, beta, initial_state=None, cu_seqle
     if st != KDA_OK:
         raise KdaError(st, "kda_forward_static_scratch")
     return out, final_state
+
+
+def kda_backward_workspace_bytes(problem: KdaProblem) -> int:
+    return int(lib().kda_backward_workspace_bytes(ctypes.byref(problem)))
+
+
+def kda_backward(q, k, v, z, A, beta, d_out, d_final_state=None, initial_state=None, cu_seqlens=None,
+                 max_seqlen: Optional[int] = None, want_d_initial: bool = True, workspace=None,
+                 g_min: float = G_MIN, stream=None):
+    """Gradients of kda_forward (see include/kda.h): for L = <d_out, out> + <d_final_state,
+    final_state>, returns (dq, dk, dv, dz, dA, dbeta, d_initial_state or None).  Shapes and dtypes
+    as for :func:`kda_forward`; d_out [T, H, d_v] in the io dtype, d_final_state [N, H, d_k, d_v]
+    fp32 or None (zero)."""
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    dev = k.device
+    dt = k.dtype
+    if cu_seqlens is not None:
+        N = cu_seqlens.shape[0] - 1
+        _need(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,), dev)
+        if max_seqlen is None:
+            max_seqlen = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if N > 0 else 0
+    else:
+        N = (initial_state.shape[0] if initial_state is not None else
+             d_final_state.shape[0] if d_final_state is not None else 1)
+        max_seqlen = T // N
+    for name, t, shp in (("q", q, (T, H, dk)), ("k", k, (T, H, dk)), ("z", z, (T, H, dk)), ("v", v, (T, H, dv)),
+                         ("d_out", d_out, (T, H, dv))):
+        _need(t, name, dt, shp, dev)
+    _need(A, "A", torch.float32, (H,), dev)
+    _need(beta, "beta", torch.float32, (T, H), dev)
+    for name, t in (("initial_state", initial_state), ("d_final_state", d_final_state)):
+        if t is not None:
+            _need(t, name, torch.float32, (N, H, dk, dv), dev)
+    dq, dk_, dz = (torch.empty((T, H, dk), dtype=dt, device=dev) for _ in range(3))
+    dv_ = torch.empty((T, H, dv), dtype=dt, device=dev)
+    dA = torch.empty((H,), dtype=torch.float32, device=dev)
+    dbeta = torch.empty((T, H), dtype=torch.float32, device=dev)
+    dS0 = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev) if want_d_initial else None
+    prob = make_problem(N, T, max_seqlen, H, dk, dv, dt, g_min)
+    wsb = kda_backward_workspace_bytes(prob)
+    if wsb == 0:
+        raise KdaError(KDA_ERR_INVALID_ARG, "kda_backward_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    st = lib().kda_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(beta), _ptr(initial_state),
+                            _ptr(cu_seqlens), _ptr(d_out), _ptr(d_final_state), _ptr(dq), _ptr(dk_), _ptr(dv_),
+                            _ptr(dz), _ptr(dA), _ptr(dbeta), _ptr(dS0), ctypes.byref(prob), _ptr(workspace),
+                            ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_backward")
+    return dq, dk_, dv_, dz, dA, dbeta, dS0
 
 
 def kda_decode_step(q, k, v, z, A, beta, state, out=None, g_min: float = G_MIN, stream=None):

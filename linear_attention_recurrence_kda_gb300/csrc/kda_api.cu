@@ -320,6 +320,109 @@ kda_status_t kda_forward(const void* q, const void* k, const void* v, const void
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+size_t kda_backward_workspace_bytes(const kda_problem_t* problem)
+{
+    if (check_descriptor(problem, Call::Forward) != KDA_OK) return 0;
+    return kda::backward_layout(*problem).total;
+}
+
+kda_status_t kda_backward(const void* q, const void* k, const void* v, const void* z, const float* A,
+                          const float* beta, const float* initial_state, const int32_t* cu_seqlens,
+                          const void* d_out, const float* d_final_state, void* dq, void* dk, void* dv, void* dz,
+                          float* dA, float* dbeta, float* d_initial_state, const kda_problem_t* problem,
+                          void* workspace, size_t workspace_bytes, void* stream)
+{
+    kda_status_t st = check_descriptor(problem, Call::Forward);
+    if (st != KDA_OK) return st;
+    const kda_problem_t& p = *problem;
+    if (p.g_min < kda::kBackwardGminLimit) return KDA_ERR_UNSUPPORTED;
+    const bool equal = cu_seqlens == nullptr;
+    if (equal && (p.total_tokens % p.num_seqs) != 0) return KDA_ERR_INVALID_ARG;
+    if (equal && (int64_t)p.max_seqlen < p.total_tokens / p.num_seqs) return KDA_ERR_INVALID_ARG;
+    const int64_t cps = chunks_per_seq(p);
+    if ((int64_t)p.num_seqs * (cps > 0 ? cps : 1) > 2147483647LL) return KDA_ERR_UNSUPPORTED;
+    const bool has_tokens = p.total_tokens > 0;
+    if (A == nullptr || dA == nullptr) return KDA_ERR_INVALID_ARG;
+    if (has_tokens && (!q || !k || !v || !z || !beta || !d_out || !dq || !dk || !dv || !dz || !dbeta))
+        return KDA_ERR_INVALID_ARG;
+
+    const size_t io = io_size(p.io_dtype);
+    const size_t tk = (size_t)p.total_tokens * p.num_heads * p.d_k;
+    const size_t tv = (size_t)p.total_tokens * p.num_heads * p.d_v;
+    const size_t th = (size_t)p.total_tokens * p.num_heads;
+    const size_t sb = (size_t)p.num_seqs * p.num_heads * p.d_k * p.d_v * sizeof(float);
+    for (const void* ptr : {q, k, v, z, d_out, (const void*)dq, (const void*)dk, (const void*)dv, (const void*)dz,
+                            (const void*)initial_state, (const void*)d_final_state, (const void*)d_initial_state}) {
+        if (!aligned(ptr, 16)) return KDA_ERR_INVALID_ARG;
+    }
+    for (const void* ptr : {(const void*)A, (const void*)beta, (const void*)cu_seqlens, (const void*)dA,
+                            (const void*)dbeta}) {
+        if (!aligned(ptr, 4)) return KDA_ERR_INVALID_ARG;
+    }
+    const Range in[10] = {range_of(q, tk * io), range_of(k, tk * io), range_of(z, tk * io), range_of(v, tv * io),
+                          range_of(A, p.num_heads * sizeof(float)), range_of(beta, th * sizeof(float)),
+                          range_of(initial_state, sb),
+                          range_of(cu_seqlens, cu_seqlens ? (size_t)(p.num_seqs + 1) * sizeof(int32_t) : 0),
+                          range_of(d_out, tv * io), range_of(d_final_state, sb)};
+    const Range out[7] = {range_of(dq, tk * io), range_of(dk, tk * io), range_of(dv, tv * io), range_of(dz, tk * io),
+                          range_of(dA, p.num_heads * sizeof(float)), range_of(dbeta, th * sizeof(float)),
+                          range_of(d_initial_state, sb)};
+    for (int i = 0; i < 7; ++i) {
+        for (const Range& r : in) {
+            if (overlaps(out[i], r)) return KDA_ERR_INVALID_ARG;
+        }
+        for (int j = 0; j < i; ++j) {
+            if (overlaps(out[i], out[j])) return KDA_ERR_INVALID_ARG;
+        }
+    }
+    const kda::BackwardLayout L = kda::backward_layout(p);
+    if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < L.total) return KDA_ERR_WORKSPACE;
+    const Range rw = range_of(workspace, L.total);
+    for (const Range& r : in) {
+        if (overlaps(rw, r)) return KDA_ERR_INVALID_ARG;
+    }
+    for (const Range& r : out) {
+        if (overlaps(rw, r)) return KDA_ERR_INVALID_ARG;
+    }
+    for (const void* ptr : {q, k, v, z, (const void*)A, (const void*)beta, (const void*)initial_state,
+                            (const void*)cu_seqlens, d_out, (const void*)d_final_state, (const void*)dq, (const void*)dk,
+                            (const void*)dv, (const void*)dz, (const void*)dA, (const void*)dbeta,
+                            (const void*)d_initial_state, (const void*)workspace}) {
+        st = check_device_pointer(ptr);
+        if (st != KDA_OK) return st;
+    }
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    kda::BackwardArgs b{};
+    kda::PrefillArgs& a = b.f;
+    a.q = q; a.k = k; a.v = v; a.z = z; a.A = A; a.beta = beta;
+    a.s0 = initial_state; a.cu = cu_seqlens; a.out = nullptr; a.s_final = nullptr;
+    a.check = reinterpret_cast<uint32_t*>(ws);
+    a.G = reinterpret_cast<float*>(ws + L.g_off);
+    a.W = reinterpret_cast<float*>(ws + L.w_off);
+    a.Ut = reinterpret_cast<float*>(ws + L.ut_off);
+    a.T_tot = p.total_tokens; a.N = p.num_seqs; a.H = p.num_heads; a.dk = p.d_k; a.dv = p.d_v;
+    a.max_seqlen = equal ? (int32_t)(p.total_tokens / p.num_seqs) : p.max_seqlen;
+    a.chunks_per_seq = (int32_t)cps;
+    a.g_min = p.g_min;
+    a.max_seg = 1;
+    a.handoff_tries = kda::kHandoffTries;
+    b.dout = d_out; b.dS_final = d_final_state;
+    b.dq = dq; b.dk = dk; b.dv = dv; b.dz = dz; b.dA = dA; b.dbeta = dbeta; b.dS0 = d_initial_state;
+    b.P = reinterpret_cast<float*>(ws + L.p_off);
+    b.U = reinterpret_cast<float*>(ws + L.u_off);
+    b.dU = reinterpret_cast<float*>(ws + L.du_off);
+    b.S_chunk = reinterpret_cast<float*>(ws + L.s_off);
+    b.dS_chunk = reinterpret_cast<float*>(ws + L.ds_off);
+    b.dA_part = reinterpret_cast<float*>(ws + L.da_off);
+    b.slots = (int64_t)L.slots;
+    if (cudaMemsetAsync(a.check, 0, sizeof(uint32_t), s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (cudaMemsetAsync(b.dA_part, 0, L.slots * p.num_heads * sizeof(float), s) != cudaSuccess) return KDA_ERR_CUDA;
+    const cudaError_t e = kda::launch_backward(b, p.io_dtype, s);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const void* z, const float* A,
                              const float* beta, float* state, void* out, const kda_problem_t* problem,
                              void* stream)

@@ -49,11 +49,24 @@ constexpr int kPair = 2 * kChunk;  // tokens per state step of the split tensor-
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// bf16 inputs with d_k = d_v = 128 run on the fused tensor-core kernel (no per-token workspace).
+// Steepest log-decay floor the tensor-core kernels take.  They scale a 16-token chunk's keys and
+// queries by Gamma and 1/Gamma referred to the chunk's first token and carry the small ones as
+// bf16 hi/lo pairs; with g_min >= -5 (K3's floor) Gamma >= e^-80 = 2^-115.4 keeps every hi and,
+// but for corrections below 2^-10.6 of the value, every lo part a normal number (the hardware
+// exp2 and the products flush subnormals), and 1/Gamma <= e^80 stays far from overflow.
+// Steeper floors run on the fp32 path, which forms every pairwise decay exp(G_r - G_i) <= 1.
+constexpr float kChunkGminLimit = -5.0f;
+// The backward's chunk factors are plain fp32 numbers (no hi/lo pairs, no flushing): with
+// g_min >= -5.4, Gamma >= e^-86.4 stays normal and 1/Gamma <= e^86.4 finite.
+constexpr float kBackwardGminLimit = -5.4f;
+
+// bf16 inputs with d_k = d_v = 128 run on the tensor-core kernels (they scale keys and queries by
+// Gamma and 1/Gamma of one chunk); other problems, and steeper floors, on the fp32 path, which
+// forms every pairwise decay exp(G_r - G_i) <= 1 directly.
 inline bool use_tensor_core_path(const kda_problem_t& p)
 {
     return p.io_dtype == KDA_BF16 && p.d_k == 128 && p.d_v == 128 && p.total_tokens > 0 &&
-           p.total_tokens < (int64_t(1) << 31);
+           p.total_tokens < (int64_t(1) << 31) && p.g_min >= kChunkGminLimit;
 }
 
 // Chunks of the longest sequence allowed by the descriptor (max_seqlen, at most T_tot).
@@ -171,6 +184,63 @@ __device__ __forceinline__ void store_seg_m(float* seg, int c, int j, float x)
     *reinterpret_cast<__nv_bfloat16*>(base + seg_m_off(c, j)) = hi;
     *reinterpret_cast<__nv_bfloat16*>(base + kSegMPlane + seg_m_off(c, j)) = lo;
 }
+
+// ---------------------------------------------------------------- backward (kda_backward)
+//
+// Workspace of kda_backward (every region 256-byte aligned, offsets from the base):
+//   [0, 256)  check word
+//   G, W, Ut  fp32 [T_tot, H, d]   the forward path's per-chunk G, W and U~ (kda_gate, kda_ut_wy)
+//   P         fp32 [T_tot, H, 16]  row r of each chunk's tril_incl((Q Gamma)(K / Gamma)^T)
+//   U, dU     fp32 [T_tot, H, d_v] U = U~ - W S_in and its gradient
+//   S_chunk   fp32 [slots][H][d_k][d_v]  state entering each chunk
+//   dS_chunk  fp32 [slots][H][d_k][d_v]  gradient reaching the state after each chunk
+//   dA_part   fp32 [slots][H]            per-chunk partial sums of dA
+// Chunk ci of sequence n uses slot cu[n] / 16 + n + ci (slots = T_tot / 16 + N + 1), so the slots
+// of consecutive sequences never overlap.
+struct BackwardLayout {
+    size_t g_off, w_off, ut_off, p_off, u_off, du_off, s_off, ds_off, da_off, total, slots;
+};
+
+inline BackwardLayout backward_layout(const kda_problem_t& p)
+{
+    BackwardLayout L{};
+    const size_t th = (size_t)p.total_tokens * (size_t)p.num_heads;
+    L.slots = (size_t)(p.total_tokens / kChunk) + (size_t)p.num_seqs + 1;
+    const size_t state = (size_t)p.d_k * p.d_v * sizeof(float);
+    L.g_off = 256;
+    L.w_off = align_up(L.g_off + th * p.d_k * sizeof(float), 256);
+    L.ut_off = align_up(L.w_off + th * p.d_k * sizeof(float), 256);
+    L.p_off = align_up(L.ut_off + th * p.d_v * sizeof(float), 256);
+    L.u_off = align_up(L.p_off + th * kChunk * sizeof(float), 256);
+    L.du_off = align_up(L.u_off + th * p.d_v * sizeof(float), 256);
+    L.s_off = align_up(L.du_off + th * p.d_v * sizeof(float), 256);
+    L.ds_off = align_up(L.s_off + L.slots * p.num_heads * state, 256);
+    L.da_off = align_up(L.ds_off + L.slots * p.num_heads * state, 256);
+    L.total = align_up(L.da_off + L.slots * p.num_heads * sizeof(float), 256);
+    return L;
+}
+
+struct BackwardArgs {
+    PrefillArgs f;            // forward inputs, sizes, check word and the G / W / Ut workspace regions
+    const void* dout;         // [T][H][d_v] io dtype
+    const float* dS_final;    // [N][H][d_k][d_v] or null (zero)
+    void* dq;                 // [T][H][d_k] io dtype
+    void* dk;                 // [T][H][d_k] io dtype
+    void* dv;                 // [T][H][d_v] io dtype
+    void* dz;                 // [T][H][d_k] io dtype
+    float* dA;                // [H]
+    float* dbeta;             // [T][H]
+    float* dS0;               // [N][H][d_k][d_v] or null (not written)
+    float* P;                 // workspace regions (see backward_layout)
+    float* U;
+    float* dU;
+    float* S_chunk;
+    float* dS_chunk;
+    float* dA_part;
+    int64_t slots;
+};
+
+cudaError_t launch_backward(const BackwardArgs& b, kda_dtype_t dt, cudaStream_t s);
 
 struct DecodeArgs {
     const void* q;

@@ -22,7 +22,7 @@ def test_reference_arm_json_line():
     assert d["value"] > 0 and d["unit"] == "Mtok/s" and d["higher_is_better"] is True
     assert d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] >= 3 and d["ms_per_step"] > 0
     assert d["vs_baseline"] is None and d["data"] == "synthetic" and d["dtype"] == "f64"
-    assert d["config"]["workload"].startswith("prefill B=1 H=16 T=4096")
+    assert d["config"]["workload"].startswith("prefill B=1 H=8 T=1048576")
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "Mtok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
@@ -53,3 +53,19 @@ def test_ncu_traffic_follows_the_source_hash():
         else:
             assert bench.ncu_traffic(kernel) is None
     assert bench.ncu_traffic("no_such_kernel") is None
+
+
+def test_oracle_sample_layout_gives_every_thread_the_same_units():
+    """The oracle sampler's (heads, value-column block) choice makes the parallel units a whole
+    multiple of the threads, so the reference arm and the cpu_baseline leg time the same work."""
+    for H, dv, nt in ((8, 128, 16), (16, 128, 16), (8, 128, 1), (32, 128, 72), (2, 32, 16), (8, 128, 12)):
+        h, cb = bench.oracle_layout(H, dv, nt)
+        assert 1 <= h <= H and 1 <= cb <= dv and dv % cb == 0
+        assert (h * (dv // cb)) % nt == 0, (H, dv, nt, h, cb)
+    assert bench.oracle_layout(8, 128, 16) == (8, 64)
+    assert bench.oracle_layout(8, 128, 1) == (1, 128)
+
+
+def test_backward_bytes():
+    # read q, k, z, v, beta, dO; write dq, dk, dz, dv, dbeta (bf16 tensors, fp32 beta)
+    assert bench.backward_bytes_per_token_head(128, 128, 2) == 2 * (4 * 128 * 2 + 4) + 128 * 2 == 2312

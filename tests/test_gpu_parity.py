@@ -263,6 +263,20 @@ def test_tensor_core_decay_extremes(monkeypatch, case, plan, seg):
     print(f"{case} {plan} seg={seg}: out {e1:.2e}, state {e2:.2e}")
 
 
+@pytest.mark.parametrize("g_min", [-5.0, -5.4, -8.0, -20.0])
+def test_steep_decay_floor_bf16_d128(g_min):
+    """The tensor-core kernels carry a 16-token chunk's Gamma and 1/Gamma as bf16 hi/lo pairs, whose
+    lo parts fall below the normal fp32 range (and are flushed) for floors steeper than K3's -5, so
+    such problems run on the fp32 path (pairwise decays); at -5 the tensor-core path runs.  Every
+    log-decay sits at the floor here."""
+    inp = I.make_inputs(1, lengths=[40, 17, 64], num_heads=2, d=128, seed=43)
+    inp["z"] = torch.full_like(inp["z"], 60.0)
+    out, sf = gpu_forward(inp, g_min=g_min)
+    ref_o, ref_s = oracle_forward(inp, g_min=g_min)
+    check(out, ref_o, torch.bfloat16, "out")
+    check(sf, ref_s, torch.bfloat16, "final_state")
+
+
 def test_in_place_carry_and_no_final_state():
     inp = I.make_inputs(1, lengths=[40, 24], num_heads=2, d=64, io_dtype=torch.float32, seed=13)
     d = to_dev(inp)
