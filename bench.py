@@ -520,6 +520,7 @@ def main():
     ap.add_argument("--no-backward", action="store_true", help="skip the backward leg")
     ap.add_argument("--no-shapes", action="store_true", help="skip the 4096-token and varlen prefill legs")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
+    ap.add_argument("--no-kcp", action="store_true", help="skip the context-parallel leg (N > 1 only)")
     ap.add_argument("--case", choices=["prefill-tc", "prefill-simt", "decode", "replay", "layer", "backward"],
                     help="run one small invocation for a profiler capture instead of the benchmark")
     ap.add_argument("--tokens", type=int, default=4096)
@@ -607,6 +608,11 @@ def main():
             backward = bench_backward(B, I, dev, stream, max_over_ranks, barrier, pk, pk_src)
         del flush
 
+    # ---- context-parallel prefill of the long context across the ranks (one exchange per call)
+    kcp = None
+    if world > 1 and not args.no_kcp:
+        kcp = bench_kcp(B, I, dev, stream, world, rank, max_over_ranks, barrier)
+
     clk = clocks.stop() if clocks else None
     launches = head["gpu_launches"]
     line = {
@@ -620,13 +626,55 @@ def main():
                    "l2": "inputs larger than L2 (10.8 GB per step), no flush"},
         "step_stats": {k: head[k] for k in ("median_ms", "p90_ms", "plan", "launches_per_step")},
         "roofline": head["roofline"], "tensor": head["tensor"], "shapes": shapes, "decode": decode, "layer": layer,
-        "backward": backward, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
+        "backward": backward, "kcp": kcp, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
     }
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def bench_kcp(B, I, dev, stream, world, rank, max_over_ranks, barrier, reps=5):
+    """Context-parallel prefill of the 1,048,576-token, 8-head sequence split by tokens over the
+    ranks: every rank summarises its range, one all-gather of the summaries (NCCL), the prefix scan
+    and the re-run from the scanned state.  The sequence's total work is fixed as ranks are added
+    (strong scaling); the time is the slowest rank's."""
+    import torch
+    from linear_attention_recurrence_kda_gb300 import context_parallel as CP
+    w = I.WORKLOADS[WORKLOAD]
+    T, H, d = sum(w.lengths), w.num_heads, w.d
+    Tr = T // world
+    gen = torch.Generator(device=dev).manual_seed(w.seed * 1000 + rank)
+
+    def tok(normalise):
+        x = torch.randn(Tr, H, d, generator=gen, device=dev)
+        if normalise:
+            x = x / torch.sqrt((x * x).sum(dim=-1, keepdim=True) + I.L2_EPS)
+        return x.to(w.io_dtype)
+    q, k, v, z = tok(True), tok(True), tok(False), tok(False)
+    A = torch.randn(H, generator=torch.Generator(device=dev).manual_seed(w.seed), device=dev) * I.A_STD
+    beta = torch.sigmoid(torch.randn(Tr, H, generator=gen, device=dev))
+    S0 = torch.randn(1, H, d, d, generator=torch.Generator(device=dev).manual_seed(w.seed), device=dev) * I.S0_STD
+
+    def run():
+        return CP.kcp_forward(q, k, v, z, A, beta, initial_state=S0, num_seqs=1)
+    for _ in range(2):
+        run()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1) / reps)
+    return {"workload": f"{w.name}, tokens split over {world} ranks", "ms_per_step": ms,
+            "value": T / (ms * 1e-3) / 1e6, "unit": "Mtok/s", "scaling": "strong",
+            "exchange_bytes_per_rank": 4 * H * d * (d + d),
+            "flow": "kda_forward_summary, one all-gather, kda_state_scan, kda_forward from the scanned state"}
 
 
 def ncu_traffic_per_token_head(kernel):

@@ -154,6 +154,49 @@ kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const 
                              const kda_problem_t* problem, void* stream);
 
 /*
+ * Context-parallel prefill (KCP) for sequences split across ranks ("Kimi K3" reading notes, section 7,
+ * "Scaling to 1M Tokens: NoPE and KDA Context Parallelism": every rank summarises its token range,
+ * the summaries are exchanged once, and a prefix scan gives every rank the state its range starts
+ * from; "Kimi K3: architecture, derivations and a pinned-source audit", section 4.5: a range of
+ * tokens acts on the state as an affine map, and such maps compose associatively).  A range maps an
+ * incoming state S to M S + S~, with M (d_k x d_k) the range's end state from the identity when
+ * every value is zero and S~ (d_k x d_v) its end state from zero.  The flow on rank r of R:
+ *     kda_forward_summary(own range)        -> (M_r, S~_r)
+ *     all-gather (M, S~) across the ranks   (the caller's collective; 4 d_k (d_k + d_v) bytes per
+ *                                            sequence and head and rank)
+ *     kda_state_scan(count = r)             -> the state the rank's range starts from
+ *     kda_forward(own range, that state)    -> outputs; on rank R - 1 the final state
+ */
+size_t kda_forward_summary_workspace_bytes(const kda_problem_t* problem);
+
+/*
+ * The affine summary of every sequence's token range ("Kimi K3" reading notes, section 7):
+ *   transition      : [N,H,d_k,d_k] fp32 output M (M[c][j]: weight of incoming state row j in row c
+ *                     of the end state).
+ *   state_from_zero : [N,H,d_k,d_v] fp32 output S~.
+ * Inputs, layouts and cu_seqlens as for kda_forward (the initial state plays no part).  Runs
+ * kda_forward twice inside (S~ from zero; M from identity states with zero values and d_v = d_k),
+ * so every kda_forward plan, precision and device check applies; the check word is read with
+ * kda_workspace_status(workspace, ...).  workspace: kda_forward_summary_workspace_bytes(problem)
+ * bytes, 256-byte aligned.  Outputs must not overlap the inputs, each other or the workspace.
+ */
+kda_status_t kda_forward_summary(const void* q, const void* k, const void* v, const void* z, const float* A,
+                                 const float* beta, const int32_t* cu_seqlens, float* transition, float* state_from_zero,
+                                 const kda_problem_t* problem, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The prefix scan of KCP ("Kimi K3" reading notes, section 7): starting from initial_state
+ * ([N,H,d_k,d_v] fp32, NULL: zeros), applies S <- M_i S + S~_i for i = 0 .. count - 1 and writes
+ * the result to state_out ([N,H,d_k,d_v] fp32; may be initial_state itself, no other overlap).
+ *   transition      : [count][N,H,d_k,d_k] fp32 (the gathered M of the ranks before this one, in order)
+ *   state_from_zero : [count][N,H,d_k,d_v] fp32 (their S~)
+ * count = 0 copies the initial state.  problem: num_seqs, num_heads, d_k, d_v (the rest unused).
+ * fp32 arithmetic.
+ */
+kda_status_t kda_state_scan(const float* transition, const float* state_from_zero, const float* initial_state,
+                            int32_t count, float* state_out, const kda_problem_t* problem, void* stream);
+
+/*
  * Bytes of device workspace kda_backward needs for this problem (0 if the descriptor is invalid):
  * per token and head 4 (2 d_k + 3 d_v + 16) bytes, plus two fp32 d_k x d_v states (the state
  * entering each 16-token chunk and the gradient reaching its end) per chunk slot and head, with
@@ -338,7 +381,7 @@ int32_t kda_profile_read(kda_kernel_time_t* out, int32_t max_entries);
 /* ABI version of this header: (major << 16) | minor. */
 uint32_t kda_abi_version(void);
 
-#define KDA_ABI_VERSION ((1u << 16) | 4u)
+#define KDA_ABI_VERSION ((1u << 16) | 5u)
 
 #ifdef __cplusplus
 }

@@ -34,7 +34,8 @@ G_MIN = -5.0
 EXPORTS = ("kda_forward_workspace_bytes", "kda_forward", "kda_decode_step", "kda_workspace_status",
            "kda_status_string", "kda_profile_enable", "kda_profile_read", "kda_abi_version",
            "kda_forward_static_scratch", "kda_forward_plan", "kda_decode_replay", "kda_prologue",
-           "kda_epilogue", "kda_static_scratch_status", "kda_backward_workspace_bytes", "kda_backward")
+           "kda_epilogue", "kda_static_scratch_status", "kda_backward_workspace_bytes", "kda_backward",
+           "kda_forward_summary_workspace_bytes", "kda_forward_summary", "kda_state_scan")
 
 # Size of the library's own scratch array used by kda_forward_static_scratch.
 KDA_STATIC_SCRATCH_BYTES = 8 << 20
@@ -105,6 +106,12 @@ def lib():
             L.kda_backward_workspace_bytes.argtypes = [P]
             L.kda_backward.restype = ctypes.c_int
             L.kda_backward.argtypes = [_vp] * 17 + [P, _vp, ctypes.c_size_t, _vp]
+            L.kda_forward_summary_workspace_bytes.restype = ctypes.c_size_t
+            L.kda_forward_summary_workspace_bytes.argtypes = [P]
+            L.kda_forward_summary.restype = ctypes.c_int
+            L.kda_forward_summary.argtypes = [_vp] * 9 + [P, _vp, ctypes.c_size_t, _vp]
+            L.kda_state_scan.restype = ctypes.c_int
+            L.kda_state_scan.argtypes = [_vp, _vp, _vp, ctypes.c_int32, _vp, P, _vp]
             L.kda_static_scratch_status.restype = ctypes.c_int
             L.kda_static_scratch_status.argtypes = [_vp]
             L.kda_forward_plan.restype = ctypes.c_int
@@ -304,6 +311,67 @@ def kda_backward(q, k, v, z, A, beta, d_out, d_final_state=None, initial_state=N
     if st != KDA_OK:
         raise KdaError(st, "kda_backward")
     return dq, dk_, dv_, dz, dA, dbeta, dS0
+
+
+def kda_forward_summary(q, k, v, z, A, beta, cu_seqlens=None, num_seqs: int = 1, max_seqlen: Optional[int] = None,
+                        workspace=None, g_min: float = G_MIN, stream=None):
+    """The affine summary (M, S~) of every sequence's token range (see include/kda.h): M
+    [N, H, d_k, d_k] and S~ [N, H, d_k, d_v] fp32, with S_end = M S_in + S~.  Inputs as for
+    :func:`kda_forward` (cu_seqlens, or ``num_seqs`` equal lengths)."""
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    dev = k.device
+    dt = k.dtype
+    if cu_seqlens is not None:
+        N = cu_seqlens.shape[0] - 1
+        _need(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,), dev)
+        if max_seqlen is None:
+            max_seqlen = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if N > 0 else 0
+    else:
+        N = int(num_seqs)
+        max_seqlen = T // N
+    for name, t, shp in (("q", q, (T, H, dk)), ("k", k, (T, H, dk)), ("z", z, (T, H, dk)), ("v", v, (T, H, dv))):
+        _need(t, name, dt, shp, dev)
+    _need(A, "A", torch.float32, (H,), dev)
+    _need(beta, "beta", torch.float32, (T, H), dev)
+    M = torch.empty((N, H, dk, dk), dtype=torch.float32, device=dev)
+    St = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    prob = make_problem(N, T, max_seqlen, H, dk, dv, dt, g_min)
+    if workspace is None:
+        wsb = int(lib().kda_forward_summary_workspace_bytes(ctypes.byref(prob)))
+        if wsb == 0:
+            raise KdaError(KDA_ERR_INVALID_ARG, "kda_forward_summary_workspace_bytes")
+        workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    st = lib().kda_forward_summary(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(beta), _ptr(cu_seqlens), _ptr(M),
+                                   _ptr(St), ctypes.byref(prob), _ptr(workspace),
+                                   ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_forward_summary")
+    return M, St
+
+
+def kda_state_scan(transition, state_from_zero, initial_state=None, count: Optional[int] = None, state_out=None,
+                   stream=None):
+    """Apply S <- M_i S + S~_i for i < count (default: all) to ``initial_state`` (None: zeros).
+    transition [R, N, H, d_k, d_k], state_from_zero [R, N, H, d_k, d_v] fp32 on one device."""
+    R, N, H, dk, dv = state_from_zero.shape
+    dev = state_from_zero.device
+    count = R if count is None else int(count)
+    if not 0 <= count <= R:
+        raise ValueError("count out of range")
+    _need(transition, "transition", torch.float32, (R, N, H, dk, dk), dev)
+    _need(state_from_zero, "state_from_zero", torch.float32, (R, N, H, dk, dv), dev)
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32, (N, H, dk, dv), dev)
+    if state_out is None:
+        state_out = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    _need(state_out, "state_out", torch.float32, (N, H, dk, dv), dev)
+    prob = make_problem(N, N, 1, H, dk, dv, torch.float32)
+    st = lib().kda_state_scan(_ptr(transition), _ptr(state_from_zero), _ptr(initial_state), ctypes.c_int32(count),
+                              _ptr(state_out), ctypes.byref(prob), _stream(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_state_scan")
+    return state_out
 
 
 def kda_decode_step(q, k, v, z, A, beta, state, out=None, g_min: float = G_MIN, stream=None):

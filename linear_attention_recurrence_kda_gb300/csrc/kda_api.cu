@@ -423,6 +423,86 @@ kda_status_t kda_backward(const void* q, const void* k, const void* v, const voi
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+size_t kda_forward_summary_workspace_bytes(const kda_problem_t* problem)
+{
+    if (check_descriptor(problem, Call::Forward) != KDA_OK) return 0;
+    return kda::summary_layout(*problem).total;
+}
+
+kda_status_t kda_forward_summary(const void* q, const void* k, const void* v, const void* z, const float* A,
+                                 const float* beta, const int32_t* cu_seqlens, float* transition, float* state_from_zero,
+                                 const kda_problem_t* problem, void* workspace, size_t workspace_bytes, void* stream)
+{
+    kda_status_t st = check_descriptor(problem, Call::Forward);
+    if (st != KDA_OK) return st;
+    const kda_problem_t& p = *problem;
+    if (transition == nullptr || state_from_zero == nullptr) return KDA_ERR_INVALID_ARG;
+    if (!aligned(transition, 16) || !aligned(state_from_zero, 16)) return KDA_ERR_INVALID_ARG;
+    const kda::SummaryLayout L = kda::summary_layout(p);
+    if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < L.total) return KDA_ERR_WORKSPACE;
+    const size_t io = io_size(p.io_dtype);
+    const size_t tk = (size_t)p.total_tokens * p.num_heads * p.d_k;
+    const size_t tv = (size_t)p.total_tokens * p.num_heads * p.d_v;
+    const size_t units = (size_t)p.num_seqs * p.num_heads;
+    const Range rm = range_of(transition, units * p.d_k * p.d_k * sizeof(float));
+    const Range rs = range_of(state_from_zero, units * p.d_k * p.d_v * sizeof(float));
+    const Range ins[7] = {range_of(q, tk * io), range_of(k, tk * io), range_of(z, tk * io), range_of(v, tv * io),
+                          range_of(A, p.num_heads * sizeof(float)),
+                          range_of(beta, (size_t)p.total_tokens * p.num_heads * sizeof(float)),
+                          range_of(cu_seqlens, cu_seqlens ? (size_t)(p.num_seqs + 1) * sizeof(int32_t) : 0)};
+    const Range rw = range_of(workspace, L.total);
+    for (const Range& r : ins) {
+        if (overlaps(rm, r) || overlaps(rs, r) || overlaps(rw, r)) return KDA_ERR_INVALID_ARG;
+    }
+    if (overlaps(rm, rs) || overlaps(rw, rm) || overlaps(rw, rs)) return KDA_ERR_INVALID_ARG;
+    if ((st = check_device_pointer(workspace)) != KDA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    void* zeros = ws + L.zeros_off;
+    float* eye = reinterpret_cast<float*>(ws + L.eye_off);
+    void* out = ws + L.out_off;
+    // S~: the range from a zero state
+    st = kda_forward(q, k, v, z, A, beta, nullptr, cu_seqlens, out, state_from_zero, problem, ws, L.fwd_bytes, stream);
+    if (st != KDA_OK) return st;
+    // M: the range from the identity with every value zero (the columns of M evolve like state columns)
+    if (p.total_tokens > 0 && cudaMemsetAsync(zeros, 0, tk * io, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (kda::launch_identity_states(eye, (int64_t)units, p.d_k, s) != cudaSuccess) return KDA_ERR_CUDA;
+    return kda_forward(q, k, zeros, z, A, beta, eye, cu_seqlens, out, transition, &L.pm, ws, L.fwd_bytes, stream);
+}
+
+kda_status_t kda_state_scan(const float* transition, const float* state_from_zero, const float* initial_state,
+                            int32_t count, float* state_out, const kda_problem_t* problem, void* stream)
+{
+    kda_status_t st = check_descriptor(problem, Call::Forward);
+    if (st != KDA_OK) return st;
+    const kda_problem_t& p = *problem;
+    if (count < 0 || state_out == nullptr) return KDA_ERR_INVALID_ARG;
+    if (count > 0 && (transition == nullptr || state_from_zero == nullptr)) return KDA_ERR_INVALID_ARG;
+    for (const void* ptr : {(const void*)transition, (const void*)state_from_zero, (const void*)initial_state,
+                            (const void*)state_out}) {
+        if (!aligned(ptr, 16)) return KDA_ERR_INVALID_ARG;
+    }
+    if ((int64_t)p.num_seqs * p.num_heads > 2147483647LL) return KDA_ERR_UNSUPPORTED;
+    const size_t units = (size_t)p.num_seqs * p.num_heads;
+    const Range rm = range_of(transition, (size_t)count * units * p.d_k * p.d_k * sizeof(float));
+    const Range rt = range_of(state_from_zero, (size_t)count * units * p.d_k * p.d_v * sizeof(float));
+    const Range ri = range_of(initial_state, units * p.d_k * p.d_v * sizeof(float));
+    const Range ro = range_of(state_out, units * p.d_k * p.d_v * sizeof(float));
+    if (overlaps(ro, rm) || overlaps(ro, rt)) return KDA_ERR_INVALID_ARG;
+    // in place (state_out == initial_state) is allowed: every CTA reads its slice before writing it
+    if (state_out != initial_state && overlaps(ro, ri)) return KDA_ERR_INVALID_ARG;
+    for (const void* ptr : {(const void*)transition, (const void*)state_from_zero, (const void*)initial_state,
+                            (const void*)state_out}) {
+        if ((st = check_device_pointer(ptr)) != KDA_OK) return st;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    kda::prof_start("kda_state_scan", s);
+    const cudaError_t e = kda::launch_state_scan(transition, state_from_zero, initial_state, state_out, p.num_seqs,
+                                                 p.num_heads, p.d_k, p.d_v, count, s);
+    kda::prof_stop(s);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const void* z, const float* A,
                              const float* beta, float* state, void* out, const kda_problem_t* problem,
                              void* stream)

@@ -242,6 +242,38 @@ struct BackwardArgs {
 
 cudaError_t launch_backward(const BackwardArgs& b, kda_dtype_t dt, cudaStream_t s);
 
+// Context-parallel pieces (kda_kcp.cu): identity states [units][dk][dk]; and the scan
+// out = fold_{i < count} (S -> M_i S + S~_i) applied to S0 (null: zeros), M [count][N][H][dk][dk],
+// S~ [count][N][H][dk][dv].
+cudaError_t launch_identity_states(float* S, int64_t units, int dk, cudaStream_t s);
+cudaError_t launch_state_scan(const float* M, const float* St, const float* S0, float* out, int N, int H, int dk, int dv,
+                              int count, cudaStream_t s);
+
+// Workspace of kda_forward_summary: a kda_forward workspace large enough for both of its runs (the
+// problem itself for S~, and the problem with d_v = d_k for M), then zero values [T][H][d_k] (io
+// dtype), identity states [N][H][d_k][d_k] fp32 and discarded outputs [T][H][max(d_k, d_v)] (io).
+struct SummaryLayout {
+    size_t fwd_bytes, zeros_off, eye_off, out_off, total;
+    kda_problem_t pm;  // the problem of the transition run
+};
+
+inline SummaryLayout summary_layout(const kda_problem_t& p)
+{
+    SummaryLayout L{};
+    L.pm = p;
+    L.pm.d_v = p.d_k;
+    const size_t a = forward_layout(p, SIZE_MAX).total, b = forward_layout(L.pm, SIZE_MAX).total;
+    const size_t io = p.io_dtype == KDA_BF16 ? 2 : 4;
+    const size_t th = (size_t)p.total_tokens * p.num_heads;
+    L.fwd_bytes = align_up(a > b ? a : b, 256);
+    L.zeros_off = L.fwd_bytes;
+    L.eye_off = align_up(L.zeros_off + th * p.d_k * io, 256);
+    L.out_off = align_up(L.eye_off + (size_t)p.num_seqs * p.num_heads * p.d_k * p.d_k * sizeof(float), 256);
+    const int dmax = p.d_k > p.d_v ? p.d_k : p.d_v;
+    L.total = align_up(L.out_off + th * dmax * io, 256);
+    return L;
+}
+
 struct DecodeArgs {
     const void* q;
     const void* k;

@@ -12,11 +12,13 @@
 //                                                  head-wise RMSNorm and sigmoid output gate
 // The projections themselves (x W) are plain GEMMs outside this library.
 //
-// Both are streaming kernels bound by HBM: every element is read and written once.  A prologue warp
-// walks 16 consecutive tokens of one head and one tensor (lane l owns channels l*VEC ..
-// l*VEC + VEC - 1), keeping the convolution window of its channels in registers, so each input row
-// is read once (plus a K-1 row halo per 16 tokens); the L2 norm is a warp reduction.  An epilogue
-// warp normalises whole token-head rows with one warp reduction each.
+// Both are streaming kernels: every element is read and written once.  A prologue warp walks 8
+// consecutive tokens of one head and one tensor (lane l owns channels l*VEC .. l*VEC + VEC - 1):
+// it issues the loads of all 8 rows first, then convolves with the window of its channels kept in
+// registers (each row read once, plus a K-1 row halo per 8 tokens that the neighbouring warp of the
+// same CTA has just read); the L2 norm is a warp reduction.  An epilogue warp normalises whole
+// token-head rows with one warp reduction each.  Swish and the gate use the hardware exponential
+// and reciprocal approximations, the norms rsqrt.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -25,7 +27,7 @@ namespace {
 
 constexpr int kLayerThreads = 256;
 constexpr int kLayerWarps = kLayerThreads / 32;
-constexpr int kProTokens = 16;  // tokens per prologue warp
+constexpr int kProTokens = 8;  // tokens per prologue warp
 
 template <typename TIO, int VEC>
 __device__ __forceinline__ void ld_vec(const TIO* p, float (&x)[VEC])
@@ -62,10 +64,15 @@ __device__ __forceinline__ void st_vec(TIO* p, const float (&x)[VEC])
     }
 }
 
+// logistic function from the hardware base-2 exponential and reciprocal approximations (relative
+// error near 2^-22): 1 / (1 + 2^(-x log2 e)); the exponential saturates to +inf for very negative x
+// and the reciprocal of +inf is 0, so no input gives a NaN
 __device__ __forceinline__ float sigmoid_f(float x)
 {
-    const float e = expf(-fabsf(x));
-    return (x >= 0.f) ? 1.f / (1.f + e) : e / (1.f + e);
+    float e, r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-1.4426950408889634f * x));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
+    return r;
 }
 
 __device__ __forceinline__ float warp_sum(float x)
@@ -139,7 +146,17 @@ __global__ void __launch_bounds__(kLayerThreads) kda_prologue_kernel(PrologueArg
         }
     }
 
-    for (int64_t t = t0; t < t1; ++t) {
+    // every token row of this warp in flight before any arithmetic
+    float xs[kProTokens][VEC];
+#pragma unroll
+    for (int j = 0; j < kProTokens; ++j) {
+        if (t0 + j < t1) ld_vec<TIO, VEC>(x + ((t0 + j) * a.H + h) * D + l * VEC, xs[j]);
+    }
+
+#pragma unroll
+    for (int j = 0; j < kProTokens; ++j) {
+        const int64_t t = t0 + j;
+        if (t >= t1) break;
         if (t >= end) {  // a new sequence starts here: the window restarts from zeros
             if (a.cu != nullptr) {
                 while (n + 1 < a.N && (int64_t)a.cu[n + 1] <= t) ++n;
@@ -152,8 +169,8 @@ __global__ void __launch_bounds__(kLayerThreads) kda_prologue_kernel(PrologueArg
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) win[i][e] = 0.f;
         }
-        float xt[VEC], yv[VEC];
-        ld_vec<TIO, VEC>(x + (t * a.H + h) * D + l * VEC, xt);
+        const float* xt = xs[j];
+        float yv[VEC];
         float ss = 0.f;
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
@@ -171,7 +188,7 @@ __global__ void __launch_bounds__(kLayerThreads) kda_prologue_kernel(PrologueArg
 #pragma unroll
         for (int e = 0; e < VEC; ++e) win[0][e] = xt[e];
         if (which < 2) {
-            const float inv = 1.f / sqrtf(warp_sum(ss) + 1e-6f);
+            const float inv = rsqrtf(warp_sum(ss) + 1e-6f);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) yv[e] *= inv;
         }
@@ -198,7 +215,7 @@ __global__ void __launch_bounds__(kLayerThreads) kda_epilogue_kernel(EpilogueArg
         float ss = 0.f;
 #pragma unroll
         for (int e = 0; e < VEC; ++e) ss += ov[e] * ov[e];
-        const float inv = 1.f / sqrtf(warp_sum(ss) * (1.f / D) + a.eps);
+        const float inv = rsqrtf(warp_sum(ss) * (1.f / D) + a.eps);
 #pragma unroll
         for (int e = 0; e < VEC; ++e) ov[e] = ov[e] * inv * wt[e] * sigmoid_f(gv[e]);
         st_vec<TIO, VEC>(y + row * D + l * VEC, ov);

@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert B.kda_abi_version() == (1 << 16) | 4
+    assert B.kda_abi_version() == (1 << 16) | 5
     for code in range(7):
         s = B.status_string(code)
         assert s.startswith("KDA_")
@@ -295,7 +295,7 @@ def test_compute_entry_points_cite_their_passage():
     names the page and section defining the operation."""
     src = open(HEADER).read()
     for name in ("kda_forward", "kda_decode_step", "kda_decode_replay", "kda_prologue", "kda_epilogue",
-                 "kda_backward"):
+                 "kda_backward", "kda_forward_summary", "kda_state_scan"):
         decl = src.index(f"kda_status_t {name}(")
         comment = src[src.rindex("/*", 0, decl):decl]
         assert "Kimi K3" in comment and "section" in comment, name
