@@ -21,14 +21,14 @@
 //
 // Kernels, in order (after kda_gate and kda_ut_wy, which fill G, W and U~):
 //   kda_bwd_gram    per (chunk, head): P = tril(QG KI^T)
-//   kda_bwd_states  per (sequence, head, value-column slice), chunks in order: the state entering
-//                   every chunk and U = U~ - W S
-//   kda_bwd_dstates per (sequence, head, value-column slice), chunks in reverse: the gradient
-//                   reaching every chunk's end state, dU, and dS0
+//   kda_bwd_states  per (sequence, head, value-column slice), one launch, two independent walks:
+//                   chunks in order for the state entering every chunk and U = U~ - W S; chunks
+//                   in reverse for the gradient reaching every chunk's end state, dU, and dS0
 //   kda_bwd_chunk   per (chunk, head): every input gradient and the chunk's share of dA
 //   kda_bwd_da      per head: dA from the chunks' shares (fixed order, deterministic)
 // Value columns are independent in both state passes (column j of S and dS only meets column j of
 // V, U, dO and dU), which is what the slices use.
+#include <algorithm>
 #include <type_traits>
 
 #include "kda_internal.cuh"
@@ -106,59 +106,109 @@ __global__ void __launch_bounds__(NT) kda_bwd_gram_kernel(BackwardArgs b)
     }
 }
 
+// ---------------------------------------------------------------- state passes (shared pieces)
+//
+// Both passes walk one (sequence, head, value-column slice) chunk by chunk.  The slice of the state
+// lives in shared memory transposed, St[j][c] (rows padded to keep 16-byte alignment), so that both
+// products of a chunk read their operands as float4 along the key channels; the next chunk's rows
+// are loaded into registers while the current chunk computes.
+
+template <int DK>
+struct RowPrefetch {
+    static constexpr int PER = C * DK / NT;  // row elements per thread and array
+    float v[PER];
+};
+
+// Rows [C][DK] of a [T][H][DK] tensor (io dtype or fp32) for the chunk at t0 of length len, this
+// thread's elements e = tid + p * NT, zero beyond len.
+template <typename T, int DK>
+__device__ __forceinline__ void load_rows(RowPrefetch<DK>& r, const T* src, int64_t t0, int len, int H, int h, int tid)
+{
+#pragma unroll
+    for (int p = 0; p < RowPrefetch<DK>::PER; ++p) {
+        const int e = tid + p * NT;
+        const int row = e / DK, c = e % DK;
+        r.v[p] = row < len ? ld_io(src, ((t0 + row) * H + h) * (int64_t)DK + c) : 0.f;
+    }
+}
+template <int DK>
+__device__ __forceinline__ void store_rows(const RowPrefetch<DK>& r, float (*dst)[DK], int tid)
+{
+#pragma unroll
+    for (int p = 0; p < RowPrefetch<DK>::PER; ++p) {
+        const int e = tid + p * NT;
+        dst[e / DK][e % DK] = r.v[p];
+    }
+}
+
 // ---------------------------------------------------------------- forward state pass (states kept)
 
 template <int DK, int JS>
 struct StatesSmem {
-    float S[DK][JS];
-    float K[C][DK];  // keys, then K e^(G_C - G)
+    static constexpr int SP = DK + 4;  // padded row of the transposed state
+    float St[JS][SP];                  // state slice, transposed: St[j][c] = S[c][j0 + j]
+    float K[C][DK];                    // keys, then K e^(G_C - G)
     float G[C][DK];
     float W[C][DK];
     float U[C][JS];
-    float GL[DK];
+    float eGL[DK];                     // e^(G_C)
 };
 
 template <typename TIO, int DK, int DV, int JS>
-__global__ void __launch_bounds__(NT) kda_bwd_states_kernel(BackwardArgs b)
+__device__ __forceinline__ void bwd_states(const BackwardArgs& b, unsigned char* smem_raw, int slice)
 {
+    using Sm = StatesSmem<DK, JS>;
     const PrefillArgs& a = b.f;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    StatesSmem<DK, JS>& sm = *reinterpret_cast<StatesSmem<DK, JS>*>(smem_raw);
+    Sm& sm = *reinterpret_cast<Sm*>(smem_raw);
     const int n = blockIdx.x;
     const int h = blockIdx.y;
-    const int j0 = blockIdx.z * JS;
+    const int j0 = slice * JS;
     const int tid = threadIdx.x;
+    const int H = a.H;
     int64_t s0, s1;
     if (!seq_range(a, n, s0, s1)) return;
     const TIO* kp = static_cast<const TIO*>(a.k);
-    const int64_t sbase = ((int64_t)n * a.H + h) * DK * DV;
+    const int64_t sbase = ((int64_t)n * H + h) * DK * DV;
     for (int e = tid; e < DK * JS; e += NT) {
         const int c = e / JS, j = e % JS;
-        sm.S[c][j] = a.s0 ? a.s0[sbase + (int64_t)c * DV + j0 + j] : 0.f;
+        sm.St[j][c] = a.s0 ? a.s0[sbase + (int64_t)c * DV + j0 + j] : 0.f;
     }
-    constexpr int NU = (C * JS + NT - 1) / NT;
+    constexpr int NU = (C * JS + NT - 1) / NT;   // U entries per thread
+    constexpr int NS = (JS * DK / 4 + NT - 1) / NT;  // (j, 4 channels) state items per thread
+    RowPrefetch<DK> pk, pg, pw;
+    float pu[NU];
+    auto fetch = [&](int64_t t0, int len) {
+        load_rows(pk, kp, t0, len, H, h, tid);
+        load_rows(pg, a.G, t0, len, H, h, tid);
+        load_rows(pw, a.W, t0, len, H, h, tid);
+#pragma unroll
+        for (int q = 0; q < NU; ++q) {
+            const int e = tid + q * NT;
+            const int r = e / JS, j = e % JS;
+            pu[q] = (e < C * JS && r < len) ? a.Ut[((t0 + r) * H + h) * (int64_t)DV + j0 + j] : 0.f;
+        }
+    };
+    if (s0 < s1) fetch(s0, (int)min((int64_t)C, s1 - s0));
     for (int64_t ci = 0; s0 + ci * C < s1; ++ci) {
         const int64_t t0 = s0 + ci * C;
         const int len = (int)min((int64_t)C, s1 - t0);
         __syncthreads();  // the previous chunk's state update is complete
-        float* dst = b.S_chunk + (chunk_slot(n, s0, ci) * a.H + h) * (int64_t)DK * DV + j0;
+        store_rows(pk, sm.K, tid);
+        store_rows(pg, sm.G, tid);
+        store_rows(pw, sm.W, tid);
+#pragma unroll
+        for (int q = 0; q < NU; ++q) {
+            const int e = tid + q * NT;
+            if (e < C * JS) sm.U[e / JS][e % JS] = pu[q];
+        }
+        float* dst = b.S_chunk + (chunk_slot(n, s0, ci) * H + h) * (int64_t)DK * DV + j0;
         for (int e = tid; e < DK * JS; e += NT) {
             const int c = e / JS, j = e % JS;
-            dst[(int64_t)c * DV + j] = sm.S[c][j];
+            dst[(int64_t)c * DV + j] = sm.St[j][c];
         }
-        for (int e = tid; e < C * DK; e += NT) {
-            const int r = e / DK, c = e % DK;
-            const bool ok = r < len;
-            const int64_t idx = ((t0 + r) * a.H + h) * (int64_t)DK + c;
-            sm.K[r][c] = ok ? ld_io(kp, idx) : 0.f;
-            sm.G[r][c] = ok ? a.G[idx] : 0.f;
-            sm.W[r][c] = ok ? a.W[idx] : 0.f;
-        }
-        for (int e = tid; e < C * JS; e += NT) {
-            const int r = e / JS, j = e % JS;
-            sm.U[r][j] = (r < len) ? a.Ut[((t0 + r) * a.H + h) * (int64_t)DV + j0 + j] : 0.f;
-        }
+        if (t0 + C < s1) fetch(t0 + C, (int)min((int64_t)C, s1 - t0 - C));
         __syncthreads();
+        // U = U~ - W S (four accumulators along the key channels); K -> K e^(G_C - G)
         float uacc[NU];
 #pragma unroll
         for (int q = 0; q < NU; ++q) {
@@ -166,13 +216,24 @@ __global__ void __launch_bounds__(NT) kda_bwd_states_kernel(BackwardArgs b)
             uacc[q] = 0.f;
             if (e < C * JS) {
                 const int r = e / JS, j = e % JS;
-                float acc = sm.U[r][j];
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
-                for (int c = 0; c < DK; ++c) acc -= sm.W[r][c] * sm.S[c][j];
-                uacc[q] = (r < len) ? acc : 0.f;
+                for (int c = 0; c < DK; c += 4) {
+                    const float4 w = *reinterpret_cast<const float4*>(&sm.W[r][c]);
+                    const float4 x = *reinterpret_cast<const float4*>(&sm.St[j][c]);
+                    acc.x = fmaf(w.x, x.x, acc.x);
+                    acc.y = fmaf(w.y, x.y, acc.y);
+                    acc.z = fmaf(w.z, x.z, acc.z);
+                    acc.w = fmaf(w.w, x.w, acc.w);
+                }
+                uacc[q] = r < len ? sm.U[r][j] - ((acc.x + acc.y) + (acc.z + acc.w)) : 0.f;
             }
         }
-        for (int c = tid; c < DK; c += NT) sm.GL[c] = sm.G[len - 1][c];
+        for (int e = tid; e < C * DK; e += NT) {
+            const int r = e / DK, c = e % DK;
+            sm.K[r][c] *= expf(sm.G[len - 1][c] - sm.G[r][c]);
+        }
+        for (int c = tid; c < DK; c += NT) sm.eGL[c] = expf(sm.G[len - 1][c]);
         __syncthreads();
 #pragma unroll
         for (int q = 0; q < NU; ++q) {
@@ -180,19 +241,29 @@ __global__ void __launch_bounds__(NT) kda_bwd_states_kernel(BackwardArgs b)
             if (e < C * JS) {
                 const int r = e / JS, j = e % JS;
                 sm.U[r][j] = uacc[q];
-                if (r < len) b.U[((t0 + r) * a.H + h) * (int64_t)DV + j0 + j] = uacc[q];
+                if (r < len) b.U[((t0 + r) * H + h) * (int64_t)DV + j0 + j] = uacc[q];
             }
         }
-        for (int e = tid; e < C * DK; e += NT) {
-            const int r = e / DK, c = e % DK;
-            sm.K[r][c] *= expf(sm.GL[c] - sm.G[r][c]);
-        }
         __syncthreads();
-        for (int e = tid; e < DK * JS; e += NT) {
-            const int c = e / JS, j = e % JS;
-            float acc = expf(sm.GL[c]) * sm.S[c][j];
-            for (int i = 0; i < len; ++i) acc += sm.K[i][c] * sm.U[i][j];
-            sm.S[c][j] = acc;
+        // S = e^G_C S + Kt^T U, four key channels of one column per item
+#pragma unroll
+        for (int q = 0; q < NS; ++q) {
+            const int e = tid + q * NT;
+            if (e < JS * DK / 4) {
+                const int j = e / (DK / 4), c = 4 * (e % (DK / 4));
+                const float4 g = *reinterpret_cast<const float4*>(&sm.eGL[c]);
+                float4 x = *reinterpret_cast<const float4*>(&sm.St[j][c]);
+                x = make_float4(g.x * x.x, g.y * x.y, g.z * x.z, g.w * x.w);
+                for (int i = 0; i < len; ++i) {
+                    const float u = sm.U[i][j];
+                    const float4 kt = *reinterpret_cast<const float4*>(&sm.K[i][c]);
+                    x.x = fmaf(kt.x, u, x.x);
+                    x.y = fmaf(kt.y, u, x.y);
+                    x.z = fmaf(kt.z, u, x.z);
+                    x.w = fmaf(kt.w, u, x.w);
+                }
+                *reinterpret_cast<float4*>(&sm.St[j][c]) = x;
+            }
         }
     }
 }
@@ -201,74 +272,97 @@ __global__ void __launch_bounds__(NT) kda_bwd_states_kernel(BackwardArgs b)
 
 template <int DK, int JS>
 struct DStatesSmem {
-    float dS[DK][JS];
-    float Q[C][DK];  // queries, then Q e^G
-    float K[C][DK];  // keys, then K e^(G_C - G)
+    static constexpr int SP = DK + 4;
+    float dSt[JS][SP];  // gradient slice, transposed: dSt[j][c] = dS[c][j0 + j]
+    float Q[C][DK];     // queries, then Q e^G
+    float K[C][DK];     // keys, then K e^(G_C - G)
     float G[C][DK];
     float W[C][DK];
     float P[C][C];
     float dO[C][JS];
     float dU[C][JS];
-    float GL[DK];
+    float eGL[DK];
 };
 
 template <typename TIO, int DK, int DV, int JS>
-__global__ void __launch_bounds__(NT) kda_bwd_dstates_kernel(BackwardArgs b)
+__device__ __forceinline__ void bwd_dstates(const BackwardArgs& b, unsigned char* smem_raw, int slice)
 {
+    using Sm = DStatesSmem<DK, JS>;
     const PrefillArgs& a = b.f;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    DStatesSmem<DK, JS>& sm = *reinterpret_cast<DStatesSmem<DK, JS>*>(smem_raw);
+    Sm& sm = *reinterpret_cast<Sm*>(smem_raw);
     const int n = blockIdx.x;
     const int h = blockIdx.y;
-    const int j0 = blockIdx.z * JS;
+    const int j0 = slice * JS;
     const int tid = threadIdx.x;
+    const int H = a.H;
     int64_t s0, s1;
     if (!seq_range(a, n, s0, s1)) return;
     const TIO* qp = static_cast<const TIO*>(a.q);
     const TIO* kp = static_cast<const TIO*>(a.k);
     const TIO* dop = static_cast<const TIO*>(b.dout);
-    const int64_t sbase = ((int64_t)n * a.H + h) * DK * DV;
+    const int64_t sbase = ((int64_t)n * H + h) * DK * DV;
     for (int e = tid; e < DK * JS; e += NT) {
         const int c = e / JS, j = e % JS;
-        sm.dS[c][j] = b.dS_final ? b.dS_final[sbase + (int64_t)c * DV + j0 + j] : 0.f;
+        sm.dSt[j][c] = b.dS_final ? b.dS_final[sbase + (int64_t)c * DV + j0 + j] : 0.f;
     }
     constexpr int NU = (C * JS + NT - 1) / NT;
+    constexpr int NS = (JS * DK / 4 + NT - 1) / NT;
+    constexpr int NP = (C * C + NT - 1) / NT;
+    RowPrefetch<DK> pq, pk, pg, pw;
+    float pp[NP], po[NU];
+    auto fetch = [&](int64_t t0, int len) {
+        load_rows(pq, qp, t0, len, H, h, tid);
+        load_rows(pk, kp, t0, len, H, h, tid);
+        load_rows(pg, a.G, t0, len, H, h, tid);
+        load_rows(pw, a.W, t0, len, H, h, tid);
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+            const int e = tid + q * NT;
+            const int r = e / C, i = e % C;
+            pp[q] = (e < C * C && r < len) ? b.P[((t0 + r) * H + h) * (int64_t)C + i] : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < NU; ++q) {
+            const int e = tid + q * NT;
+            const int r = e / JS, j = e % JS;
+            po[q] = (e < C * JS && r < len) ? ld_io(dop, ((t0 + r) * H + h) * (int64_t)DV + j0 + j) : 0.f;
+        }
+    };
     const int64_t nch = (s1 - s0 + C - 1) / C;
+    auto chunk_len = [&](int64_t ci) { return (int)min((int64_t)C, s1 - (s0 + ci * C)); };
+    if (nch > 0) fetch(s0 + (nch - 1) * C, chunk_len(nch - 1));
     for (int64_t ci = nch - 1; ci >= 0; --ci) {
         const int64_t t0 = s0 + ci * C;
-        const int len = (int)min((int64_t)C, s1 - t0);
+        const int len = chunk_len(ci);
         __syncthreads();  // the previous (later) chunk's update is complete
-        float* dst = b.dS_chunk + (chunk_slot(n, s0, ci) * a.H + h) * (int64_t)DK * DV + j0;
+        store_rows(pq, sm.Q, tid);
+        store_rows(pk, sm.K, tid);
+        store_rows(pg, sm.G, tid);
+        store_rows(pw, sm.W, tid);
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+            const int e = tid + q * NT;
+            if (e < C * C) sm.P[e / C][e % C] = pp[q];
+        }
+#pragma unroll
+        for (int q = 0; q < NU; ++q) {
+            const int e = tid + q * NT;
+            if (e < C * JS) sm.dO[e / JS][e % JS] = po[q];
+        }
+        float* dst = b.dS_chunk + (chunk_slot(n, s0, ci) * H + h) * (int64_t)DK * DV + j0;
         for (int e = tid; e < DK * JS; e += NT) {
             const int c = e / JS, j = e % JS;
-            dst[(int64_t)c * DV + j] = sm.dS[c][j];
+            dst[(int64_t)c * DV + j] = sm.dSt[j][c];
         }
-        for (int e = tid; e < C * DK; e += NT) {
-            const int r = e / DK, c = e % DK;
-            const bool ok = r < len;
-            const int64_t idx = ((t0 + r) * a.H + h) * (int64_t)DK + c;
-            sm.Q[r][c] = ok ? ld_io(qp, idx) : 0.f;
-            sm.K[r][c] = ok ? ld_io(kp, idx) : 0.f;
-            sm.G[r][c] = ok ? a.G[idx] : 0.f;
-            sm.W[r][c] = ok ? a.W[idx] : 0.f;
-        }
-        for (int e = tid; e < C * C; e += NT) {
-            const int r = e / C, i = e % C;
-            sm.P[r][i] = (r < len) ? b.P[((t0 + r) * a.H + h) * (int64_t)C + i] : 0.f;
-        }
-        for (int e = tid; e < C * JS; e += NT) {
-            const int r = e / JS, j = e % JS;
-            sm.dO[r][j] = (r < len) ? ld_io(dop, ((t0 + r) * a.H + h) * (int64_t)DV + j0 + j) : 0.f;
-        }
-        __syncthreads();
-        for (int c = tid; c < DK; c += NT) sm.GL[c] = sm.G[len - 1][c];
+        if (ci > 0) fetch(t0 - C, chunk_len(ci - 1));
         __syncthreads();
         for (int e = tid; e < C * DK; e += NT) {
             const int r = e / DK, c = e % DK;
             const float g = sm.G[r][c];
             sm.Q[r][c] *= expf(g);
-            sm.K[r][c] *= expf(sm.GL[c] - g);
+            sm.K[r][c] *= expf(sm.G[len - 1][c] - g);
         }
+        for (int c = tid; c < DK; c += NT) sm.eGL[c] = expf(sm.G[len - 1][c]);
         __syncthreads();
         // dU = Kt dS' + P^T dO
         float uacc[NU];
@@ -278,13 +372,21 @@ __global__ void __launch_bounds__(NT) kda_bwd_dstates_kernel(BackwardArgs b)
             uacc[q] = 0.f;
             if (e < C * JS) {
                 const int r = e / JS, j = e % JS;
-                float acc = 0.f;
                 if (r < len) {
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
-                    for (int c = 0; c < DK; ++c) acc += sm.K[r][c] * sm.dS[c][j];
-                    for (int i = r; i < len; ++i) acc += sm.P[i][r] * sm.dO[i][j];
+                    for (int c = 0; c < DK; c += 4) {
+                        const float4 kt = *reinterpret_cast<const float4*>(&sm.K[r][c]);
+                        const float4 x = *reinterpret_cast<const float4*>(&sm.dSt[j][c]);
+                        acc.x = fmaf(kt.x, x.x, acc.x);
+                        acc.y = fmaf(kt.y, x.y, acc.y);
+                        acc.z = fmaf(kt.z, x.z, acc.z);
+                        acc.w = fmaf(kt.w, x.w, acc.w);
+                    }
+                    float pd = 0.f;
+                    for (int i = r; i < len; ++i) pd = fmaf(sm.P[i][r], sm.dO[i][j], pd);
+                    uacc[q] = ((acc.x + acc.y) + (acc.z + acc.w)) + pd;
                 }
-                uacc[q] = acc;
             }
         }
 #pragma unroll
@@ -293,47 +395,78 @@ __global__ void __launch_bounds__(NT) kda_bwd_dstates_kernel(BackwardArgs b)
             if (e < C * JS) {
                 const int r = e / JS, j = e % JS;
                 sm.dU[r][j] = uacc[q];
-                if (r < len) b.dU[((t0 + r) * a.H + h) * (int64_t)DV + j0 + j] = uacc[q];
+                if (r < len) b.dU[((t0 + r) * H + h) * (int64_t)DV + j0 + j] = uacc[q];
             }
         }
         __syncthreads();
-        // dS = e^G_C dS' + QG^T dO - W^T dU
-        for (int e = tid; e < DK * JS; e += NT) {
-            const int c = e / JS, j = e % JS;
-            float acc = expf(sm.GL[c]) * sm.dS[c][j];
-            for (int r = 0; r < len; ++r) acc += sm.Q[r][c] * sm.dO[r][j] - sm.W[r][c] * sm.dU[r][j];
-            sm.dS[c][j] = acc;
+        // dS = e^G_C dS' + QG^T dO - W^T dU, four key channels of one column per item
+#pragma unroll
+        for (int q = 0; q < NS; ++q) {
+            const int e = tid + q * NT;
+            if (e < JS * DK / 4) {
+                const int j = e / (DK / 4), c = 4 * (e % (DK / 4));
+                const float4 g = *reinterpret_cast<const float4*>(&sm.eGL[c]);
+                float4 x = *reinterpret_cast<const float4*>(&sm.dSt[j][c]);
+                x = make_float4(g.x * x.x, g.y * x.y, g.z * x.z, g.w * x.w);
+                for (int r = 0; r < len; ++r) {
+                    const float o = sm.dO[r][j], du = sm.dU[r][j];
+                    const float4 qg = *reinterpret_cast<const float4*>(&sm.Q[r][c]);
+                    const float4 w = *reinterpret_cast<const float4*>(&sm.W[r][c]);
+                    x.x = fmaf(qg.x, o, fmaf(-w.x, du, x.x));
+                    x.y = fmaf(qg.y, o, fmaf(-w.y, du, x.y));
+                    x.z = fmaf(qg.z, o, fmaf(-w.z, du, x.z));
+                    x.w = fmaf(qg.w, o, fmaf(-w.w, du, x.w));
+                }
+                *reinterpret_cast<float4*>(&sm.dSt[j][c]) = x;
+            }
         }
     }
     __syncthreads();
     if (b.dS0) {
         for (int e = tid; e < DK * JS; e += NT) {
             const int c = e / JS, j = e % JS;
-            b.dS0[sbase + (int64_t)c * DV + j0 + j] = sm.dS[c][j];
+            b.dS0[sbase + (int64_t)c * DV + j0 + j] = sm.dSt[j][c];
         }
+    }
+}
+
+// The two state passes do not depend on each other (the reverse pass needs no forward state), so
+// one launch runs both: CTAs with blockIdx.z < DV / JS walk forward, the others backward.  States
+// from the forward pass are needed only by the per-chunk kernel that follows.
+template <typename TIO, int DK, int DV, int JS>
+__global__ void __launch_bounds__(NT) kda_bwd_states_kernel(BackwardArgs b, int with_forward)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    constexpr int NSL = DV / JS;
+    const int z = (int)blockIdx.z;
+    if (with_forward && z < NSL) {
+        bwd_states<TIO, DK, DV, JS>(b, smem_raw, z);
+    } else {
+        bwd_dstates<TIO, DK, DV, JS>(b, smem_raw, with_forward ? z - NSL : z);
     }
 }
 
 // ---------------------------------------------------------------- per-chunk gradients
 
+// Rows of the [16][d] tiles are padded by four floats: rows stay 16-byte aligned for float4 reads
+// along a row, and the 16 rows of one column fall on 8 distinct banks (the 16 x 16 products read
+// columns of 16 rows at once).
 template <int DK, int DV>
 struct ChunkGradSmem {
     static constexpr int JB = DV < 32 ? DV : 32;  // value columns per staged state tile
-    float EG[C][DK];   // e^G
-    float K[C][DK];
-    float G[C][DK];
-    float KG[C][DK];
-    float KI[C][DK];
-    float QG[C][DK];
-    float dKt[C][DK];
-    float dQa[C][DK];  // dO S^T
-    float dW[C][DK];   // -dU S^T, later dG
-    float TdW[C][DK];
-    float V[C][DV];
-    float dO[C][DV];
-    float U[C][DV];
-    float dU[C][DV];
-    float TdU[C][DV];
+    static constexpr int PK = DK + 4, PV = DV + 4;
+    float K[C][PK];
+    float G[C][PK];
+    float KG[C][PK];
+    float KI[C][PK];
+    float QG[C][PK];
+    float dKt[C][PK];  // U dS'^T, later dG
+    float dQa[C][PK];  // dO S^T
+    float dW[C][PK];   // -dU S^T, later T^T dW
+    float V[C][PV];
+    float dO[C][PV];
+    float U[C][PV];
+    float dU[C][PV];   // later T^T dU
     float Sin[DK][JB + 1];
     float dSo[DK][JB + 1];
     float M[C][C], P[C][C], T[C][C], dP[C][C], dTn[C][C], X[C][C], dA[C][C];
@@ -376,7 +509,6 @@ __global__ void __launch_bounds__(NT) kda_bwd_chunk_kernel(BackwardArgs b)
             g = a.G[idx];
         }
         const float eg = expf(g);
-        sm.EG[r][c] = eg;
         sm.K[r][c] = k;
         sm.G[r][c] = g;
         sm.KG[r][c] = k * eg;
@@ -416,16 +548,24 @@ __global__ void __launch_bounds__(NT) kda_bwd_chunk_kernel(BackwardArgs b)
                 sm.dSo[c2][j] = dSg[(int64_t)c2 * DV + jb + j];
             }
             __syncthreads();
-#pragma unroll 4
-            for (int j = 0; j < JB; ++j) {
-                const float s = sm.Sin[c][j], d = sm.dSo[c][j];
-                rsum += s * d;
+#pragma unroll 2
+            for (int j = 0; j < JB; j += 4) {
+                float sv[4], dv[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    sv[q] = sm.Sin[c][j + q];
+                    dv[q] = sm.dSo[c][j + q];
+                    rsum = fmaf(sv[q], dv[q], rsum);
+                }
 #pragma unroll
                 for (int rr = 0; rr < RPT; ++rr) {
                     const int r = grp * RPT + rr;
-                    akt[rr] += sm.U[r][jb + j] * d;
-                    aqa[rr] += sm.dO[r][jb + j] * s;
-                    aw[rr] -= sm.dU[r][jb + j] * s;
+                    const float4 u = *reinterpret_cast<const float4*>(&sm.U[r][jb + j]);
+                    const float4 o = *reinterpret_cast<const float4*>(&sm.dO[r][jb + j]);
+                    const float4 du = *reinterpret_cast<const float4*>(&sm.dU[r][jb + j]);
+                    akt[rr] = fmaf(u.x, dv[0], fmaf(u.y, dv[1], fmaf(u.z, dv[2], fmaf(u.w, dv[3], akt[rr]))));
+                    aqa[rr] = fmaf(o.x, sv[0], fmaf(o.y, sv[1], fmaf(o.z, sv[2], fmaf(o.w, sv[3], aqa[rr]))));
+                    aw[rr] = fmaf(-du.x, sv[0], fmaf(-du.y, sv[1], fmaf(-du.z, sv[2], fmaf(-du.w, sv[3], aw[rr]))));
                 }
             }
         }
@@ -447,16 +587,23 @@ __global__ void __launch_bounds__(NT) kda_bwd_chunk_kernel(BackwardArgs b)
     //    colsum(dKt Kt) per key channel
     {
         const int r = tid / C, i = tid % C;
-        float m = 0.f;
+        float m0 = 0.f, m1 = 0.f;
 #pragma unroll 8
-        for (int c = 0; c < DK; ++c) m += sm.KG[r][c] * sm.KI[i][c];
-        float dp = 0.f;
+        for (int c = 0; c < DK; c += 2) {
+            m0 = fmaf(sm.KG[r][c], sm.KI[i][c], m0);
+            m1 = fmaf(sm.KG[r][c + 1], sm.KI[i][c + 1], m1);
+        }
+        float dp0 = 0.f, dp1 = 0.f;
         if (i <= r) {
 #pragma unroll 8
-            for (int j = 0; j < DV; ++j) dp += sm.dO[r][j] * sm.U[i][j];
+            for (int j = 0; j < DV; j += 2) {
+                dp0 = fmaf(sm.dO[r][j], sm.U[i][j], dp0);
+                dp1 = fmaf(sm.dO[r][j + 1], sm.U[i][j + 1], dp1);
+            }
         }
+        const float m = m0 + m1;
         sm.M[r][i] = m;
-        sm.dP[r][i] = dp;
+        sm.dP[r][i] = dp0 + dp1;
         sm.X[r][i] = (i < r) ? sm.beta[r] * m : 0.f;
     }
     for (int c = tid; c < DK; c += NT) {
@@ -466,17 +613,17 @@ __global__ void __launch_bounds__(NT) kda_bwd_chunk_kernel(BackwardArgs b)
     }
     __syncthreads();
 
-    // 4. T = (I + A)^-1 by forward substitution, one thread per column
+    // 4. T = (I + A)^-1 by column-oriented forward substitution, one lane per column
     if (tid < C) {
         const int j = tid;
         float col[C];
 #pragma unroll
-        for (int r = 0; r < C; ++r) {
-            float t = (r == j) ? 1.f : 0.f;
-            if (r > j) {
-                for (int i = j; i < r; ++i) t -= sm.X[r][i] * col[i];
-            }
-            col[r] = t;
+        for (int r = 0; r < C; ++r) col[r] = (r == j) ? 1.f : 0.f;
+#pragma unroll
+        for (int i = 0; i < C; ++i) {
+            const float ti = col[i];
+#pragma unroll
+            for (int r = i + 1; r < C; ++r) col[r] = fmaf(-sm.X[r][i], ti, col[r]);
         }
 #pragma unroll
         for (int r = 0; r < C; ++r) sm.T[r][j] = col[r];
@@ -486,12 +633,18 @@ __global__ void __launch_bounds__(NT) kda_bwd_chunk_kernel(BackwardArgs b)
     // 5. dT = dU (diag(b) V)^T + dW (diag(b) KG)^T
     {
         const int r = tid / C, i = tid % C;
-        float acc = 0.f;
+        float a0 = 0.f, a1 = 0.f;
 #pragma unroll 8
-        for (int j = 0; j < DV; ++j) acc += sm.dU[r][j] * sm.V[i][j];
+        for (int j = 0; j < DV; j += 2) {
+            a0 = fmaf(sm.dU[r][j], sm.V[i][j], a0);
+            a1 = fmaf(sm.dU[r][j + 1], sm.V[i][j + 1], a1);
+        }
 #pragma unroll 8
-        for (int c = 0; c < DK; ++c) acc += sm.dW[r][c] * sm.KG[i][c];
-        sm.dTn[r][i] = sm.beta[i] * acc;
+        for (int c = 0; c < DK; c += 2) {
+            a0 = fmaf(sm.dW[r][c], sm.KG[i][c], a0);
+            a1 = fmaf(sm.dW[r][c + 1], sm.KG[i][c + 1], a1);
+        }
+        sm.dTn[r][i] = sm.beta[i] * (a0 + a1);
     }
     __syncthreads();
     // 6. dA = -tril_strict(T^T dT T^T)
@@ -510,24 +663,41 @@ __global__ void __launch_bounds__(NT) kda_bwd_chunk_kernel(BackwardArgs b)
         for (int s = 0; s < C; ++s) acc += sm.X[r][s] * sm.T[i][s];
         sm.dA[r][i] = (i < r) ? -acc : 0.f;
     }
-    // 7. T^T dU and T^T dW
-    for (int e = tid; e < C * DV; e += NT) {
+    // 7. T^T dU and T^T dW, in place of dU and dW once every thread has its values
+    constexpr int NTU = (C * DV + NT - 1) / NT, NTW = (C * DK + NT - 1) / NT;
+    float tdu[NTU], tdw[NTW];
+#pragma unroll
+    for (int q = 0; q < NTU; ++q) {
+        const int e = tid + q * NT;
         const int r = e / DV, j = e % DV;
         float acc = 0.f;
 #pragma unroll
-        for (int s = 0; s < C; ++s) acc += sm.T[s][r] * sm.dU[s][j];
-        sm.TdU[r][j] = acc;
+        for (int s = 0; s < C; ++s) acc = fmaf(sm.T[s][r], sm.dU[s][j], acc);
+        tdu[q] = acc;
     }
-    for (int e = tid; e < C * DK; e += NT) {
+#pragma unroll
+    for (int q = 0; q < NTW; ++q) {
+        const int e = tid + q * NT;
         const int r = e / DK, c = e % DK;
         float acc = 0.f;
 #pragma unroll
-        for (int s = 0; s < C; ++s) acc += sm.T[s][r] * sm.dW[s][c];
-        sm.TdW[r][c] = acc;
+        for (int s = 0; s < C; ++s) acc = fmaf(sm.T[s][r], sm.dW[s][c], acc);
+        tdw[q] = acc;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < NTU; ++q) {
+        const int e = tid + q * NT;
+        sm.dU[e / DV][e % DV] = tdu[q];
+    }
+#pragma unroll
+    for (int q = 0; q < NTW; ++q) {
+        const int e = tid + q * NT;
+        sm.dW[e / DK][e % DK] = tdw[q];
     }
     __syncthreads();
 
-    // 8. dq, dk and dG per element
+    // 8. dq, dk and dG per element (dG into dKt's place: each entry is read only by its own thread)
     TIO* dqp = static_cast<TIO*>(b.dq);
     TIO* dkp = static_cast<TIO*>(b.dk);
     for (int e = tid; e < C * DK; e += NT) {
@@ -535,37 +705,38 @@ __global__ void __launch_bounds__(NT) kda_bwd_chunk_kernel(BackwardArgs b)
         if (r >= len) continue;
         const float br = sm.beta[r];
         float t = 0.f;
-        for (int i = 0; i < r; ++i) t += sm.dA[r][i] * sm.KI[i][c];
-        const float dKG = br * (sm.TdW[r][c] + t);
+        for (int i = 0; i < r; ++i) t = fmaf(sm.dA[r][i], sm.KI[i][c], t);
+        const float dKG = br * (sm.dW[r][c] + t);
         float dKI = 0.f;
-        for (int s = r + 1; s < len; ++s) dKI += sm.beta[s] * sm.dA[s][r] * sm.KG[s][c];
-        for (int s = r; s < len; ++s) dKI += sm.dP[s][r] * sm.QG[s][c];
+        for (int s = r + 1; s < len; ++s) dKI = fmaf(sm.beta[s] * sm.dA[s][r], sm.KG[s][c], dKI);
+        for (int s = r; s < len; ++s) dKI = fmaf(sm.dP[s][r], sm.QG[s][c], dKI);
         float dQG = sm.dQa[r][c];
-        for (int i = 0; i <= r; ++i) dQG += sm.dP[r][i] * sm.KI[i][c];
+        for (int i = 0; i <= r; ++i) dQG = fmaf(sm.dP[r][i], sm.KI[i][c], dQG);
         const float dKt = sm.dKt[r][c];
         const float g = sm.G[r][c];
+        const float eg = expf(g);
         const float ekt = expf(sm.GL[c] - g);
         const float k = sm.K[r][c];
         const int64_t idx = ((t0 + r) * H + h) * (int64_t)DK + c;
-        st_io(dkp, idx, dKG * sm.EG[r][c] + dKI * expf(-g) + dKt * ekt);
-        st_io(dqp, idx, dQG * sm.EG[r][c]);
+        st_io(dkp, idx, dKG * eg + dKI * expf(-g) + dKt * ekt);
+        st_io(dqp, idx, dQG * eg);
         float dG = dKG * sm.KG[r][c] + dQG * sm.QG[r][c] - dKI * sm.KI[r][c] - dKt * k * ekt;
         if (r == len - 1) dG += sm.ktsum[c] + expf(sm.GL[c]) * sm.rs[c];
-        sm.dW[r][c] = dG;  // dW is no longer read (steps 5 and 7 are done)
+        sm.dKt[r][c] = dG;
     }
-    // 9. dv and dbeta
+    // 9. dv and dbeta (T^T dU now in dU, T^T dW in dW)
     TIO* dvp = static_cast<TIO*>(b.dv);
     for (int e = tid; e < C * DV; e += NT) {
         const int r = e / DV, j = e % DV;
-        if (r < len) st_io(dvp, ((t0 + r) * H + h) * (int64_t)DV + j, sm.beta[r] * sm.TdU[r][j]);
+        if (r < len) st_io(dvp, ((t0 + r) * H + h) * (int64_t)DV + j, sm.beta[r] * sm.dU[r][j]);
     }
     {
         const int w = tid >> 5, lane = tid & 31;
         for (int r = w; r < len; r += NT / 32) {
             float acc = 0.f;
-            for (int j = lane; j < DV; j += 32) acc += sm.TdU[r][j] * sm.V[r][j];
-            for (int c = lane; c < DK; c += 32) acc += sm.TdW[r][c] * sm.KG[r][c];
-            if (lane < C) acc += sm.dA[r][lane] * sm.M[r][lane];
+            for (int j = lane; j < DV; j += 32) acc = fmaf(sm.dU[r][j], sm.V[r][j], acc);
+            for (int c = lane; c < DK; c += 32) acc = fmaf(sm.dW[r][c], sm.KG[r][c], acc);
+            if (lane < C) acc = fmaf(sm.dA[r][lane], sm.M[r][lane], acc);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
             if (lane == 0) b.dbeta[(t0 + r) * H + h] = acc;
@@ -580,7 +751,7 @@ __global__ void __launch_bounds__(NT) kda_bwd_chunk_kernel(BackwardArgs b)
     for (int c = tid; c < DK; c += NT) {
         float dg = 0.f;
         for (int r = len - 1; r >= 0; --r) {
-            dg += sm.dW[r][c];
+            dg += sm.dKt[r][c];
             const int64_t idx = ((t0 + r) * H + h) * (int64_t)DK + c;
             const float x = expA * ld_io(zp, idx);
             const float dx = dg * a.g_min * sigmoid_slope(x);
@@ -652,48 +823,29 @@ cudaError_t launch_backward_t(const BackwardArgs& b, cudaStream_t s)
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     // value-column slices of the state passes: 32 columns, or 16 when that is needed to give every
-    // SM a chain
-    const int64_t chains32 = (int64_t)a.N * a.H * (DV >= 32 ? DV / 32 : 1);
+    // SM a chain; the forward pass is skipped when no sequence has a token (the reverse pass still
+    // writes dS0 = dS_final)
+    const int64_t chains32 = 2 * (int64_t)a.N * a.H * (DV >= 32 ? DV / 32 : 1);
     const bool narrow = DV >= 32 && chains32 < sm_count_of_current_device();
-    if (a.chunks_per_seq > 0) {
-        if (narrow) {
-            constexpr int JS = 16;
-            const size_t smem = sizeof(StatesSmem<DK, JS>);
-            auto kern = kda_bwd_states_kernel<TIO, DK, DV, JS>;
-            if ((e = set_smem(kern, smem)) != cudaSuccess) return e;
-            prof_start("kda_bwd_states", s);
-            kern<<<dim3((unsigned)a.N, (unsigned)a.H, DV / JS), NT, smem, s>>>(b);
-            prof_stop(s);
-        } else {
-            constexpr int JS = DV < 32 ? DV : 32;
-            const size_t smem = sizeof(StatesSmem<DK, JS>);
-            auto kern = kda_bwd_states_kernel<TIO, DK, DV, JS>;
-            if ((e = set_smem(kern, smem)) != cudaSuccess) return e;
-            prof_start("kda_bwd_states", s);
-            kern<<<dim3((unsigned)a.N, (unsigned)a.H, DV / JS), NT, smem, s>>>(b);
-            prof_stop(s);
-        }
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-    // the reverse pass also runs for empty sequences (dS0 = dS_final)
+    const int with_forward = a.chunks_per_seq > 0 ? 1 : 0;
+    auto launch_states = [&](auto kern, size_t smem, int nsl) -> cudaError_t {
+        cudaError_t err = set_smem(kern, smem);
+        if (err != cudaSuccess) return err;
+        prof_start("kda_bwd_states", s);
+        kern<<<dim3((unsigned)a.N, (unsigned)a.H, (unsigned)(nsl * (1 + with_forward))), NT, smem, s>>>(b, with_forward);
+        prof_stop(s);
+        return cudaGetLastError();
+    };
     if (narrow) {
         constexpr int JS = 16;
-        const size_t smem = sizeof(DStatesSmem<DK, JS>);
-        auto kern = kda_bwd_dstates_kernel<TIO, DK, DV, JS>;
-        if ((e = set_smem(kern, smem)) != cudaSuccess) return e;
-        prof_start("kda_bwd_dstates", s);
-        kern<<<dim3((unsigned)a.N, (unsigned)a.H, DV / JS), NT, smem, s>>>(b);
-        prof_stop(s);
+        const size_t smem = std::max(sizeof(StatesSmem<DK, JS>), sizeof(DStatesSmem<DK, JS>));
+        e = launch_states(kda_bwd_states_kernel<TIO, DK, DV, JS>, smem, DV / JS);
     } else {
         constexpr int JS = DV < 32 ? DV : 32;
-        const size_t smem = sizeof(DStatesSmem<DK, JS>);
-        auto kern = kda_bwd_dstates_kernel<TIO, DK, DV, JS>;
-        if ((e = set_smem(kern, smem)) != cudaSuccess) return e;
-        prof_start("kda_bwd_dstates", s);
-        kern<<<dim3((unsigned)a.N, (unsigned)a.H, DV / JS), NT, smem, s>>>(b);
-        prof_stop(s);
+        const size_t smem = std::max(sizeof(StatesSmem<DK, JS>), sizeof(DStatesSmem<DK, JS>));
+        e = launch_states(kda_bwd_states_kernel<TIO, DK, DV, JS>, smem, DV / JS);
     }
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (e != cudaSuccess) return e;
     if (a.chunks_per_seq > 0) {
         const size_t smem = sizeof(ChunkGradSmem<DK, DV>);
         auto kern = kda_bwd_chunk_kernel<TIO, DK, DV>;
