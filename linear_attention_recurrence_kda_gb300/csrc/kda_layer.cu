@@ -12,12 +12,12 @@
 //                                                  head-wise RMSNorm and sigmoid output gate
 // The projections themselves (x W) are plain GEMMs outside this library.
 //
-// Both are streaming kernels: every element is read and written once.  A prologue warp walks 8
-// consecutive tokens of one head and one tensor (lane l owns channels l*VEC .. l*VEC + VEC - 1):
-// it issues the loads of all 8 rows first, then convolves with the window of its channels kept in
-// registers (each row read once, plus a K-1 row halo per 8 tokens that the neighbouring warp of the
-// same CTA has just read); the L2 norm is a warp reduction.  An epilogue warp normalises whole
-// token-head rows with one warp reduction each.  Swish and the gate use the hardware exponential
+// Both are streaming kernels: every element is read and written once.  A prologue CTA takes 64
+// consecutive tokens of one head and one tensor: its threads first copy the 64 rows (and the K-1
+// rows before them) into shared memory with asynchronous 16-byte copies, so that a whole tile is in
+// flight at once, then every warp walks 8 of the tokens (lane l owns channels l*VEC ..
+// l*VEC + VEC - 1), convolving from the staged rows (zero before each sequence start); the L2 norm is
+// a warp reduction.  An epilogue warp normalises whole token-head rows with one warp reduction each.  Swish and the gate use the hardware exponential
 // and reciprocal approximations, the norms rsqrt.
 #include "kda_internal.cuh"
 
@@ -28,6 +28,7 @@ namespace {
 constexpr int kLayerThreads = 256;
 constexpr int kLayerWarps = kLayerThreads / 32;
 constexpr int kProTokens = 8;  // tokens per prologue warp
+constexpr int kProTile = kLayerWarps * kProTokens;  // tokens per prologue CTA
 
 template <typename TIO, int VEC>
 __device__ __forceinline__ void ld_vec(const TIO* p, float (&x)[VEC])
@@ -62,6 +63,30 @@ __device__ __forceinline__ void st_vec(TIO* p, const float (&x)[VEC])
 #pragma unroll
         for (int e = 0; e < VEC; ++e) st_io(p, e, x[e]);
     }
+}
+
+template <typename TIO, int VEC>
+__device__ __forceinline__ void lds_vec(const TIO* p, float (&x)[VEC])
+{
+    if constexpr (sizeof(TIO) == 2 && VEC == 4) {
+        const uint2 u = *reinterpret_cast<const uint2*>(p);
+        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
+        x[0] = __low2float(a); x[1] = __high2float(a); x[2] = __low2float(b); x[3] = __high2float(b);
+    } else if constexpr (sizeof(TIO) == 4 && VEC == 4) {
+        const float4 f = *reinterpret_cast<const float4*>(p);
+        x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+    } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) x[e] = ld_io(p, e);
+    }
+}
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem_dst)),
+                 "l"(gmem_src)
+                 : "memory");
 }
 
 // logistic function from the hardware base-2 exponential and reciprocal approximations (relative
@@ -101,31 +126,34 @@ template <typename TIO, int VEC>
 __global__ void __launch_bounds__(kLayerThreads) kda_prologue_kernel(PrologueArgs a, int first)
 {
     constexpr int D = 32 * VEC;
+    constexpr int HALO = kMaxConv - 1;
+    constexpr int CH = D * (int)sizeof(TIO) / 16;  // 16-byte pieces per row
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    TIO* rows = reinterpret_cast<TIO*>(smem_raw);  // [HALO + kProTile][D]: row HALO + r is token t0 + r
     const int which = first + blockIdx.z;  // 0: q, 1: k, 2: v
     const int h = blockIdx.y;
     const int w = threadIdx.x >> 5;
     const int l = threadIdx.x & 31;
-    const int64_t t0 = ((int64_t)blockIdx.x * kLayerWarps + w) * kProTokens;
+    const int64_t t0 = (int64_t)blockIdx.x * kProTile;
     if (t0 >= a.T) return;
-    const int64_t t1 = min(t0 + (int64_t)kProTokens, a.T);
     // selected without indexing the parameter arrays (which would copy them to local memory)
     const TIO* x = static_cast<const TIO*>(which == 0 ? a.x[0] : which == 1 ? a.x[1] : a.x[2]);
     TIO* y = static_cast<TIO*>(which == 0 ? a.y[0] : which == 1 ? a.y[1] : a.y[2]);
     const float* wt = which == 0 ? a.w[0] : which == 1 ? a.w[1] : a.w[2];
     const int K = a.K;
 
-    // the sequence of t0: [start, end)
-    int64_t start, end;
-    int n = 0;
-    if (a.cu != nullptr) {
-        n = find_seq(a.cu, a.N, t0);
-        start = min((int64_t)max(a.cu[n], 0), t0);
-        end = max((int64_t)a.cu[n + 1], t0 + 1);
-    } else {
-        const int64_t len = a.T / a.N;
-        start = (t0 / len) * len;
-        end = start + len;
+    // the tile's rows and the K-1 rows before it (tokens outside [0, T) are not copied and never read)
+    const int64_t r_lo = t0 - HALO;
+    const int nrows = HALO + kProTile;
+    for (int e = threadIdx.x; e < nrows * CH; e += kLayerThreads) {
+        const int r = e / CH, ch = e - r * CH;
+        const int64_t t = r_lo + r;
+        if (t >= 0 && t < a.T) {
+            cp_async16(reinterpret_cast<unsigned char*>(rows + r * D) + ch * 16,
+                       reinterpret_cast<const unsigned char*>(x + (t * a.H + h) * D) + ch * 16);
+        }
     }
+    asm volatile("cp.async.commit_group;" ::: "memory");
 
     float wk[VEC][kMaxConv];
 #pragma unroll
@@ -133,60 +161,61 @@ __global__ void __launch_bounds__(kLayerThreads) kda_prologue_kernel(PrologueArg
 #pragma unroll
         for (int i = 0; i < kMaxConv; ++i) wk[e][i] = (i < K) ? wt[((int64_t)h * D + l * VEC + e) * K + i] : 0.f;
 
-    // win[i] holds x_{t-1-i} of this lane's channels (zero before the sequence start)
-    float win[kMaxConv - 1][VEC];
-#pragma unroll
-    for (int i = 0; i < kMaxConv - 1; ++i) {
-        const int64_t ts = t0 - 1 - i;
-        if (i + 1 < K && ts >= start) {
-            ld_vec<TIO, VEC>(x + (ts * a.H + h) * D + l * VEC, win[i]);
+    // this warp's tokens [tw, tw1) and the start of the sequence holding tw
+    const int64_t tw = t0 + (int64_t)w * kProTokens;
+    const int64_t tw1 = min(tw + (int64_t)kProTokens, a.T);
+    int64_t start = 0, end = 0;
+    int n = 0;
+    if (tw < a.T) {
+        if (a.cu != nullptr) {
+            n = find_seq(a.cu, a.N, tw);
+            start = min((int64_t)max(a.cu[n], 0), tw);
+            end = max((int64_t)a.cu[n + 1], tw + 1);
         } else {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) win[i][e] = 0.f;
+            const int64_t len = a.T / a.N;
+            start = (tw / len) * len;
+            end = start + len;
         }
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
 
-    // every token row of this warp in flight before any arithmetic
-    float xs[kProTokens][VEC];
-#pragma unroll
-    for (int j = 0; j < kProTokens; ++j) {
-        if (t0 + j < t1) ld_vec<TIO, VEC>(x + ((t0 + j) * a.H + h) * D + l * VEC, xs[j]);
-    }
-
-#pragma unroll
-    for (int j = 0; j < kProTokens; ++j) {
-        const int64_t t = t0 + j;
-        if (t >= t1) break;
-        if (t >= end) {  // a new sequence starts here: the window restarts from zeros
+    for (int64_t t = tw; t < tw1; ++t) {
+        if (t >= end) {  // a new sequence starts here
             if (a.cu != nullptr) {
                 while (n + 1 < a.N && (int64_t)a.cu[n + 1] <= t) ++n;
+                start = t;
                 end = max((int64_t)a.cu[n + 1], t + 1);
             } else {
+                start = t;
                 end = t + a.T / a.N;
             }
-#pragma unroll
-            for (int i = 0; i < kMaxConv - 1; ++i)
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) win[i][e] = 0.f;
         }
-        const float* xt = xs[j];
+        const int r = (int)(t - r_lo);
+        float s[VEC];
+        {
+            float xt[VEC];
+            lds_vec<TIO, VEC>(rows + r * D + l * VEC, xt);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) s[e] = wk[e][0] * xt[e];
+        }
+#pragma unroll
+        for (int i = 1; i < kMaxConv; ++i) {
+            if (i < K && t - i >= start) {
+                float xp[VEC];
+                lds_vec<TIO, VEC>(rows + (r - i) * D + l * VEC, xp);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) s[e] = fmaf(wk[e][i], xp[e], s[e]);
+            }
+        }
         float yv[VEC];
         float ss = 0.f;
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
-            float s = wk[e][0] * xt[e];
-#pragma unroll
-            for (int i = 1; i < kMaxConv; ++i) s += wk[e][i] * win[i - 1][e];
-            const float sw = s * sigmoid_f(s);
+            const float sw = s[e] * sigmoid_f(s[e]);
             yv[e] = sw;
-            ss += sw * sw;
+            ss = fmaf(sw, sw, ss);
         }
-#pragma unroll
-        for (int i = kMaxConv - 2; i > 0; --i)
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) win[i][e] = win[i - 1][e];
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) win[0][e] = xt[e];
         if (which < 2) {
             const float inv = rsqrtf(warp_sum(ss) + 1e-6f);
 #pragma unroll
@@ -225,13 +254,14 @@ __global__ void __launch_bounds__(kLayerThreads) kda_epilogue_kernel(EpilogueArg
 template <typename TIO>
 static cudaError_t launch_prologue_io(const PrologueArgs& a, cudaStream_t s)
 {
-    const unsigned gx = (unsigned)((a.T + (int64_t)kLayerWarps * kProTokens - 1) / ((int64_t)kLayerWarps * kProTokens));
+    const unsigned gx = (unsigned)((a.T + kProTile - 1) / kProTile);
     if (gx == 0) return cudaSuccess;
     auto go = [&](int d, int first, int count) -> cudaError_t {
         const dim3 grid(gx, (unsigned)a.H, (unsigned)count);
-        if (d == 32) kda_prologue_kernel<TIO, 1><<<grid, kLayerThreads, 0, s>>>(a, first);
-        else if (d == 64) kda_prologue_kernel<TIO, 2><<<grid, kLayerThreads, 0, s>>>(a, first);
-        else if (d == 128) kda_prologue_kernel<TIO, 4><<<grid, kLayerThreads, 0, s>>>(a, first);
+        const size_t smem = (size_t)(kMaxConv - 1 + kProTile) * d * sizeof(TIO);
+        if (d == 32) kda_prologue_kernel<TIO, 1><<<grid, kLayerThreads, smem, s>>>(a, first);
+        else if (d == 64) kda_prologue_kernel<TIO, 2><<<grid, kLayerThreads, smem, s>>>(a, first);
+        else if (d == 128) kda_prologue_kernel<TIO, 4><<<grid, kLayerThreads, smem, s>>>(a, first);
         else return cudaErrorInvalidValue;
         return cudaGetLastError();
     };
