@@ -198,9 +198,9 @@ kda_status_t kda_state_scan(const float* transition, const float* state_from_zer
 
 /*
  * Bytes of device workspace kda_backward needs for this problem (0 if the descriptor is invalid):
- * per token and head 4 (2 d_k + 3 d_v + 16) bytes, plus two fp32 d_k x d_v states (the state
+ * per token and head 4 (4 d_k + 3 d_v + 16) bytes, plus two fp32 d_k x d_v states (the state
  * entering each 16-token chunk and the gradient reaching its end) per chunk slot and head, with
- * T_tot / 16 + N + 1 slots -- about 10.6 KiB per token and head at d_k = d_v = 128.
+ * T_tot / 16 + N + 1 slots -- about 11.6 KiB per token and head at d_k = d_v = 128.
  */
 size_t kda_backward_workspace_bytes(const kda_problem_t* problem);
 

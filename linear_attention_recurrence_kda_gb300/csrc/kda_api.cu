@@ -411,6 +411,8 @@ kda_status_t kda_backward(const void* q, const void* k, const void* v, const voi
     b.dout = d_out; b.dS_final = d_final_state;
     b.dq = dq; b.dk = dk; b.dv = dv; b.dz = dz; b.dA = dA; b.dbeta = dbeta; b.dS0 = d_initial_state;
     b.P = reinterpret_cast<float*>(ws + L.p_off);
+    b.QG = reinterpret_cast<float*>(ws + L.qg_off);
+    b.Kt = reinterpret_cast<float*>(ws + L.kt_off);
     b.U = reinterpret_cast<float*>(ws + L.u_off);
     b.dU = reinterpret_cast<float*>(ws + L.du_off);
     b.S_chunk = reinterpret_cast<float*>(ws + L.s_off);

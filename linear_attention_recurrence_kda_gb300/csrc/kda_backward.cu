@@ -20,7 +20,7 @@
 // g_min >= -5.4 every factor of one chunk is a finite fp32 number (e^-G <= e^86.4).
 //
 // Kernels, in order (after kda_gate and kda_ut_wy, which fill G, W and U~):
-//   kda_bwd_gram    per (chunk, head): P = tril(QG KI^T)
+//   kda_bwd_gram    per (chunk, head): P = tril(QG KI^T), and QG, Kt for the walks
 //   kda_bwd_states  per (sequence, head, value-column slice), one launch, two independent walks:
 //                   chunks in order for the state entering every chunk and U = U~ - W S; chunks
 //                   in reverse for the gradient reaching every chunk's end state, dU, and dS0
@@ -85,14 +85,21 @@ __global__ void __launch_bounds__(NT) kda_bwd_gram_kernel(BackwardArgs b)
     for (int e = tid; e < C * DK; e += NT) {
         const int r = e / DK, c = e % DK;
         float q = 0.f, k = 0.f, g = 0.f;
+        const int64_t idx = ((t0 + r) * a.H + h) * (int64_t)DK + c;
         if (r < len) {
-            const int64_t idx = ((t0 + r) * a.H + h) * (int64_t)DK + c;
             q = ld_io(qp, idx);
             k = ld_io(kp, idx);
             g = a.G[idx];
         }
-        QG[r][c] = q * expf(g);
+        const float qg = q * expf(g);
+        QG[r][c] = qg;
         KI[r][c] = k * expf(-g);
+        if (r < len) {
+            // Q Gamma and K Gamma_C / Gamma for the sequential state walks
+            const float gl = a.G[((t0 + len - 1) * a.H + h) * (int64_t)DK + c];
+            b.QG[idx] = qg;
+            b.Kt[idx] = k * expf(gl - g);
+        }
     }
     __syncthreads();
     const int r = tid / C, i = tid % C;
@@ -108,38 +115,50 @@ __global__ void __launch_bounds__(NT) kda_bwd_gram_kernel(BackwardArgs b)
 
 // ---------------------------------------------------------------- state passes (shared pieces)
 //
-// Both passes walk one (sequence, head, value-column slice) chunk by chunk.  The slice of the state
+// Both walks visit one (sequence, head, value-column slice) chunk by chunk.  The slice of the state
 // lives in shared memory transposed, St[j][c] (rows padded to keep 16-byte alignment), so that both
-// products of a chunk read their operands as float4 along the key channels; the next chunk's rows
-// are loaded into registers while the current chunk computes.
+// products of a chunk read their operands as float4 along the key channels.  The rows of the next
+// two chunks travel into a three-slot ring by asynchronous 16-byte copies while the current chunk
+// computes (rows past the sequence end are zero-filled by the copies themselves; every iteration
+// commits one copy group, empty near the end, so that "all but the newest group" is always the
+// current chunk).
 
-template <int DK>
-struct RowPrefetch {
-    static constexpr int PER = C * DK / NT;  // row elements per thread and array
-    float v[PER];
-};
-
-// Rows [C][DK] of a [T][H][DK] tensor (io dtype or fp32) for the chunk at t0 of length len, this
-// thread's elements e = tid + p * NT, zero beyond len.
-template <typename T, int DK>
-__device__ __forceinline__ void load_rows(RowPrefetch<DK>& r, const T* src, int64_t t0, int len, int H, int h, int tid)
+__device__ __forceinline__ void cp_async16_zfill(void* smem_dst, const void* gmem_src, bool valid)
 {
-#pragma unroll
-    for (int p = 0; p < RowPrefetch<DK>::PER; ++p) {
-        const int e = tid + p * NT;
-        const int row = e / DK, c = e % DK;
-        r.v[p] = row < len ? ld_io(src, ((t0 + row) * H + h) * (int64_t)DK + c) : 0.f;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(smem_dst)),
+                 "l"(gmem_src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gmem_src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(smem_dst)),
+                 "l"(gmem_src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// every copy group but the most recent one has landed
+__device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+constexpr int kBufs = 3;  // chunks in shared memory: the current one and two in flight
+
+// Copy `rows` rows of `bytes_per_row` bytes (a multiple of 16) of a chunk into dst (row pitch
+// `pitch` bytes); row r of the chunk starts at src + r * src_stride bytes; rows r >= len are zeroed.
+__device__ __forceinline__ void copy_rows(unsigned char* dst, int pitch, const unsigned char* src, int64_t src_stride,
+                                          int rows, int bytes_per_row, int len, int tid)
+{
+    const int per = bytes_per_row / 16;
+    for (int e = tid; e < rows * per; e += NT) {
+        const int r = e / per, c = e - r * per;
+        const bool ok = r < len;
+        cp_async16_zfill(dst + r * pitch + c * 16, ok ? src + r * src_stride + c * 16 : src, ok);
     }
 }
-template <int DK>
-__device__ __forceinline__ void store_rows(const RowPrefetch<DK>& r, float (*dst)[DK], int tid)
-{
-#pragma unroll
-    for (int p = 0; p < RowPrefetch<DK>::PER; ++p) {
-        const int e = tid + p * NT;
-        dst[e / DK][e % DK] = r.v[p];
-    }
-}
+
+template <typename T>
+__device__ __forceinline__ float to_f(T x) { return static_cast<float>(x); }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
 
 // ---------------------------------------------------------------- forward state pass (states kept)
 
@@ -147,9 +166,10 @@ template <int DK, int JS>
 struct StatesSmem {
     static constexpr int SP = DK + 4;  // padded row of the transposed state
     float St[JS][SP];                  // state slice, transposed: St[j][c] = S[c][j0 + j]
-    float K[C][DK];                    // keys, then K e^(G_C - G)
-    float G[C][DK];
-    float W[C][DK];
+    float K[kBufs][C][DK];             // K e^(G_C - G), ring of chunks
+    float W[kBufs][C][DK];
+    float Ut[kBufs][C][JS];            // U~ slice
+    float GL[kBufs][DK];               // G of the chunk's last token
     float U[C][JS];
     float eGL[DK];                     // e^(G_C)
 };
@@ -167,48 +187,47 @@ __device__ __forceinline__ void bwd_states(const BackwardArgs& b, unsigned char*
     const int H = a.H;
     int64_t s0, s1;
     if (!seq_range(a, n, s0, s1)) return;
-    const TIO* kp = static_cast<const TIO*>(a.k);
     const int64_t sbase = ((int64_t)n * H + h) * DK * DV;
     for (int e = tid; e < DK * JS; e += NT) {
         const int c = e / JS, j = e % JS;
         sm.St[j][c] = a.s0 ? a.s0[sbase + (int64_t)c * DV + j0 + j] : 0.f;
     }
-    constexpr int NU = (C * JS + NT - 1) / NT;   // U entries per thread
+    constexpr int NU = (C * JS + NT - 1) / NT;       // U entries per thread
     constexpr int NS = (JS * DK / 4 + NT - 1) / NT;  // (j, 4 channels) state items per thread
-    RowPrefetch<DK> pk, pg, pw;
-    float pu[NU];
-    auto fetch = [&](int64_t t0, int len) {
-        load_rows(pk, kp, t0, len, H, h, tid);
-        load_rows(pg, a.G, t0, len, H, h, tid);
-        load_rows(pw, a.W, t0, len, H, h, tid);
-#pragma unroll
-        for (int q = 0; q < NU; ++q) {
-            const int e = tid + q * NT;
-            const int r = e / JS, j = e % JS;
-            pu[q] = (e < C * JS && r < len) ? a.Ut[((t0 + r) * H + h) * (int64_t)DV + j0 + j] : 0.f;
-        }
+    const int64_t rowk = (int64_t)H * DK * 4, rowv = (int64_t)H * DV * 4;  // bytes between token rows
+    auto fetch = [&](int buf, int64_t t0, int len) {
+        const int64_t base = (t0 * H + h);
+        copy_rows(reinterpret_cast<unsigned char*>(sm.K[buf]), DK * 4,
+                  reinterpret_cast<const unsigned char*>(b.Kt + base * DK), rowk, C, DK * 4, len, tid);
+        copy_rows(reinterpret_cast<unsigned char*>(sm.W[buf]), DK * 4,
+                  reinterpret_cast<const unsigned char*>(a.W + base * DK), rowk, C, DK * 4, len, tid);
+        copy_rows(reinterpret_cast<unsigned char*>(sm.Ut[buf]), JS * 4,
+                  reinterpret_cast<const unsigned char*>(a.Ut + base * DV + j0), rowv, C, JS * 4, len, tid);
+        copy_rows(reinterpret_cast<unsigned char*>(sm.GL[buf]), DK * 4,
+                  reinterpret_cast<const unsigned char*>(a.G + ((t0 + len - 1) * H + h) * DK), 0, 1, DK * 4, 1, tid);
+        cp_async_commit();
     };
-    if (s0 < s1) fetch(s0, (int)min((int64_t)C, s1 - s0));
+    auto fetch_chunk = [&](int64_t c) {  // chunk c into its ring slot (an empty group past the end)
+        const int64_t t = s0 + c * C;
+        if (t < s1) fetch((int)(c % kBufs), t, (int)min((int64_t)C, s1 - t));
+        else cp_async_commit();
+    };
+    fetch_chunk(0);
+    fetch_chunk(1);
     for (int64_t ci = 0; s0 + ci * C < s1; ++ci) {
         const int64_t t0 = s0 + ci * C;
         const int len = (int)min((int64_t)C, s1 - t0);
-        __syncthreads();  // the previous chunk's state update is complete
-        store_rows(pk, sm.K, tid);
-        store_rows(pg, sm.G, tid);
-        store_rows(pw, sm.W, tid);
-#pragma unroll
-        for (int q = 0; q < NU; ++q) {
-            const int e = tid + q * NT;
-            if (e < C * JS) sm.U[e / JS][e % JS] = pu[q];
-        }
+        const int buf = (int)(ci % kBufs);
+        cp_async_wait_prev();
+        __syncthreads();  // this chunk's rows have landed; the previous chunk's update is complete
+        fetch_chunk(ci + 2);
+        if (tid < DK) sm.eGL[tid] = expf(sm.GL[buf][tid]);
         float* dst = b.S_chunk + (chunk_slot(n, s0, ci) * H + h) * (int64_t)DK * DV + j0;
         for (int e = tid; e < DK * JS; e += NT) {
             const int c = e / JS, j = e % JS;
             dst[(int64_t)c * DV + j] = sm.St[j][c];
         }
-        if (t0 + C < s1) fetch(t0 + C, (int)min((int64_t)C, s1 - t0 - C));
-        __syncthreads();
-        // U = U~ - W S (four accumulators along the key channels); K -> K e^(G_C - G)
+        // U = U~ - W S (four accumulators along the key channels)
         float uacc[NU];
 #pragma unroll
         for (int q = 0; q < NU; ++q) {
@@ -216,25 +235,17 @@ __device__ __forceinline__ void bwd_states(const BackwardArgs& b, unsigned char*
             uacc[q] = 0.f;
             if (e < C * JS) {
                 const int r = e / JS, j = e % JS;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll 8
                 for (int c = 0; c < DK; c += 4) {
-                    const float4 w = *reinterpret_cast<const float4*>(&sm.W[r][c]);
+                    const float4 w = *reinterpret_cast<const float4*>(&sm.W[buf][r][c]);
                     const float4 x = *reinterpret_cast<const float4*>(&sm.St[j][c]);
-                    acc.x = fmaf(w.x, x.x, acc.x);
-                    acc.y = fmaf(w.y, x.y, acc.y);
-                    acc.z = fmaf(w.z, x.z, acc.z);
-                    acc.w = fmaf(w.w, x.w, acc.w);
+                    a01 = __ffma2_rn(make_float2(w.x, w.y), make_float2(x.x, x.y), a01);
+                    a23 = __ffma2_rn(make_float2(w.z, w.w), make_float2(x.z, x.w), a23);
                 }
-                uacc[q] = r < len ? sm.U[r][j] - ((acc.x + acc.y) + (acc.z + acc.w)) : 0.f;
+                uacc[q] = r < len ? sm.Ut[buf][r][j] - ((a01.x + a01.y) + (a23.x + a23.y)) : 0.f;
             }
         }
-        for (int e = tid; e < C * DK; e += NT) {
-            const int r = e / DK, c = e % DK;
-            sm.K[r][c] *= expf(sm.G[len - 1][c] - sm.G[r][c]);
-        }
-        for (int c = tid; c < DK; c += NT) sm.eGL[c] = expf(sm.G[len - 1][c]);
-        __syncthreads();
 #pragma unroll
         for (int q = 0; q < NU; ++q) {
             const int e = tid + q * NT;
@@ -244,7 +255,7 @@ __device__ __forceinline__ void bwd_states(const BackwardArgs& b, unsigned char*
                 if (r < len) b.U[((t0 + r) * H + h) * (int64_t)DV + j0 + j] = uacc[q];
             }
         }
-        __syncthreads();
+        __syncthreads();  // U and e^G_C complete; every thread has read the old state
         // S = e^G_C S + Kt^T U, four key channels of one column per item
 #pragma unroll
         for (int q = 0; q < NS; ++q) {
@@ -252,17 +263,17 @@ __device__ __forceinline__ void bwd_states(const BackwardArgs& b, unsigned char*
             if (e < JS * DK / 4) {
                 const int j = e / (DK / 4), c = 4 * (e % (DK / 4));
                 const float4 g = *reinterpret_cast<const float4*>(&sm.eGL[c]);
-                float4 x = *reinterpret_cast<const float4*>(&sm.St[j][c]);
-                x = make_float4(g.x * x.x, g.y * x.y, g.z * x.z, g.w * x.w);
-                for (int i = 0; i < len; ++i) {
+                const float4 x = *reinterpret_cast<const float4*>(&sm.St[j][c]);
+                float2 x01 = __fmul2_rn(make_float2(g.x, g.y), make_float2(x.x, x.y));
+                float2 x23 = __fmul2_rn(make_float2(g.z, g.w), make_float2(x.z, x.w));
+#pragma unroll
+                for (int i = 0; i < C; ++i) {  // rows past the chunk's end are zero
                     const float u = sm.U[i][j];
-                    const float4 kt = *reinterpret_cast<const float4*>(&sm.K[i][c]);
-                    x.x = fmaf(kt.x, u, x.x);
-                    x.y = fmaf(kt.y, u, x.y);
-                    x.z = fmaf(kt.z, u, x.z);
-                    x.w = fmaf(kt.w, u, x.w);
+                    const float4 kt = *reinterpret_cast<const float4*>(&sm.K[buf][i][c]);
+                    x01 = __ffma2_rn(make_float2(kt.x, kt.y), make_float2(u, u), x01);
+                    x23 = __ffma2_rn(make_float2(kt.z, kt.w), make_float2(u, u), x23);
                 }
-                *reinterpret_cast<float4*>(&sm.St[j][c]) = x;
+                *reinterpret_cast<float4*>(&sm.St[j][c]) = make_float4(x01.x, x01.y, x23.x, x23.y);
             }
         }
     }
@@ -270,16 +281,16 @@ __device__ __forceinline__ void bwd_states(const BackwardArgs& b, unsigned char*
 
 // ---------------------------------------------------------------- reverse state pass
 
-template <int DK, int JS>
+template <typename TIO, int DK, int JS>
 struct DStatesSmem {
     static constexpr int SP = DK + 4;
-    float dSt[JS][SP];  // gradient slice, transposed: dSt[j][c] = dS[c][j0 + j]
-    float Q[C][DK];     // queries, then Q e^G
-    float K[C][DK];     // keys, then K e^(G_C - G)
-    float G[C][DK];
-    float W[C][DK];
-    float P[C][C];
-    float dO[C][JS];
+    float dSt[JS][SP];      // gradient slice, transposed: dSt[j][c] = dS[c][j0 + j]
+    float Q[kBufs][C][DK];      // Q e^G, double buffered
+    float K[kBufs][C][DK];      // K e^(G_C - G)
+    float W[kBufs][C][DK];
+    float P[kBufs][C][C];
+    TIO dO[kBufs][C][JS];   // raw dO slice
+    float GL[kBufs][DK];
     float dU[C][JS];
     float eGL[DK];
 };
@@ -287,7 +298,7 @@ struct DStatesSmem {
 template <typename TIO, int DK, int DV, int JS>
 __device__ __forceinline__ void bwd_dstates(const BackwardArgs& b, unsigned char* smem_raw, int slice)
 {
-    using Sm = DStatesSmem<DK, JS>;
+    using Sm = DStatesSmem<TIO, DK, JS>;
     const PrefillArgs& a = b.f;
     Sm& sm = *reinterpret_cast<Sm*>(smem_raw);
     const int n = blockIdx.x;
@@ -297,8 +308,6 @@ __device__ __forceinline__ void bwd_dstates(const BackwardArgs& b, unsigned char
     const int H = a.H;
     int64_t s0, s1;
     if (!seq_range(a, n, s0, s1)) return;
-    const TIO* qp = static_cast<const TIO*>(a.q);
-    const TIO* kp = static_cast<const TIO*>(a.k);
     const TIO* dop = static_cast<const TIO*>(b.dout);
     const int64_t sbase = ((int64_t)n * H + h) * DK * DV;
     for (int e = tid; e < DK * JS; e += NT) {
@@ -307,63 +316,47 @@ __device__ __forceinline__ void bwd_dstates(const BackwardArgs& b, unsigned char
     }
     constexpr int NU = (C * JS + NT - 1) / NT;
     constexpr int NS = (JS * DK / 4 + NT - 1) / NT;
-    constexpr int NP = (C * C + NT - 1) / NT;
-    RowPrefetch<DK> pq, pk, pg, pw;
-    float pp[NP], po[NU];
-    auto fetch = [&](int64_t t0, int len) {
-        load_rows(pq, qp, t0, len, H, h, tid);
-        load_rows(pk, kp, t0, len, H, h, tid);
-        load_rows(pg, a.G, t0, len, H, h, tid);
-        load_rows(pw, a.W, t0, len, H, h, tid);
-#pragma unroll
-        for (int q = 0; q < NP; ++q) {
-            const int e = tid + q * NT;
-            const int r = e / C, i = e % C;
-            pp[q] = (e < C * C && r < len) ? b.P[((t0 + r) * H + h) * (int64_t)C + i] : 0.f;
-        }
-#pragma unroll
-        for (int q = 0; q < NU; ++q) {
-            const int e = tid + q * NT;
-            const int r = e / JS, j = e % JS;
-            po[q] = (e < C * JS && r < len) ? ld_io(dop, ((t0 + r) * H + h) * (int64_t)DV + j0 + j) : 0.f;
-        }
+    const int64_t rowk = (int64_t)H * DK * 4, rowp = (int64_t)H * C * 4, rowo = (int64_t)H * DV * sizeof(TIO);
+    auto fetch = [&](int buf, int64_t t0, int len) {
+        const int64_t base = (t0 * H + h);
+        copy_rows(reinterpret_cast<unsigned char*>(sm.Q[buf]), DK * 4,
+                  reinterpret_cast<const unsigned char*>(b.QG + base * DK), rowk, C, DK * 4, len, tid);
+        copy_rows(reinterpret_cast<unsigned char*>(sm.K[buf]), DK * 4,
+                  reinterpret_cast<const unsigned char*>(b.Kt + base * DK), rowk, C, DK * 4, len, tid);
+        copy_rows(reinterpret_cast<unsigned char*>(sm.W[buf]), DK * 4,
+                  reinterpret_cast<const unsigned char*>(a.W + base * DK), rowk, C, DK * 4, len, tid);
+        copy_rows(reinterpret_cast<unsigned char*>(sm.P[buf]), C * 4,
+                  reinterpret_cast<const unsigned char*>(b.P + base * C), rowp, C, C * 4, len, tid);
+        copy_rows(reinterpret_cast<unsigned char*>(sm.dO[buf]), JS * (int)sizeof(TIO),
+                  reinterpret_cast<const unsigned char*>(dop + base * DV + j0), rowo, C, JS * (int)sizeof(TIO), len, tid);
+        copy_rows(reinterpret_cast<unsigned char*>(sm.GL[buf]), DK * 4,
+                  reinterpret_cast<const unsigned char*>(a.G + ((t0 + len - 1) * H + h) * DK), 0, 1, DK * 4, 1, tid);
+        cp_async_commit();
     };
     const int64_t nch = (s1 - s0 + C - 1) / C;
     auto chunk_len = [&](int64_t ci) { return (int)min((int64_t)C, s1 - (s0 + ci * C)); };
-    if (nch > 0) fetch(s0 + (nch - 1) * C, chunk_len(nch - 1));
-    for (int64_t ci = nch - 1; ci >= 0; --ci) {
+    // the chunks are visited last first: visit v is chunk nch - 1 - v, in ring slot v mod kBufs
+    auto fetch_visit = [&](int64_t vis) {
+        const int64_t c = nch - 1 - vis;
+        if (c >= 0) fetch((int)(vis % kBufs), s0 + c * C, chunk_len(c));
+        else cp_async_commit();
+    };
+    fetch_visit(0);
+    fetch_visit(1);
+    for (int64_t vis = 0; vis < nch; ++vis) {
+        const int64_t ci = nch - 1 - vis;
         const int64_t t0 = s0 + ci * C;
         const int len = chunk_len(ci);
-        __syncthreads();  // the previous (later) chunk's update is complete
-        store_rows(pq, sm.Q, tid);
-        store_rows(pk, sm.K, tid);
-        store_rows(pg, sm.G, tid);
-        store_rows(pw, sm.W, tid);
-#pragma unroll
-        for (int q = 0; q < NP; ++q) {
-            const int e = tid + q * NT;
-            if (e < C * C) sm.P[e / C][e % C] = pp[q];
-        }
-#pragma unroll
-        for (int q = 0; q < NU; ++q) {
-            const int e = tid + q * NT;
-            if (e < C * JS) sm.dO[e / JS][e % JS] = po[q];
-        }
+        const int buf = (int)(vis % kBufs);
+        cp_async_wait_prev();
+        __syncthreads();  // this chunk's rows have landed; the previous (later) chunk's update is complete
+        fetch_visit(vis + 2);
+        if (tid < DK) sm.eGL[tid] = expf(sm.GL[buf][tid]);
         float* dst = b.dS_chunk + (chunk_slot(n, s0, ci) * H + h) * (int64_t)DK * DV + j0;
         for (int e = tid; e < DK * JS; e += NT) {
             const int c = e / JS, j = e % JS;
             dst[(int64_t)c * DV + j] = sm.dSt[j][c];
         }
-        if (ci > 0) fetch(t0 - C, chunk_len(ci - 1));
-        __syncthreads();
-        for (int e = tid; e < C * DK; e += NT) {
-            const int r = e / DK, c = e % DK;
-            const float g = sm.G[r][c];
-            sm.Q[r][c] *= expf(g);
-            sm.K[r][c] *= expf(sm.G[len - 1][c] - g);
-        }
-        for (int c = tid; c < DK; c += NT) sm.eGL[c] = expf(sm.G[len - 1][c]);
-        __syncthreads();
         // dU = Kt dS' + P^T dO
         float uacc[NU];
 #pragma unroll
@@ -373,19 +366,19 @@ __device__ __forceinline__ void bwd_dstates(const BackwardArgs& b, unsigned char
             if (e < C * JS) {
                 const int r = e / JS, j = e % JS;
                 if (r < len) {
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll 8
                     for (int c = 0; c < DK; c += 4) {
-                        const float4 kt = *reinterpret_cast<const float4*>(&sm.K[r][c]);
+                        const float4 kt = *reinterpret_cast<const float4*>(&sm.K[buf][r][c]);
                         const float4 x = *reinterpret_cast<const float4*>(&sm.dSt[j][c]);
-                        acc.x = fmaf(kt.x, x.x, acc.x);
-                        acc.y = fmaf(kt.y, x.y, acc.y);
-                        acc.z = fmaf(kt.z, x.z, acc.z);
-                        acc.w = fmaf(kt.w, x.w, acc.w);
+                        a01 = __ffma2_rn(make_float2(kt.x, kt.y), make_float2(x.x, x.y), a01);
+                        a23 = __ffma2_rn(make_float2(kt.z, kt.w), make_float2(x.z, x.w), a23);
                     }
+                    // P^T dO over the rows i >= r (P is lower triangular and zero past the chunk's end)
                     float pd = 0.f;
-                    for (int i = r; i < len; ++i) pd = fmaf(sm.P[i][r], sm.dO[i][j], pd);
-                    uacc[q] = ((acc.x + acc.y) + (acc.z + acc.w)) + pd;
+#pragma unroll
+                    for (int i = 0; i < C; ++i) pd = fmaf(sm.P[buf][i][r], to_f(sm.dO[buf][i][j]), pd);
+                    uacc[q] = ((a01.x + a01.y) + (a23.x + a23.y)) + pd;
                 }
             }
         }
@@ -398,7 +391,7 @@ __device__ __forceinline__ void bwd_dstates(const BackwardArgs& b, unsigned char
                 if (r < len) b.dU[((t0 + r) * H + h) * (int64_t)DV + j0 + j] = uacc[q];
             }
         }
-        __syncthreads();
+        __syncthreads();  // dU and e^G_C complete; every thread has read the old gradient
         // dS = e^G_C dS' + QG^T dO - W^T dU, four key channels of one column per item
 #pragma unroll
         for (int q = 0; q < NS; ++q) {
@@ -406,18 +399,20 @@ __device__ __forceinline__ void bwd_dstates(const BackwardArgs& b, unsigned char
             if (e < JS * DK / 4) {
                 const int j = e / (DK / 4), c = 4 * (e % (DK / 4));
                 const float4 g = *reinterpret_cast<const float4*>(&sm.eGL[c]);
-                float4 x = *reinterpret_cast<const float4*>(&sm.dSt[j][c]);
-                x = make_float4(g.x * x.x, g.y * x.y, g.z * x.z, g.w * x.w);
-                for (int r = 0; r < len; ++r) {
-                    const float o = sm.dO[r][j], du = sm.dU[r][j];
-                    const float4 qg = *reinterpret_cast<const float4*>(&sm.Q[r][c]);
-                    const float4 w = *reinterpret_cast<const float4*>(&sm.W[r][c]);
-                    x.x = fmaf(qg.x, o, fmaf(-w.x, du, x.x));
-                    x.y = fmaf(qg.y, o, fmaf(-w.y, du, x.y));
-                    x.z = fmaf(qg.z, o, fmaf(-w.z, du, x.z));
-                    x.w = fmaf(qg.w, o, fmaf(-w.w, du, x.w));
+                const float4 x = *reinterpret_cast<const float4*>(&sm.dSt[j][c]);
+                float2 x01 = __fmul2_rn(make_float2(g.x, g.y), make_float2(x.x, x.y));
+                float2 x23 = __fmul2_rn(make_float2(g.z, g.w), make_float2(x.z, x.w));
+#pragma unroll
+                for (int r = 0; r < C; ++r) {  // rows past the chunk's end are zero
+                    const float o = to_f(sm.dO[buf][r][j]), mdu = -sm.dU[r][j];
+                    const float4 qg = *reinterpret_cast<const float4*>(&sm.Q[buf][r][c]);
+                    const float4 w = *reinterpret_cast<const float4*>(&sm.W[buf][r][c]);
+                    x01 = __ffma2_rn(make_float2(qg.x, qg.y), make_float2(o, o),
+                                     __ffma2_rn(make_float2(w.x, w.y), make_float2(mdu, mdu), x01));
+                    x23 = __ffma2_rn(make_float2(qg.z, qg.w), make_float2(o, o),
+                                     __ffma2_rn(make_float2(w.z, w.w), make_float2(mdu, mdu), x23));
                 }
-                *reinterpret_cast<float4*>(&sm.dSt[j][c]) = x;
+                *reinterpret_cast<float4*>(&sm.dSt[j][c]) = make_float4(x01.x, x01.y, x23.x, x23.y);
             }
         }
     }
@@ -467,8 +462,8 @@ struct ChunkGradSmem {
     float dO[C][PV];
     float U[C][PV];
     float dU[C][PV];   // later T^T dU
-    float Sin[DK][JB + 1];
-    float dSo[DK][JB + 1];
+    float Sin[2][DK][JB + 1];  // double-buffered state tiles (odd pitch: no bank conflicts)
+    float dSo[2][DK][JB + 1];
     float M[C][C], P[C][C], T[C][C], dP[C][C], dTn[C][C], X[C][C], dA[C][C];
     float rs[DK], GL[DK], ktsum[DK];
     float beta[C];
@@ -497,6 +492,20 @@ __global__ void __launch_bounds__(NT) kda_bwd_chunk_kernel(BackwardArgs b)
     const int64_t slot = chunk_slot(n, s0, ci);
     const float* Sg = b.S_chunk + (slot * H + h) * (int64_t)DK * DV;
     const float* dSg = b.dS_chunk + (slot * H + h) * (int64_t)DK * DV;
+    constexpr int NTILE = DV / JB;
+    // state tile t (value columns t JB .. t JB + JB - 1) into slot t & 1 by asynchronous 4-byte copies
+    auto issue_tile = [&](int t) {
+        if (t < NTILE) {
+            const int jb = t * JB;
+            for (int e = tid; e < DK * JB; e += NT) {
+                const int c2 = e / JB, j = e % JB;
+                cp_async4(&sm.Sin[t & 1][c2][j], Sg + (int64_t)c2 * DV + jb + j);
+                cp_async4(&sm.dSo[t & 1][c2][j], dSg + (int64_t)c2 * DV + jb + j);
+            }
+        }
+        cp_async_commit();
+    };
+    issue_tile(0);  // in flight while the chunk's rows are read
 
     // 1. the chunk's rows (absent tokens as zeros)
     for (int e = tid; e < C * DK; e += NT) {
@@ -535,46 +544,60 @@ __global__ void __launch_bounds__(NT) kda_bwd_chunk_kernel(BackwardArgs b)
     {
         constexpr int CG = NT / DK;   // thread groups per key channel
         constexpr int RPT = C / CG;   // rows per thread
+        constexpr int RP = RPT / 2;   // row pairs per thread (packed fp32 arithmetic on a pair)
         const int c = tid % DK, grp = tid / DK;
-        float akt[RPT], aqa[RPT], aw[RPT];
+        float2 akt[RP], aqa[RP], aw[RP];
 #pragma unroll
-        for (int rr = 0; rr < RPT; ++rr) akt[rr] = aqa[rr] = aw[rr] = 0.f;
+        for (int rp = 0; rp < RP; ++rp) akt[rp] = aqa[rp] = aw[rp] = make_float2(0.f, 0.f);
         float rsum = 0.f;
-        for (int jb = 0; jb < DV; jb += JB) {
-            __syncthreads();  // the previous tile is consumed (and step 1 is complete)
-            for (int e = tid; e < DK * JB; e += NT) {
-                const int c2 = e / JB, j = e % JB;
-                sm.Sin[c2][j] = Sg[(int64_t)c2 * DV + jb + j];
-                sm.dSo[c2][j] = dSg[(int64_t)c2 * DV + jb + j];
-            }
-            __syncthreads();
+        for (int t = 0; t < NTILE; ++t) {
+            const int jb = t * JB, sl = t & 1;
+            issue_tile(t + 1);  // its slot was consumed before the previous iteration's last barrier
+            cp_async_wait_prev();
+            __syncthreads();    // tile t has landed (and step 1 is complete)
 #pragma unroll 2
             for (int j = 0; j < JB; j += 4) {
                 float sv[4], dv[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    sv[q] = sm.Sin[c][j + q];
-                    dv[q] = sm.dSo[c][j + q];
+                    sv[q] = sm.Sin[sl][c][j + q];
+                    dv[q] = sm.dSo[sl][c][j + q];
                     rsum = fmaf(sv[q], dv[q], rsum);
                 }
 #pragma unroll
-                for (int rr = 0; rr < RPT; ++rr) {
-                    const int r = grp * RPT + rr;
-                    const float4 u = *reinterpret_cast<const float4*>(&sm.U[r][jb + j]);
-                    const float4 o = *reinterpret_cast<const float4*>(&sm.dO[r][jb + j]);
-                    const float4 du = *reinterpret_cast<const float4*>(&sm.dU[r][jb + j]);
-                    akt[rr] = fmaf(u.x, dv[0], fmaf(u.y, dv[1], fmaf(u.z, dv[2], fmaf(u.w, dv[3], akt[rr]))));
-                    aqa[rr] = fmaf(o.x, sv[0], fmaf(o.y, sv[1], fmaf(o.z, sv[2], fmaf(o.w, sv[3], aqa[rr]))));
-                    aw[rr] = fmaf(-du.x, sv[0], fmaf(-du.y, sv[1], fmaf(-du.z, sv[2], fmaf(-du.w, sv[3], aw[rr]))));
+                for (int rp = 0; rp < RP; ++rp) {
+                    const int r = grp * RPT + 2 * rp;
+                    const float4 u0 = *reinterpret_cast<const float4*>(&sm.U[r][jb + j]);
+                    const float4 u1 = *reinterpret_cast<const float4*>(&sm.U[r + 1][jb + j]);
+                    const float4 o0 = *reinterpret_cast<const float4*>(&sm.dO[r][jb + j]);
+                    const float4 o1 = *reinterpret_cast<const float4*>(&sm.dO[r + 1][jb + j]);
+                    const float4 d0 = *reinterpret_cast<const float4*>(&sm.dU[r][jb + j]);
+                    const float4 d1 = *reinterpret_cast<const float4*>(&sm.dU[r + 1][jb + j]);
+                    akt[rp] = __ffma2_rn(make_float2(u0.x, u1.x), make_float2(dv[0], dv[0]), akt[rp]);
+                    akt[rp] = __ffma2_rn(make_float2(u0.y, u1.y), make_float2(dv[1], dv[1]), akt[rp]);
+                    akt[rp] = __ffma2_rn(make_float2(u0.z, u1.z), make_float2(dv[2], dv[2]), akt[rp]);
+                    akt[rp] = __ffma2_rn(make_float2(u0.w, u1.w), make_float2(dv[3], dv[3]), akt[rp]);
+                    aqa[rp] = __ffma2_rn(make_float2(o0.x, o1.x), make_float2(sv[0], sv[0]), aqa[rp]);
+                    aqa[rp] = __ffma2_rn(make_float2(o0.y, o1.y), make_float2(sv[1], sv[1]), aqa[rp]);
+                    aqa[rp] = __ffma2_rn(make_float2(o0.z, o1.z), make_float2(sv[2], sv[2]), aqa[rp]);
+                    aqa[rp] = __ffma2_rn(make_float2(o0.w, o1.w), make_float2(sv[3], sv[3]), aqa[rp]);
+                    aw[rp] = __ffma2_rn(make_float2(-d0.x, -d1.x), make_float2(sv[0], sv[0]), aw[rp]);
+                    aw[rp] = __ffma2_rn(make_float2(-d0.y, -d1.y), make_float2(sv[1], sv[1]), aw[rp]);
+                    aw[rp] = __ffma2_rn(make_float2(-d0.z, -d1.z), make_float2(sv[2], sv[2]), aw[rp]);
+                    aw[rp] = __ffma2_rn(make_float2(-d0.w, -d1.w), make_float2(sv[3], sv[3]), aw[rp]);
                 }
             }
+            __syncthreads();  // tile t is consumed: its slot can take tile t + 2
         }
 #pragma unroll
-        for (int rr = 0; rr < RPT; ++rr) {
-            const int r = grp * RPT + rr;
-            sm.dKt[r][c] = akt[rr];
-            sm.dQa[r][c] = aqa[rr];
-            sm.dW[r][c] = aw[rr];
+        for (int rp = 0; rp < RP; ++rp) {
+            const int r = grp * RPT + 2 * rp;
+            sm.dKt[r][c] = akt[rp].x;
+            sm.dKt[r + 1][c] = akt[rp].y;
+            sm.dQa[r][c] = aqa[rp].x;
+            sm.dQa[r + 1][c] = aqa[rp].y;
+            sm.dW[r][c] = aw[rp].x;
+            sm.dW[r + 1][c] = aw[rp].y;
         }
         if (grp == 0) {
             sm.rs[c] = rsum;
@@ -587,23 +610,21 @@ __global__ void __launch_bounds__(NT) kda_bwd_chunk_kernel(BackwardArgs b)
     //    colsum(dKt Kt) per key channel
     {
         const int r = tid / C, i = tid % C;
-        float m0 = 0.f, m1 = 0.f;
+        float2 m2 = make_float2(0.f, 0.f);
 #pragma unroll 8
-        for (int c = 0; c < DK; c += 2) {
-            m0 = fmaf(sm.KG[r][c], sm.KI[i][c], m0);
-            m1 = fmaf(sm.KG[r][c + 1], sm.KI[i][c + 1], m1);
-        }
-        float dp0 = 0.f, dp1 = 0.f;
+        for (int c = 0; c < DK; c += 2)
+            m2 = __ffma2_rn(*reinterpret_cast<const float2*>(&sm.KG[r][c]), *reinterpret_cast<const float2*>(&sm.KI[i][c]),
+                            m2);
+        float2 dp2 = make_float2(0.f, 0.f);
         if (i <= r) {
 #pragma unroll 8
-            for (int j = 0; j < DV; j += 2) {
-                dp0 = fmaf(sm.dO[r][j], sm.U[i][j], dp0);
-                dp1 = fmaf(sm.dO[r][j + 1], sm.U[i][j + 1], dp1);
-            }
+            for (int j = 0; j < DV; j += 2)
+                dp2 = __ffma2_rn(*reinterpret_cast<const float2*>(&sm.dO[r][j]), *reinterpret_cast<const float2*>(&sm.U[i][j]),
+                                 dp2);
         }
-        const float m = m0 + m1;
+        const float m = m2.x + m2.y;
         sm.M[r][i] = m;
-        sm.dP[r][i] = dp0 + dp1;
+        sm.dP[r][i] = dp2.x + dp2.y;
         sm.X[r][i] = (i < r) ? sm.beta[r] * m : 0.f;
     }
     for (int c = tid; c < DK; c += NT) {
@@ -633,18 +654,14 @@ __global__ void __launch_bounds__(NT) kda_bwd_chunk_kernel(BackwardArgs b)
     // 5. dT = dU (diag(b) V)^T + dW (diag(b) KG)^T
     {
         const int r = tid / C, i = tid % C;
-        float a0 = 0.f, a1 = 0.f;
+        float2 a2 = make_float2(0.f, 0.f);
 #pragma unroll 8
-        for (int j = 0; j < DV; j += 2) {
-            a0 = fmaf(sm.dU[r][j], sm.V[i][j], a0);
-            a1 = fmaf(sm.dU[r][j + 1], sm.V[i][j + 1], a1);
-        }
+        for (int j = 0; j < DV; j += 2)
+            a2 = __ffma2_rn(*reinterpret_cast<const float2*>(&sm.dU[r][j]), *reinterpret_cast<const float2*>(&sm.V[i][j]), a2);
 #pragma unroll 8
-        for (int c = 0; c < DK; c += 2) {
-            a0 = fmaf(sm.dW[r][c], sm.KG[i][c], a0);
-            a1 = fmaf(sm.dW[r][c + 1], sm.KG[i][c + 1], a1);
-        }
-        sm.dTn[r][i] = sm.beta[i] * (a0 + a1);
+        for (int c = 0; c < DK; c += 2)
+            a2 = __ffma2_rn(*reinterpret_cast<const float2*>(&sm.dW[r][c]), *reinterpret_cast<const float2*>(&sm.KG[i][c]), a2);
+        sm.dTn[r][i] = sm.beta[i] * (a2.x + a2.y);
     }
     __syncthreads();
     // 6. dA = -tril_strict(T^T dT T^T)
@@ -838,11 +855,11 @@ cudaError_t launch_backward_t(const BackwardArgs& b, cudaStream_t s)
     };
     if (narrow) {
         constexpr int JS = 16;
-        const size_t smem = std::max(sizeof(StatesSmem<DK, JS>), sizeof(DStatesSmem<DK, JS>));
+        const size_t smem = std::max(sizeof(StatesSmem<DK, JS>), sizeof(DStatesSmem<TIO, DK, JS>));
         e = launch_states(kda_bwd_states_kernel<TIO, DK, DV, JS>, smem, DV / JS);
     } else {
         constexpr int JS = DV < 32 ? DV : 32;
-        const size_t smem = std::max(sizeof(StatesSmem<DK, JS>), sizeof(DStatesSmem<DK, JS>));
+        const size_t smem = std::max(sizeof(StatesSmem<DK, JS>), sizeof(DStatesSmem<TIO, DK, JS>));
         e = launch_states(kda_bwd_states_kernel<TIO, DK, DV, JS>, smem, DV / JS);
     }
     if (e != cudaSuccess) return e;

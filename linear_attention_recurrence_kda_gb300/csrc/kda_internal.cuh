@@ -191,6 +191,7 @@ __device__ __forceinline__ void store_seg_m(float* seg, int c, int j, float x)
 //   [0, 256)  check word
 //   G, W, Ut  fp32 [T_tot, H, d]   the forward path's per-chunk G, W and U~ (kda_gate, kda_ut_wy)
 //   P         fp32 [T_tot, H, 16]  row r of each chunk's tril_incl((Q Gamma)(K / Gamma)^T)
+//   QG, Kt    fp32 [T_tot, H, d_k] Q Gamma and K Gamma_C / Gamma of every chunk
 //   U, dU     fp32 [T_tot, H, d_v] U = U~ - W S_in and its gradient
 //   S_chunk   fp32 [slots][H][d_k][d_v]  state entering each chunk
 //   dS_chunk  fp32 [slots][H][d_k][d_v]  gradient reaching the state after each chunk
@@ -198,7 +199,7 @@ __device__ __forceinline__ void store_seg_m(float* seg, int c, int j, float x)
 // Chunk ci of sequence n uses slot cu[n] / 16 + n + ci (slots = T_tot / 16 + N + 1), so the slots
 // of consecutive sequences never overlap.
 struct BackwardLayout {
-    size_t g_off, w_off, ut_off, p_off, u_off, du_off, s_off, ds_off, da_off, total, slots;
+    size_t g_off, w_off, ut_off, p_off, qg_off, kt_off, u_off, du_off, s_off, ds_off, da_off, total, slots;
 };
 
 inline BackwardLayout backward_layout(const kda_problem_t& p)
@@ -211,7 +212,9 @@ inline BackwardLayout backward_layout(const kda_problem_t& p)
     L.w_off = align_up(L.g_off + th * p.d_k * sizeof(float), 256);
     L.ut_off = align_up(L.w_off + th * p.d_k * sizeof(float), 256);
     L.p_off = align_up(L.ut_off + th * p.d_v * sizeof(float), 256);
-    L.u_off = align_up(L.p_off + th * kChunk * sizeof(float), 256);
+    L.qg_off = align_up(L.p_off + th * kChunk * sizeof(float), 256);
+    L.kt_off = align_up(L.qg_off + th * p.d_k * sizeof(float), 256);
+    L.u_off = align_up(L.kt_off + th * p.d_k * sizeof(float), 256);
     L.du_off = align_up(L.u_off + th * p.d_v * sizeof(float), 256);
     L.s_off = align_up(L.du_off + th * p.d_v * sizeof(float), 256);
     L.ds_off = align_up(L.s_off + L.slots * p.num_heads * state, 256);
@@ -232,6 +235,8 @@ struct BackwardArgs {
     float* dbeta;             // [T][H]
     float* dS0;               // [N][H][d_k][d_v] or null (not written)
     float* P;                 // workspace regions (see backward_layout)
+    float* QG;
+    float* Kt;
     float* U;
     float* dU;
     float* S_chunk;
