@@ -176,3 +176,25 @@ def test_backward_config1_sampled():
     dA = got[4].double().cpu().numpy()[heads]
     scale = np.abs(ref[3] * z).sum(axis=(0, 2))
     assert np.all(np.abs(dA - ref[4]) <= 1e-3 * scale)
+
+
+def test_backward_config2_varlen_sampled():
+    """The varlen workload (8 sequences of 1,024 .. 16,384 tokens, 32 heads, bf16): all gradients on the
+    GPU; the oracle's gradients for the shortest sequence on heads 0 and 17 (sequences and heads are
+    independent, so the sample is exact)."""
+    inp = I.make_inputs(2)
+    d_out, dsf = _cotangents(inp, seed=74)
+    got = _run(inp, d_out, dsf)
+    torch.cuda.synchronize()
+    lengths = inp["lengths"]
+    n = int(np.argmin(lengths))
+    cu = inp["cu_seqlens"].numpy()
+    t0, t1 = int(cu[n]), int(cu[n + 1])
+    heads = [0, 17]
+    sub = {x: inp[x][t0:t1][:, heads] for x in ("q", "k", "v", "z", "beta")}
+    ref = oracle.backward(sub["q"], sub["k"], sub["v"], sub["z"], inp["A"][heads], sub["beta"],
+                          d_out[t0:t1][:, heads], dsf[n:n + 1][:, heads], S0=inp["S0"][n:n + 1][:, heads])
+    for name, g, r in zip(("dq", "dk", "dv", "dz"), got[:4], ref[:4]):
+        check(g[t0:t1][:, heads], r, torch.bfloat16, f"config 2 {name}")
+    check(got[5][t0:t1][:, heads], ref[5], torch.bfloat16, "config 2 dbeta")
+    check(got[6][n:n + 1][:, heads], ref[6], torch.bfloat16, "config 2 dS0")

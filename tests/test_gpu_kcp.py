@@ -92,3 +92,31 @@ def test_kcp_flow_emulated_on_one_gpu(ranks, io, d):
                                   cu_seqlens=inp["cu_seqlens"])
     check(out, ref_o, io, f"KCP outputs over {ranks} ranges")
     check(last, ref_s, io, f"KCP final state over {ranks} ranges")
+
+
+def test_summaries_compose_at_length():
+    """A property that holds at any size: for a 65,536-token range split into halves r1, r2, the maps
+    compose, M(r) = M(r2) M(r1) and S~(r) = M(r2) S~(r1) + S~(r2), with each summary computed by
+    kda_forward_summary on the tensor-core path (segmented inside for the whole range and the halves)."""
+    T, H, d = 65536, 2, 128
+    g = torch.Generator(device="cuda").manual_seed(84)
+    import cases
+    q, k, v, z = cases.device_tokens(g, (T, H), d, torch.bfloat16, torch.device("cuda"))
+    A = (torch.randn(H, generator=g, device="cuda") * I.A_STD).float()
+    beta = torch.sigmoid(torch.randn(T, H, generator=g, device="cuda")).float()
+    M, St = B.kda_forward_summary(q, k, v, z, A, beta)
+    h = T // 2
+    halves = [B.kda_forward_summary(*(t[a:b].contiguous() for t in (q, k, v, z)), A, beta[a:b].contiguous())
+              for a, b in ((0, h), (h, T))]
+    (M1, S1), (M2, S2) = halves
+    Mc = M2.double() @ M1.double()
+    Sc = M2.double() @ S1.double() + S2.double()
+    torch.cuda.synchronize()
+    check(M, Mc.cpu().numpy(), torch.bfloat16, "composed transition")
+    check(St, Sc.cpu().numpy(), torch.bfloat16, "composed state from zero")
+    # and applying the composed map to a state equals running the range from it
+    S0 = (torch.randn(1, H, d, d, generator=g, device="cuda") * I.S0_STD).float()
+    _, S_run = B.kda_forward(q, k, v, z, A, beta, initial_state=S0)
+    S_map = B.kda_state_scan(torch.stack([M1, M2]), torch.stack([S1, S2]), initial_state=S0)
+    torch.cuda.synchronize()
+    check(S_map, S_run.double().cpu().numpy(), torch.bfloat16, "scanned halves vs the run")
