@@ -600,7 +600,7 @@ def _layer_inputs(lengths, H, dk, dv, K, io, seed):
 
 @pytest.mark.parametrize("io", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 @pytest.mark.parametrize("dk,dv", [(32, 32), (64, 128), (128, 128)])
-@pytest.mark.parametrize("K", [1, 2, 4])
+@pytest.mark.parametrize("K", [1, 2, 3, 4])
 def test_prologue_matches_oracle(io, dk, dv, K):
     lengths = [5, 0, 40, 16, 1, 130, 17]
     H = 3
@@ -637,6 +637,30 @@ def test_epilogue_matches_oracle(io, dv):
     torch.cuda.synchronize()
     check(y, ref, io, "epilogue")
     assert torch.equal(y, y2)
+
+
+@pytest.mark.parametrize("io", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_layer_kernels_at_extreme_inputs(io):
+    """Inputs far out on both tails of the logistic function (convolution outputs and gates near
+    +-100): Swish and the gate saturate to 0 and to the identity without NaNs, and both kernels
+    still match the oracle; also nine heads at d = 32, so that a warp's group of heads is split."""
+    lengths, H, d, K = [90, 3, 64], 9, 32, 4
+    x, w, cu = _layer_inputs(lengths, H, d, d, K, io, seed=31)
+    x = [(t.float() * 40).to(io) for t in x]
+    q, k, v = B.kda_prologue(*(t.cuda() for t in x), *(t.cuda() for t in w), cu_seqlens=cu.cuda())
+    torch.cuda.synchronize()
+    for name, got, xi, wi, norm in (("q", q, x[0], w[0], True), ("v", v, x[2], w[2], False)):
+        assert torch.isfinite(got).all()
+        check(got, oracle.prologue(xi, wi, cu_seqlens=cu.numpy(), normalise=norm), io, f"extreme prologue {name}")
+    g = torch.Generator().manual_seed(32)
+    T = sum(lengths)
+    o = torch.randn(T, H, d, generator=g).to(io)
+    gate = (torch.randn(T, H, d, generator=g) * 60).to(io)
+    wt = torch.randn(d, generator=g).float()
+    y = B.kda_epilogue(o.cuda(), gate.cuda(), wt.cuda(), eps=1e-5)
+    torch.cuda.synchronize()
+    assert torch.isfinite(y).all()
+    check(y, oracle.epilogue(o, gate, wt, 1e-5), io, "extreme epilogue")
 
 
 def test_layer_chain_prologue_forward_epilogue():
