@@ -412,19 +412,23 @@ __global__ void __launch_bounds__(kRepThreads, 2) kda_decode_replay_d128_kernel(
 // along k_t; every earlier write k_i u_i^T reaches it scaled by Gamma_t / Gamma_i).  Per element of S
 // that is two multiply-adds per token instead of four, and no barrier per token.  [KG; QG] S is a
 // 16 x 128 x 128 product per (sequence, head): warp w computes value columns 16w .. 16w + 15 with
-// mma.sync m16n8k8 tf32, every operand split into a tf32 pair (x = hi + lo, products hi.hi + hi.lo +
-// lo.hi with fp32 accumulation: about fp32 accuracy).  The snapshot goes from shared memory straight
-// into B-fragment registers (rows of the staged copy XOR-swizzled in 16-byte pieces so those loads
-// are free of bank conflicts), which frees the copy buffer for the next unit early.
+// mma.sync m16n8k16 bf16, every operand split into a bf16 pair (x = hi + lo, products hi.hi +
+// hi.lo + lo.hi with fp32 accumulation: relative error about 2^-16, far below the bf16 outputs'
+// rounding).  [KG; QG] and KI are staged as bf16 hi/lo tiles and read with ldmatrix / 32-bit loads;
+// the snapshot goes from shared memory straight into split B-fragment registers (rows of the staged
+// copy XOR-swizzled in 16-byte pieces so those loads are free of bank conflicts), which frees the
+// copy buffer for the next unit early.  The in-window products U and O (K = 8 tokens) stay on the
+// split tf32 form.
 struct RepVLayout {
     static constexpr int kRow = kRepD + 4;                              // padded fp32 row of the token-row tiles
     static constexpr int kStage = 0;                                    // fp32 [128][128], swizzled
     static constexpr int kRaw = kStage + kRepD * kRepD * 4;             // bf16 [token][q, k, z, v][128]
     static constexpr int kRawBeta = kRaw + kRepGroup * 4 * kRepD * 2;   // fp32 [token]
-    static constexpr int kKQhi = kRawBeta + kRepGroup * 4;              // tf32 [16][kRow]: KG rows 0..7, QG rows 8..15
-    static constexpr int kKQlo = kKQhi + 16 * kRow * 4;
-    static constexpr int kKI = kKQlo + 16 * kRow * 4;                   // fp32 [token][kRow]
-    static constexpr int kV = kKI + kRepGroup * kRow * 4;               // fp32 [token][128]
+    static constexpr int kBRow = kRepD + 8;                             // padded bf16 row of the split operand tiles
+    static constexpr int kKQhi = kRawBeta + kRepGroup * 4;              // bf16 [16][kBRow]: KG rows 0..7, QG rows 8..15
+    static constexpr int kKQlo = kKQhi + 16 * kBRow * 2;                //   (hi; then lo).  Later U fp32 [token][kRow]
+    static constexpr int kKI = kKQlo + 16 * kBRow * 2;                  // bf16 [token][kBRow] hi, then lo
+    static constexpr int kV = kKI + 2 * kRepGroup * kBRow * 2;          // fp32 [token][128]
     static constexpr int kWY = kV + kRepGroup * kRepD * 4;              // fp32 [16][kRow]: W0 rows 0..7, Y0 rows 8..15;
                                                                         // before that, the base-2 log-decays [token][128]
     static constexpr int kGram = kWY + 16 * kRow * 4;                   // fp32 [warp][16][8]: partial [KG; QG] KI^T
@@ -433,13 +437,52 @@ struct RepVLayout {
     static constexpr int kBeta = kT + 64 * 4;
     static constexpr int kBytes = kBeta + kRepGroup * 4;
 };
-static_assert(RepVLayout::kKQhi % 16 == 0 && RepVLayout::kWY % 16 == 0 && RepVLayout::kGram % 16 == 0, "alignment");
+static_assert(RepVLayout::kKQhi % 16 == 0 && RepVLayout::kKQlo % 16 == 0 && RepVLayout::kKI % 16 == 0 &&
+                  RepVLayout::kV % 16 == 0 && RepVLayout::kWY % 16 == 0 && RepVLayout::kGram % 16 == 0,
+              "alignment");
+static_assert(kRepGroup * RepVLayout::kRow * 4 <= 16 * RepVLayout::kBRow * 2, "U fits in the KG/QG hi tile");
 static_assert(2 * (RepVLayout::kBytes + 1024) <= 228 * 1024, "two CTAs per SM");
 
 // word offset of element (c, j) of the staged snapshot: 16-byte piece j/4 of row c moves to
-// (j/4) xor 2 (c mod 4), so that the B fragments (four rows x eight columns per warp load) hit 32
-// different banks
-__device__ __forceinline__ int vstage_word(int c, int j) { return c * kRepD + ((((j >> 2) ^ ((c & 3) << 1)) << 2) | (j & 3)); }
+// (j/4) xor 2 ((c/2) mod 4), so that the B-fragment loads (rows c0 + 2t for t = 0..3, eight
+// consecutive columns) hit 32 different banks
+__device__ __forceinline__ int vstage_piece(int c, int piece) { return piece ^ (((c >> 1) & 3) << 1); }
+__device__ __forceinline__ int vstage_word(int c, int j) { return c * kRepD + ((vstage_piece(c, j >> 2) << 2) | (j & 3)); }
+
+// (x0, x1) = hi + lo as packed bf16 pairs (x0 in the low half)
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo)
+{
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 r = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&r);
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// acc += (ah + al)(bh + bl), dropping al.bl
+__device__ __forceinline__ void mma_bf16x3(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4],
+                                           const uint32_t (&bh)[2], const uint32_t (&bl)[2])
+{
+    mma_bf16(d, al, bh[0], bh[1]);
+    mma_bf16(d, ah, bl[0], bl[1]);
+    mma_bf16(d, ah, bh[0], bh[1]);
+}
+
+// A fragments (rows 0..15, columns k0 .. k0 + 15) of a row-major bf16 tile with rows `row` elements apart
+__device__ __forceinline__ void ldsm_a(const __nv_bfloat16* tile, int row, int k0, int lane, uint32_t (&r)[4])
+{
+    const __nv_bfloat16* p = tile + ((lane & 7) + 8 * ((lane >> 3) & 1)) * row + k0 + 8 * (lane >> 4);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"((uint32_t)__cvta_generic_to_shared(p)));
+}
 
 __device__ __forceinline__ uint32_t to_tf32(float x)
 {
@@ -488,9 +531,11 @@ __global__ void __launch_bounds__(kRepThreads, 2) kda_decode_replay_verify_d128_
     float* stage = reinterpret_cast<float*>(smem + RepVLayout::kStage);
     unsigned char* raw = smem + RepVLayout::kRaw;
     float* raw_beta = reinterpret_cast<float*>(smem + RepVLayout::kRawBeta);
-    float* s_kqhi = reinterpret_cast<float*>(smem + RepVLayout::kKQhi);
-    float* s_kqlo = reinterpret_cast<float*>(smem + RepVLayout::kKQlo);
-    float* s_ki = reinterpret_cast<float*>(smem + RepVLayout::kKI);
+    constexpr int BR = RepVLayout::kBRow;
+    __nv_bfloat16* s_kqhi = reinterpret_cast<__nv_bfloat16*>(smem + RepVLayout::kKQhi);
+    __nv_bfloat16* s_kqlo = reinterpret_cast<__nv_bfloat16*>(smem + RepVLayout::kKQlo);
+    __nv_bfloat16* s_kihi = reinterpret_cast<__nv_bfloat16*>(smem + RepVLayout::kKI);
+    __nv_bfloat16* s_kilo = s_kihi + kRepGroup * BR;
     float* s_v = reinterpret_cast<float*>(smem + RepVLayout::kV);
     float* s_wy = reinterpret_cast<float*>(smem + RepVLayout::kWY);
     float* s_g2 = s_wy;  // the log-decays live there until the products overwrite them
@@ -522,7 +567,7 @@ __global__ void __launch_bounds__(kRepThreads, 2) kda_decode_replay_verify_d128_
         for (int i = 0; i < D * D / 4 / kRepThreads; ++i) {
             const int e4 = tid + kRepThreads * i;  // 16-byte piece e4 % 32 of row e4 / 32
             const int c = e4 >> 5;
-            cp_async16(stage + c * D + (((e4 & 31) ^ ((c & 3) << 1)) << 2), S + 4 * e4);
+            cp_async16(stage + c * D + (vstage_piece(c, e4 & 31) << 2), S + 4 * e4);
         }
         constexpr int CH = D * 2 / 16;
         const int64_t tok0 = (int64_t)n * L;
@@ -552,15 +597,21 @@ __global__ void __launch_bounds__(kRepThreads, 2) kda_decode_replay_verify_d128_
         asm volatile("cp.async.wait_all;" ::: "memory");
         __syncthreads();  // (1) this unit's snapshot and tokens are in shared memory
 
-        // the snapshot columns 16w .. 16w + 15 as B fragments: [k step][n tile][b0, b1]
-        float bf[D / 8][2][2];
+        // the snapshot columns 16w .. 16w + 15 as split B fragments: [k step][n tile][b0, b1]
+        // (b0: rows 16 ks + 2 t4, + 1; b1: rows 16 ks + 2 t4 + 8, + 9; column 16 w + 8 nt + g8)
+        uint32_t bh[D / 16][2][2], bl[D / 16][2][2];
 #pragma unroll
-        for (int ks = 0; ks < D / 8; ++ks)
+        for (int ks = 0; ks < D / 16; ++ks)
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 const int j = 16 * w + 8 * nt + g8;
-                bf[ks][nt][0] = stage[vstage_word(8 * ks + t4, j)];
-                bf[ks][nt][1] = stage[vstage_word(8 * ks + t4 + 4, j)];
+                const int c0 = 16 * ks + 2 * t4;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int c = c0 + 8 * hf;
+                    split_bf16x2(stage[vstage_word(c, j)], stage[vstage_word(c + 1, j)], bh[ks][nt][hf],
+                                 bl[ks][nt][hf]);
+                }
             }
         // gate of every (token, key channel) in base 2, and v, over all threads
 #pragma unroll
@@ -595,12 +646,14 @@ __global__ void __launch_bounds__(kRepThreads, 2) kda_decode_replay_verify_d128_
                     qg = raw_at(t, 0, c) * gam;
                     ki = kc * igam;
                 }
-                const uint32_t kh = to_tf32(kg), qh = to_tf32(qg);
-                s_kqhi[t * R + c] = __uint_as_float(kh);
-                s_kqlo[t * R + c] = __uint_as_float(to_tf32(kg - __uint_as_float(kh)));
-                s_kqhi[(8 + t) * R + c] = __uint_as_float(qh);
-                s_kqlo[(8 + t) * R + c] = __uint_as_float(to_tf32(qg - __uint_as_float(qh)));
-                s_ki[t * R + c] = ki;
+                const __nv_bfloat16 kh = __float2bfloat16_rn(kg), qh = __float2bfloat16_rn(qg);
+                const __nv_bfloat16 ih = __float2bfloat16_rn(ki);
+                s_kqhi[t * BR + c] = kh;
+                s_kqlo[t * BR + c] = __float2bfloat16_rn(kg - __bfloat162float(kh));
+                s_kqhi[(8 + t) * BR + c] = qh;
+                s_kqlo[(8 + t) * BR + c] = __float2bfloat16_rn(qg - __bfloat162float(qh));
+                s_kihi[t * BR + c] = ih;
+                s_kilo[t * BR + c] = __float2bfloat16_rn(ki - __bfloat162float(ih));
             }
         }
         __syncthreads();  // (2) staged; the copy buffers are free for the next unit
@@ -614,15 +667,20 @@ __global__ void __launch_bounds__(kRepThreads, 2) kda_decode_replay_verify_d128_
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
 #pragma unroll
-        for (int ks = 0; ks < D / 8; ++ks) {
-            const int k0 = 8 * ks + t4;
-            const uint32_t ah[4] = {__float_as_uint(s_kqhi[g8 * R + k0]), __float_as_uint(s_kqhi[(g8 + 8) * R + k0]),
-                                    __float_as_uint(s_kqhi[g8 * R + k0 + 4]), __float_as_uint(s_kqhi[(g8 + 8) * R + k0 + 4])};
-            const uint32_t al[4] = {__float_as_uint(s_kqlo[g8 * R + k0]), __float_as_uint(s_kqlo[(g8 + 8) * R + k0]),
-                                    __float_as_uint(s_kqlo[g8 * R + k0 + 4]), __float_as_uint(s_kqlo[(g8 + 8) * R + k0 + 4])};
+        for (int ks = 0; ks < D / 16; ++ks) {
+            uint32_t ah[4], al[4];
+            ldsm_a(s_kqhi, BR, 16 * ks, l, ah);
+            ldsm_a(s_kqlo, BR, 16 * ks, l, al);
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) mma_tf32x3(acc[nt], ah, al, bf[ks][nt][0], bf[ks][nt][1]);
-            if ((ks >> 1) == w) mma_tf32x3(gacc, ah, al, s_ki[g8 * R + k0], s_ki[g8 * R + k0 + 4]);
+            for (int nt = 0; nt < 2; ++nt) mma_bf16x3(acc[nt], ah, al, bh[ks][nt], bl[ks][nt]);
+            if (ks == w) {  // this warp's k step of the Gram block: B[k][n] = KI[token n][channel k]
+                const int k0 = 16 * ks + 2 * t4;
+                const uint32_t gh[2] = {*reinterpret_cast<const uint32_t*>(s_kihi + g8 * BR + k0),
+                                        *reinterpret_cast<const uint32_t*>(s_kihi + g8 * BR + k0 + 8)};
+                const uint32_t gl[2] = {*reinterpret_cast<const uint32_t*>(s_kilo + g8 * BR + k0),
+                                        *reinterpret_cast<const uint32_t*>(s_kilo + g8 * BR + k0 + 8)};
+                mma_bf16x3(gacc, ah, al, gh, gl);
+            }
         }
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
@@ -681,7 +739,7 @@ __global__ void __launch_bounds__(kRepThreads, 2) kda_decode_replay_verify_d128_
             uint32_t tl[4] = {to_tf32(tA0 - __uint_as_float(th[0])), 0u, to_tf32(tA2 - __uint_as_float(th[2])), 0u};
             uint32_t ph[4] = {to_tf32(pA0), 0u, to_tf32(pA2), 0u};
             uint32_t pl[4] = {to_tf32(pA0 - __uint_as_float(ph[0])), 0u, to_tf32(pA2 - __uint_as_float(ph[2])), 0u};
-            float* s_u = s_kqhi;  // [token][kRow]; the operand tiles are no longer read
+            float* s_u = reinterpret_cast<float*>(s_kqhi);  // [token][kRow]; the operand tiles are no longer read
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 const int jb = 16 * w + 8 * nt + g8;  // B-fragment column

@@ -553,6 +553,29 @@ def test_replay_verify_only(L):
     check(out, _f64(out_rec), torch.bfloat16, "chunk-form verify vs recurrence")
 
 
+@pytest.mark.parametrize("decay", ["floor", "none", "mixed"])
+def test_replay_verify_only_decay_extremes(decay):
+    """The verify form at the ends of the gate's range over a full 8-token window: every log-decay
+    at g_min (Gamma down to e^-40, 1/Gamma up to e^40 in the split bf16 operands), no decay, and
+    half the key channels at each end."""
+    N, L, H, d_ = 24, 8, 4, 128
+    inp = _replay_case(N, L, H, d_, d_, torch.bfloat16, seed=95)
+    z = inp["z"].float()
+    if decay == "floor":
+        z = torch.full_like(z, 60.0)
+    elif decay == "none":
+        z = torch.full_like(z, -60.0)
+    else:
+        z[..., : d_ // 2] = 60.0
+        z[..., d_ // 2:] = -60.0
+    inp["z"] = z.to(torch.bfloat16)
+    ref_o, _ = _oracle_replay(inp)
+    d = to_dev(inp)
+    out, _ = B.kda_decode_replay(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], d["S0"], want_state=False)
+    torch.cuda.synchronize()
+    check(out, ref_o, torch.bfloat16, f"verify outputs, decay {decay}")
+
+
 def test_replay_clamps_accepted_counts():
     N, L, H, dk, dv = 4, 6, 2, 64, 64
     inp = _replay_case(N, L, H, dk, dv, torch.float32, seed=79)
