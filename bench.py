@@ -1008,14 +1008,25 @@ def bench_e2e(args, B, d, dev, max_over_ranks, barrier, world, depth=2):
     steps = max(3, min(args.steps, 10))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s_in)
+    # each step's upload end: the uploads are the pipeline's bottleneck and run back to back, so the
+    # spacing between consecutive ends is the step time in the steady state
+    ends = []
     for _ in range(steps):
         step()
+        ends.append(torch.cuda.Event(enable_timing=True))
+        ends[-1].record(s_in)
     e1.record(s_out)
     torch.cuda.synchronize()
     barrier()
-    ms = max_over_ranks(e0.elapsed_time(e1) / steps)
+    mean_ms = max_over_ranks(e0.elapsed_time(e1) / steps)
+    spacing = [e0.elapsed_time(ends[0])] + [ends[i - 1].elapsed_time(ends[i]) for i in range(1, steps)]
+    ms = max_over_ranks(statistics.median(spacing))
     res = {"value": T * world / (ms * 1e-3) / 1e6, "unit": "Mtok/s", "h2d_bytes_per_step": total,
            "d2h_bytes_per_step": o_total, "ms_per_step": ms, "steps": steps,
+           "statistic": "median of the per-step spacings (upload end to upload end); the mean over the "
+                        "window, last step's compute and download included, is beside it",
+           "mean_ms_per_step": mean_ms, "mean_value": T * world / (mean_ms * 1e-3) / 1e6,
+           "step_spacing_ms": [round(x, 2) for x in spacing],
            "pipeline": f"{depth} device buffer sets over H2D / compute / D2H streams; one copy each way per step"}
     del d_all, dbuf, d_out_all, dout, ws
     return res
