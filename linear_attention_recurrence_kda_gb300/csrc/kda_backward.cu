@@ -507,8 +507,12 @@ __global__ void __launch_bounds__(NT) kda_bwd_chunk_kernel(BackwardArgs b)
     };
     issue_tile(0);  // in flight while the chunk's rows are read
 
-    // 1. the chunk's rows (absent tokens as zeros)
-    for (int e = tid; e < C * DK; e += NT) {
+    // 1. the chunk's rows (absent tokens as zeros); the loops are unrolled so that every load of a
+    //    thread is in flight at once
+    static_assert((C * DK) % NT == 0 && (C * DV) % NT == 0, "whole rows per pass");
+#pragma unroll
+    for (int pass = 0; pass < C * DK / NT; ++pass) {
+        const int e = tid + pass * NT;
         const int r = e / DK, c = e % DK;
         float q = 0.f, k = 0.f, g = 0.f;
         if (r < len) {
@@ -524,7 +528,9 @@ __global__ void __launch_bounds__(NT) kda_bwd_chunk_kernel(BackwardArgs b)
         sm.KI[r][c] = k * expf(-g);
         sm.QG[r][c] = q * eg;
     }
-    for (int e = tid; e < C * DV; e += NT) {
+#pragma unroll
+    for (int pass = 0; pass < C * DV / NT; ++pass) {
+        const int e = tid + pass * NT;
         const int r = e / DV, j = e % DV;
         const bool ok = r < len;
         const int64_t idx = ((t0 + r) * H + h) * (int64_t)DV + j;
@@ -766,11 +772,16 @@ __global__ void __launch_bounds__(NT) kda_bwd_chunk_kernel(BackwardArgs b)
     const float expA = expf(a.A[h]);
     float da = 0.f;
     for (int c = tid; c < DK; c += NT) {
+        float zr[C];  // the channel's z over the chunk, every load in flight at once
+#pragma unroll
+        for (int r = 0; r < C; ++r) zr[r] = r < len ? ld_io(zp, ((t0 + r) * H + h) * (int64_t)DK + c) : 0.f;
         float dg = 0.f;
-        for (int r = len - 1; r >= 0; --r) {
+#pragma unroll
+        for (int r = C - 1; r >= 0; --r) {
+            if (r >= len) continue;
             dg += sm.dKt[r][c];
             const int64_t idx = ((t0 + r) * H + h) * (int64_t)DK + c;
-            const float x = expA * ld_io(zp, idx);
+            const float x = expA * zr[r];
             const float dx = dg * a.g_min * sigmoid_slope(x);
             st_io(dzp, idx, dx * expA);
             da += dx * x;
