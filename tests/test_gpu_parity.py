@@ -635,6 +635,30 @@ def test_prologue_matches_oracle(io, dk, dv, K):
         check(got, ref, io, f"prologue {name}")
 
 
+@pytest.mark.parametrize("io,d,H", [(torch.bfloat16, 128, 4), (torch.float32, 32, 9), (torch.bfloat16, 64, 5)],
+                         ids=["bf16-128", "f32-32", "bf16-64"])
+def test_prologue_many_tiles_per_cta(io, d, H):
+    """More 64-token tiles than the persistent grid has CTAs (over 2 x 152), so CTAs walk several
+    consecutive tiles: double-buffered staging, taps kept across tiles of one head group and reloaded
+    at the next, and the sequence bounds carried from tile to tile across ragged sequence starts."""
+    lengths = [1000, 3, 0, 2049, 64, 1, 3500, 777, 130]
+    x, w, cu = _layer_inputs(lengths, H, d, d, 4, io, seed=33 + d)
+    q, k, v = B.kda_prologue(*(t.cuda() for t in x), *(t.cuda() for t in w), cu_seqlens=cu.cuda())
+    torch.cuda.synchronize()
+    for name, got, xi, wi, norm in (("q", q, x[0], w[0], True), ("k", k, x[1], w[1], True), ("v", v, x[2], w[2], False)):
+        check(got, oracle.prologue(xi, wi, cu_seqlens=cu.numpy(), normalise=norm), io, f"many-tile prologue {name}")
+    # and equal lengths without offsets over the same number of tokens
+    T = sum(lengths)
+    N = 7
+    Teq = T - T % N
+    xe = [t[:Teq].contiguous() for t in x]
+    qe, _, ve = B.kda_prologue(*(t.cuda() for t in xe), *(t.cuda() for t in w), num_seqs=N)
+    torch.cuda.synchronize()
+    cue = np.arange(N + 1) * (Teq // N)
+    check(qe, oracle.prologue(xe[0], w[0], cu_seqlens=cue), io, "many-tile prologue q, equal lengths")
+    check(ve, oracle.prologue(xe[2], w[2], cu_seqlens=cue, normalise=False), io, "many-tile prologue v, equal lengths")
+
+
 def test_prologue_equal_lengths_without_offsets():
     H, d, K, N, Ls = 2, 128, 4, 3, 50
     x, w, _ = _layer_inputs([Ls] * N, H, d, d, K, torch.bfloat16, seed=11)
