@@ -158,6 +158,19 @@ def test_backward_steep_floor_is_unsupported():
     assert e.value.status == B.KDA_ERR_UNSUPPORTED
 
 
+def test_backward_many_short_sequences():
+    """120 sequences of 0 to 40 tokens, bf16 d = 128: per-sequence chunk slots, states and dS0 at a
+    large N."""
+    g = torch.Generator().manual_seed(36)
+    lengths = torch.randint(0, 41, (120,), generator=g).tolist()
+    inp = I.make_inputs(1, lengths=lengths, num_heads=2, d=128, io_dtype=torch.bfloat16, seed=37, random_s0=True)
+    d_out, dsf = _cotangents(inp, seed=38)
+    got = _run(inp, d_out, dsf)
+    torch.cuda.synchronize()
+    ref = _oracle(inp, d_out, dsf)
+    _check_all(got, ref, inp, torch.bfloat16, what="120 short sequences")
+
+
 def test_backward_config1_sampled():
     """The 4096-token, 16-head, d = 128 bf16 workload: all heads on the GPU, the oracle's gradients
     on heads 0 and 9 (heads are independent)."""

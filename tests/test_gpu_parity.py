@@ -71,6 +71,23 @@ def test_config2_varlen_full():
     print(f"config 2 lengths {inp['lengths']}: out {e1:.2e}, state {e2:.2e}")
 
 
+@pytest.mark.parametrize("io,d", [(torch.bfloat16, 128), (torch.float32, 64)], ids=["bf16-128-tc", "f32-64"])
+def test_many_short_sequences(io, d):
+    """300 sequences of 0 to 40 tokens (many empty, many shorter than a chunk, ragged pairs): the
+    per-sequence block slots, chunk grids and final states at a large N."""
+    g = torch.Generator().manual_seed(34)
+    lengths = torch.randint(0, 41, (300,), generator=g).tolist()
+    inp = I.make_inputs(1, lengths=lengths, num_heads=2, d=d, io_dtype=io, seed=35, random_s0=True)
+    out, sf = gpu_forward(inp)
+    ref_o, ref_s = oracle_forward(inp)
+    check(out, ref_o, io, "out")
+    check(sf, ref_s, io, "final_state")
+    # a sequence without tokens hands its initial state through unchanged
+    for n, L in enumerate(lengths):
+        if L == 0:
+            assert torch.equal(sf[n].cpu(), inp["S0"][n].float())
+
+
 @pytest.mark.slow
 def test_config3_long_context_sampled_and_split():
     """1M tokens, 8 heads.  The oracle checks heads 0-1 over the first 65,536 tokens and the
