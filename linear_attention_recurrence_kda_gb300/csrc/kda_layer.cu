@@ -17,10 +17,12 @@
 //   * a lane owns one 16-byte vector of a row (8 bf16 or 4 fp32 channels), so a row of d channels
 //     is a group of G = d / 8 (or d / 4) lanes, a warp covers 32 / G consecutive rows (heads) of a
 //     token at once, and the row reductions are log2(G) shuffles within the group;
-//   * arithmetic runs on packed fp32 pairs, and the two logistic functions of a channel pair share
-//     one hardware reciprocal (1/a = b / (ab), 1/b = a / (ab));
-//   * a prologue CTA stages 64 tokens (and the K-1 before them) of its heads with asynchronous
-//     16-byte copies; each warp then walks 8 consecutive tokens with the convolution's window of
+//   * arithmetic runs on packed fp32 pairs; the logistic function of a channel pair is one packed
+//     half-precision tanh where the result is rounded to bf16, and otherwise two exponentials
+//     sharing one hardware reciprocal (1/a = b / (ab), 1/b = a / (ab));
+//   * the prologue is a persistent grid: a CTA walks consecutive tiles of 64 tokens (and the K-1
+//     before them) of its heads, staged with asynchronous 16-byte copies into two alternating
+//     buffers; each warp walks 8 consecutive tokens of a tile with the convolution's window of
 //     earlier inputs held in registers, so every input vector is read from shared memory once.
 #include <cuda_fp16.h>
 
