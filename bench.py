@@ -932,103 +932,120 @@ def bench_replay(B, dev, g, toks, A, state, decode_ms, max_over_ranks, barrier, 
             "gpu_launches": 2 * reps}
 
 
-def bench_e2e(args, B, d, dev, max_over_ranks, barrier, world, depth=2):
-    """The prefill end to end through kda_forward with host buffers: every step copies its inputs
-    from pinned host memory to the device, runs the prefill and copies the outputs and final state
-    back to pinned host memory.  Steps stream through three CUDA streams with `depth` sets of device
-    buffers, so step i+1's inputs travel while step i computes and step i-1's outputs travel back
-    (a stream of independent prefill requests); the time per step is the steady-state spacing."""
-    import torch
-    keys = ("q", "k", "v", "z", "A", "beta", "S0")
-    T, H, dk = d["k"].shape
-    dv = d["v"].shape[2]
-    N = len(d["lengths"])
-    io = d["k"].dtype
-    # a step's inputs live back to back in one pinned host buffer and travel as one copy into one
-    # device buffer; the call gets views of it (256-byte aligned)
-    offs, total = {}, 0
-    for k in keys:
-        offs[k] = total
-        total += (d[k].numel() * d[k].element_size() + 255) // 256 * 256
-    h_all = torch.empty(total, dtype=torch.uint8).pin_memory()
+class E2EPipeline:
+    """Prefill requests from pinned host memory through kda_forward and back: every step copies its
+    inputs from one pinned host buffer to one of `depth` device buffer sets, runs the prefill and
+    copies the outputs and final states back to pinned host memory, over three CUDA streams (step
+    i+1's inputs travel while step i computes and step i-1's outputs travel back).  Inputs are
+    packed back to back in the host buffer (256-byte aligned) and the call gets views of the device
+    copy.  `outputs()` are views of the pinned output buffer (valid after a synchronize)."""
 
-    def views(buf):
-        return {k: buf[offs[k]:offs[k] + d[k].numel() * d[k].element_size()].view(d[k].dtype).view(d[k].shape)
-                for k in keys}
-    host = views(h_all)
-    for k in keys:
-        host[k].copy_(d[k])
-    d_all = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(depth)]
-    dbuf = [views(b) for b in d_all]
-    o_bytes = T * H * dv * d["k"].element_size()
-    f_off = (o_bytes + 255) // 256 * 256
-    o_total = f_off + N * H * dk * dv * 4
+    KEYS = ("q", "k", "v", "z", "A", "beta", "S0")
 
-    def out_views(buf):
-        return (buf[:o_bytes].view(io).view(T, H, dv), buf[f_off:o_total].view(torch.float32).view(N, H, dk, dv))
-    d_out_all = [torch.empty(o_total, dtype=torch.uint8, device=dev) for _ in range(depth)]
-    dout = [out_views(b) for b in d_out_all]
-    h_out_all = torch.empty(o_total, dtype=torch.uint8).pin_memory()
-    ml = max(d["lengths"])
-    prob = B.make_problem(N, T, ml, H, dk, dv, io)
-    ws = torch.empty(B.kda_forward_workspace_bytes(prob), dtype=torch.uint8, device=dev)
-    cu = d["cu_seqlens"]
-    s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(depth)]
-    ev_cmp = [torch.cuda.Event() for _ in range(depth)]
-    ev_out = [torch.cuda.Event() for _ in range(depth)]
-    count = [0]
+    def __init__(self, B, d, dev, depth=2):
+        import torch
+        self.B, self.depth, self.dev = B, depth, dev
+        T, H, dk = d["k"].shape
+        dv = d["v"].shape[2]
+        N = len(d["lengths"])
+        io = d["k"].dtype
+        shapes = {k: (d[k].dtype, d[k].shape, d[k].numel() * d[k].element_size()) for k in self.KEYS}
+        offs, total = {}, 0
+        for k in self.KEYS:
+            offs[k] = total
+            total += (shapes[k][2] + 255) // 256 * 256
 
-    def step():
-        i = count[0]
+        def views(buf):
+            return {k: buf[offs[k]:offs[k] + shapes[k][2]].view(shapes[k][0]).view(shapes[k][1]) for k in self.KEYS}
+        self.h_all = torch.empty(total, dtype=torch.uint8).pin_memory()
+        host = views(self.h_all)
+        for k in self.KEYS:
+            host[k].copy_(d[k])
+        self.d_all = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(depth)]
+        self.dbuf = [views(x) for x in self.d_all]
+        o_bytes = T * H * dv * d["k"].element_size()
+        f_off = (o_bytes + 255) // 256 * 256
+        o_total = f_off + N * H * dk * dv * 4
+
+        def out_views(buf):
+            return (buf[:o_bytes].view(io).view(T, H, dv), buf[f_off:o_total].view(torch.float32).view(N, H, dk, dv))
+        self.d_out_all = [torch.empty(o_total, dtype=torch.uint8, device=dev) for _ in range(depth)]
+        self.dout = [out_views(x) for x in self.d_out_all]
+        self.h_out_all = torch.empty(o_total, dtype=torch.uint8).pin_memory()
+        self.host_out = out_views(self.h_out_all)
+        self.h2d_bytes, self.d2h_bytes = total, o_total
+        self.ml = max(d["lengths"])
+        prob = B.make_problem(N, T, self.ml, H, dk, dv, io)
+        self.ws = torch.empty(B.kda_forward_workspace_bytes(prob), dtype=torch.uint8, device=dev)
+        self.cu = d["cu_seqlens"]
+        self.s_in, self.s_cmp, self.s_out = (torch.cuda.Stream(dev) for _ in range(3))
+        self.ev_in = [torch.cuda.Event() for _ in range(depth)]
+        self.ev_cmp = [torch.cuda.Event() for _ in range(depth)]
+        self.ev_out = [torch.cuda.Event() for _ in range(depth)]
+        self.count = 0
+
+    def step(self):
+        import torch
+        i, depth = self.count, self.depth
         b = i % depth
-        with torch.cuda.stream(s_in):
+        with torch.cuda.stream(self.s_in):
             if i >= depth:
-                s_in.wait_event(ev_cmp[b])   # the compute of step i - depth has read these inputs
-            d_all[b].copy_(h_all, non_blocking=True)
-            ev_in[b].record(s_in)
-        with torch.cuda.stream(s_cmp):
-            s_cmp.wait_event(ev_in[b])
+                self.s_in.wait_event(self.ev_cmp[b])   # the compute of step i - depth has read these inputs
+            self.d_all[b].copy_(self.h_all, non_blocking=True)
+            self.ev_in[b].record(self.s_in)
+        with torch.cuda.stream(self.s_cmp):
+            self.s_cmp.wait_event(self.ev_in[b])
             if i >= depth:
-                s_cmp.wait_event(ev_out[b])  # the outputs of step i - depth have left
-            x = dbuf[b]
-            B.kda_forward(x["q"], x["k"], x["v"], x["z"], x["A"], x["beta"], initial_state=x["S0"], cu_seqlens=cu,
-                          out=dout[b][0], final_state=dout[b][1], max_seqlen=ml, workspace=ws, stream=s_cmp)
-            ev_cmp[b].record(s_cmp)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_cmp[b])
-            h_out_all.copy_(d_out_all[b], non_blocking=True)
-            ev_out[b].record(s_out)
-        count[0] += 1
+                self.s_cmp.wait_event(self.ev_out[b])  # the outputs of step i - depth have left
+            x = self.dbuf[b]
+            self.B.kda_forward(x["q"], x["k"], x["v"], x["z"], x["A"], x["beta"], initial_state=x["S0"],
+                               cu_seqlens=self.cu, out=self.dout[b][0], final_state=self.dout[b][1],
+                               max_seqlen=self.ml, workspace=self.ws, stream=self.s_cmp)
+            self.ev_cmp[b].record(self.s_cmp)
+        with torch.cuda.stream(self.s_out):
+            self.s_out.wait_event(self.ev_cmp[b])
+            self.h_out_all.copy_(self.d_out_all[b], non_blocking=True)
+            self.ev_out[b].record(self.s_out)
+        self.count += 1
 
+    def outputs(self):
+        return self.host_out
+
+
+def bench_e2e(args, B, d, dev, max_over_ranks, barrier, world, depth=2):
+    """The prefill end to end through kda_forward with host buffers (E2EPipeline: inputs uploaded,
+    outputs and final states downloaded every step); the time per step is the steady-state spacing."""
+    import torch
+    T = d["k"].shape[0]
+    pipe = E2EPipeline(B, d, dev, depth)
     for _ in range(3):
-        step()
+        pipe.step()
     torch.cuda.synchronize()
     barrier()
     steps = max(3, min(args.steps, 10))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s_in)
+    e0.record(pipe.s_in)
     # each step's upload end: the uploads are the pipeline's bottleneck and run back to back, so the
     # spacing between consecutive ends is the step time in the steady state
     ends = []
     for _ in range(steps):
-        step()
+        pipe.step()
         ends.append(torch.cuda.Event(enable_timing=True))
-        ends[-1].record(s_in)
-    e1.record(s_out)
+        ends[-1].record(pipe.s_in)
+    e1.record(pipe.s_out)
     torch.cuda.synchronize()
     barrier()
     mean_ms = max_over_ranks(e0.elapsed_time(e1) / steps)
     spacing = [e0.elapsed_time(ends[0])] + [ends[i - 1].elapsed_time(ends[i]) for i in range(1, steps)]
     ms = max_over_ranks(statistics.median(spacing))
-    res = {"value": T * world / (ms * 1e-3) / 1e6, "unit": "Mtok/s", "h2d_bytes_per_step": total,
-           "d2h_bytes_per_step": o_total, "ms_per_step": ms, "steps": steps,
+    res = {"value": T * world / (ms * 1e-3) / 1e6, "unit": "Mtok/s", "h2d_bytes_per_step": pipe.h2d_bytes,
+           "d2h_bytes_per_step": pipe.d2h_bytes, "ms_per_step": ms, "steps": steps,
            "statistic": "median of the per-step spacings (upload end to upload end); the mean over the "
                         "window, last step's compute and download included, is beside it",
            "mean_ms_per_step": mean_ms, "mean_value": T * world / (mean_ms * 1e-3) / 1e6,
            "step_spacing_ms": [round(x, 2) for x in spacing],
            "pipeline": f"{depth} device buffer sets over H2D / compute / D2H streams; one copy each way per step"}
-    del d_all, dbuf, d_out_all, dout, ws
+    del pipe
     return res
 
 
