@@ -221,10 +221,68 @@ __device__ __forceinline__ void prologue_tokens(const unsigned char* st, TIO* y,
             for (int p = 0; p < P; ++p) xw[0][p] = x[p];
         }
     };
+    // two tokens at once (the common case): one butterfly reduces both rows' sums of squares, the
+    // two halves of a lane group holding one token's total each after log2(G) levels, and one more
+    // exchange hands each half the other's
+    auto step2 = [&](int j) {
+        float2 x0[P], x1[P];
+        V::unpack(*reinterpret_cast<const uint4*>(st + j * kWarpRowBytes), x0);
+        V::unpack(*reinterpret_cast<const uint4*>(st + (j + 1) * kWarpRowBytes), x1);
+        float2 s0[P], s1[P];
+        float2 q0 = make_float2(0.f, 0.f), q1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            s0[p] = __fmul2_rn(wk[0][p], x0[p]);
+            s1[p] = __fmul2_rn(wk[0][p], x1[p]);
+            if (KT > 1) s1[p] = __ffma2_rn(wk[1][p], x0[p], s1[p]);
+#pragma unroll
+            for (int i = 1; i < KT; ++i) s0[p] = __ffma2_rn(wk[i][p], xw[i - 1][p], s0[p]);
+#pragma unroll
+            for (int i = 2; i < KT; ++i) s1[p] = __ffma2_rn(wk[i][p], xw[i - 2][p], s1[p]);
+            s0[p] = swish_io<TIO>(s0[p]);
+            s1[p] = swish_io<TIO>(s1[p]);
+            q0 = __ffma2_rn(s0[p], s0[p], q0);
+            q1 = __ffma2_rn(s1[p], s1[p], q1);
+        }
+        if (norm) {
+            const bool upper = (threadIdx.x & (G / 2)) != 0;
+            const float a0 = q0.x + q0.y, a1 = q1.x + q1.y;
+            float keep = upper ? a1 : a0;
+            keep += __shfl_xor_sync(0xffffffffu, upper ? a0 : a1, G / 2);
+#pragma unroll
+            for (int off = G / 4; off > 0; off >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, off);
+            const float other = __shfl_xor_sync(0xffffffffu, keep, G / 2);
+            const float inv0 = rsqrtf((upper ? other : keep) + 1e-6f);
+            const float inv1 = rsqrtf((upper ? keep : other) + 1e-6f);
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                s0[p] = __fmul2_rn(s0[p], make_float2(inv0, inv0));
+                s1[p] = __fmul2_rn(s1[p], make_float2(inv1, inv1));
+            }
+        }
+        if (store) {
+            *reinterpret_cast<uint4*>(y + j * ystride) = V::pack(s0);
+            *reinterpret_cast<uint4*>(y + (j + 1) * ystride) = V::pack(s1);
+        }
+        // the window moves on by two tokens
+#pragma unroll
+        for (int i = KT - 2; i > 1; --i)
+#pragma unroll
+            for (int p = 0; p < P; ++p) xw[i][p] = xw[i - 2][p];
+        if (KT > 2) {
+#pragma unroll
+            for (int p = 0; p < P; ++p) xw[1][p] = x0[p];
+        }
+        if (KT > 1) {
+#pragma unroll
+            for (int p = 0; p < P; ++p) xw[0][p] = x1[p];
+        }
+    };
     if (run == kProTokens && fresh == 0u) {
         // the common case: straight-line code over the run, so the tokens' work interleaves
+        static_assert(kProTokens % 2 == 0, "token pairs");
 #pragma unroll
-        for (int j = 0; j < kProTokens; ++j) step(j);
+        for (int j = 0; j < kProTokens; j += 2) step2(j);
         return;
     }
     for (int j = 0; j < run; ++j) {
